@@ -1,0 +1,161 @@
+/*
+ * cr.h - C ABI of the GB300 canonical reduce / scan library (libcr).
+ *
+ * What is computed: "Canonical Parallel Reduction and Scan" (github README
+ * andyD123/canonical-reduce):
+ *   P4016R0, Key Design Points - the input is split across L interleaved
+ *     lanes by i mod L; each lane is reduced by the iterative pairwise
+ *     (shift-reduce) tree; the lane results are combined by the same tree
+ *     rule; init is combined once, after the tree, as op(init, R).
+ *   P4229R0, Summary and Key Design Points - named expression policies
+ *     left_fold, pairwise, iterated_pairwise and block_dyadic<B>; the scan
+ *     returns the prefix observations of the named expression.
+ * op is IEEE-754 addition in the element type, round to nearest even, no
+ * contraction, subnormals kept (the page's FP environment: --fmad=false).
+ * Every result is bit-identical to the expression: it does not depend on the
+ * GPU, the SM count, the grid or the tile sizes.
+ *
+ * Conventions for every call:
+ *   - Pointers named x, out, ws are DEVICE pointers; init_host points to ONE
+ *     element of the call's dtype in HOST memory (read before the call
+ *     returns). The caller owns every buffer; libcr allocates nothing and
+ *     frees nothing.
+ *   - All work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream). Calls return without synchronising; results are
+ *     valid once the stream reaches that point.
+ *   - Sizes and strides are counted in ELEMENTS, not bytes. x must be aligned
+ *     to its element size.
+ *   - ws is a device workspace of at least the size the matching
+ *     *_workspace_bytes() call returns, 256-byte aligned. A call may use it
+ *     until the stream passes the call; two calls that overlap in time must
+ *     not share one workspace.
+ *   - Errors: CR_ERR_INVALID_ARG for a bad argument (nothing is enqueued),
+ *     CR_ERR_WORKSPACE when ws is NULL, misaligned or too small (nothing is
+ *     enqueued), CR_ERR_UNSUPPORTED for a valid request this build does not
+ *     implement, CR_ERR_CUDA when a launch fails. A device-side wait that
+ *     gives up after its bounded spin is reported later by cr_sync_status().
+ */
+#ifndef CR_H_
+#define CR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { CR_F32 = 1, CR_F64 = 2 } cr_dtype;
+
+/* Scan expression policies (P4229R0, Summary). */
+typedef enum {
+  CR_LEFT_FOLD = 0,         /* y[i] = (((x0 op x1) op x2) ... op xi)                */
+  CR_PAIRWISE = 1,          /* maximal complete subtrees covering x[0..i], folded   */
+                            /* from the left (prefix observation of one tree)       */
+  CR_ITERATED_PAIRWISE = 2, /* y[i] = tree(x[0..i]), the P4016 tree with L = 1      */
+  CR_BLOCK_DYADIC = 3       /* tree inside blocks of B, blocks chained left to right */
+} cr_policy;
+
+typedef enum {
+  CR_OK = 0,
+  CR_ERR_INVALID_ARG = 1,
+  CR_ERR_UNSUPPORTED = 2,
+  CR_ERR_WORKSPACE = 3,
+  CR_ERR_CUDA = 4,
+  CR_ERR_TIMEOUT = 5
+} cr_status;
+
+/* ---------------------------------------------------------------- reduce */
+
+/* Workspace bytes for cr_reduce(n, L, dt). Never 0 (the status word lives
+ * there). Returns 0 only for invalid arguments. */
+size_t cr_reduce_workspace_bytes(int64_t n, int32_t L, cr_dtype dt);
+
+/* Canonical reduction (P4016R0, Key Design Points):
+ *   result = op(init, tree(R_0, ..., R_{m-1})),  m = min(n, L),
+ *   R_j    = tree(x[j], x[j+L], x[j+2L], ...)   (lane j: i mod L == j),
+ *   tree() = the iterative pairwise shift-reduce tree (operands pushed left
+ *            to right, the two topmost partial trees combined while they
+ *            cover equally many operands, the rest folded from the top down).
+ * Empty lanes (n < L) are omitted; n == 0 gives init.
+ *   x         device, n contiguous elements of dt
+ *   n         >= 0
+ *   L         lane count, >= 1 (the sole topology coordinate)
+ *   init_host host pointer to one element of dt
+ *   out_dev   device pointer to one element of dt, written by the stream
+ * Errors: INVALID_ARG if n < 0, L < 1, x/out/init NULL, bad dt. */
+cr_status cr_reduce(const void* x, int64_t n, int32_t L, const void* init_host, cr_dtype dt,
+                    void* out_dev, void* ws, size_t ws_bytes, void* stream);
+
+/* Workspace bytes for cr_reduce_batched with these sizes. */
+size_t cr_reduce_batched_workspace_bytes(int64_t batch, int64_t n, int32_t L, cr_dtype dt);
+
+/* A batch of independent canonical reductions with one L and one init:
+ * sequence b has elements x[b*batch_stride + i*elem_stride], i < n, and
+ * out_dev[b] = reduce(sequence b, n, L, init). Strides may be any values
+ * (e.g. rows: elem_stride 1, batch_stride ncols; columns of a level-major
+ * array: elem_stride ncols, batch_stride 1), but sequences must not alias
+ * out_dev. batch >= 0, n >= 0, L >= 1. */
+cr_status cr_reduce_batched(const void* x, void* out_dev, int64_t batch, int64_t n,
+                            int64_t elem_stride, int64_t batch_stride, int32_t L,
+                            const void* init_host, cr_dtype dt, void* ws, size_t ws_bytes,
+                            void* stream);
+
+/* ------------------------------------------------------------------ scan */
+
+/* Workspace bytes for cr_inclusive_scan(n, p, B, dt). */
+size_t cr_scan_workspace_bytes(int64_t n, cr_policy p, int64_t B, cr_dtype dt);
+
+/* Inclusive scan: out[i] = the prefix observation at i of the expression
+ * named by p (P4229R0, Summary / Key Design Points):
+ *   CR_LEFT_FOLD          out[i] = out[i-1] op x[i]
+ *   CR_ITERATED_PAIRWISE  out[i] = tree(x[0..i])  (consistent: equals the
+ *                         reduce of the prefix under the same expression)
+ *   CR_PAIRWISE           the maximal complete subtrees of the one tree over
+ *                         x that cover x[0..i], folded from the left (not
+ *                         consistent in general)
+ *   CR_BLOCK_DYADIC       blocks k = [kB, kB+B): P(i) = tree(x[kB..i]),
+ *                         T_k = P(end of block k), C_0 = T_0,
+ *                         C_k = C_{k-1} op T_k; out[i] = P(i) in block 0,
+ *                         else C_{k-1} op P(i)
+ * B is used only by CR_BLOCK_DYADIC and must then be a power of two >= 1.
+ * x, out device, n contiguous elements; out == x (in place) is allowed, any
+ * other overlap is INVALID_ARG. n == 0 writes nothing. No init: a scan
+ * observes the expression itself. */
+cr_status cr_inclusive_scan(const void* x, void* out, int64_t n, cr_policy p, int64_t B,
+                            cr_dtype dt, void* ws, size_t ws_bytes, void* stream);
+
+/* Workspace bytes for cr_inclusive_scan_batched with these sizes. */
+size_t cr_scan_batched_workspace_bytes(int64_t batch, int64_t n, cr_policy p, int64_t B,
+                                       cr_dtype dt);
+
+/* A batch of independent inclusive scans with one policy and B: sequence b is
+ * x[b*batch_stride + i*elem_stride], i < n, and its result goes to the same
+ * positions of out (out uses x's strides). Typical use: columns of a
+ * level-major (levels x ncols) array scanned along the levels, elem_stride =
+ * ncols, batch_stride = 1. out == x is allowed; sequences must not overlap
+ * one another. */
+cr_status cr_inclusive_scan_batched(const void* x, void* out, int64_t batch, int64_t n,
+                                    int64_t elem_stride, int64_t batch_stride, cr_policy p,
+                                    int64_t B, cr_dtype dt, void* ws, size_t ws_bytes,
+                                    void* stream);
+
+/* ------------------------------------------------------------- utilities */
+
+/* Synchronises `stream`, then reports the device-side status of the most
+ * recent call that used `ws`: CR_ERR_TIMEOUT if one of its bounded
+ * cross-block waits gave up (the output is then incomplete), CR_ERR_CUDA if
+ * the stream reports an error, else CR_OK. */
+cr_status cr_sync_status(void* ws, void* stream);
+
+/* Static text for a status code. */
+const char* cr_status_string(cr_status s);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int cr_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CR_H_ */

@@ -1,0 +1,258 @@
+"""GB300 canonical reduce / scan: a thin Python binding of libcr (C ABI).
+
+Every computation runs in libcr's CUDA kernels (``csrc/``, declared in
+``include/cr.h``); this module only marshals torch tensors, streams and the
+workspace into the C calls. PyTorch provides device memory and streams. There
+is no CPU path: if the CUDA library has not been built, importing the binding
+raises.
+
+What is computed ("Canonical Parallel Reduction and Scan", github README
+andyD123/canonical-reduce):
+  * ``reduce(x, L, init)``: P4016R0's canonical reduction - lanes i mod L,
+    each reduced by the iterative pairwise (shift-reduce) tree, lane results
+    combined by the same tree, then op(init, R) once;
+  * ``inclusive_scan(x, policy, B)``: P4229R0's prefix observations of the
+    named expression policies left_fold, pairwise, iterated_pairwise,
+    block_dyadic<B>;
+  * batched/strided variants of both over one axis of a 2-D tensor.
+Results are bit-identical to the named expression on any GPU and launch shape.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libcr.so")
+
+CR_F32, CR_F64 = 1, 2
+POLICIES = {"left_fold": 0, "pairwise": 1, "iterated_pairwise": 2, "block_dyadic": 3}
+STATUS = {0: "CR_OK", 1: "CR_ERR_INVALID_ARG", 2: "CR_ERR_UNSUPPORTED",
+          3: "CR_ERR_WORKSPACE", 4: "CR_ERR_CUDA", 5: "CR_ERR_TIMEOUT"}
+
+# every symbol include/cr.h declares: name -> (restype, argtypes)
+_P, _I64, _I32, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+_INT = ctypes.c_int
+SIGNATURES = {
+    "cr_reduce_workspace_bytes": (_SZ, [_I64, _I32, _INT]),
+    "cr_reduce": (_INT, [_P, _I64, _I32, _P, _INT, _P, _P, _SZ, _P]),
+    "cr_reduce_batched_workspace_bytes": (_SZ, [_I64, _I64, _I32, _INT]),
+    "cr_reduce_batched": (_INT, [_P, _P, _I64, _I64, _I64, _I64, _I32, _P, _INT, _P, _SZ, _P]),
+    "cr_scan_workspace_bytes": (_SZ, [_I64, _INT, _I64, _INT]),
+    "cr_inclusive_scan": (_INT, [_P, _P, _I64, _INT, _I64, _INT, _P, _SZ, _P]),
+    "cr_scan_batched_workspace_bytes": (_SZ, [_I64, _I64, _INT, _I64, _INT]),
+    "cr_inclusive_scan_batched": (_INT, [_P, _P, _I64, _I64, _I64, _I64, _INT, _I64, _INT, _P,
+                                         _SZ, _P]),
+    "cr_sync_status": (_INT, [_P, _P]),
+    "cr_status_string": (ctypes.c_char_p, [_INT]),
+    "cr_version": (_INT, []),
+}
+
+
+class CrError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__("%s failed: %s (%s)" % (what, STATUS.get(code, code),
+                                                 lib().cr_status_string(code).decode()))
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libcr (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(
+                "libcr.so is missing (%s): build it first with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+lib()  # fail at import time when the CUDA library is absent
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float64:
+        return CR_F64
+    if t.dtype == torch.float32:
+        return CR_F32
+    raise TypeError("libcr computes in float32 or float64, got %s" % t.dtype)
+
+
+def _stream_ptr(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+class _Workspace:
+    """One growing device workspace per (device, stream); calls on one stream
+    are ordered, so they may share it."""
+
+    def __init__(self):
+        self._bufs = {}
+        self._lock = threading.Lock()
+
+    def get(self, device: torch.device, stream, nbytes: int) -> torch.Tensor:
+        s = torch.cuda.current_stream(device) if stream is None else stream
+        key = (device.index, int(s.cuda_stream))
+        with self._lock:
+            buf = self._bufs.get(key)
+            if buf is None or buf.numel() < nbytes:
+                with torch.cuda.stream(s):  # allocated on the stream that uses it
+                    buf = torch.empty(max(nbytes, 4096), dtype=torch.uint8, device=device)
+                self._bufs[key] = buf
+            return buf
+
+
+_WS = _Workspace()
+
+
+def workspace(device, stream=None, nbytes: int = 4096) -> torch.Tensor:
+    return _WS.get(torch.device(device), stream, nbytes)
+
+
+def _check(code: int, what: str) -> None:
+    if code != 0:
+        raise CrError(code, what)
+
+
+def _init_buffer(init, dt_code):
+    if dt_code == CR_F64:
+        return ctypes.c_double(float(init))
+    return ctypes.c_float(float(init))
+
+
+def _on_device(x: torch.Tensor):
+    """Host tensors are copied in (the result is copied back by the caller)."""
+    if x.is_cuda:
+        return x, False
+    return x.to("cuda", non_blocking=True), True
+
+
+# ---------------------------------------------------------------- reduce
+def reduce(x: torch.Tensor, L: int, init=0.0, out: torch.Tensor | None = None,
+           stream=None) -> torch.Tensor:
+    """Canonical reduction of a 1-D tensor: op(init, tree over lane trees).
+
+    Returns a 1-element tensor of x's dtype on x's device (a host tensor in
+    gives a host tensor back, through pinned-memory copies)."""
+    if x.dim() != 1:
+        raise ValueError("reduce expects a 1-D tensor; use reduce_batched for 2-D")
+    xd, host = _on_device(x.contiguous() if x.is_cuda else x)
+    xd = xd.contiguous()
+    dt = _dtype_code(xd)
+    n = xd.numel()
+    o = out if out is not None else torch.empty(1, dtype=xd.dtype, device=xd.device)
+    sp = _stream_ptr(stream)
+    nb = lib().cr_reduce_workspace_bytes(n, int(L), dt)
+    if nb == 0:
+        raise ValueError("invalid reduce arguments (n=%d, L=%d)" % (n, L))
+    ws = _WS.get(xd.device, stream, nb)
+    ini = _init_buffer(init, dt)
+    _check(lib().cr_reduce(xd.data_ptr() if n else None, n, int(L), ctypes.byref(ini), dt,
+                           o.data_ptr(), ws.data_ptr(), ws.numel(), sp), "cr_reduce")
+    return o.to("cpu") if host else o
+
+
+def reduce_batched(x: torch.Tensor, L: int, init=0.0, dim: int = -1,
+                   out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """One canonical reduction per line of a 2-D tensor along ``dim`` (any
+    strides): dim=-1 reduces rows, dim=0 reduces columns."""
+    if x.dim() != 2:
+        raise ValueError("reduce_batched expects a 2-D tensor")
+    xd, host = _on_device(x)
+    dt = _dtype_code(xd)
+    d = dim % 2
+    n = xd.shape[d]
+    batch = xd.shape[1 - d]
+    es, bs = xd.stride(d), xd.stride(1 - d)
+    o = out if out is not None else torch.empty(batch, dtype=xd.dtype, device=xd.device)
+    sp = _stream_ptr(stream)
+    nb = lib().cr_reduce_batched_workspace_bytes(batch, n, int(L), dt)
+    if nb == 0:
+        raise ValueError("invalid reduce_batched arguments")
+    ws = _WS.get(xd.device, stream, nb)
+    ini = _init_buffer(init, dt)
+    _check(lib().cr_reduce_batched(xd.data_ptr(), o.data_ptr(), batch, n, es, bs, int(L),
+                                   ctypes.byref(ini), dt, ws.data_ptr(), ws.numel(), sp),
+           "cr_reduce_batched")
+    return o.to("cpu") if host else o
+
+
+# ------------------------------------------------------------------ scan
+def _policy(policy) -> int:
+    return POLICIES[policy] if isinstance(policy, str) else int(policy)
+
+
+def inclusive_scan(x: torch.Tensor, policy="iterated_pairwise", B: int = 1,
+                   out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Inclusive scan of a 1-D tensor under a named expression policy.
+    ``out`` may be ``x`` itself (in place)."""
+    if x.dim() != 1:
+        raise ValueError("inclusive_scan expects a 1-D tensor")
+    xd, host = _on_device(x)
+    xd = xd.contiguous()
+    dt = _dtype_code(xd)
+    n = xd.numel()
+    o = out if out is not None else torch.empty_like(xd)
+    p = _policy(policy)
+    sp = _stream_ptr(stream)
+    nb = lib().cr_scan_workspace_bytes(n, p, int(B), dt)
+    if nb == 0:
+        raise ValueError("invalid scan arguments (policy=%s, B=%d)" % (policy, B))
+    ws = _WS.get(xd.device, stream, nb)
+    _check(lib().cr_inclusive_scan(xd.data_ptr(), o.data_ptr(), n, p, int(B), dt,
+                                   ws.data_ptr(), ws.numel(), sp), "cr_inclusive_scan")
+    return o.to("cpu") if host else o
+
+
+def inclusive_scan_batched(x: torch.Tensor, policy="left_fold", B: int = 1, dim: int = 0,
+                           out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Independent inclusive scans along ``dim`` of a 2-D tensor (dim=0 scans
+    each column of a level-major array along its levels); the result has x's
+    strides."""
+    if x.dim() != 2:
+        raise ValueError("inclusive_scan_batched expects a 2-D tensor")
+    xd, host = _on_device(x)
+    dt = _dtype_code(xd)
+    d = dim % 2
+    n, batch = xd.shape[d], xd.shape[1 - d]
+    es, bs = xd.stride(d), xd.stride(1 - d)
+    o = out if out is not None else torch.empty_strided(xd.shape, xd.stride(), dtype=xd.dtype,
+                                                        device=xd.device)
+    if o.stride() != xd.stride():
+        raise ValueError("out must have x's strides")
+    p = _policy(policy)
+    sp = _stream_ptr(stream)
+    nb = lib().cr_scan_batched_workspace_bytes(batch, n, p, int(B), dt)
+    if nb == 0:
+        raise ValueError("invalid scan arguments")
+    ws = _WS.get(xd.device, stream, nb)
+    _check(lib().cr_inclusive_scan_batched(xd.data_ptr(), o.data_ptr(), batch, n, es, bs, p,
+                                           int(B), dt, ws.data_ptr(), ws.numel(), sp),
+           "cr_inclusive_scan_batched")
+    return o.to("cpu") if host else o
+
+
+def sync_status(device=None, stream=None) -> None:
+    """Synchronise the stream and raise if the last call on its workspace
+    reported a device-side timeout."""
+    dev = torch.device("cuda" if device is None else device)
+    sp = _stream_ptr(stream)
+    ws = _WS.get(dev, stream, 4096)
+    _check(lib().cr_sync_status(ws.data_ptr(), sp), "cr_sync_status")
+
+
+__all__ = ["reduce", "reduce_batched", "inclusive_scan", "inclusive_scan_batched",
+           "sync_status", "lib", "workspace", "CrError", "POLICIES", "SIGNATURES"]

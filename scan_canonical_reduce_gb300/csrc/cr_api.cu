@@ -1,0 +1,172 @@
+// C ABI front end of libcr: argument checks, workspace sizing and launch
+// dispatch. Declarations and the contract of every call are in include/cr.h.
+#include <cstdint>
+#include <cstring>
+
+#include "cr.h"
+#include "cr_plan.h"
+#include "cr_scan.h"
+
+namespace {
+
+size_t esize(cr_dtype dt) {
+  switch (dt) {
+    case CR_F32: return 4;
+    case CR_F64: return 8;
+    default: return 0;
+  }
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+cr_status check_ws(void* ws, size_t ws_bytes, size_t need) {
+  if (ws == nullptr || !aligned(ws, 256) || ws_bytes < need) return CR_ERR_WORKSPACE;
+  return CR_OK;
+}
+
+cr_status from_cuda(cudaError_t e) { return e == cudaSuccess ? CR_OK : CR_ERR_CUDA; }
+
+// Every call starts by clearing the workspace status word (see cr_sync_status).
+cudaError_t clear_status(void* ws, cudaStream_t s) {
+  return cudaMemsetAsync(ws, 0, sizeof(int), s);
+}
+
+cr_status reduce_impl(const void* x, void* out, int64_t batch, int64_t n, int64_t es,
+                      int64_t bs, int32_t L, const void* init_host, cr_dtype dt, void* ws,
+                      size_t ws_bytes, void* stream) {
+  const size_t sz = esize(dt);
+  if (sz == 0 || n < 0 || batch < 0 || L < 1 || init_host == nullptr) return CR_ERR_INVALID_ARG;
+  if (batch > 0 && out == nullptr) return CR_ERR_INVALID_ARG;
+  if (batch > 0 && n > 0 && x == nullptr) return CR_ERR_INVALID_ARG;
+  if ((x && !aligned(x, sz)) || (out && !aligned(out, sz))) return CR_ERR_INVALID_ARG;
+  const cr::ReducePlan plan = cr::plan_reduce(batch, n, L, es, bs, sz);
+  const cr_status ws_ok = check_ws(ws, ws_bytes, plan.ws_bytes);
+  if (ws_ok != CR_OK) return ws_ok;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = clear_status(ws, s);
+  if (e != cudaSuccess) return CR_ERR_CUDA;
+  char* w = static_cast<char*>(ws);
+  if (dt == CR_F64) {
+    double init;
+    std::memcpy(&init, init_host, sizeof(init));
+    e = cr::run_reduce<double>(plan, static_cast<const double*>(x), static_cast<double*>(out),
+                               init, w, s);
+  } else {
+    float init;
+    std::memcpy(&init, init_host, sizeof(init));
+    e = cr::run_reduce<float>(plan, static_cast<const float*>(x), static_cast<float*>(out),
+                              init, w, s);
+  }
+  return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t cr_reduce_workspace_bytes(int64_t n, int32_t L, cr_dtype dt) {
+  if (esize(dt) == 0 || n < 0 || L < 1) return 0;
+  return cr::plan_reduce(1, n, L, 1, n, esize(dt)).ws_bytes;
+}
+
+cr_status cr_reduce(const void* x, int64_t n, int32_t L, const void* init_host, cr_dtype dt,
+                    void* out_dev, void* ws, size_t ws_bytes, void* stream) {
+  if (out_dev == nullptr) return CR_ERR_INVALID_ARG;
+  return reduce_impl(x, out_dev, 1, n, 1, n, L, init_host, dt, ws, ws_bytes, stream);
+}
+
+size_t cr_reduce_batched_workspace_bytes(int64_t batch, int64_t n, int32_t L, cr_dtype dt) {
+  if (esize(dt) == 0 || n < 0 || batch < 0 || L < 1) return 0;
+  // the plan does not depend on the strides
+  return cr::plan_reduce(batch, n, L, 1, n, esize(dt)).ws_bytes;
+}
+
+cr_status cr_reduce_batched(const void* x, void* out_dev, int64_t batch, int64_t n,
+                            int64_t elem_stride, int64_t batch_stride, int32_t L,
+                            const void* init_host, cr_dtype dt, void* ws, size_t ws_bytes,
+                            void* stream) {
+  return reduce_impl(x, out_dev, batch, n, elem_stride, batch_stride, L, init_host, dt, ws,
+                     ws_bytes, stream);
+}
+
+size_t cr_scan_workspace_bytes(int64_t n, cr_policy p, int64_t B, cr_dtype dt) {
+  if (esize(dt) == 0 || n < 0) return 0;
+  if (!cr::scan_args_ok(p, B)) return 0;
+  return cr::plan_scan(1, n, p, B, esize(dt)).ws_bytes;
+}
+
+size_t cr_scan_batched_workspace_bytes(int64_t batch, int64_t n, cr_policy p, int64_t B,
+                                       cr_dtype dt) {
+  if (esize(dt) == 0 || n < 0 || batch < 0) return 0;
+  if (!cr::scan_args_ok(p, B)) return 0;
+  return cr::plan_scan(batch, n, p, B, esize(dt)).ws_bytes;
+}
+
+static cr_status scan_impl(const void* x, void* out, int64_t batch, int64_t n, int64_t es,
+                           int64_t bs, cr_policy p, int64_t B, cr_dtype dt, void* ws,
+                           size_t ws_bytes, void* stream, bool contiguous) {
+  const size_t sz = esize(dt);
+  if (sz == 0 || n < 0 || batch < 0 || !cr::scan_args_ok(p, B)) return CR_ERR_INVALID_ARG;
+  if (batch > 0 && n > 0 && (x == nullptr || out == nullptr)) return CR_ERR_INVALID_ARG;
+  if ((x && !aligned(x, sz)) || (out && !aligned(out, sz))) return CR_ERR_INVALID_ARG;
+  if (contiguous && x != out && n > 0) {
+    const char* a = static_cast<const char*>(x);
+    const char* o = static_cast<const char*>(out);
+    const size_t bytes = (size_t)n * sz;
+    if (a < o + bytes && o < a + bytes) return CR_ERR_INVALID_ARG;  // partial overlap
+  }
+  const cr::ScanPlan plan = cr::plan_scan(batch, n, p, B, sz);
+  const cr_status ws_ok = check_ws(ws, ws_bytes, plan.ws_bytes);
+  if (ws_ok != CR_OK) return ws_ok;
+  if (!plan.supported) return CR_ERR_UNSUPPORTED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = clear_status(ws, s);
+  if (e != cudaSuccess) return CR_ERR_CUDA;
+  char* w = static_cast<char*>(ws);
+  if (dt == CR_F64)
+    e = cr::run_scan<double>(plan, static_cast<const double*>(x), static_cast<double*>(out),
+                             es, bs, w, s);
+  else
+    e = cr::run_scan<float>(plan, static_cast<const float*>(x), static_cast<float*>(out), es,
+                            bs, w, s);
+  return from_cuda(e);
+}
+
+cr_status cr_inclusive_scan(const void* x, void* out, int64_t n, cr_policy p, int64_t B,
+                            cr_dtype dt, void* ws, size_t ws_bytes, void* stream) {
+  return scan_impl(x, out, 1, n, 1, n, p, B, dt, ws, ws_bytes, stream, true);
+}
+
+cr_status cr_inclusive_scan_batched(const void* x, void* out, int64_t batch, int64_t n,
+                                    int64_t elem_stride, int64_t batch_stride, cr_policy p,
+                                    int64_t B, cr_dtype dt, void* ws, size_t ws_bytes,
+                                    void* stream) {
+  return scan_impl(x, out, batch, n, elem_stride, batch_stride, p, B, dt, ws, ws_bytes, stream,
+                   false);
+}
+
+cr_status cr_sync_status(void* ws, void* stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return CR_ERR_CUDA;
+  if (ws == nullptr) return CR_ERR_WORKSPACE;
+  int status = 0;
+  if (cudaMemcpy(&status, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return CR_ERR_CUDA;
+  return status == 0 ? CR_OK : CR_ERR_TIMEOUT;
+}
+
+const char* cr_status_string(cr_status s) {
+  switch (s) {
+    case CR_OK: return "ok";
+    case CR_ERR_INVALID_ARG: return "invalid argument";
+    case CR_ERR_UNSUPPORTED: return "unsupported request";
+    case CR_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case CR_ERR_CUDA: return "CUDA error";
+    case CR_ERR_TIMEOUT: return "a bounded device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int cr_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,329 @@
+// Canonical reduction kernels (P4016R0 on "Canonical Parallel Reduction and
+// Scan", Key Design Points):
+//   reduce(x, n, L, init) = op(init, tree(R_0 .. R_{m-1})),  m = min(n, L),
+//   R_j = tree(x_j, x_{j+L}, ...),  tree = iterative pairwise shift-reduce.
+//
+// Data view. Lane j of a sequence is column j of a row-major (rows x L)
+// matrix: row t holds x[tL .. tL + L). R = floor(n / L) rows are full; lanes
+// j < r = n mod L have one more element in row R. Reading a row is a
+// coalesced read of L consecutive elements, so each thread owns one lane and
+// walks down its column.
+//
+// Passes. One launch per level h of a pyramid:
+//   * leaf blocks: a chunk of T = G * P full rows x W lanes; thread (lane j,
+//     group g) reduces its run of P rows to a perfect tree in registers (16
+//     loads in flight, then a register shift-reduce stack), the G run values
+//     of a lane are combined in shared memory into the perfect tree over the
+//     chunk, which becomes one element of the level h+1 matrix. Chunks start
+//     at multiples of T, so every value is a node of the lane's tree.
+//   * tail blocks (same launch): the rows after the last full chunk. Their
+//     shift-reduce stack is folded, smallest block first, onto the lane's
+//     running right-hand part `acc` (the finer levels' tails lie to the
+//     right), or, when the tail is itself a full chunk (only possible for
+//     the lanes that own row R), written as the ragged row of level h+1.
+//   * final pass: everything left is tail; then, when one block holds all
+//     lanes, the cross-lane tree over R_0..R_{m-1} and op(init, .) follow in
+//     the same block. Otherwise the lane results are a new sequence reduced
+//     by the same passes with L = 1.
+// No value is ever combined with an atomic; the grid shape changes which
+// block evaluates a node, never the node.
+#include <algorithm>
+#include <cstring>
+#include <vector>
+
+#include "cr_device.cuh"
+#include "cr_plan.h"
+
+namespace cr {
+
+constexpr int kThreads = 256;
+constexpr int kLV = 10;  // stack levels: a run of up to 512 operands
+
+template <class T, int U>
+__global__ void __launch_bounds__(kThreads)
+lane_pass_kernel(const T* __restrict__ in_base, int64_t in_seg, int64_t in_row,
+                 int64_t in_lane, T* __restrict__ next, T* __restrict__ acc,
+                 int* __restrict__ has, T* __restrict__ out, T init, PassArgs a) {
+  constexpr int LOGU = (U == 1) ? 0 : (U == 2) ? 1 : (U == 4) ? 2 : (U == 8) ? 3 : 4;
+  __shared__ T vals[kThreads];
+  __shared__ T lane_val[kThreads];
+  __shared__ int lane_has[kThreads];
+
+  const int tid = threadIdx.x;
+  const int jl = tid % a.W;
+  const int g = tid / a.W;
+
+  int64_t item = blockIdx.x;
+  const bool leaf = item < a.n_leaf_items;
+  int64_t b, c;
+  int w;
+  if (leaf) {
+    w = (int)(item % a.tiles);
+    const int64_t rest = item / a.tiles;
+    c = rest % a.C;
+    b = rest / a.C;
+  } else {
+    item -= a.n_leaf_items;
+    w = (int)(item % a.tiles);
+    b = item / a.tiles;
+    c = a.C;
+  }
+  const int64_t j = (int64_t)w * a.W + jl;
+  const bool lane_ok = (g < a.G) && (j < a.L);
+  const int64_t nj = lane_ok ? a.R + (j < a.r ? 1 : 0) : 0;  // values of lane j
+  const int64_t run0 = c * a.T + (int64_t)g * a.P;             // first row of my run
+  int64_t cnt;
+  if (leaf) {
+    cnt = lane_ok ? a.P : 0;
+  } else {
+    cnt = nj - run0;
+    cnt = cnt < 0 ? 0 : (cnt > a.P ? a.P : cnt);
+  }
+
+  // ---- my run: perfect blocks of U rows, then single rows, into the stack
+  RegStack<T, kLV> st;
+  st.reset();
+  if (cnt > 0) {
+    const T* p = in_base + b * in_seg + run0 * in_row + j * in_lane;
+    int64_t k = 0;
+    for (; k + U <= cnt; k += U) {
+      T v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) v[u] = ldg(p + (k + u) * in_row);
+      st.push(perfect_tree<T, U>(v), LOGU);
+    }
+    for (; k < cnt; ++k) st.push(ldg(p + k * in_row), 0);
+  }
+
+  auto V = [&](int gg) -> T& { return vals[gg * a.W + jl]; };
+
+  if (leaf) {
+    // all G runs of the chunk are full: perfect tree over them
+    if (lane_ok) {
+      T v = T(0);
+      st.fold_onto(v, false);
+      V(g) = v;
+    }
+    __syncthreads();
+    smem_pyramid<T>(V, lane_ok ? g : a.G, a.G, a.G);
+    if (lane_ok && g == 0) next[b * a.next_seg + c * a.L + j] = V(0);
+    return;
+  }
+
+  // ---- tail of this level (and, in the final pass, everything)
+  const int64_t tau = lane_ok ? (nj - c * a.T) : 0;  // tail length, 0 <= tau <= T
+  const int F = (int)(tau / a.P);                      // full runs
+  const int part = (int)(tau % a.P);                   // length of the partial run
+  const bool to_next = !a.final_pass && tau == a.T;    // ragged lanes' extra chunk
+
+  if (lane_ok && g < F) {
+    T v = T(0);
+    st.fold_onto(v, false);
+    V(g) = v;
+  }
+  if (lane_ok && to_next && a.first_level && g == 0) has[b * a.L + j] = 0;  // acc empty
+  if (lane_ok && !to_next) {
+    // innermost first: the previous levels' part, then my partial run
+    const bool writer = part > 0 ? (g == F) : (g == 0);
+    if (writer) {
+      T av = T(0);  // read only when ah is set
+      bool ah = false;
+      if (!a.first_level && has[b * a.L + j]) {
+        av = acc[b * a.L + j];
+        ah = true;
+      }
+      if (part > 0) ah = st.fold_onto(av, ah);
+      lane_val[jl] = av;
+      lane_has[jl] = ah ? 1 : 0;
+    }
+  }
+  __syncthreads();
+  smem_pyramid<T>(V, lane_ok ? g : a.G, a.G, lane_ok ? F : 0);
+
+  if (lane_ok && g == 0) {
+    if (to_next) {
+      next[b * a.next_seg + c * a.L + j] = V(0);  // F == G: the chunk's perfect tree
+    } else {
+      T av = lane_val[jl];
+      bool ah = lane_has[jl] != 0;
+      ah = fold_blocks<T>(V, F, av, ah);
+      if (a.fuse_cross) {
+        lane_val[jl] = av;  // R_j (every lane j < m holds at least one operand)
+      } else {
+        acc[b * a.L + j] = av;
+        has[b * a.L + j] = ah ? 1 : 0;
+      }
+    }
+  }
+  if (!a.fuse_cross) return;
+
+  // ---- cross-lane tree over R_0..R_{m-1} (all in this block), then init
+  __syncthreads();
+  auto LVv = [&](int gg) -> T& { return lane_val[gg]; };
+  const int mm = (int)a.m;
+  int Gp = 1;
+  while (Gp < mm) Gp *= 2;
+  smem_pyramid<T>(LVv, tid < mm ? tid : Gp, Gp, mm);
+  if (tid == 0) {
+    T r = T(0);
+    fold_blocks<T>(LVv, mm, r, false);
+    out[b] = add_rn(init, r);
+  }
+}
+
+template <class T>
+__global__ void write_init_kernel(T* out, int64_t batch, T init) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < batch) out[i] = init;
+}
+
+// ------------------------------------------------------------------ planning
+namespace {
+
+int64_t pow2floor(int64_t v) {
+  int64_t p = 1;
+  while (p * 2 <= v) p *= 2;
+  return p;
+}
+int64_t pow2ceil(int64_t v) {
+  int64_t p = 1;
+  while (p < v) p *= 2;
+  return p;
+}
+
+struct Bump {
+  size_t off;
+  size_t take(size_t bytes) {
+    const size_t o = off;
+    off += (bytes + 255) & ~size_t(255);
+    return o;
+  }
+};
+
+// Appends the passes that reduce `batch` sequences held as a (R x Lanes)
+// matrix (+ r ragged lanes) to lane results. If the last pass cannot fuse the
+// cross-lane tree, recurses with L = 1 over the lane results.
+void plan_tree(ReducePlan& plan, Bump& ws, int64_t batch, int64_t R, int64_t r,
+               int64_t Lanes, int64_t m, MatRef in, size_t esize) {
+  const int W = (int)std::min<int64_t>(Lanes, kThreads);
+  const int G = (int)pow2floor(kThreads / W);
+  const int tiles = (int)((Lanes + W - 1) / W);
+  const size_t acc_off = ws.take(batch * Lanes * esize);
+  const size_t has_off = ws.take(batch * Lanes * sizeof(int));
+  bool first = true;
+  for (;;) {
+    PassPlan pp{};
+    PassArgs& a = pp.a;
+    a.R = R;
+    a.r = r;
+    a.L = Lanes;
+    a.W = W;
+    a.G = G;
+    a.tiles = tiles;
+    a.m = m;
+    a.first_level = first ? 1 : 0;
+    pp.in = in;
+    pp.acc_off = acc_off;
+    pp.has_off = has_off;
+    const bool final_pass = R * W <= 4096;
+    if (final_pass) {
+      int64_t T = std::max<int64_t>(G, pow2ceil(R + (r > 0 ? 1 : 0)));
+      a.T = T;
+      a.P = (int)(T / G);
+      a.C = 0;
+      a.n_leaf_items = 0;
+      a.final_pass = 1;
+      a.fuse_cross = tiles == 1 ? 1 : 0;
+      a.next_seg = 0;
+      pp.next_off = 0;
+      pp.grid = batch * tiles;
+      plan.passes.push_back(pp);
+      if (!a.fuse_cross) {
+        // lane results acc[b][0..m) form a new sequence per segment; L = 1
+        MatRef acc_in{true, acc_off, Lanes, 1, 1};
+        plan_tree(plan, ws, batch, m, 0, 1, 1, acc_in, esize);
+      }
+      return;
+    }
+    const int64_t target = std::max<int64_t>(1, 608 / (batch * tiles));
+    int64_t P = pow2floor(std::max<int64_t>(1, R / (G * target)));
+    P = std::min<int64_t>(P, 256);
+    if ((int64_t)G * P * W < 4096)
+      P = std::min<int64_t>(pow2floor(std::max<int64_t>(1, R / G)),
+                            pow2ceil((4096 + G * W - 1) / (G * W)));
+    if (G * P < 2) P = 2;
+    P = std::min<int64_t>(P, 256);
+    const int64_t T = G * P;
+    const int64_t C = R / T;
+    a.T = T;
+    a.P = (int)P;
+    a.C = C;
+    a.n_leaf_items = batch * C * tiles;
+    a.final_pass = 0;
+    a.fuse_cross = 0;
+    a.next_seg = (C + 1) * Lanes;
+    pp.next_off = ws.take(batch * (C + 1) * Lanes * esize);
+    pp.grid = a.n_leaf_items + batch * tiles;
+    plan.passes.push_back(pp);
+    const int64_t r_next = (R % T == T - 1) ? r : 0;
+    in = MatRef{true, pp.next_off, a.next_seg, Lanes, 1};
+    R = C;
+    r = r_next;
+    first = false;
+  }
+}
+
+}  // namespace
+
+ReducePlan plan_reduce(int64_t batch, int64_t n, int64_t L, int64_t elem_stride,
+                       int64_t batch_stride, size_t esize) {
+  ReducePlan plan;
+  Bump ws{kHeaderBytes};
+  plan.batch = batch;
+  if (n == 0 || batch == 0) {
+    plan.ws_bytes = ws.off;
+    return plan;
+  }
+  const int64_t Leff = (L >= n) ? 1 : L;  // L >= n gives the same tree as L = 1
+  const int64_t R = n / Leff, r = n % Leff;
+  const int64_t m = std::min<int64_t>(n, Leff);
+  MatRef x_in{false, 0, batch_stride, Leff * elem_stride, elem_stride};
+  plan_tree(plan, ws, batch, R, r, Leff, m, x_in, esize);
+  plan.ws_bytes = ws.off;
+  return plan;
+}
+
+template <class T>
+cudaError_t run_reduce(const ReducePlan& plan, const T* x, T* out, T init, char* ws,
+                       cudaStream_t s) {
+  if (plan.passes.empty()) {
+    if (plan.batch > 0)
+      write_init_kernel<T><<<(unsigned)((plan.batch + 255) / 256), 256, 0, s>>>(
+          out, plan.batch, init);
+    return cudaGetLastError();
+  }
+  for (const PassPlan& pp : plan.passes) {
+    const T* in_base = pp.in.in_ws ? reinterpret_cast<const T*>(ws + pp.in.ws_off) : x;
+    T* next = pp.a.final_pass ? nullptr : reinterpret_cast<T*>(ws + pp.next_off);
+    T* acc = reinterpret_cast<T*>(ws + pp.acc_off);
+    int* has = reinterpret_cast<int*>(ws + pp.has_off);
+    if (pp.grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    // runs shorter than 16 rows use smaller register blocks
+    if (pp.a.P >= 16)
+      lane_pass_kernel<T, 16><<<(unsigned)pp.grid, kThreads, 0, s>>>(
+          in_base, pp.in.seg, pp.in.row, pp.in.lane, next, acc, has, out, init, pp.a);
+    else
+      lane_pass_kernel<T, 4><<<(unsigned)pp.grid, kThreads, 0, s>>>(
+          in_base, pp.in.seg, pp.in.row, pp.in.lane, next, acc, has, out, init, pp.a);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+template cudaError_t run_reduce<double>(const ReducePlan&, const double*, double*, double,
+                                        char*, cudaStream_t);
+template cudaError_t run_reduce<float>(const ReducePlan&, const float*, float*, float, char*,
+                                       cudaStream_t);
+
+}  // namespace cr

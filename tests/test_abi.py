@@ -1,0 +1,99 @@
+"""The C ABI library: builds, loads, exports every function include/cr.h
+declares, and rejects bad arguments on the host (no GPU needed: argument
+checks and workspace sizing run before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "cr.h")
+
+
+@pytest.fixture(scope="module")
+def scr():
+    import __graft_entry__
+    __graft_entry__.build()
+    import scan_canonical_reduce_gb300 as m
+    return m
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(cr_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(scr):
+    names = declared_functions()
+    assert len(names) >= 11
+    lib = ctypes.CDLL(scr.LIB_PATH)
+    for name in names:
+        assert hasattr(lib, name), name
+    # and the binding declares a signature for each
+    assert sorted(scr.SIGNATURES) == names
+
+
+def test_status_strings_and_version(scr):
+    L = scr.lib()
+    for code in range(6):
+        assert L.cr_status_string(code)
+    assert L.cr_status_string(99) == b"unknown status"
+    assert L.cr_version() >= 100
+
+
+def test_workspace_sizes(scr):
+    L = scr.lib()
+    for n in (0, 1, 17, 1 << 20, (1 << 28) + 37):
+        for lanes in (1, 16, 128, 1024):
+            for dt in (1, 2):
+                nb = L.cr_reduce_workspace_bytes(n, lanes, dt)
+                assert nb >= 256 and nb % 256 == 0
+    assert L.cr_reduce_workspace_bytes(-1, 16, 2) == 0
+    assert L.cr_reduce_workspace_bytes(10, 0, 2) == 0
+    assert L.cr_reduce_workspace_bytes(10, 16, 3) == 0
+    assert L.cr_reduce_batched_workspace_bytes(65536, 4096, 128, 1) >= 256
+    assert L.cr_scan_workspace_bytes(100, 3, 3, 2) == 0   # B not a power of two
+    assert L.cr_scan_workspace_bytes(100, 9, 1, 2) == 0   # unknown policy
+    assert L.cr_scan_workspace_bytes(100, 3, 16, 2) >= 256
+
+
+def test_host_side_argument_errors(scr):
+    L = scr.lib()
+    one = ctypes.c_double(0.0)
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: checks fail first
+    # n < 0, L < 1, bad dtype, missing init/out
+    assert L.cr_reduce(fake, -1, 16, ctypes.byref(one), 2, fake, fake, 1 << 20, None) == 1
+    assert L.cr_reduce(fake, 10, 0, ctypes.byref(one), 2, fake, fake, 1 << 20, None) == 1
+    assert L.cr_reduce(fake, 10, 16, ctypes.byref(one), 7, fake, fake, 1 << 20, None) == 1
+    assert L.cr_reduce(fake, 10, 16, None, 2, fake, fake, 1 << 20, None) == 1
+    assert L.cr_reduce(fake, 10, 16, ctypes.byref(one), 2, None, fake, 1 << 20, None) == 1
+    # misaligned element pointer
+    assert L.cr_reduce(ctypes.c_void_p(0x10004), 10, 16, ctypes.byref(one), 2, fake, fake,
+                       1 << 20, None) == 1
+    # workspace missing / misaligned / too small
+    assert L.cr_reduce(fake, 10, 16, ctypes.byref(one), 2, fake, None, 1 << 20, None) == 3
+    assert L.cr_reduce(fake, 10, 16, ctypes.byref(one), 2, fake, ctypes.c_void_p(0x10008),
+                       1 << 20, None) == 3
+    assert L.cr_reduce(fake, 1 << 20, 16, ctypes.byref(one), 2, fake, fake, 256, None) == 3
+    # scans: bad policy, B not a power of two, partial overlap
+    assert L.cr_inclusive_scan(fake, fake, 10, 9, 1, 2, fake, 1 << 20, None) == 1
+    assert L.cr_inclusive_scan(fake, fake, 10, 3, 6, 2, fake, 1 << 20, None) == 1
+    assert L.cr_inclusive_scan(fake, ctypes.c_void_p(0x10008), 10, 2, 1, 2, fake, 1 << 20,
+                               None) == 1
+    assert L.cr_reduce_batched(fake, fake, -1, 10, 1, 10, 16, ctypes.byref(one), 2, fake,
+                               1 << 20, None) == 1
+
+
+def test_binding_fails_loudly_without_library(tmp_path, scr):
+    """The binding has no CPU fallback: with the library absent it raises."""
+    import importlib.util
+    import shutil
+    pkg = tmp_path / "scan_canonical_reduce_gb300"
+    shutil.copytree(os.path.dirname(scr.__file__), pkg,
+                    ignore=shutil.ignore_patterns("_build", "__pycache__"))
+    spec = importlib.util.spec_from_file_location("scr_nolib", pkg / "__init__.py")
+    mod = importlib.util.module_from_spec(spec)
+    with pytest.raises(ImportError):
+        spec.loader.exec_module(mod)
