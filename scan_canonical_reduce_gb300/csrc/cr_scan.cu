@@ -1,9 +1,344 @@
-// Canonical scan kernels (placeholder: no policy implemented yet).
+// Canonical scan kernels (P4229R0 on "Canonical Parallel Reduction and
+// Scan", Summary / Key Design Points): prefix observations of the named
+// expressions left_fold, pairwise, iterated_pairwise and block_dyadic<B>.
+//
+// iterated_pairwise: out[i] = tree(x[0..i]) = N_1 op (N_2 op (... op N_m)),
+// N_1..N_m the perfect subtrees over the aligned blocks of the binary
+// decomposition of i + 1, largest first. Writing i = (b*256 + t)*8 + e
+// (tile b, thread t, element e), the nodes split by bit ranges:
+//   out[i] = [tile-level nodes of b] op ([thread-level nodes of t] op w[e]),
+// with w[e] the thread-local scan of its 8 elements and each level folded
+// from its lowest set bit up (right-nested). A node at level p starting at
+// q*2^p is the perfect tree over aligned thread (tile) aggregates.
+// block_dyadic<B>: the same restricted to the position inside the block (only
+// the bits below log2 B), then out[i] = C_{k-1} op P(i) for blocks k >= 1,
+// where C_0 = T_0 and C_k = C_{k-1} op T_k over the block totals T_k.
+//
+// Passes of a 1-D scan (contiguous x):
+//   up    per tile: thread and tile aggregates, block totals of blocks that
+//         lie inside a tile; the node pyramid over full tiles is completed
+//         by arrival tickets: of two sibling nodes, the block that arrives
+//         second computes the parent as left op right (counters only, values
+//         never pass through an atomic, nothing waits);
+//   chain block_dyadic only: the serial left fold of the block totals - a
+//         dependency of the expression itself;
+//   down  per tile: local scans, prefix nodes, carry; one write of out.
+// Batched / strided scans (e.g. columns of a level-major array, which are
+// adjacent in memory) run one thread per sequence with a register
+// shift-reduce stack.
+#include <algorithm>
+#include <vector>
+
 #include "cr_device.cuh"
 #include "cr_scan.h"
 
 namespace cr {
 
+constexpr int kScanThreads = 256;
+constexpr int kE = 8;                     // elements per thread
+constexpr int kTile = kScanThreads * kE;  // 2048 elements per tile
+constexpr int kLogE = 3;
+constexpr int kLogTile = 11;
+
+__device__ __forceinline__ int64_t imin(int64_t a, int64_t b) { return a < b ? a : b; }
+__device__ __forceinline__ int64_t imax(int64_t a, int64_t b) { return a > b ? a : b; }
+
+template <int N>
+struct Log2 {
+  static constexpr int value = 1 + Log2<N / 2>::value;
+};
+template <>
+struct Log2<1> {
+  static constexpr int value = 0;
+};
+
+// Thread-local scan of E register values in segments of S (S | E): within a
+// segment, w[e] = tree(v[segment start .. e]); agg[s] = tree(segment s).
+// The loops unroll completely, so every "is this slot occupied" test is a
+// compile-time constant and only the adds of the tree are emitted.
+template <class T, int E, int S>
+__device__ __forceinline__ void local_scan(const T (&v)[E], T (&w)[E], T (&agg)[E / S]) {
+  constexpr int LS = Log2<S>::value;
+#pragma unroll
+  for (int s = 0; s < E / S; ++s) {
+    T slot[LS + 1];
+#pragma unroll
+    for (int e = 0; e < S; ++e) {
+      T c = v[s * S + e];
+      bool placed = false;
+#pragma unroll
+      for (int lv = 0; lv <= LS; ++lv) {
+        if (!placed) {
+          if ((e >> lv) & 1) {
+            c = add_rn(slot[lv], c);  // older block is the left operand
+          } else {
+            slot[lv] = c;
+            placed = true;
+          }
+        }
+      }
+      const int n1 = e + 1;
+      T acc = T(0);
+      bool has = false;
+#pragma unroll
+      for (int lv = 0; lv <= LS; ++lv) {
+        if ((n1 >> lv) & 1) {
+          acc = has ? add_rn(slot[lv], acc) : slot[lv];
+          has = true;
+        }
+      }
+      w[s * S + e] = acc;
+    }
+    agg[s] = slot[LS];
+  }
+}
+
+// In-block pyramid over the 256 thread aggregates, all levels kept:
+// level p (p = 0..8) holds 256 >> p nodes at lvl[lvl_base(p) + q].
+__device__ __forceinline__ int lvl_base(int p) {
+  return 2 * kScanThreads - ((2 * kScanThreads) >> p);
+}
+
+template <class T>
+__device__ __forceinline__ void build_tile_pyramid(T* lvl, int t, int full_threads) {
+  __syncthreads();
+  for (int p = 1; p <= 8; ++p) {
+    const int c = full_threads >> p;  // complete nodes only
+    if (t < c)
+      lvl[lvl_base(p) + t] =
+          add_rn(lvl[lvl_base(p - 1) + 2 * t], lvl[lvl_base(p - 1) + 2 * t + 1]);
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------------------------------ up pass
+template <class T, int S>
+__global__ void __launch_bounds__(kScanThreads)
+scan_up_kernel(const T* __restrict__ x, T* __restrict__ pyr, int* __restrict__ counters,
+               T* __restrict__ totals, ScanArgs a) {
+  __shared__ T lvl[2 * kScanThreads];
+  constexpr int NS = kE / S;
+  constexpr int LS = Log2<S>::value;
+  const int t = threadIdx.x;
+  const int64_t b = blockIdx.x;
+  const int64_t i0 = b * kTile + (int64_t)t * kE;
+  const int64_t cnt = imax(0, imin(kE, a.n - i0));
+  const int full_threads = (int)imin(kScanThreads, (a.n - b * kTile) / kE);
+
+  T v[kE];
+#pragma unroll
+  for (int e = 0; e < kE; ++e) v[e] = (e < cnt) ? ldg(x + i0 + e) : T(0);
+  T w[kE], agg[NS];
+  local_scan<T, kE, S>(v, w, agg);
+  if (a.totals_level == 0) {  // blocks of B = S <= kE elements inside a thread
+#pragma unroll
+    for (int s = 0; s < NS; ++s)
+      if ((s + 1) * S <= cnt) totals[(i0 >> LS) + s] = agg[s];
+  }
+  T tagg;
+  if (NS == 1) {
+    tagg = agg[0];
+  } else {
+    T vv[kE];
+#pragma unroll
+    for (int e = 0; e < kE; ++e) vv[e] = v[e];
+    tagg = perfect_tree<T, kE>(vv);
+  }
+  if (t < full_threads) lvl[t] = tagg;
+  build_tile_pyramid(lvl, t, full_threads);
+
+  // blocks of kE < B < kTile elements: complete nodes of the tile pyramid
+  if (a.totals_level > 0) {
+    const int p = a.totals_level;
+    if (t < (full_threads >> p)) totals[((b * kTile) >> a.logB) + t] = lvl[lvl_base(p) + t];
+  }
+  if (a.pyr_levels == 0 || t != 0 || b >= a.full_tiles) return;
+
+  // tile aggregate = level 0 of the global pyramid; climb by arrival tickets
+  T node = lvl[lvl_base(8)];
+  pyr[a.pyr_off[0] + b] = node;
+  int64_t q = b;
+  for (int p = 1; p < a.pyr_levels; ++p) {
+    const int64_t parent = q >> 1;
+    if (parent >= (a.full_tiles >> p)) break;  // the parent is not a complete node
+    __threadfence();
+    const int ticket = atomicAdd(counters + a.cnt_off[p] + parent, 1);
+    if (ticket == 0) break;  // the sibling is still running; it will climb
+    __threadfence();
+    const T left = __ldcg(pyr + a.pyr_off[p - 1] + 2 * parent);
+    const T right = __ldcg(pyr + a.pyr_off[p - 1] + 2 * parent + 1);
+    node = add_rn(left, right);
+    pyr[a.pyr_off[p] + parent] = node;
+    q = parent;
+  }
+}
+
+// ---------------------------------------------------------------- down pass
+template <class T, int S>
+__global__ void __launch_bounds__(kScanThreads)
+scan_down_kernel(const T* x, T* out, const T* __restrict__ pyr, const T* __restrict__ carries,
+                 ScanArgs a) {
+  __shared__ T lvl[2 * kScanThreads];
+  __shared__ T tile_nodes[64];
+  __shared__ T tile_carry;
+  constexpr int NS = kE / S;
+  const int t = threadIdx.x;
+  const int64_t b = blockIdx.x;
+  const int64_t i0 = b * kTile + (int64_t)t * kE;
+  const int64_t cnt = imax(0, imin(kE, a.n - i0));
+  const int full_threads = (int)imin(kScanThreads, (a.n - b * kTile) / kE);
+  // global pyramid levels that lie inside a block (bits of b below log2(B/kTile))
+  const int tile_bits = (int)imin(a.pyr_levels, imax(0, a.logB - kLogTile));
+  const int thread_bits = (int)imin(8, imax(0, a.logB - kLogE));
+
+  if (t < tile_bits && ((b >> t) & 1)) tile_nodes[t] = pyr[a.pyr_off[t] + (b >> t) - 1];
+  if (t == 0 && a.carry && a.logB >= kLogTile) {
+    const int64_t k = (b * kTile) >> a.logB;  // whole tile in block k
+    tile_carry = (k >= 1) ? carries[k - 1] : T(0);
+  }
+
+  T v[kE];
+  if (cnt == kE) {
+#pragma unroll
+    for (int e = 0; e < kE; ++e) v[e] = x[i0 + e];
+  } else {
+#pragma unroll
+    for (int e = 0; e < kE; ++e) v[e] = (e < cnt) ? x[i0 + e] : T(0);
+  }
+  T w[kE], agg[NS];
+  local_scan<T, kE, S>(v, w, agg);
+  T tagg;
+  if (NS == 1) {
+    tagg = agg[0];
+  } else {
+    T vv[kE];
+#pragma unroll
+    for (int e = 0; e < kE; ++e) vv[e] = v[e];
+    tagg = perfect_tree<T, kE>(vv);
+  }
+  if (t < full_threads) lvl[t] = tagg;
+  build_tile_pyramid(lvl, t, full_threads);  // also publishes tile_nodes/tile_carry
+  if (cnt == 0) return;
+
+  // thread-level prefix nodes, lowest bit first (right-nested)
+  for (int p = 0; p < thread_bits; ++p) {
+    if ((t >> p) & 1) {
+      const T nd = lvl[lvl_base(p) + (t >> p) - 1];
+#pragma unroll
+      for (int e = 0; e < kE; ++e) w[e] = add_rn(nd, w[e]);
+    }
+  }
+  // tile-level prefix nodes, lowest bit first
+  for (int p = 0; p < tile_bits; ++p) {
+    if ((b >> p) & 1) {
+      const T nd = tile_nodes[p];
+#pragma unroll
+      for (int e = 0; e < kE; ++e) w[e] = add_rn(nd, w[e]);
+    }
+  }
+  // block carry: out[i] = C_{k-1} op P(i) for blocks k >= 1
+  if (a.carry) {
+    if (a.logB >= kLogTile) {
+      if (((b * kTile) >> a.logB) >= 1) {
+        const T c = tile_carry;
+#pragma unroll
+        for (int e = 0; e < kE; ++e) w[e] = add_rn(c, w[e]);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < kE; ++e) {
+        const int64_t k = (i0 + e) >> a.logB;
+        if (k >= 1 && e < cnt) w[e] = add_rn(ldg(carries + k - 1), w[e]);
+      }
+    }
+  }
+  if (cnt == kE) {
+#pragma unroll
+    for (int e = 0; e < kE; ++e) out[i0 + e] = w[e];
+  } else {
+    for (int e = 0; e < cnt; ++e) out[i0 + e] = w[e];
+  }
+}
+
+// --------------------------------------------------------------- carry chain
+// carries[0] = src[0], carries[k] = carries[k-1] op src[k], k < K. A serial
+// chain by definition of the expression; one thread, loads issued ahead of
+// the dependent adds. Also the whole 1-D left_fold scan (src = x, carries =
+// out, possibly the same array: plain loads, each read before its write).
+template <class T>
+__global__ void carry_chain_kernel(const T* src, T* carries, int64_t K) {
+  if (threadIdx.x != 0 || blockIdx.x != 0 || K <= 0) return;
+  T c = src[0];
+  carries[0] = c;
+  int64_t k = 1;
+  constexpr int D = 32;
+  for (; k + D <= K; k += D) {
+    T tv[D];
+#pragma unroll
+    for (int d = 0; d < D; ++d) tv[d] = src[k + d];
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+      c = add_rn(c, tv[d]);
+      carries[k + d] = c;
+    }
+  }
+  for (; k < K; ++k) {
+    c = add_rn(c, src[k]);
+    carries[k] = c;
+  }
+}
+
+// ------------------------------------------------ batched: thread per sequence
+// Sequence q: element k at x[q*bs + k*es]; its result at out[q*bs + k*es].
+template <class T, int LV>
+__global__ void __launch_bounds__(256)
+scan_seq_kernel(const T* x, T* out, int64_t batch, int64_t n, int64_t es, int64_t bs,
+                int policy, int64_t B) {
+  const int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (q >= batch) return;
+  const T* xp = x + q * bs;
+  T* yp = out + q * bs;
+  if (policy == CR_LEFT_FOLD) {
+    T acc = xp[0];
+    yp[0] = acc;
+    for (int64_t k = 1; k < n; ++k) {
+      acc = add_rn(acc, xp[k * es]);
+      yp[k * es] = acc;
+    }
+    return;
+  }
+  const int64_t blk = (policy == CR_BLOCK_DYADIC) ? B : n;
+  T carry = T(0);
+  for (int64_t k0 = 0; k0 < n; k0 += blk) {
+    const int64_t len = imin(blk, n - k0);
+    RegStack<T, LV> st;
+    st.reset();
+    for (int64_t e = 0; e < len; ++e) {
+      st.push(xp[(k0 + e) * es], 0);
+      T acc = T(0);
+      if (policy == CR_PAIRWISE) {  // maximal subtrees folded from the left
+        bool has = false;
+#pragma unroll
+        for (int lv = LV - 1; lv >= 0; --lv) {
+          if ((st.count >> lv) & 1u) {
+            acc = has ? add_rn(acc, st.slot[lv]) : st.slot[lv];
+            has = true;
+          }
+        }
+      } else {  // tree(prefix): folded from the top down (right-nested)
+        st.fold_onto(acc, false);
+      }
+      yp[(k0 + e) * es] = (k0 == 0) ? acc : add_rn(carry, acc);
+    }
+    if (policy == CR_BLOCK_DYADIC && k0 + blk < n) {
+      T tk = T(0);
+      st.fold_onto(tk, false);
+      carry = (k0 == 0) ? tk : add_rn(carry, tk);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- planning
 bool scan_args_ok(cr_policy p, int64_t B) {
   switch (p) {
     case CR_LEFT_FOLD:
@@ -14,20 +349,158 @@ bool scan_args_ok(cr_policy p, int64_t B) {
   }
 }
 
-ScanPlan plan_scan(int64_t batch, int64_t n, cr_policy p, int64_t B, size_t) {
+namespace {
+int ilog2(int64_t v) {
+  int l = 0;
+  while ((int64_t(1) << (l + 1)) <= v) ++l;
+  return l;
+}
+size_t round256(size_t v) { return (v + 255) & ~size_t(255); }
+}  // namespace
+
+ScanPlan plan_scan(int64_t batch, int64_t n, cr_policy p, int64_t B, size_t esize) {
   ScanPlan plan;
   plan.batch = batch;
   plan.n = n;
   plan.policy = p;
-  plan.B = B;
-  plan.supported = false;
+  plan.B = (p == CR_BLOCK_DYADIC) ? B : 0;
+  size_t off = kHeaderBytes;
+  plan.supported = true;
+  if (n == 0 || batch == 0) {
+    plan.kind = ScanPlan::kEmpty;
+    plan.ws_bytes = off;
+    return plan;
+  }
+  const bool block = (p == CR_BLOCK_DYADIC);
+  if (batch > 1) {
+    const int64_t depth_n = block ? (B < n ? B : n) : n;
+    plan.kind = ScanPlan::kPerSequence;
+    plan.stack_levels = ilog2(depth_n) + 1;
+    plan.supported = (p == CR_LEFT_FOLD) || n < (int64_t(1) << 31);
+    plan.ws_bytes = off;
+    return plan;
+  }
+  if (p == CR_LEFT_FOLD || (block && B == 1)) {
+    plan.kind = ScanPlan::kChainOnly;  // every element is its own block
+    plan.ws_bytes = off;
+    return plan;
+  }
+  if (p == CR_PAIRWISE) {  // 1-D pairwise: not in this build yet
+    plan.kind = ScanPlan::kEmpty;
+    plan.supported = false;
+    plan.ws_bytes = off;
+    return plan;
+  }
+  plan.kind = ScanPlan::kTiled;
+  const int logB = block ? ilog2(B) : 62;
+  plan.logB = logB;
+  plan.n_tiles = (n + kTile - 1) / kTile;
+  plan.full_tiles = n / kTile;
+  // global pyramid levels: every level inside a block that has a complete node
+  int levels = 0;
+  if (plan.full_tiles >= 1) {
+    levels = ilog2(plan.full_tiles) + 1;
+    if (block) levels = std::min(levels, std::max(0, logB - kLogTile + 1));
+  }
+  plan.pyr_levels = levels;
+  int64_t pyr_elems = 0, cnt_elems = 0;
+  for (int l = 0; l < levels; ++l) {
+    plan.pyr_off[l] = pyr_elems;
+    plan.cnt_off[l] = cnt_elems;
+    pyr_elems += plan.full_tiles >> l;
+    if (l >= 1) cnt_elems += plan.full_tiles >> l;
+  }
+  plan.pyr_ws = off;
+  off += round256((size_t)pyr_elems * esize);
+  plan.cnt_ws = off;
+  plan.cnt_bytes = (size_t)cnt_elems * sizeof(int);
+  off += round256(plan.cnt_bytes);
+  if (block) {
+    plan.K = (n + B - 1) / B;
+    // totals: inside a thread (level 0 flag), inside a tile (pyramid level p),
+    // or spanning tiles (a level of the global pyramid)
+    if (logB <= kLogE) plan.totals_level = 0;
+    else if (logB < kLogTile + 0) plan.totals_level = logB - kLogE;
+    else plan.totals_level = -1;  // read from the global pyramid
+    plan.totals_ws = off;
+    off += round256((size_t)plan.K * esize);
+    plan.carries_ws = off;
+    off += round256((size_t)plan.K * esize);
+  } else {
+    plan.totals_level = -1;
+  }
+  plan.ws_bytes = off;
   return plan;
 }
 
 template <class T>
-cudaError_t run_scan(const ScanPlan&, const T*, T*, int64_t, int64_t, char*, cudaStream_t) {
-  return cudaErrorNotSupported;
+cudaError_t run_scan(const ScanPlan& plan, const T* x, T* out, int64_t es, int64_t bs,
+                     char* ws, cudaStream_t s) {
+  cudaError_t e = cudaSuccess;
+  switch (plan.kind) {
+    case ScanPlan::kEmpty: return cudaSuccess;
+    case ScanPlan::kPerSequence: {
+      if ((plan.batch + 255) / 256 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+      const unsigned grid = (unsigned)((plan.batch + 255) / 256);
+      const int LV = plan.stack_levels;
+#define CR_SEQ(LVV)                                                                  \
+  scan_seq_kernel<T, LVV><<<grid, 256, 0, s>>>(x, out, plan.batch, plan.n, es, bs,   \
+                                               (int)plan.policy, plan.B)
+      if (LV <= 5) CR_SEQ(5);
+      else if (LV <= 9) CR_SEQ(9);
+      else if (LV <= 17) CR_SEQ(17);
+      else CR_SEQ(32);
+#undef CR_SEQ
+      return cudaGetLastError();
+    }
+    case ScanPlan::kChainOnly:
+      carry_chain_kernel<T><<<1, 32, 0, s>>>(x, out, plan.n);
+      return cudaGetLastError();
+    case ScanPlan::kTiled: break;
+  }
+  const bool block = plan.policy == CR_BLOCK_DYADIC;
+  ScanArgs a{};
+  a.n = plan.n;
+  a.full_tiles = plan.full_tiles;
+  a.logB = plan.logB;
+  a.pyr_levels = plan.pyr_levels;
+  a.carry = block ? 1 : 0;
+  a.totals_level = block ? plan.totals_level : -1;
+  for (int l = 0; l < kMaxLevels; ++l) {
+    a.pyr_off[l] = plan.pyr_off[l];
+    a.cnt_off[l] = plan.cnt_off[l];
+  }
+  T* pyr = reinterpret_cast<T*>(ws + plan.pyr_ws);
+  int* counters = reinterpret_cast<int*>(ws + plan.cnt_ws);
+  T* totals = block ? reinterpret_cast<T*>(ws + plan.totals_ws) : nullptr;
+  T* carries = block ? reinterpret_cast<T*>(ws + plan.carries_ws) : nullptr;
+  if (plan.cnt_bytes > 0) {
+    if ((e = cudaMemsetAsync(counters, 0, plan.cnt_bytes, s)) != cudaSuccess) return e;
+  }
+  if (plan.n_tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const int S = block ? (int)(plan.B < kE ? plan.B : kE) : kE;
+  const unsigned grid = (unsigned)plan.n_tiles;
+  const bool up_needed = plan.pyr_levels > 0 || (block && plan.totals_level >= 0);
+  if (up_needed) {
+    if (S == 8) scan_up_kernel<T, 8><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
+    else if (S == 4) scan_up_kernel<T, 4><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
+    else scan_up_kernel<T, 2><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (block && plan.K >= 2) {
+    // blocks 1..K-1 need C_0..C_{K-2}; those blocks are all complete
+    const T* src = (plan.totals_level >= 0)
+                       ? totals
+                       : pyr + plan.pyr_off[plan.logB - kLogTile];
+    carry_chain_kernel<T><<<1, 32, 0, s>>>(src, carries, plan.K - 1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (S == 8) scan_down_kernel<T, 8><<<grid, kScanThreads, 0, s>>>(x, out, pyr, carries, a);
+  else if (S == 4) scan_down_kernel<T, 4><<<grid, kScanThreads, 0, s>>>(x, out, pyr, carries, a);
+  else scan_down_kernel<T, 2><<<grid, kScanThreads, 0, s>>>(x, out, pyr, carries, a);
+  return cudaGetLastError();
 }
+
 template cudaError_t run_scan<double>(const ScanPlan&, const double*, double*, int64_t,
                                       int64_t, char*, cudaStream_t);
 template cudaError_t run_scan<float>(const ScanPlan&, const float*, float*, int64_t, int64_t,

@@ -11,11 +11,37 @@
 
 namespace cr {
 
+constexpr int kMaxLevels = 40;  // global pyramid levels (tiles up to 2^39)
+
+// Kernel arguments of the tiled 1-D scan passes (passed by value).
+struct ScanArgs {
+  int64_t n;
+  int64_t full_tiles;        // tiles of 2048 elements that are complete
+  int32_t logB;              // log2 of the block size; 62 = one block
+  int32_t pyr_levels;        // global pyramid levels kept (level 0: tile aggregates)
+  int32_t carry;             // block_dyadic: apply C_{k-1}
+  int32_t totals_level;      // block totals: 0 in-thread, p > 0 tile pyramid level, -1 global
+  int64_t pyr_off[kMaxLevels];  // element offset of each pyramid level
+  int64_t cnt_off[kMaxLevels];  // offset of each level's arrival counters
+};
+
 struct ScanPlan {
+  enum Kind { kEmpty, kPerSequence, kChainOnly, kTiled };
   bool supported = false;
+  Kind kind = kEmpty;
   int64_t batch = 0, n = 0;
   cr_policy policy = CR_LEFT_FOLD;
-  int64_t B = 1;
+  int64_t B = 0;
+  int stack_levels = 0;      // per-sequence kernel
+  int logB = 62;
+  int64_t n_tiles = 0, full_tiles = 0;
+  int pyr_levels = 0;
+  int64_t pyr_off[kMaxLevels] = {};
+  int64_t cnt_off[kMaxLevels] = {};
+  size_t pyr_ws = 0, cnt_ws = 0, cnt_bytes = 0;
+  int64_t K = 0;             // blocks (block_dyadic)
+  int totals_level = -1;
+  size_t totals_ws = 0, carries_ws = 0;
   size_t ws_bytes = kHeaderBytes;
 };
 

@@ -1,0 +1,138 @@
+"""GPU parity of the canonical scans against the oracle, 0 ULP (raw bits).
+
+1-D scans over sizes that cover one and several 2048-element tiles, ragged
+last tiles and threads, blocks inside a thread, inside a tile and spanning
+tiles, the full-size benchmark shapes; in-place scans; batched column and row
+scans; scan/reduce consistency including GPU scan vs GPU reduce."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def scr():
+    import scan_canonical_reduce_gb300 as m
+    return m
+
+
+def bits(a):
+    return np.asarray(a).tobytes()
+
+
+def first_diff(a, b):
+    a = np.asarray(a).view(np.uint8 if a.dtype.itemsize == 1 else
+                           (np.uint64 if a.dtype.itemsize == 8 else np.uint32))
+    b = np.asarray(b).view(a.dtype)
+    idx = np.nonzero(a != b)[0]
+    return (int(idx[0]), len(idx)) if len(idx) else None
+
+
+def check_scan(scr, x, policy, B):
+    got = scr.inclusive_scan(torch.from_numpy(x).to(DEV), policy, B).cpu().numpy()
+    want = oracle.scan(x, policy, B)
+    assert bits(got) == bits(want), (x.size, policy, B, first_diff(got, want))
+
+
+SIZES = [1, 2, 3, 7, 8, 9, 15, 16, 17, 100, 255, 256, 257, 2047, 2048, 2049, 4095, 4096,
+         4097, 2048 * 3 + 5, 2048 * 7, 100003, (1 << 20) + 37]
+
+
+@pytest.mark.parametrize("dtype", [np.float64, np.float32])
+@pytest.mark.parametrize("policy,B", [("iterated_pairwise", 1), ("left_fold", 1),
+                                      ("block_dyadic", 1), ("block_dyadic", 2),
+                                      ("block_dyadic", 4), ("block_dyadic", 8),
+                                      ("block_dyadic", 16), ("block_dyadic", 32),
+                                      ("block_dyadic", 256), ("block_dyadic", 2048),
+                                      ("block_dyadic", 4096), ("block_dyadic", 1 << 16)])
+def test_scan_sizes(scr, dtype, policy, B):
+    for n in SIZES:
+        if policy == "left_fold" and n > 200000:
+            continue
+        x = W.signed_pow2(n, W.seed_for(3, n % 101), dtype, -20, 20)
+        check_scan(scr, x, policy, B)
+
+
+def test_scan_empty(scr):
+    x = torch.empty(0, dtype=torch.float64, device=DEV)
+    for policy, B in (("iterated_pairwise", 1), ("block_dyadic", 16), ("left_fold", 1)):
+        assert scr.inclusive_scan(x, policy, B).numel() == 0
+
+
+@pytest.mark.parametrize("policy,B", [("iterated_pairwise", 1), ("block_dyadic", 16),
+                                      ("block_dyadic", 4096), ("left_fold", 1)])
+def test_scan_in_place(scr, policy, B):
+    x = W.family3(2048 * 5 + 77)
+    t = torch.from_numpy(x).to(DEV)
+    scr.inclusive_scan(t, policy, B, out=t)
+    assert bits(t.cpu().numpy()) == bits(oracle.scan(x, policy, B))
+
+
+def test_scan_rejects_bad_block_and_overlap(scr):
+    t = torch.zeros(100, dtype=torch.float64, device=DEV)
+    with pytest.raises(ValueError):
+        scr.inclusive_scan(t, "block_dyadic", 6)
+    with pytest.raises(scr.CrError):
+        scr.inclusive_scan(t[:90], "iterated_pairwise", 1, out=t[5:95])
+
+
+@pytest.mark.parametrize("dtype", [np.float64, np.float32])
+@pytest.mark.parametrize("policy,B", [("left_fold", 1), ("block_dyadic", 16),
+                                      ("block_dyadic", 4), ("block_dyadic", 256),
+                                      ("iterated_pairwise", 1), ("pairwise", 1)])
+def test_scan_batched_columns_and_rows(scr, dtype, policy, B):
+    levels, cols = 90, 1001
+    buf = W.signed_pow2(levels * cols, W.seed_for(5, 3), dtype)
+    t = torch.from_numpy(buf).to(DEV).view(levels, cols)
+    got = scr.inclusive_scan_batched(t, policy, B, dim=0).cpu().numpy().reshape(-1)
+    want = oracle.scan_batched(buf, cols, levels, cols, 1, policy, B)
+    assert bits(got) == bits(want)
+    # rows of a (cols x levels) array: elem_stride 1, batch_stride levels
+    t2 = torch.from_numpy(buf).to(DEV).view(cols, levels)
+    got2 = scr.inclusive_scan_batched(t2, policy, B, dim=1).cpu().numpy().reshape(-1)
+    want2 = oracle.scan_batched(buf, cols, levels, 1, levels, policy, B)
+    assert bits(got2) == bits(want2)
+
+
+@pytest.mark.parametrize("policy,B", [("block_dyadic", 16), ("left_fold", 1)])
+def test_column_scan_full_size(scr, policy, B):
+    """The weather-column shape: 90 levels x 200,000 columns, level-major,
+    lognormal values; every column checked."""
+    levels, cols = 90, 200000
+    buf = W.family5(levels, cols)
+    t = torch.from_numpy(buf).to(DEV).view(levels, cols)
+    got = scr.inclusive_scan_batched(t, policy, B, dim=0).cpu().numpy().reshape(-1)
+    want = oracle.scan_batched(buf, cols, levels, cols, 1, policy, B)
+    assert bits(got) == bits(want), first_diff(got, want)
+
+
+@pytest.mark.parametrize("policy,B", [("iterated_pairwise", 1), ("block_dyadic", 16),
+                                      ("block_dyadic", 256)])
+def test_scan_full_size(scr, policy, B):
+    """n = 2^24 and 2^28 (the benchmark sizes), U[-1, 1) values: every element
+    compared with the oracle, and the scan's back element equals reduce<E>."""
+    for n in (1 << 24, 1 << 28):
+        x = W.family3(n)
+        got = scr.inclusive_scan(torch.from_numpy(x).to(DEV), policy, B).cpu().numpy()
+        want = oracle.scan(x, policy, B)
+        assert bits(got) == bits(want), (n, first_diff(got, want))
+        r = oracle.reduce_policy(x, policy, B)
+        assert bits(got[-1]) == bits(r)
+
+
+def test_scan_reduce_consistency_on_gpu(scr):
+    """iterated_pairwise is the P4016 tree with L = 1 applied to every prefix,
+    and -0.0 is the exact identity of init: the GPU scan's element i equals the
+    GPU reduce of x[0..i] with L = 1 and init = -0.0 (two different kernels)."""
+    x = W.family3((1 << 20) + 13)
+    xd = torch.from_numpy(x).to(DEV)
+    y = scr.inclusive_scan(xd, "iterated_pairwise").cpu().numpy()
+    rng = np.random.default_rng(3)
+    for i in list(rng.choice(x.size, 40, replace=False)) + [0, x.size - 1]:
+        r = scr.reduce(xd[: i + 1], 1, -0.0).cpu().numpy()[0]
+        assert bits(y[i]) == bits(r), i
