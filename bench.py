@@ -1,0 +1,518 @@
+#!/usr/bin/env python
+"""Benchmark of the canonical reduce / scan hot path on GB300.
+
+One step = one pass over every row of the hot path, each on its own seeded
+synthetic input (inputs larger than L2, resident in HBM before the timed
+region):
+  reduce_f64_L{16,128,1024}  canonical reduce, fp64, n = 2^28, family-2 values
+  scan_iterated_pairwise     inclusive scan, fp64, n = 2^28, U[-1, 1)
+  scan_block_dyadic_{16,256} inclusive scan, fp64, n = 2^28, U[-1, 1)
+  reduce_rows_f32_L128       batched row reduce, fp32, 65,536 x 4,096
+  colscan_{block_dyadic16,left_fold}  batched column scan, fp64, 90 x 200,000
+value = algorithmic bytes of all rows / device time of the step (GB/s);
+e2e   = the same through the public API with pinned host buffers, the
+        host->device copy of the inputs and the device->host copy of every
+        result inside the timed region.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+With N > 1 (torchrun) every rank runs the same step on its own GPU
+(replicas: the rows are independent problems, no exchange); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "canonical reduce/scan GB/s (fp64, N=2^28) & % of HBM roofline; 0-ULP vs oracle"
+N = 1 << 28
+COLS_LEVELS, COLS_N = 90, 200000
+ROWS_R, ROWS_C = 65536, 4096
+
+
+# ------------------------------------------------------- algorithmic counts
+def popcount_sum(n: int) -> int:
+    """sum of popcount(j) for j = 1..n."""
+    total, bit = 0, 0
+    while (1 << bit) <= n:
+        period = 1 << (bit + 1)
+        full = (n + 1) // period
+        total += full * (1 << bit) + max(0, (n + 1) % period - (1 << bit))
+        bit += 1
+    return total
+
+
+def adds_iterated(n: int) -> int:
+    """Adds of an iterated_pairwise scan: every complete aligned node
+    (n - popcount(n)) plus popcount(i+1) - 1 right-nested combinations."""
+    return (n - bin(n).count("1")) + (popcount_sum(n) - n)
+
+
+def adds_block_dyadic(n: int, B: int) -> int:
+    full, rem = divmod(n, B)
+    a = full * adds_iterated(B) + (adds_iterated(rem) if rem else 0)
+    return a + max(0, n - B) + max(0, -(-n // B) - 2)  # carries applied + chain
+
+
+def rows_spec():
+    """(name, kind, params, algorithmic bytes, algorithmic adds, dtype)."""
+    rs = []
+    for L in (16, 128, 1024):
+        rs.append(("reduce_f64_L%d" % L, "reduce", {"L": L}, 8 * N, N, "f64"))
+    rs.append(("scan_iterated_pairwise", "scan", {"policy": "iterated_pairwise", "B": 1},
+               16 * N, adds_iterated(N), "f64"))
+    for B in (16, 256):
+        rs.append(("scan_block_dyadic_%d" % B, "scan", {"policy": "block_dyadic", "B": B},
+                   16 * N, adds_block_dyadic(N, B), "f64"))
+    rs.append(("reduce_rows_f32_L128", "rows", {"L": 128},
+               4 * ROWS_R * ROWS_C + 4 * ROWS_R, ROWS_R * ROWS_C, "f32"))
+    for pol, B in (("block_dyadic", 16), ("left_fold", 1)):
+        name = "colscan_%s%s" % (pol, B if pol == "block_dyadic" else "")
+        adds = COLS_N * (adds_block_dyadic(COLS_LEVELS, B) if pol == "block_dyadic"
+                         else COLS_LEVELS - 1)
+        rs.append((name, "cols", {"policy": pol, "B": B}, 16 * COLS_LEVELS * COLS_N, adds,
+                   "f64"))
+    return rs
+
+
+# ----------------------------------------------------------------- inputs
+def host_inputs():
+    return {
+        "f2": W.family2(N),                      # reduce
+        "f3": W.family3(N),                      # 1-D scans
+        "f4": W.family4(ROWS_R, ROWS_C),         # row reduce
+        "f5": W.family5(COLS_LEVELS, COLS_N),    # column scans
+    }
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_uuid: str | None):
+        self.uuid = gpu_uuid
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------- GPU arm
+def run_native(args):
+    import torch
+
+    import scan_canonical_reduce_gb300 as scr
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.gpus != world:
+        raise SystemExit("--gpus %d but WORLD_SIZE=%d" % (args.gpus, world))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    rows = rows_spec()
+    hin = host_inputs()
+    # device-resident inputs and outputs
+    x2 = torch.from_numpy(hin["f2"]).to(dev)
+    x3 = torch.from_numpy(hin["f3"]).to(dev)
+    x4 = torch.from_numpy(hin["f4"]).to(dev)
+    x5 = torch.from_numpy(hin["f5"]).to(dev).view(COLS_LEVELS, COLS_N)
+    y_scan = torch.empty_like(x3)
+    y_cols = torch.empty_like(x5)
+    r_out = torch.empty(1, dtype=torch.float64, device=dev)
+    rows_out = torch.empty(ROWS_R, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def run_row(row):
+        name, kind, p = row[0], row[1], row[2]
+        if kind == "reduce":
+            scr.reduce(x2, p["L"], 0.0, out=r_out)
+        elif kind == "scan":
+            scr.inclusive_scan(x3, p["policy"], p["B"], out=y_scan)
+        elif kind == "rows":
+            scr.reduce_batched(x4, p["L"], 0.0, dim=-1, out=rows_out)
+        elif kind == "cols":
+            scr.inclusive_scan_batched(x5, p["policy"], p["B"], dim=0, out=y_cols)
+
+    def step():
+        for row in rows:
+            run_row(row)
+
+    # ALU roofline denominators, measured on this GPU by libcr's calibration
+    dadd_rate, dadd_lat = scr.measure_add_peak(torch.float64, dev)
+    fadd_rate, _ = scr.measure_add_peak(torch.float32, dev)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    # ---- timed region: K steps; per-row and per-launch events on the stream
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = None
+    sampler = ClockSampler(uuid)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    launches0 = scr.launch_count()
+    scr.profile_enable(True)
+    ev = {r[0]: [] for r in rows}
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        for row in rows:
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            run_row(row)
+            b.record(stream)
+            ev[row[0]].append((a, b))
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    scr.profile_enable(False)
+    launches = scr.launch_count() - launches0
+    prof = scr.profile_collect()
+    clocks = sampler.stop()
+    ms_total = t0.elapsed_time(t1)
+    if dist:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+        dist.barrier()
+
+    step_bytes = sum(r[3] for r in rows)
+    ms_per_step = ms_total / args.steps
+    value = step_bytes * args.steps * world / (ms_total * 1e-3) / 1e9
+    peaks = measured_peaks()
+    hbm_peak = peaks.get("hbm_gbs")
+
+    row_stats = {}
+    for r in rows:
+        ms = statistics.median([a.elapsed_time(b) for a, b in ev[r[0]]])
+        gbs = r[3] / (ms * 1e-3) / 1e9
+        add_rate = r[4] / (ms * 1e-3)
+        peak_add = dadd_rate if r[5] == "f64" else fadd_rate
+        row_stats[r[0]] = {"ms": round(ms, 4), "gb_s": round(gbs, 1),
+                           "hbm_frac": round(gbs / hbm_peak, 4) if hbm_peak else None,
+                           "adds_per_s": add_rate, "alu_frac": round(add_rate / peak_add, 4),
+                           "bytes": r[3], "adds": r[4], "dtype": r[5]}
+
+    # per-kernel launch list from libcr's event pairs
+    kern = {}
+    for name, ms in prof:
+        k = kern.setdefault(name, [0, 0.0])
+        k[0] += 1
+        k[1] += ms
+    tot_k = sum(v[1] for v in kern.values()) or 1.0
+    kernels = {k: {"launches": v[0], "ms_total": round(v[1], 3), "share": round(v[1] / tot_k, 4)}
+               for k, v in sorted(kern.items(), key=lambda kv: -kv[1][1])}
+    roofline = dominant_roofline(kernels, prof, row_stats, dadd_rate, dadd_lat, hbm_peak,
+                                 args.steps)
+
+    # ---- e2e through the public API with pinned host buffers
+    e2e = run_e2e(args, scr, torch, dev, hin, rows, world, dist)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(seconds=args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded SplitMix64 families; no dataset)",
+            "config": {"workload": "all hot-path rows at n = 2^28 fp64 "
+                                   "(reduce L=16/128/1024, iterated_pairwise and "
+                                   "block_dyadic<16>/<256> scans) + 65536x4096 fp32 "
+                                   "row reduce + 90x200000 fp64 column scans",
+                       "n": N, "l2": "every input larger than L2 (>=144 MB); no flush",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "rows": row_stats, "kernels": kernels, "roofline": roofline,
+            "peaks": {"hbm_gbs": hbm_peak, "dadd_per_s": dadd_rate, "dadd_latency_ns": dadd_lat,
+                      "fadd_per_s": fadd_rate},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+        }
+        print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except OSError:
+        return {"hbm_gbs": 6800.0, "note": "fallback"}
+
+
+def dominant_roofline(kernels, prof, row_stats, dadd_rate, dadd_lat, hbm_peak, steps):
+    """Roofline of the kernel with the largest share of device time."""
+    if not kernels:
+        return None
+    top = next(iter(kernels))
+    launches = kernels[top]["launches"]
+    avg_ms = kernels[top]["ms_total"] / max(1, launches)
+    if top == "carry_chain_kernel":
+        # the serial chain of block_dyadic<16>: bound by dependent-add latency
+        K = N // 16 - 1
+        chains = [ms for nm, ms in prof if nm == top]
+        ms = max(chains) if chains else avg_ms
+        achieved = K / (ms * 1e-3)
+        peak = 1e9 / dadd_lat
+        return {"kernel": top, "bound": "alu", "achieved": achieved, "peak": peak,
+                "unit": "dependent adds/s", "frac": round(achieved / peak, 4),
+                "traffic": None, "note": "serial carry chain of block_dyadic<16>, "
+                                         "K = 2^24 - 1 dependent fp64 adds; peak = 1 / "
+                                         "measured dependent-add latency"}
+    if top == "scan_down_kernel":
+        r = row_stats["scan_iterated_pairwise"]
+        achieved = r["adds"] / (r["ms"] * 1e-3)
+        return {"kernel": top, "bound": "alu", "achieved": achieved, "peak": dadd_rate,
+                "unit": "fp64 adds/s", "frac": round(achieved / dadd_rate, 4), "traffic": None}
+    if top == "lane_pass_kernel":
+        r = row_stats["reduce_f64_L16"]
+        achieved = r["bytes"] / (r["ms"] * 1e-3) / 1e9
+        return {"kernel": top, "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
+                "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": None}
+    return {"kernel": top, "bound": "alu", "achieved": None, "peak": dadd_rate,
+            "unit": "fp64 adds/s", "frac": None, "traffic": None}
+
+
+def run_e2e(args, scr, torch, dev, hin, rows, world, dist):
+    """Same rows through the public API on pinned host tensors: each call
+    copies its input in and its result out, inside the timed region."""
+    h2 = torch.from_numpy(hin["f2"]).pin_memory()
+    h3 = torch.from_numpy(hin["f3"]).pin_memory()
+    h4 = torch.from_numpy(hin["f4"]).pin_memory()
+    h5 = torch.from_numpy(hin["f5"]).view(COLS_LEVELS, COLS_N).pin_memory()
+    h2d = d2h = 0
+    for r in rows:
+        kind = r[1]
+        if kind == "reduce":
+            h2d += h2.numel() * 8
+            d2h += 8
+        elif kind == "scan":
+            h2d += h3.numel() * 8
+            d2h += h3.numel() * 8
+        elif kind == "rows":
+            h2d += h4.numel() * 4
+            d2h += ROWS_R * 4
+        else:
+            h2d += h5.numel() * 8
+            d2h += h5.numel() * 8
+
+    def step():
+        for r in rows:
+            kind, p = r[1], r[2]
+            if kind == "reduce":
+                scr.reduce(h2, p["L"], 0.0)
+            elif kind == "scan":
+                scr.inclusive_scan(h3, p["policy"], p["B"])
+            elif kind == "rows":
+                scr.reduce_batched(h4, p["L"], 0.0, dim=-1)
+            else:
+                scr.inclusive_scan_batched(h5, p["policy"], p["B"], dim=0)
+
+    step()
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    t = time.perf_counter()
+    steps = max(1, min(args.steps, 3))
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize(dev)
+    sec = time.perf_counter() - t
+    if dist:
+        tt = torch.tensor([sec], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        sec = float(tt.item())
+    step_bytes = sum(r[3] for r in rows)
+    return {"value": round(step_bytes * steps * world / sec / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+# ------------------------------------------------------- oracle (CPU) leg
+def cpu_sample_rows(scale: int):
+    """Bounded sample of every row for the oracle: same families, n / scale."""
+    n = N // scale
+    rs = []
+    for L in (16, 128, 1024):
+        rs.append(("reduce_f64_L%d" % L, "reduce", {"L": L}, 8 * n))
+    rs.append(("scan_iterated_pairwise", "scan", {"policy": "iterated_pairwise", "B": 1}, 16 * n))
+    for B in (16, 256):
+        rs.append(("scan_block_dyadic_%d" % B, "scan", {"policy": "block_dyadic", "B": B}, 16 * n))
+    rr = max(1, ROWS_R // scale)
+    rs.append(("reduce_rows_f32_L128", "rows", {"L": 128, "rows": rr}, 4 * rr * ROWS_C))
+    cc = max(1, COLS_N // scale)
+    for pol, B in (("block_dyadic", 16), ("left_fold", 1)):
+        rs.append(("colscan", "cols", {"policy": pol, "B": B, "cols": cc},
+                   16 * COLS_LEVELS * cc))
+    return n, rs
+
+
+def oracle_step(scale: int, cache={}):
+    import oracle
+    n, rs = cpu_sample_rows(scale)
+    if scale not in cache:
+        cache.clear()
+        cache[scale] = {
+            "f2": W.family2(n), "f3": W.family3(n),
+            "f4": W.family4(ROWS_R, ROWS_C)[: max(1, ROWS_R // scale)].copy(),
+            "f5": W.family5(COLS_LEVELS, COLS_N).reshape(COLS_LEVELS, COLS_N)
+                 [:, : max(1, COLS_N // scale)].copy().reshape(-1),
+        }
+    c = cache[scale]
+    t = time.perf_counter()
+    for name, kind, p, _ in rs:
+        if kind == "reduce":
+            oracle.reduce(c["f2"], p["L"], 0.0)
+        elif kind == "scan":
+            oracle.scan(c["f3"], p["policy"], p["B"])
+        elif kind == "rows":
+            oracle.reduce_batched(c["f4"].reshape(-1), p["rows"], ROWS_C, 1, ROWS_C, p["L"],
+                                  np.float32(0.0))
+        else:
+            oracle.scan_batched(c["f5"], p["cols"], COLS_LEVELS, p["cols"], 1, p["policy"], p["B"])
+    sec = time.perf_counter() - t
+    return sum(r[3] for r in rs), sec, n
+
+
+def cpu_baseline(seconds: float = 15.0):
+    """The oracle as it stands, single-threaded on this host, on a bounded
+    sample of the same workload (every row at 1/scale of its size)."""
+    scale = 64
+    b, s, n = oracle_step(scale)
+    # grow or shrink the sample toward the time budget
+    if s < seconds / 4 and scale > 8:
+        scale = max(8, int(scale * s / (seconds / 2)))
+        scale = 1 << max(3, int(np.log2(max(1, scale))))
+        b, s, n = oracle_step(scale)
+    return {"value": round(b / s / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "host_cores_visible": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "seconds": round(s, 2),
+            "sample": "every row at 1/%d of its size (1-D n = %d; row reduce %d rows; "
+                      "column scans %d columns), same value families" %
+                      (scale, n, max(1, ROWS_R // scale), max(1, COLS_N // scale))}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    scale = args.ref_scale
+    oracle_step(scale)  # build + inputs, untimed
+    for _ in range(args.warmup):
+        oracle_step(scale)
+    tot_b = tot_s = 0.0
+    for _ in range(args.steps):
+        b, s, n = oracle_step(scale)
+        tot_b += b
+        tot_s += s
+    value = tot_b / tot_s / 1e9
+    line = {
+        "metric": METRIC, "impl": "reference", "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tot_s / args.steps * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "all hot-path rows, each at 1/%d of the GPU arm's size "
+                               "(the oracle is single-threaded)" % scale, "n": n},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "every row at 1/%d of its size" % scale},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-scale", type=int, default=32)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "native":
+        raise SystemExit("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -154,6 +154,39 @@ const char* cr_status_string(cr_status s);
 /* Library version as major*10000 + minor*100 + patch. */
 int cr_version(void);
 
+/* ----------------------------------------------------------- diagnostics
+ * Not part of the pages' operations: launch accounting used by the
+ * benchmark and by profiling tools. */
+
+/* Number of kernels libcr has enqueued since it was loaded. */
+uint64_t cr_launch_count(void);
+
+/* on != 0: every later launch is bracketed by two CUDA events recorded on its
+ * stream (a small per-launch cost); on == 0: stop recording. */
+void cr_profile_enable(int on);
+
+/* Waits for the recorded events, writes up to max_records (kernel id, device
+ * milliseconds) pairs in launch order, forgets them and returns how many
+ * launches were recorded (possibly more than max_records). */
+int cr_profile_collect(int* kernel_ids, float* ms, int max_records);
+
+/* Static name of a kernel id returned by cr_profile_collect(). */
+const char* cr_kernel_name(int id);
+
+/* Device scratch bytes cr_measure_add_peak() needs on the current device
+ * (0 if no device is usable). */
+size_t cr_measure_add_peak_scratch_bytes(void);
+
+/* Measures, on the current device and `stream`, the throughput of
+ * independent round-to-nearest adds of dt (adds per second over all SMs) and
+ * the latency of one dependent chain of them (ns per add): the ALU roofline
+ * denominators of add-bound kernels. Synchronises the stream. scratch_dev:
+ * caller-owned device memory of at least the bytes above. Either output
+ * pointer may be NULL. */
+cr_status cr_measure_add_peak(cr_dtype dt, void* scratch_dev, size_t scratch_bytes,
+                              void* stream, double* adds_per_second,
+                              double* dependent_latency_ns);
+
 #ifdef __cplusplus
 }
 #endif

@@ -49,6 +49,13 @@ SIGNATURES = {
     "cr_sync_status": (_INT, [_P, _P]),
     "cr_status_string": (ctypes.c_char_p, [_INT]),
     "cr_version": (_INT, []),
+    "cr_launch_count": (ctypes.c_uint64, []),
+    "cr_profile_enable": (None, [_INT]),
+    "cr_profile_collect": (_INT, [_P, _P, _INT]),
+    "cr_kernel_name": (ctypes.c_char_p, [_INT]),
+    "cr_measure_add_peak_scratch_bytes": (_SZ, []),
+    "cr_measure_add_peak": (_INT, [_INT, _P, _SZ, _P, ctypes.POINTER(ctypes.c_double),
+                                   ctypes.POINTER(ctypes.c_double)]),
 }
 
 
@@ -254,5 +261,39 @@ def sync_status(device=None, stream=None) -> None:
     _check(lib().cr_sync_status(ws.data_ptr(), sp), "cr_sync_status")
 
 
+def launch_count() -> int:
+    """Kernels libcr has enqueued since it was loaded."""
+    return int(lib().cr_launch_count())
+
+
+def profile_enable(on: bool = True) -> None:
+    """Bracket every later libcr launch with CUDA events on its stream."""
+    lib().cr_profile_enable(1 if on else 0)
+
+
+def profile_collect():
+    """[(kernel name, device ms)] of the launches recorded since the last call."""
+    cap = 1 << 16
+    ids = (ctypes.c_int * cap)()
+    ms = (ctypes.c_float * cap)()
+    n = lib().cr_profile_collect(ids, ms, cap)
+    return [(lib().cr_kernel_name(ids[i]).decode(), float(ms[i])) for i in range(min(n, cap))]
+
+
+def measure_add_peak(dtype=torch.float64, device="cuda", stream=None):
+    """(adds per second over the GPU, dependent-add latency in ns) of
+    round-to-nearest adds of ``dtype``, measured by libcr's calibration
+    kernels on ``device``."""
+    dt = CR_F64 if dtype == torch.float64 else CR_F32
+    with torch.cuda.device(torch.device(device)):
+        nb = lib().cr_measure_add_peak_scratch_bytes()
+        scratch = torch.empty(max(int(nb), 256), dtype=torch.uint8, device=device)
+        rate, lat = ctypes.c_double(0), ctypes.c_double(0)
+        _check(lib().cr_measure_add_peak(dt, scratch.data_ptr(), scratch.numel(),
+                                         _stream_ptr(stream), ctypes.byref(rate),
+                                         ctypes.byref(lat)), "cr_measure_add_peak")
+    return rate.value, lat.value
+
+
 __all__ = ["reduce", "reduce_batched", "inclusive_scan", "inclusive_scan_batched",
-           "sync_status", "lib", "workspace", "CrError", "POLICIES", "SIGNATURES"]
+           "sync_status", "lib", "workspace", "launch_count", "profile_enable", "profile_collect", "measure_add_peak", "CrError", "POLICIES", "SIGNATURES"]

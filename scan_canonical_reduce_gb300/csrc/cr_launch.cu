@@ -1,0 +1,89 @@
+// Launch counting and event-based per-launch timing (see cr_launch.h).
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include "cr.h"
+#include "cr_launch.h"
+
+namespace cr {
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+std::atomic<int> g_profiling{0};
+
+struct Record {
+  int id;
+  cudaEvent_t start, stop;
+};
+
+std::mutex g_mu;
+std::vector<Record> g_records;      // launches recorded since the last collect
+std::vector<cudaEvent_t> g_free;    // reusable events
+
+cudaEvent_t take_event() {
+  if (!g_free.empty()) {
+    cudaEvent_t e = g_free.back();
+    g_free.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+}  // namespace
+
+const char* kernel_name(int id) {
+  static const char* names[kKernelCount] = {"lane_pass_kernel",   "write_init_kernel",
+                                            "scan_up_kernel",     "scan_down_kernel",
+                                            "carry_chain_kernel", "scan_seq_kernel"};
+  return (id >= 0 && id < kKernelCount) ? names[id] : "unknown";
+}
+
+LaunchScope::LaunchScope(int id_, cudaStream_t s) : id(id_), stream(s), slot(-1) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (!g_profiling.load(std::memory_order_relaxed)) return;
+  std::lock_guard<std::mutex> lk(g_mu);
+  Record r{id_, take_event(), take_event()};
+  if (!r.start || !r.stop) return;
+  cudaEventRecord(r.start, s);
+  g_records.push_back(r);
+  slot = (int)g_records.size() - 1;
+}
+
+LaunchScope::~LaunchScope() {
+  if (slot < 0) return;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (slot < (int)g_records.size()) cudaEventRecord(g_records[slot].stop, stream);
+}
+
+}  // namespace cr
+
+extern "C" {
+
+uint64_t cr_launch_count(void) { return cr::g_launches.load(); }
+
+void cr_profile_enable(int on) { cr::g_profiling.store(on ? 1 : 0); }
+
+int cr_profile_collect(int* kernel_ids, float* ms, int max_records) {
+  std::lock_guard<std::mutex> lk(cr::g_mu);
+  int n = 0;
+  for (const cr::Record& r : cr::g_records) {
+    float t = -1.0f;
+    if (cudaEventSynchronize(r.stop) == cudaSuccess) cudaEventElapsedTime(&t, r.start, r.stop);
+    if (n < max_records) {
+      if (kernel_ids) kernel_ids[n] = r.id;
+      if (ms) ms[n] = t;
+    }
+    ++n;
+    cr::g_free.push_back(r.start);
+    cr::g_free.push_back(r.stop);
+  }
+  cr::g_records.clear();
+  return n;
+}
+
+const char* cr_kernel_name(int id) { return cr::kernel_name(id); }
+
+}  // extern "C"

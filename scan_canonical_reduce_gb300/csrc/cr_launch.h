@@ -1,0 +1,40 @@
+// Launch bookkeeping of libcr: every kernel launch goes through launch(),
+// which counts it and, while profiling is on, brackets it with a pair of CUDA
+// events recorded on the launching stream. Reading the events back gives the
+// device duration of each launch without an external profiler.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace cr {
+
+enum KernelId : int {
+  kKLanePass = 0,
+  kKWriteInit,
+  kKScanUp,
+  kKScanDown,
+  kKCarryChain,
+  kKScanSeq,
+  kKernelCount
+};
+
+const char* kernel_name(int id);
+
+struct LaunchScope {
+  LaunchScope(int id, cudaStream_t s);
+  ~LaunchScope();
+  int id;
+  cudaStream_t stream;
+  int slot;
+};
+
+// Usage: CR_LAUNCH(kKScanUp, stream, kernel<<<grid, block, 0, stream>>>(...));
+#define CR_LAUNCH(ID, STREAM, ...)                  \
+  do {                                              \
+    ::cr::LaunchScope cr_launch_scope_((ID), (STREAM)); \
+    __VA_ARGS__;                                    \
+  } while (0)
+
+}  // namespace cr

@@ -32,6 +32,7 @@
 #include <vector>
 
 #include "cr_device.cuh"
+#include "cr_launch.h"
 #include "cr_plan.h"
 
 namespace cr {
@@ -298,8 +299,9 @@ cudaError_t run_reduce(const ReducePlan& plan, const T* x, T* out, T init, char*
                        cudaStream_t s) {
   if (plan.passes.empty()) {
     if (plan.batch > 0)
-      write_init_kernel<T><<<(unsigned)((plan.batch + 255) / 256), 256, 0, s>>>(
-          out, plan.batch, init);
+      CR_LAUNCH(kKWriteInit, s,
+                write_init_kernel<T><<<(unsigned)((plan.batch + 255) / 256), 256, 0, s>>>(
+                    out, plan.batch, init));
     return cudaGetLastError();
   }
   for (const PassPlan& pp : plan.passes) {
@@ -310,11 +312,15 @@ cudaError_t run_reduce(const ReducePlan& plan, const T* x, T* out, T init, char*
     if (pp.grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     // runs shorter than 16 rows use smaller register blocks
     if (pp.a.P >= 16)
-      lane_pass_kernel<T, 16><<<(unsigned)pp.grid, kThreads, 0, s>>>(
-          in_base, pp.in.seg, pp.in.row, pp.in.lane, next, acc, has, out, init, pp.a);
+      CR_LAUNCH(kKLanePass, s,
+                lane_pass_kernel<T, 16><<<(unsigned)pp.grid, kThreads, 0, s>>>(
+                    in_base, pp.in.seg, pp.in.row, pp.in.lane, next, acc, has, out, init,
+                    pp.a));
     else
-      lane_pass_kernel<T, 4><<<(unsigned)pp.grid, kThreads, 0, s>>>(
-          in_base, pp.in.seg, pp.in.row, pp.in.lane, next, acc, has, out, init, pp.a);
+      CR_LAUNCH(kKLanePass, s,
+                lane_pass_kernel<T, 4><<<(unsigned)pp.grid, kThreads, 0, s>>>(
+                    in_base, pp.in.seg, pp.in.row, pp.in.lane, next, acc, has, out, init,
+                    pp.a));
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

@@ -30,6 +30,7 @@
 #include <vector>
 
 #include "cr_device.cuh"
+#include "cr_launch.h"
 #include "cr_scan.h"
 
 namespace cr {
@@ -444,8 +445,9 @@ cudaError_t run_scan(const ScanPlan& plan, const T* x, T* out, int64_t es, int64
       const unsigned grid = (unsigned)((plan.batch + 255) / 256);
       const int LV = plan.stack_levels;
 #define CR_SEQ(LVV)                                                                  \
-  scan_seq_kernel<T, LVV><<<grid, 256, 0, s>>>(x, out, plan.batch, plan.n, es, bs,   \
-                                               (int)plan.policy, plan.B)
+  CR_LAUNCH(kKScanSeq, s,                                                            \
+            scan_seq_kernel<T, LVV><<<grid, 256, 0, s>>>(x, out, plan.batch, plan.n, \
+                                                         es, bs, (int)plan.policy, plan.B))
       if (LV <= 5) CR_SEQ(5);
       else if (LV <= 9) CR_SEQ(9);
       else if (LV <= 17) CR_SEQ(17);
@@ -454,7 +456,7 @@ cudaError_t run_scan(const ScanPlan& plan, const T* x, T* out, int64_t es, int64
       return cudaGetLastError();
     }
     case ScanPlan::kChainOnly:
-      carry_chain_kernel<T><<<1, 32, 0, s>>>(x, out, plan.n);
+      CR_LAUNCH(kKCarryChain, s, carry_chain_kernel<T><<<1, 32, 0, s>>>(x, out, plan.n));
       return cudaGetLastError();
     case ScanPlan::kTiled: break;
   }
@@ -482,9 +484,11 @@ cudaError_t run_scan(const ScanPlan& plan, const T* x, T* out, int64_t es, int64
   const unsigned grid = (unsigned)plan.n_tiles;
   const bool up_needed = plan.pyr_levels > 0 || (block && plan.totals_level >= 0);
   if (up_needed) {
-    if (S == 8) scan_up_kernel<T, 8><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
-    else if (S == 4) scan_up_kernel<T, 4><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
-    else scan_up_kernel<T, 2><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
+    CR_LAUNCH(kKScanUp, s, {
+      if (S == 8) scan_up_kernel<T, 8><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
+      else if (S == 4) scan_up_kernel<T, 4><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
+      else scan_up_kernel<T, 2><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
+    });
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (block && plan.K >= 2) {
@@ -492,12 +496,14 @@ cudaError_t run_scan(const ScanPlan& plan, const T* x, T* out, int64_t es, int64
     const T* src = (plan.totals_level >= 0)
                        ? totals
                        : pyr + plan.pyr_off[plan.logB - kLogTile];
-    carry_chain_kernel<T><<<1, 32, 0, s>>>(src, carries, plan.K - 1);
+    CR_LAUNCH(kKCarryChain, s, carry_chain_kernel<T><<<1, 32, 0, s>>>(src, carries, plan.K - 1));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  if (S == 8) scan_down_kernel<T, 8><<<grid, kScanThreads, 0, s>>>(x, out, pyr, carries, a);
-  else if (S == 4) scan_down_kernel<T, 4><<<grid, kScanThreads, 0, s>>>(x, out, pyr, carries, a);
-  else scan_down_kernel<T, 2><<<grid, kScanThreads, 0, s>>>(x, out, pyr, carries, a);
+  CR_LAUNCH(kKScanDown, s, {
+    if (S == 8) scan_down_kernel<T, 8><<<grid, kScanThreads, 0, s>>>(x, out, pyr, carries, a);
+    else if (S == 4) scan_down_kernel<T, 4><<<grid, kScanThreads, 0, s>>>(x, out, pyr, carries, a);
+    else scan_down_kernel<T, 2><<<grid, kScanThreads, 0, s>>>(x, out, pyr, carries, a);
+  });
   return cudaGetLastError();
 }
 
