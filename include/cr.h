@@ -140,6 +140,27 @@ cr_status cr_inclusive_scan_batched(const void* x, void* out, int64_t batch, int
                                     int64_t B, cr_dtype dt, void* ws, size_t ws_bytes,
                                     void* stream);
 
+/* Allocation-free canonical reduction. The paper has no counterpart: this
+ * serves callers that cannot allocate device memory, such as a plugin whose
+ * host framework owns all device memory through its own pool, or a
+ * latency-critical path that must not pay cudaMalloc's possible
+ * device-wide synchronisation. Same result and arguments as cr_reduce(), but
+ * no workspace argument: the scratch is one 16 MiB device array built into
+ * libcr, present on every GPU that loads the library until the process
+ * exits.
+ *   - Calls whose cr_reduce_workspace_bytes(n, L, dt) exceeds 16 MiB return
+ *     CR_ERR_WORKSPACE and enqueue nothing (every n <= 2^28 fits for
+ *     L <= 4096).
+ *   - The first call on a device (that device current) looks up the array's
+ *     device address; make that first call before any stream capture.
+ *   - All calls on a device share the one array, which keeps the previous
+ *     call's contents: two calls that may overlap on the GPU (different
+ *     streams, no ordering between them) race and give wrong results.
+ *     Serialise them, e.g. on one stream.
+ *   - It allocates no device memory and frees none. */
+cr_status cr_reduce_noalloc(const void* x, int64_t n, int32_t L, const void* init_host,
+                            cr_dtype dt, void* out_dev, void* stream);
+
 /* ------------------------------------------------------------- utilities */
 
 /* Synchronises `stream`, then reports the device-side status of the most

@@ -39,6 +39,7 @@ _INT = ctypes.c_int
 SIGNATURES = {
     "cr_reduce_workspace_bytes": (_SZ, [_I64, _I32, _INT]),
     "cr_reduce": (_INT, [_P, _I64, _I32, _P, _INT, _P, _P, _SZ, _P]),
+    "cr_reduce_noalloc": (_INT, [_P, _I64, _I32, _P, _INT, _P, _P]),
     "cr_reduce_batched_workspace_bytes": (_SZ, [_I64, _I64, _I32, _INT]),
     "cr_reduce_batched": (_INT, [_P, _P, _I64, _I64, _I64, _I64, _I32, _P, _INT, _P, _SZ, _P]),
     "cr_scan_workspace_bytes": (_SZ, [_I64, _INT, _I64, _INT]),
