@@ -1,0 +1,25 @@
+// Exact parallel left fold C_0 = T_0, C_k = fl(C_{k-1} + T_k) (see cr_chain.cu).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace cr {
+
+struct ChainPlan {
+  int64_t K = 0, ntiles = 0, seg_cap = 0;
+  size_t tsum_off = 0, toff_off = 0, pre_off = 0, q_off = 0, meta_off = 0, nseg_off = 0,
+         segbase_off = 0, segs_off = 0, min_off = 0, misc_off = 0;
+  size_t bytes = 0;  // workspace bytes (offsets are relative to the chain's base)
+};
+
+ChainPlan plan_chain(int64_t K);
+
+// dst[k] = C_k for k < K. src and dst must not overlap (the fallback re-reads
+// src). ws: plan.bytes of 256-byte aligned device memory.
+template <class T>
+cudaError_t run_chain(const ChainPlan& plan, const T* src, T* dst, char* ws, cudaStream_t s);
+
+}  // namespace cr

@@ -35,9 +35,12 @@ cudaEvent_t take_event() {
 }  // namespace
 
 const char* kernel_name(int id) {
-  static const char* names[kKernelCount] = {"lane_pass_kernel",   "write_init_kernel",
-                                            "scan_up_kernel",     "scan_down_kernel",
-                                            "carry_chain_kernel", "scan_seq_kernel"};
+  static const char* names[kKernelCount] = {
+      "lane_pass_kernel",      "write_init_kernel",     "scan_up_kernel",
+      "scan_down_kernel",      "carry_chain_kernel",    "scan_seq_kernel",
+      "chain_tile_sum_kernel", "chain_offsets_kernel",  "chain_prefix_kernel",
+      "chain_classify_kernel", "chain_segments_kernel", "chain_walk_kernel",
+      "chain_fill_kernel",     "chain_fallback_kernel"};
   return (id >= 0 && id < kKernelCount) ? names[id] : "unknown";
 }
 

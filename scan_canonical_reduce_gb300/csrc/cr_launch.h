@@ -17,6 +17,14 @@ enum KernelId : int {
   kKScanDown,
   kKCarryChain,
   kKScanSeq,
+  kKChainTileSum,
+  kKChainOffsets,
+  kKChainPrefix,
+  kKChainClassify,
+  kKChainSegments,
+  kKChainWalk,
+  kKChainFill,
+  kKChainFallback,
   kKernelCount
 };
 

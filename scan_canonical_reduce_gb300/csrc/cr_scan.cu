@@ -40,6 +40,7 @@ constexpr int kE = 8;                     // elements per thread
 constexpr int kTile = kScanThreads * kE;  // 2048 elements per tile
 constexpr int kLogE = 3;
 constexpr int kLogTile = 11;
+constexpr int64_t kParallelChainMin = 1024;  // shorter chains: serial kernel
 
 __device__ __forceinline__ int64_t imin(int64_t a, int64_t b) { return a < b ? a : b; }
 __device__ __forceinline__ int64_t imax(int64_t a, int64_t b) { return a > b ? a : b; }
@@ -383,6 +384,14 @@ ScanPlan plan_scan(int64_t batch, int64_t n, cr_policy p, int64_t B, size_t esiz
   }
   if (p == CR_LEFT_FOLD || (block && B == 1)) {
     plan.kind = ScanPlan::kChainOnly;  // every element is its own block
+    if (n >= kParallelChainMin) {
+      plan.parallel_chain = true;
+      plan.chain = plan_chain(n);
+      plan.chain_ws = off;
+      off += round256(plan.chain.bytes);
+      plan.copy_ws = off;  // used only when out == x
+      off += round256((size_t)n * esize);
+    }
     plan.ws_bytes = off;
     return plan;
   }
@@ -427,6 +436,12 @@ ScanPlan plan_scan(int64_t batch, int64_t n, cr_policy p, int64_t B, size_t esiz
     off += round256((size_t)plan.K * esize);
     plan.carries_ws = off;
     off += round256((size_t)plan.K * esize);
+    if (plan.K - 1 >= kParallelChainMin) {
+      plan.parallel_chain = true;
+      plan.chain = plan_chain(plan.K - 1);
+      plan.chain_ws = off;
+      off += round256(plan.chain.bytes);
+    }
   } else {
     plan.totals_level = -1;
   }
@@ -455,9 +470,20 @@ cudaError_t run_scan(const ScanPlan& plan, const T* x, T* out, int64_t es, int64
 #undef CR_SEQ
       return cudaGetLastError();
     }
-    case ScanPlan::kChainOnly:
-      CR_LAUNCH(kKCarryChain, s, carry_chain_kernel<T><<<1, 32, 0, s>>>(x, out, plan.n));
-      return cudaGetLastError();
+    case ScanPlan::kChainOnly: {
+      if (!plan.parallel_chain) {
+        CR_LAUNCH(kKCarryChain, s, carry_chain_kernel<T><<<1, 32, 0, s>>>(x, out, plan.n));
+        return cudaGetLastError();
+      }
+      const T* src = x;
+      if (x == out) {  // the chain's fallback re-reads its input: keep a copy
+        T* copy = reinterpret_cast<T*>(ws + plan.copy_ws);
+        e = cudaMemcpyAsync(copy, x, (size_t)plan.n * sizeof(T), cudaMemcpyDeviceToDevice, s);
+        if (e != cudaSuccess) return e;
+        src = copy;
+      }
+      return run_chain<T>(plan.chain, src, out, ws + plan.chain_ws, s);
+    }
     case ScanPlan::kTiled: break;
   }
   const bool block = plan.policy == CR_BLOCK_DYADIC;
@@ -496,8 +522,14 @@ cudaError_t run_scan(const ScanPlan& plan, const T* x, T* out, int64_t es, int64
     const T* src = (plan.totals_level >= 0)
                        ? totals
                        : pyr + plan.pyr_off[plan.logB - kLogTile];
-    CR_LAUNCH(kKCarryChain, s, carry_chain_kernel<T><<<1, 32, 0, s>>>(src, carries, plan.K - 1));
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (plan.parallel_chain) {
+      e = run_chain<T>(plan.chain, src, carries, ws + plan.chain_ws, s);
+    } else {
+      CR_LAUNCH(kKCarryChain, s,
+                carry_chain_kernel<T><<<1, 32, 0, s>>>(src, carries, plan.K - 1));
+      e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) return e;
   }
   CR_LAUNCH(kKScanDown, s, {
     if (S == 8) scan_down_kernel<T, 8><<<grid, kScanThreads, 0, s>>>(x, out, pyr, carries, a);

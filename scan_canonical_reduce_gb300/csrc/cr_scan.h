@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include "cr.h"
+#include "cr_chain.h"
 #include "cr_plan.h"
 
 namespace cr {
@@ -42,6 +43,12 @@ struct ScanPlan {
   int64_t K = 0;             // blocks (block_dyadic)
   int totals_level = -1;
   size_t totals_ws = 0, carries_ws = 0;
+  // left folds (block carries, 1-D left_fold) longer than this use the
+  // exact parallel chain; shorter ones the serial chain kernel
+  bool parallel_chain = false;
+  ChainPlan chain;
+  size_t chain_ws = 0;
+  size_t copy_ws = 0;        // 1-D left_fold in place: private copy of x
   size_t ws_bytes = kHeaderBytes;
 };
 

@@ -52,8 +52,6 @@ SIZES = [1, 2, 3, 7, 8, 9, 15, 16, 17, 100, 255, 256, 257, 2047, 2048, 2049, 409
                                       ("block_dyadic", 4096), ("block_dyadic", 1 << 16)])
 def test_scan_sizes(scr, dtype, policy, B):
     for n in SIZES:
-        if policy == "left_fold" and n > 200000:
-            continue
         x = W.signed_pow2(n, W.seed_for(3, n % 101), dtype, -20, 20)
         check_scan(scr, x, policy, B)
 
