@@ -4,37 +4,39 @@
 // Reduction and Scan": blocks chained left to right) and the whole 1-D
 // left_fold scan. The result is bit-identical to the serial chain.
 //
-// Why it can be parallel. Let u = 2^(e - p) be the unit in the last place of
-// binade e (|v| in [2^e, 2^(e+1)), p = 52 or 23 fraction bits). If C_{k-1}
-// is an integer multiple M of u and the exact sum s = C_{k-1} + T_k lies in
-// binade e, then fl(s) = u * RNE(M + T_k/u). With T_k/u = q + f (q integer,
-// 0 <= f < 1): fl(s)/u = A + d, A = M + q, d = [f > 1/2] or, when f is
-// exactly 1/2, [A odd] (ties to even). So inside a stretch of steps whose
-// sums stay in one binade, every rounded add is an integer step
-//     M -> M + b[parity(M)],   b[p] = q + d(f, p xor (q & 1)),
-// and such maps compose associatively: (first g, then h)
-//     b[p] = g.b[p] + h.b[(p + g.b[p]) & 1].
-// The only sequential work left is where the binade changes ("breaks").
+// Why it can be parallel. Let u_e = 2^(e - p) be the unit in the last place
+// of binade e (|v| in [2^e, 2^(e+1)), p = 52 or 23 fraction bits). If C_{k-1}
+// is an integer multiple M of u_e and the exact sum s = C_{k-1} + T_k lies in
+// binade e, then fl(s) = u_e * RNE(M + T_k/u_e). With T_k/u_e = q + f
+// (q integer, 0 <= f < 1): fl(s)/u_e = A + d, A = M + q, d = [f > 1/2] or,
+// for f exactly 1/2, [A odd] (ties to even). When the sum drops to a lower
+// binade e' (u_e' = u_e / 2^j), C_{k-1} = (2^j M) u_e' is still a multiple
+// of the new unit, so the step is M -> 2^j M + q + d in the new unit. Every
+// such step is an integer map
+//     M -> a M + b[parity(M)],     a = 2^j,
+// and these maps compose associatively (first g, then h):
+//     a = a_h a_g,  b[p] = a_h b_g[p] + b_h[p'],  p' = parity(a_g M + b_g[p]).
+// Arithmetic is modulo 2^64: every true intermediate is below 2^54 in
+// magnitude whenever the steps are valid, so the residues are the values.
+// What cannot compose is a rise to a higher binade (the sum is rounded to a
+// coarser unit: an exact division by 2^j with round-half-even) and a step
+// whose binade is uncertain (a real add). These are "breaks", evaluated in
+// order by one thread from integers only (real adds only when uncertain).
 //
-// Passes (tile = 2048 steps, 8 per thread):
-//   1 tile sums of T             (approximate prefix, any order)
-//   2 tile offsets               (one block)
-//   3 prefix P~_k + max |P~|      (the chain stays within a proven margin
-//                                  mu = K * ulp(2 max|P~|) of P~_k)
-//   4 classify each step: binade and sign of s_k from P~_k when the whole
-//     interval P~_k +- mu lies inside one binade; else "uncertain". A step
-//     starts a new segment (break) when its class differs from the previous
-//     step's or is uncertain. Non-break steps store (q_k, f class).
-//   5 segment bases (one block), 6 segment maps (composition per segment),
-//   7 walk (one thread): at each break C = fl(C + T_k) with a real add, then
-//     M = C / u (checked integral), then the segment's composed map,
-//   8 fill: every step recomputed from its segment's entry value with an
-//     exact range check that s_k really lies in the predicted binade and
-//     sign; C_k = M_k * u.
-//   9 if any check failed (or segments overflowed their buffer), the plain
-//     serial chain recomputes everything on the device (no host sync).
-// Every fp add of the chain is therefore either the real add (breaks,
-// fallback) or proven equal to it by integer arithmetic.
+// Passes (tile = 4096 steps, 16 per thread):
+//   1 tile sums, 2 tile offsets (one block), 3 prefix P~_k and max|P~|;
+//   4 classify: the binade and sign of s_k from P~_k, certain when the whole
+//     interval P~_k +- mu (mu = K ulp(2 max|P~|) bounds both |C_k - P_k| and
+//     |P~_k - P_k|) lies inside one binade; step types MAP (same or lower
+//     binade), UP (higher binade, integer break), FP (uncertain: real add);
+//   5 segment bases (one block), 6 segment records: each break (or tile
+//     start) and the composed map of the MAP steps that follow it;
+//   7 walk: the breaks in order, from integers; M entering every segment;
+//   8 fill: every MAP step recomputed from its segment's entry value with an
+//     exact 128-bit test that s_k lies in the predicted binade and sign;
+//   9 if any test failed (or the segment buffer overflowed), the serial chain
+//     recomputes everything on the device (no host sync).
+// Every add of the chain is therefore the real add or proven equal to it.
 #include <cstdint>
 
 #include "cr_chain.h"
@@ -44,81 +46,123 @@
 namespace cr {
 namespace {
 
-constexpr int kCT = 256;          // threads per tile
-constexpr int kCE = 8;            // steps per thread
-constexpr int kCTile = kCT * kCE; // 2048 steps per tile
+constexpr int kCT = 256;           // threads per tile
+constexpr int kCE = 16;            // steps per thread
+constexpr int kCTile = kCT * kCE;  // 4096 steps per tile
 
 template <class T>
 struct FP;
 template <>
 struct FP<double> {
   using U = uint64_t;
-  static constexpr int P = 52, BIAS = 1023, EMIN = -1022, EMAX = 1023;
+  static constexpr int P = 52, BIAS = 1023, EMIN = -1022, EMAX = 1023, W = 64;
   __device__ static U bits(double v) { return (U)__double_as_longlong(v); }
+  __device__ static double from_bits(U b) { return __longlong_as_double((long long)b); }
 };
 template <>
 struct FP<float> {
   using U = uint32_t;
-  static constexpr int P = 23, BIAS = 127, EMIN = -126, EMAX = 127;
+  static constexpr int P = 23, BIAS = 127, EMIN = -126, EMAX = 127, W = 32;
   __device__ static U bits(float v) { return (U)__float_as_uint(v); }
+  __device__ static float from_bits(U b) { return __uint_as_float(b); }
 };
 
-// f classes of T/u - q
+// ---- step meta word: type, certain, negative, f class, jump d, binade e
+enum : uint32_t { kMap = 0, kUp = 1, kFp = 2, kStart = 3 };
 enum : uint32_t { kFZero = 0, kFLow = 1, kFHalf = 2, kFHigh = 3 };
-// meta word of a step: bit0 break, bit1 certain, bit2 negative sign,
-// bits 3-4 f class, bits 8..19 binade e + 2048
-__device__ __forceinline__ uint32_t make_meta(bool brk, bool certain, bool neg, uint32_t fcls,
-                                              int e) {
-  return (brk ? 1u : 0u) | (certain ? 2u : 0u) | (neg ? 4u : 0u) | (fcls << 3) |
-         ((uint32_t)(e + 2048) << 8);
+__device__ __forceinline__ uint32_t make_meta(uint32_t type, bool certain, bool neg,
+                                              uint32_t fcls, int d, int e) {
+  return type | (certain ? 4u : 0u) | (neg ? 8u : 0u) | (fcls << 4) | ((uint32_t)d << 6) |
+         ((uint32_t)(e + 2048) << 12);
 }
-__device__ __forceinline__ bool meta_break(uint32_t m) { return m & 1u; }
-__device__ __forceinline__ bool meta_certain(uint32_t m) { return m & 2u; }
-__device__ __forceinline__ bool meta_neg(uint32_t m) { return m & 4u; }
-__device__ __forceinline__ uint32_t meta_fcls(uint32_t m) { return (m >> 3) & 3u; }
-__device__ __forceinline__ int meta_e(uint32_t m) { return (int)((m >> 8) & 0xFFFu) - 2048; }
+__device__ __forceinline__ uint32_t m_type(uint32_t m) { return m & 3u; }
+__device__ __forceinline__ bool m_certain(uint32_t m) { return m & 4u; }
+__device__ __forceinline__ bool m_neg(uint32_t m) { return m & 8u; }
+__device__ __forceinline__ uint32_t m_fcls(uint32_t m) { return (m >> 4) & 3u; }
+__device__ __forceinline__ int m_d(uint32_t m) { return (int)((m >> 6) & 63u); }
+__device__ __forceinline__ int m_e(uint32_t m) { return (int)((m >> 12) & 0xFFFu) - 2048; }
 
-struct Map {  // M -> M + b[parity(M)] (two's complement, wraps like the hardware)
-  uint64_t b0, b1;
+// ---- integer maps M -> a M + b[parity(M)] (mod 2^64)
+struct Map {
+  uint64_t a, b0, b1;
 };
-__device__ __forceinline__ Map map_id() { return Map{0, 0}; }
-__device__ __forceinline__ Map compose(Map g, Map h) {  // first g, then h
-  const uint64_t g0 = g.b0, g1 = g.b1;
-  return Map{g0 + ((g0 & 1) ? h.b1 : h.b0), g1 + (((1 + g1) & 1) ? h.b1 : h.b0)};
+__device__ __forceinline__ Map map_id() { return Map{1, 0, 0}; }
+__device__ __forceinline__ uint64_t bsel(const Map& g, uint64_t p) { return p ? g.b1 : g.b0; }
+__device__ __forceinline__ Map compose(const Map& g, const Map& h) {  // first g, then h
+  const uint64_t p0 = (g.b0 & 1);                         // parity after g, from even M
+  const uint64_t p1 = ((g.a & 1) ^ g.b1) & 1;            // parity after g, from odd M
+  return Map{h.a * g.a, h.a * g.b0 + bsel(h, p0), h.a * g.b1 + bsel(h, p1)};
 }
-__device__ __forceinline__ uint64_t apply(Map g, uint64_t M) {
-  return M + ((M & 1) ? g.b1 : g.b0);
+__device__ __forceinline__ uint64_t apply(const Map& g, uint64_t M) {
+  return g.a * M + bsel(g, M & 1);
 }
-__device__ __forceinline__ uint32_t delta(uint32_t fcls, uint64_t A) {
-  return fcls == kFHigh ? 1u : (fcls == kFHalf ? (uint32_t)(A & 1) : 0u);
+__device__ __forceinline__ uint32_t delta(uint32_t fcls, uint64_t parity) {
+  return fcls == kFHigh ? 1u : (fcls == kFHalf ? (uint32_t)(parity & 1) : 0u);
 }
-__device__ __forceinline__ Map step_map(int64_t q, uint32_t fcls) {
-  const uint64_t uq = (uint64_t)q;
-  // p = parity of the incoming M; A = M + q has parity p ^ (q & 1)
-  return Map{uq + delta(fcls, uq & 1), uq + delta(fcls, (uq & 1) ^ 1)};
+// A MAP step: M -> 2^d M + q + delta, delta from the parity of A = 2^d M + q.
+__device__ __forceinline__ Map step_map(int d, int64_t q, uint32_t fcls) {
+  const uint64_t uq = (uint64_t)q, a = d >= 64 ? 0 : (uint64_t(1) << d);
+  if (d == 0) return Map{1, uq + delta(fcls, uq & 1), uq + delta(fcls, (uq & 1) ^ 1)};
+  const uint64_t b = uq + delta(fcls, uq & 1);  // 2^d M is even
+  return Map{a, b, b};
 }
 
-// T / 2^(e - P) = q + f, 0 <= f < 1, classified. Returns false when q would
-// not fit (|T| far above the unit: never a valid in-binade step).
+// ---- exact conversions between T values and (integer, binade) pairs
+// unit of binade e as T (exact, possibly subnormal)
+template <class T>
+__device__ __forceinline__ T unit_of(int e) {
+  using F = FP<T>;
+  const int ue = e - F::P;
+  typename F::U b;
+  if (ue >= F::EMIN) b = (typename F::U)(ue + F::BIAS) << F::P;
+  else b = (typename F::U)1 << (ue - (F::EMIN - F::P));
+  return F::from_bits(b);
+}
+template <class T>
+__device__ __forceinline__ T m_to_value(int64_t M, int e) {  // M * u_e, exact when valid
+  return (T)M * unit_of<T>(e);
+}
+// value -> M with value = M u_e exactly; false if not an integer multiple or
+// the multiple does not fit
+template <class T>
+__device__ __forceinline__ bool value_to_m(T v, int e, int64_t& M) {
+  using F = FP<T>;
+  const typename F::U b = F::bits(v);
+  const int bexp = (int)((b >> F::P) & ((1u << (F::W - 1 - F::P)) - 1));
+  uint64_t mant = (uint64_t)(b & ((typename F::U(1) << F::P) - 1));
+  if (bexp == (1 << (F::W - 1 - F::P)) - 1) return false;  // inf / nan
+  if (bexp == 0 && mant == 0) { M = 0; return true; }
+  int ev;  // v = mant 2^(ev - P)
+  if (bexp == 0) ev = F::EMIN;
+  else { mant |= uint64_t(1) << F::P; ev = bexp - F::BIAS; }
+  const int sh = ev - e;  // v / u_e = mant 2^sh
+  uint64_t m;
+  if (sh >= 0) {
+    if (sh > 9) return false;
+    m = mant << sh;
+  } else {
+    if (sh < -63) return false;
+    if (mant & ((uint64_t(1) << (-sh)) - 1)) return false;
+    m = mant >> (-sh);
+  }
+  const bool neg = (b >> (F::W - 1)) & 1;
+  M = neg ? -(int64_t)m : (int64_t)m;
+  return true;
+}
+
+// T / u_e = q + f, 0 <= f < 1, classified. False when q would not fit.
 template <class T>
 __device__ __forceinline__ bool split_unit(T t, int e, int64_t& q, uint32_t& fcls) {
   using F = FP<T>;
   const typename F::U b = F::bits(t);
-  const int bexp = (int)((b >> F::P) & ((1u << (sizeof(T) * 8 - 1 - F::P)) - 1));
+  const int bexp = (int)((b >> F::P) & ((1u << (F::W - 1 - F::P)) - 1));
   uint64_t mant = (uint64_t)(b & ((typename F::U(1) << F::P) - 1));
-  if (bexp == 0 && mant == 0) {
-    q = 0;
-    fcls = kFZero;
-    return true;
-  }
+  if (bexp == (1 << (F::W - 1 - F::P)) - 1) return false;  // inf / nan
+  if (bexp == 0 && mant == 0) { q = 0; fcls = kFZero; return true; }
   int et;  // t = mant * 2^et
-  if (bexp == 0) {
-    et = F::EMIN - F::P;  // subnormal
-  } else {
-    mant |= uint64_t(1) << F::P;
-    et = bexp - F::BIAS - F::P;
-  }
-  const bool neg = (b >> (sizeof(T) * 8 - 1)) & 1;
+  if (bexp == 0) et = F::EMIN - F::P;
+  else { mant |= uint64_t(1) << F::P; et = bexp - F::BIAS - F::P; }
+  const bool neg = (b >> (F::W - 1)) & 1;
   const int sh = et - (e - F::P);  // t / u = mant * 2^sh
   if (sh >= 0) {
     if (sh > 62 - F::P - 1) return false;
@@ -148,19 +192,31 @@ __device__ __forceinline__ bool split_unit(T t, int e, int64_t& q, uint32_t& fcl
   return true;
 }
 
-// s = M*u + T lies in the predicted binade and sign: exact integer test on
-// A = M + q (see the header comment).
+// s / u = A + f lies in the predicted binade and sign (exact integer test).
 template <class T>
-__device__ __forceinline__ bool in_binade(int64_t A, bool neg, uint32_t fcls) {
+__device__ __forceinline__ bool in_binade(__int128 A, bool neg, uint32_t fcls) {
   constexpr int64_t LO = int64_t(1) << FP<T>::P, HI = int64_t(1) << (FP<T>::P + 1);
   if (!neg) return A >= LO && A <= HI - 1;
   const bool fz = fcls == kFZero;
   return (fz ? A <= -LO : A <= -LO - 1) && (fz ? A >= -HI + 1 : A >= -HI);
 }
 
+// A rise by d binades: M (old unit) -> RNE((M + q + f) / 2^d) in the new
+// unit, with the in-binade test of the new sum. False if the test fails.
 template <class T>
-__device__ __forceinline__ T scale_pow2(int64_t M, int e) {  // M * 2^(e - P), exact
-  return (T)ldexp((double)M, e - FP<T>::P);
+__device__ __forceinline__ bool up_step(uint64_t& M, int64_t q, uint32_t fcls, int d, bool neg) {
+  const int64_t A = (int64_t)M + q;   // |M| <= 2^54, |q| < 2^62
+  const int64_t hi = A >> d;          // floor
+  const uint64_t lo = (uint64_t)A & ((uint64_t(1) << d) - 1);
+  const uint64_t half = uint64_t(1) << (d - 1);
+  uint32_t f2;
+  if (lo == 0 && fcls == kFZero) f2 = kFZero;
+  else if (lo < half) f2 = kFLow;
+  else if (lo == half && fcls == kFZero) f2 = kFHalf;
+  else f2 = kFHigh;
+  if (!in_binade<T>(hi, neg, f2)) return false;
+  M = (uint64_t)(hi + (int64_t)delta(f2, (uint64_t)hi & 1));
+  return true;
 }
 
 // ---------------------------------------------------------------- pass 1
@@ -171,6 +227,7 @@ __global__ void __launch_bounds__(kCT) chain_tile_sum_kernel(const T* src, int64
   const int t = threadIdx.x;
   const int64_t k0 = (int64_t)blockIdx.x * kCTile + (int64_t)t * kCE;
   double s = 0.0;
+#pragma unroll
   for (int i = 0; i < kCE; ++i)
     if (k0 + i < K) s += (double)src[k0 + i];
   sh[t] = s;
@@ -182,57 +239,32 @@ __global__ void __launch_bounds__(kCT) chain_tile_sum_kernel(const T* src, int64
   if (t == 0) tsum[blockIdx.x] = sh[0];
 }
 
-// ---------------------------------------------------------------- pass 2
-// Exclusive prefix over the tile sums, and the segment bases (same shape).
-__global__ void __launch_bounds__(1024) chain_offsets_kernel(const double* tsum, double* toff,
-                                                             int64_t ntiles) {
-  __shared__ double sh[1024];
-  __shared__ double carry;
+// ---------------------------------------------------------------- pass 2 / 5
+template <class V>
+__global__ void __launch_bounds__(1024) exclusive_scan_1block(const V* in, V* out, int64_t n,
+                                                              V* total) {
+  __shared__ V sh[1024];
+  __shared__ V carry;
   const int t = threadIdx.x;
-  if (t == 0) carry = 0.0;
+  if (t == 0) carry = V(0);
   __syncthreads();
-  for (int64_t base = 0; base < ntiles; base += 1024) {
+  for (int64_t base = 0; base < n; base += 1024) {
     const int64_t i = base + t;
-    const double v = i < ntiles ? tsum[i] : 0.0;
+    const V v = i < n ? in[i] : V(0);
     sh[t] = v;
     __syncthreads();
     for (int off = 1; off < 1024; off <<= 1) {
-      const double a = t >= off ? sh[t - off] : 0.0;
+      const V a = t >= off ? sh[t - off] : V(0);
       __syncthreads();
       sh[t] += a;
       __syncthreads();
     }
-    if (i < ntiles) toff[i] = carry + sh[t] - v;
+    if (i < n) out[i] = carry + sh[t] - v;
     __syncthreads();
     if (t == 0) carry += sh[1023];
     __syncthreads();
   }
-}
-
-__global__ void __launch_bounds__(1024) chain_seg_base_kernel(const int* nseg, int64_t* base,
-                                                              int64_t ntiles, int64_t* total) {
-  __shared__ int64_t sh[1024];
-  __shared__ int64_t carry;
-  const int t = threadIdx.x;
-  if (t == 0) carry = 0;
-  __syncthreads();
-  for (int64_t b0 = 0; b0 < ntiles; b0 += 1024) {
-    const int64_t i = b0 + t;
-    const int64_t v = i < ntiles ? nseg[i] : 0;
-    sh[t] = v;
-    __syncthreads();
-    for (int off = 1; off < 1024; off <<= 1) {
-      const int64_t a = t >= off ? sh[t - off] : 0;
-      __syncthreads();
-      sh[t] += a;
-      __syncthreads();
-    }
-    if (i < ntiles) base[i] = carry + sh[t] - v;
-    __syncthreads();
-    if (t == 0) carry += sh[1023];
-    __syncthreads();
-  }
-  if (t == 0) *total = carry;
+  if (t == 0 && total) *total = carry;
 }
 
 // ---------------------------------------------------------------- pass 3
@@ -245,6 +277,7 @@ __global__ void __launch_bounds__(kCT) chain_prefix_kernel(const T* src, int64_t
   const int64_t k0 = (int64_t)blockIdx.x * kCTile + (int64_t)t * kCE;
   double v[kCE];
   double s = 0.0;
+#pragma unroll
   for (int i = 0; i < kCE; ++i) {
     v[i] = (k0 + i < K) ? (double)src[k0 + i] : 0.0;
     s += v[i];
@@ -259,6 +292,7 @@ __global__ void __launch_bounds__(kCT) chain_prefix_kernel(const T* src, int64_t
   }
   double run = toff[blockIdx.x] + (sh[t] - s);
   double mx = 0.0;
+#pragma unroll
   for (int i = 0; i < kCE; ++i) {
     if (k0 + i < K) {
       run += v[i];
@@ -266,12 +300,26 @@ __global__ void __launch_bounds__(kCT) chain_prefix_kernel(const T* src, int64_t
       mx = fmax(mx, fabs(run));
     }
   }
-  if (!(mx <= 1.7e308)) mx = 1.7e308;  // non-finite: classify as uncertain later
-  atomicMax(maxabs, (unsigned long long)__double_as_longlong(mx));
+  if (!(mx <= 1.7e308)) mx = 1.7e308;  // non-finite: those steps are uncertain anyway
+  __syncthreads();
+  sh[t] = mx;
+  __syncthreads();
+  for (int w = kCT / 2; w > 0; w >>= 1) {
+    if (t < w) sh[t] = fmax(sh[t], sh[t + w]);
+    __syncthreads();
+  }
+  if (t == 0) atomicMax(maxabs, (unsigned long long)__double_as_longlong(sh[0]));
 }
 
 // ---------------------------------------------------------------- pass 4
-// Class of the exact sum s_k from P~_k: (certain, negative, binade e).
+// Binade exponent of a positive finite double from its bits.
+__device__ __forceinline__ int dexp(double a) {
+  return (int)((FP<double>::bits(a) >> 52) & 0x7FF) - 1023;
+}
+__device__ __forceinline__ double dpow2(int e) {  // 2^e, normal range
+  return FP<double>::from_bits((uint64_t)(e + 1023) << 52);
+}
+
 template <class T>
 __device__ __forceinline__ void classify(double p, double mu, bool& certain, bool& neg, int& e) {
   certain = false;
@@ -279,11 +327,10 @@ __device__ __forceinline__ void classify(double p, double mu, bool& certain, boo
   e = 0;
   const double a = fabs(p);
   if (!(a <= 1e300)) return;  // non-finite
-  if (a - mu <= 0.0) return;  // sign or zero uncertain
-  const int ee = ilogb(a);
-  if (ee < FP<T>::EMIN + 2 || ee > FP<T>::EMAX - 2) return;  // near subnormal / overflow
-  const double lo = ldexp(1.0, ee), hi = ldexp(1.0, ee + 1);
-  const double ulp = ldexp(1.0, ee - FP<T>::P);
+  if (a <= mu || a < 1e-290) return;  // sign, zero or the subnormal range uncertain
+  const int ee = dexp(a);
+  if (ee < FP<T>::EMIN + 2 || ee > FP<T>::EMAX - 2) return;
+  const double lo = dpow2(ee), hi = dpow2(ee + 1), ulp = dpow2(ee - FP<T>::P);
   if (a - mu < lo || a + mu + ulp >= hi) return;  // interval crosses a binade edge
   certain = true;
   e = ee;
@@ -292,41 +339,46 @@ __device__ __forceinline__ void classify(double p, double mu, bool& certain, boo
 template <class T>
 __global__ void __launch_bounds__(kCT) chain_classify_kernel(
     const T* src, int64_t K, const double* pre, const unsigned long long* maxabs, int64_t* qv,
-    uint32_t* meta, int* tile_nseg) {
+    uint32_t* meta, int64_t* tile_nseg) {
   __shared__ int cnt[kCT];
   const int t = threadIdx.x;
   const int64_t k0 = (int64_t)blockIdx.x * kCTile + (int64_t)t * kCE;
-  // margin mu = K * ulp(2 max|P~|) bounds both |C_k - P_k| (K roundings of at
-  // most half an ulp of |C| <= 2 max|P~|) and |P~_k - P_k|
-  const double mx = __longlong_as_double((long long)*maxabs);
   double mu;
   {
-    const double m2 = 2.0 * mx;
-    const int em = m2 > 0 ? ilogb(m2) : -1074;
-    mu = (double)K * ldexp(1.0, em - FP<T>::P);
-    if (!(mu <= 1e300)) mu = 1e300;
+    const double m2 = 2.0 * __longlong_as_double((long long)*maxabs);
+    mu = m2 > 1e-290 && m2 < 1e300 ? (double)K * dpow2(dexp(m2) - FP<T>::P) : 1e300;
+    if (m2 <= 1e-290) mu = 1e-280;
   }
   int nbrk = 0;
-  bool pc, pn;
-  int pe;
-  if (k0 == 0 || k0 > K) {
-    pc = false; pn = false; pe = 0;
-  } else {
-    classify<T>(pre[k0 - 1], mu, pc, pn, pe);
-  }
+  bool pc = false, pn = false;
+  int pe = 0;
+  if (k0 > 0 && k0 < K) classify<T>(pre[k0 - 1], mu, pc, pn, pe);
   for (int i = 0; i < kCE; ++i) {
     const int64_t k = k0 + i;
     if (k >= K) break;
     bool c, n;
     int e;
     classify<T>(pre[k], mu, c, n, e);
-    bool brk = (k == 0) || !c || !pc || n != pn || e != pe;
+    uint32_t type;
+    int d = 0;
     int64_t q = 0;
     uint32_t f = 0;
-    if (!brk && !split_unit<T>(src[k], e, q, f)) brk = true;
-    meta[k] = make_meta(brk, c, n, f, e);
+    const T tv = src[k];
+    if (k == 0) {
+      type = kStart;
+    } else if (!c || !pc) {
+      type = kFp;
+    } else if (e <= pe) {  // same or lower binade: a composable step
+      d = pe - e;
+      type = (d <= 63 && split_unit<T>(tv, e, q, f)) ? kMap : kFp;
+    } else {  // rise: integer break, T split in the old (finer) unit
+      d = e - pe;
+      type = (d <= 8 && split_unit<T>(tv, pe, q, f)) ? kUp : kFp;
+    }
+    if (type == kFp) d = 0;
+    meta[k] = make_meta(type, c, n, f, d, e);
     qv[k] = q;
-    nbrk += brk ? 1 : 0;
+    nbrk += type != kMap ? 1 : 0;
     pc = c; pn = n; pe = e;
   }
   cnt[t] = nbrk;
@@ -335,50 +387,45 @@ __global__ void __launch_bounds__(kCT) chain_classify_kernel(
     if (t < w) cnt[t] += cnt[t + w];
     __syncthreads();
   }
-  if (t == 0) {
-    // segments of this tile: one per break, plus one if the tile starts
-    // inside a run (its first step is not a break)
+  if (t == 0) {  // one segment per break, plus one if the tile starts inside a run
     const int64_t first = (int64_t)blockIdx.x * kCTile;
-    tile_nseg[blockIdx.x] = cnt[0] + (meta_break(meta[first]) ? 0 : 1);
+    tile_nseg[blockIdx.x] = cnt[0] + (m_type(meta[first]) == kMap ? 1 : 0);
   }
 }
 
 // ---------------------------------------------------------------- pass 6
-// Per-thread summary for the in-tile segmented scan:
-//   map: composition of the steps after the thread's last break (or all)
-//   brk: number of breaks in the thread
-struct Summ {
+struct Summ {  // composition after the last break of a thread's steps
   Map map;
   int brk;
 };
-__device__ __forceinline__ Summ combine(Summ l, Summ r) {
+__device__ __forceinline__ Summ combine(const Summ& l, const Summ& r) {
   return r.brk ? Summ{r.map, l.brk + r.brk} : Summ{compose(l.map, r.map), l.brk};
 }
 
-// Segment record. A segment starts at a break (its first step is done with a
-// real add) or at a tile start inside a run (continuation); `map` composes
-// its remaining steps.
+// Segment record: a break (or a tile start inside a run) and the composed
+// map of the MAP steps after it, up to the next break or the tile end.
 struct SegRec {
   int64_t start;
   Map map;
-  int32_t e;
-  int32_t flags;  // bit0 starts with a break, bit1 class certain
+  int64_t q;        // up: T split in the old unit
+  uint32_t meta;    // meta word of the start step (type kMap marks a continuation)
+  int32_t e_prev;   // fp break: binade of the previous step (if certain)
+  int32_t prev_certain;
+  int32_t nsteps;   // MAP steps in the map
 };
 
-template <class T>
 __device__ __forceinline__ void thread_scan(const int64_t* qv, const uint32_t* meta,
-                                            int64_t k0, int64_t K, Summ& in_excl,
-                                            Summ* sh) {
+                                            int64_t k0, int64_t K, Summ& in_excl, Summ* sh) {
   Summ me{map_id(), 0};
   for (int i = 0; i < kCE; ++i) {
     const int64_t k = k0 + i;
     if (k >= K) break;
     const uint32_t m = meta[k];
-    if (meta_break(m)) {
+    if (m_type(m) != kMap) {
       me.map = map_id();
       me.brk += 1;
     } else {
-      me.map = compose(me.map, step_map(qv[k], meta_fcls(m)));
+      me.map = compose(me.map, step_map(m_d(m), qv[k], m_fcls(m)));
     }
   }
   const int t = threadIdx.x;
@@ -397,26 +444,27 @@ __device__ __forceinline__ void thread_scan(const int64_t* qv, const uint32_t* m
 
 template <class T>
 __global__ void __launch_bounds__(kCT) chain_segments_kernel(
-    const int64_t* qv, const uint32_t* meta, int64_t K, const int64_t* seg_base,
-    SegRec* segs, int64_t seg_cap, int* fail) {
+    const int64_t* qv, const uint32_t* meta, int64_t K, const int64_t* seg_base, SegRec* segs,
+    int64_t seg_cap, int* fail) {
   __shared__ Summ sh[kCT];
   const int t = threadIdx.x;
   const int64_t tile0 = (int64_t)blockIdx.x * kCTile;
   const int64_t k0 = tile0 + (int64_t)t * kCE;
   Summ in;
-  thread_scan<T>(qv, meta, k0, K, in, sh);
-  const bool cont = !meta_break(meta[tile0]);  // tile begins inside a run
-  // segment ordinal (within the tile) of the segment open at my first step
-  int64_t ord = (cont ? 1 : 0) + in.brk - 1;
+  thread_scan(qv, meta, k0, K, in, sh);
+  const bool cont = m_type(meta[tile0]) == kMap;
+  int64_t ord = (cont ? 1 : 0) + in.brk - 1;  // segment open at my first step
   Map cur = in.map;
+  int steps = 0;  // MAP steps of the open segment seen by this thread
   const int64_t base = seg_base[blockIdx.x];
   if (t == 0 && cont) {
     if (base < seg_cap) {
       SegRec& r = segs[base];
       r.start = tile0;
-      const uint32_t m = meta[tile0];
-      r.e = meta_e(m);
-      r.flags = meta_certain(m) ? 2 : 0;
+      r.meta = meta[tile0];
+      r.q = 0;
+      r.e_prev = 0;
+      r.prev_certain = 0;
     } else {
       atomicExch(fail, 2);
     }
@@ -425,91 +473,116 @@ __global__ void __launch_bounds__(kCT) chain_segments_kernel(
     const int64_t k = k0 + i;
     if (k >= K) break;
     const uint32_t m = meta[k];
-    if (meta_break(m)) {
-      if (ord >= 0 && base + ord < seg_cap) segs[base + ord].map = cur;  // close
+    if (m_type(m) != kMap) {
+      if (ord >= 0 && base + ord < seg_cap) {  // close the open segment
+        segs[base + ord].map = cur;
+        if (steps) atomicAdd(&segs[base + ord].nsteps, steps);
+      }
       ord += 1;
       cur = map_id();
+      steps = 0;
       if (base + ord < seg_cap) {
         SegRec& r = segs[base + ord];
         r.start = k;
-        r.e = meta_e(m);
-        r.flags = 1 | (meta_certain(m) ? 2 : 0);
+        r.meta = m;
+        r.q = qv[k];
+        const uint32_t pm = meta[k > 0 ? k - 1 : 0];
+        r.e_prev = m_e(pm);
+        r.prev_certain = (k > 0 && m_certain(pm)) ? 1 : 0;
       } else {
         atomicExch(fail, 2);
       }
     } else {
-      cur = compose(cur, step_map(qv[k], meta_fcls(m)));
+      cur = compose(cur, step_map(m_d(m), qv[k], m_fcls(m)));
+      steps += 1;
     }
   }
-  // the thread holding the tile's last step closes the open segment
-  const int64_t last = (tile0 + kCTile < K ? tile0 + kCTile : K) - 1;
-  if (k0 <= last && last < k0 + kCE && ord >= 0 && base + ord < seg_cap)
-    segs[base + ord].map = cur;
+  if (ord >= 0 && base + ord < seg_cap) {
+    // my trailing MAP steps belong to the segment still open; the thread
+    // holding the tile's last step closes it
+    if (steps) atomicAdd(&segs[base + ord].nsteps, steps);
+    const int64_t last = (tile0 + kCTile < K ? tile0 + kCTile : K) - 1;
+    if (k0 <= last && last < k0 + kCE) segs[base + ord].map = cur;
+  }
 }
 
 // ---------------------------------------------------------------- pass 7
-// One warp: all lanes load the next 32 segment records (and the break
-// operands) while lane 0 runs the current 32 in order; records move to lane 0
-// by shuffles, so the sequential part never waits on memory.
+// Breaks in order, in one thread. Records are staged through shared memory by
+// the whole warp one batch ahead, so the sequential part never waits on
+// global memory.
 template <class T>
-__global__ void chain_walk_kernel(const T* src, T* dst, const SegRec* segs,
-                                  const int64_t* nseg_total, int64_t seg_cap, int64_t* m_in,
-                                  int* fail) {
-  if (blockIdx.x != 0) return;
+__global__ void __launch_bounds__(32) chain_walk_kernel(const T* src, T* dst, const SegRec* segs,
+                                                        const int64_t* nseg_total,
+                                                        int64_t seg_cap, int64_t* m_in,
+                                                        int* fail) {
+  __shared__ SegRec buf[2][32];
+  __shared__ T tval[2][32];
   const int lane = threadIdx.x;
   const int64_t nseg = *nseg_total;
   if (*fail || nseg > seg_cap) {
     if (lane == 0) atomicExch(fail, 2);
     return;
   }
-  T C = src[0];
-  uint64_t M = 0;
-  bool bad = false;
-  // registers of the batch being loaded
   SegRec nr{};
   T nt = T(0);
   if (lane < nseg) {
     nr = segs[lane];
     nt = src[nr.start];
   }
-  for (int64_t b0 = 0; b0 < nseg; b0 += 32) {
-    const SegRec cr = nr;
-    const T ct = nt;
+  uint64_t M = 0;
+  T C = T(0);
+  bool cval = false;  // C holds the current chain value
+  int ecur = 0;       // binade of M's unit
+  bool bad = false;
+  for (int64_t b0 = 0, it = 0; b0 < nseg; b0 += 32, ++it) {
+    const int slot = (int)(it & 1);
+    buf[slot][lane] = nr;  // loaded one batch ago
+    tval[slot][lane] = nt;
+    __syncwarp();
     const int64_t nb = b0 + 32 + lane;
-    if (nb < nseg) {  // prefetch the next batch
+    if (nb < nseg) {
       nr = segs[nb];
       nt = src[nr.start];
     }
-    const int cnt = (int)(nseg - b0 < 32 ? nseg - b0 : 32);
-    for (int j = 0; j < cnt; ++j) {
-      const int64_t start = __shfl_sync(0xffffffffu, cr.start, j);
-      const uint64_t mb0 = __shfl_sync(0xffffffffu, cr.map.b0, j);
-      const uint64_t mb1 = __shfl_sync(0xffffffffu, cr.map.b1, j);
-      const int e = __shfl_sync(0xffffffffu, cr.e, j);
-      const int flags = __shfl_sync(0xffffffffu, cr.flags, j);
-      const T tv = __shfl_sync(0xffffffffu, ct, j);
-      if (lane == 0 && !bad) {
-        if (flags & 1) {  // break: the real add
-          C = (start == 0) ? tv : add_rn(C, tv);
-          dst[start] = C;
-          if (flags & 2) {  // certain class: enter integer units of binade e
-            const double v = ldexp((double)C, FP<T>::P - e);
-            const double iv = trunc(v);
-            if (!(iv == v) || !(fabs(v) <= ldexp(1.0, FP<T>::P + 1))) bad = true;
-            M = (uint64_t)(int64_t)iv;
+    if (lane == 0 && !bad) {
+      const int cnt = (int)(nseg - b0 < 32 ? nseg - b0 : 32);
+      for (int j = 0; j < cnt; ++j) {
+        const SegRec& r = buf[slot][j];
+        const uint32_t m = r.meta;
+        const uint32_t type = m_type(m);
+        const int e = m_e(m);
+        if (type == kStart || type == kFp) {  // the real add
+          if (type == kStart) {
+            C = tval[slot][j];
+          } else {
+            if (!cval) {
+              if (!r.prev_certain) { bad = true; break; }
+              C = m_to_value<T>((int64_t)M, r.e_prev);
+            }
+            C = add_rn(C, tval[slot][j]);
           }
+          dst[r.start] = C;
+          cval = true;
+          if (m_certain(m)) {
+            int64_t Mi;
+            if (!value_to_m<T>(C, e, Mi)) { bad = true; break; }
+            M = (uint64_t)Mi;
+            ecur = e;
+          }
+        } else if (type == kUp) {
+          if (!up_step<T>(M, r.q, m_fcls(m), m_d(m), m_neg(m))) { bad = true; break; }
+          ecur = e;
+          cval = false;
         }
         m_in[b0 + j] = (int64_t)M;
-        if (!bad && (flags & 2)) {
-          M = apply(Map{mb0, mb1}, M);
-          const int64_t Ms = (int64_t)M;
-          if (Ms > (int64_t(1) << (FP<T>::P + 1)) || Ms < -(int64_t(1) << (FP<T>::P + 1)))
-            bad = true;
-          else
-            C = scale_pow2<T>(Ms, e);
+        if (r.nsteps > 0) {
+          M = apply(r.map, M);
+          cval = false;
         }
       }
+      (void)ecur;
     }
+    __syncwarp();
   }
   if (lane == 0 && bad) atomicExch(fail, 1);
 }
@@ -519,46 +592,38 @@ template <class T>
 __global__ void __launch_bounds__(kCT) chain_fill_kernel(const int64_t* qv, const uint32_t* meta,
                                                          int64_t K, const int64_t* seg_base,
                                                          const SegRec* segs, int64_t seg_cap,
-                                                         const int64_t* m_in, T* dst,
-                                                         int* fail) {
+                                                         const int64_t* m_in, T* dst, int* fail) {
   __shared__ Summ sh[kCT];
   const int t = threadIdx.x;
   const int64_t tile0 = (int64_t)blockIdx.x * kCTile;
   const int64_t k0 = tile0 + (int64_t)t * kCE;
   Summ in;
-  thread_scan<T>(qv, meta, k0, K, in, sh);
+  thread_scan(qv, meta, k0, K, in, sh);
   if (*fail) return;
-  const bool cont = !meta_break(meta[tile0]);
+  const bool cont = m_type(meta[tile0]) == kMap;
   int64_t seg = seg_base[blockIdx.x] + (cont ? 1 : 0) + in.brk - 1;
   uint64_t M = 0;
-  int e = 0;
-  bool live = false;  // M is meaningful (segment of certain class)
-  if (k0 < K && seg >= 0 && seg < seg_cap) {
-    const SegRec r = segs[seg];
-    live = (r.flags & 2) != 0;
-    e = r.e;
-    M = apply(in.map, (uint64_t)m_in[seg]);
-  }
+  if (k0 < K && seg >= 0 && seg < seg_cap) M = apply(in.map, (uint64_t)m_in[seg]);
   bool ok = true;
   for (int i = 0; i < kCE; ++i) {
     const int64_t k = k0 + i;
     if (k >= K) break;
     const uint32_t m = meta[k];
-    if (meta_break(m)) {  // value written by the walk; enter the next segment
+    const uint32_t type = m_type(m);
+    if (type != kMap) {  // enter the next segment
       seg += 1;
       if (seg >= seg_cap) { ok = false; break; }
-      const SegRec r = segs[seg];
-      live = (r.flags & 2) != 0;
-      e = r.e;
       M = (uint64_t)m_in[seg];
+      if (type == kUp) dst[k] = m_to_value<T>((int64_t)M, m_e(m));  // walk wrote fp breaks
       continue;
     }
-    if (!live) { ok = false; break; }
-    const int64_t A = (int64_t)M + qv[k];
-    const uint32_t f = meta_fcls(m);
-    if (!in_binade<T>(A, meta_neg(m), f)) { ok = false; break; }
-    M = (uint64_t)(A + (int64_t)delta(f, (uint64_t)A));
-    dst[k] = scale_pow2<T>((int64_t)M, e);
+    const int d = m_d(m);
+    const __int128 A = (__int128)(int64_t)M * ((__int128)1 << d) + (__int128)qv[k];
+    const uint32_t f = m_fcls(m);
+    if (!in_binade<T>(A, m_neg(m), f)) { ok = false; break; }
+    const int64_t A64 = (int64_t)A;
+    M = (uint64_t)(A64 + (int64_t)delta(f, (uint64_t)A64 & 1));
+    dst[k] = m_to_value<T>((int64_t)M, m_e(m));
   }
   if (!ok) atomicExch(fail, 1);
 }
@@ -590,7 +655,7 @@ ChainPlan plan_chain(int64_t K) {
   p.pre_off = off; off += r256(K * sizeof(double));
   p.q_off = off; off += r256(K * sizeof(int64_t));
   p.meta_off = off; off += r256(K * sizeof(uint32_t));
-  p.nseg_off = off; off += r256(p.ntiles * sizeof(int));
+  p.nseg_off = off; off += r256(p.ntiles * sizeof(int64_t));
   p.segbase_off = off; off += r256(p.ntiles * sizeof(int64_t));
   p.segs_off = off; off += r256(p.seg_cap * sizeof(SegRec));
   p.min_off = off; off += r256(p.seg_cap * sizeof(int64_t));
@@ -607,7 +672,7 @@ cudaError_t run_chain(const ChainPlan& p, const T* src, T* dst, char* ws, cudaSt
   double* pre = reinterpret_cast<double*>(ws + p.pre_off);
   int64_t* qv = reinterpret_cast<int64_t*>(ws + p.q_off);
   uint32_t* meta = reinterpret_cast<uint32_t*>(ws + p.meta_off);
-  int* nseg = reinterpret_cast<int*>(ws + p.nseg_off);
+  int64_t* nseg = reinterpret_cast<int64_t*>(ws + p.nseg_off);
   int64_t* segbase = reinterpret_cast<int64_t*>(ws + p.segbase_off);
   SegRec* segs = reinterpret_cast<SegRec*>(ws + p.segs_off);
   int64_t* m_in = reinterpret_cast<int64_t*>(ws + p.min_off);
@@ -616,27 +681,29 @@ cudaError_t run_chain(const ChainPlan& p, const T* src, T* dst, char* ws, cudaSt
   int* fail = reinterpret_cast<int*>(ws + p.misc_off + 16);
   cudaError_t e = cudaMemsetAsync(ws + p.misc_off, 0, 256, s);
   if (e != cudaSuccess) return e;
+  // per-segment MAP step counts are accumulated with atomics: clear them
+  e = cudaMemsetAsync(segs, 0, (size_t)p.seg_cap * sizeof(SegRec), s);
+  if (e != cudaSuccess) return e;
   if (p.ntiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const unsigned g = (unsigned)p.ntiles;
   CR_LAUNCH(kKChainTileSum, s, chain_tile_sum_kernel<T><<<g, kCT, 0, s>>>(src, p.K, tsum));
-  CR_LAUNCH(kKChainOffsets, s, chain_offsets_kernel<<<1, 1024, 0, s>>>(tsum, toff, p.ntiles));
+  CR_LAUNCH(kKChainOffsets, s,
+            exclusive_scan_1block<double><<<1, 1024, 0, s>>>(tsum, toff, p.ntiles, nullptr));
   CR_LAUNCH(kKChainPrefix, s,
             chain_prefix_kernel<T><<<g, kCT, 0, s>>>(src, p.K, toff, pre, maxabs));
   CR_LAUNCH(kKChainClassify, s,
             chain_classify_kernel<T><<<g, kCT, 0, s>>>(src, p.K, pre, maxabs, qv, meta, nseg));
   CR_LAUNCH(kKChainOffsets, s,
-            chain_seg_base_kernel<<<1, 1024, 0, s>>>(nseg, segbase, p.ntiles, total));
+            exclusive_scan_1block<int64_t><<<1, 1024, 0, s>>>(nseg, segbase, p.ntiles, total));
   CR_LAUNCH(kKChainSegments, s,
             chain_segments_kernel<T><<<g, kCT, 0, s>>>(qv, meta, p.K, segbase, segs, p.seg_cap,
                                                        fail));
   CR_LAUNCH(kKChainWalk, s,
-            chain_walk_kernel<T><<<1, 32, 0, s>>>(src, dst, segs, total, p.seg_cap, m_in,
-                                                  fail));
+            chain_walk_kernel<T><<<1, 32, 0, s>>>(src, dst, segs, total, p.seg_cap, m_in, fail));
   CR_LAUNCH(kKChainFill, s,
-            chain_fill_kernel<T><<<g, kCT, 0, s>>>(qv, meta, p.K, segbase, segs, p.seg_cap,
-                                                   m_in, dst, fail));
-  CR_LAUNCH(kKChainFallback, s,
-            chain_fallback_kernel<T><<<1, 32, 0, s>>>(src, dst, p.K, fail));
+            chain_fill_kernel<T><<<g, kCT, 0, s>>>(qv, meta, p.K, segbase, segs, p.seg_cap, m_in,
+                                                   dst, fail));
+  CR_LAUNCH(kKChainFallback, s, chain_fallback_kernel<T><<<1, 32, 0, s>>>(src, dst, p.K, fail));
   return cudaGetLastError();
 }
 
