@@ -225,6 +225,7 @@ def run_native(args):
     launches0 = scr.launch_count()
     scr.profile_enable(True)
     ev = {r[0]: [] for r in rows}
+    row_launches = {r[0]: [] for r in rows}
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
@@ -233,7 +234,9 @@ def run_native(args):
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
+            before = scr.launch_count()
             run_row(row)
+            row_launches[row[0]].append(scr.launch_count() - before)
             b.record(stream)
             ev[row[0]].append((a, b))
     t1.record(stream)
@@ -265,6 +268,18 @@ def run_native(args):
                            "hbm_frac": round(gbs / hbm_peak, 4) if hbm_peak else None,
                            "adds_per_s": add_rate, "alu_frac": round(add_rate / peak_add, 4),
                            "bytes": r[3], "adds": r[4], "dtype": r[5]}
+
+    # per-row kernel times: the launch list is in issue order, rows in turn
+    per_row = {r[0]: {} for r in rows}
+    pos = 0
+    for _ in range(args.steps):
+        for r in rows:
+            cnt = row_launches[r[0]].pop(0)
+            for name, ms in prof[pos:pos + cnt]:
+                per_row[r[0]][name] = per_row[r[0]].get(name, 0.0) + ms / args.steps
+            pos += cnt
+    for r in rows:
+        row_stats[r[0]]["kernels_ms"] = {k: round(v, 4) for k, v in per_row[r[0]].items()}
 
     # per-kernel launch list from libcr's event pairs
     kern = {}

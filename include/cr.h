@@ -191,6 +191,13 @@ void cr_profile_enable(int on);
  * launches were recorded (possibly more than max_records). */
 int cr_profile_collect(int* kernel_ids, float* ms, int max_records);
 
+/* Test hook for the bounded waits: while tile >= 0, the single-pass
+ * iterated_pairwise scan's tile number `tile` (2048 elements each, counted
+ * in start order) does not publish its aggregate, so the tiles that need it
+ * give up waiting and the call's cr_sync_status() reports CR_ERR_TIMEOUT
+ * (the output is then wrong). -1 turns it off. Process-wide. */
+void cr_debug_skip_publish(int64_t tile);
+
 /* Static name of a kernel id returned by cr_profile_collect(). */
 const char* cr_kernel_name(int id);
 
@@ -207,6 +214,18 @@ size_t cr_measure_add_peak_scratch_bytes(void);
 cr_status cr_measure_add_peak(cr_dtype dt, void* scratch_dev, size_t scratch_bytes,
                               void* stream, double* adds_per_second,
                               double* dependent_latency_ns);
+
+/* out[i] = a[i] + b[i] (binary64, round to nearest even) computed by the
+ * integer-pipe add that libcr's fp64 kernels use for part of their adds
+ * (device pointers, n elements, enqueued on `stream`). Exposed so that the
+ * add can be checked bit for bit against the hardware add. */
+cr_status cr_add_pairs_int(const double* a, const double* b, double* out, int64_t n,
+                           void* stream);
+
+/* Throughput of that integer-pipe add over all SMs (adds per second; same
+ * scratch as cr_measure_add_peak). Synchronises the stream. */
+cr_status cr_measure_int_add_rate(void* scratch_dev, size_t scratch_bytes, void* stream,
+                                  double* adds_per_second);
 
 #ifdef __cplusplus
 }

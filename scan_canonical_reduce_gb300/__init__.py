@@ -51,10 +51,13 @@ SIGNATURES = {
     "cr_status_string": (ctypes.c_char_p, [_INT]),
     "cr_version": (_INT, []),
     "cr_launch_count": (ctypes.c_uint64, []),
+    "cr_debug_skip_publish": (None, [_I64]),
     "cr_profile_enable": (None, [_INT]),
     "cr_profile_collect": (_INT, [_P, _P, _INT]),
     "cr_kernel_name": (ctypes.c_char_p, [_INT]),
     "cr_measure_add_peak_scratch_bytes": (_SZ, []),
+    "cr_add_pairs_int": (_INT, [_P, _P, _P, _I64, _P]),
+    "cr_measure_int_add_rate": (_INT, [_P, _SZ, _P, ctypes.POINTER(ctypes.c_double)]),
     "cr_measure_add_peak": (_INT, [_INT, _P, _SZ, _P, ctypes.POINTER(ctypes.c_double),
                                    ctypes.POINTER(ctypes.c_double)]),
 }
@@ -103,6 +106,14 @@ def _stream_ptr(stream) -> int:
     return int(s.cuda_stream)
 
 
+def _resolve(device) -> torch.device:
+    """A CUDA device with an explicit index ('cuda' means the current one)."""
+    d = torch.device(device)
+    if d.type != "cuda":
+        raise ValueError("libcr runs on CUDA devices, got %s" % d)
+    return d if d.index is not None else torch.device("cuda", torch.cuda.current_device())
+
+
 class _Workspace:
     """One growing device workspace per (device, stream); calls on one stream
     are ordered, so they may share it."""
@@ -112,6 +123,7 @@ class _Workspace:
         self._lock = threading.Lock()
 
     def get(self, device: torch.device, stream, nbytes: int) -> torch.Tensor:
+        device = _resolve(device)
         s = torch.cuda.current_stream(device) if stream is None else stream
         key = (device.index, int(s.cuda_stream))
         with self._lock:
@@ -256,7 +268,7 @@ def inclusive_scan_batched(x: torch.Tensor, policy="left_fold", B: int = 1, dim:
 def sync_status(device=None, stream=None) -> None:
     """Synchronise the stream and raise if the last call on its workspace
     reported a device-side timeout."""
-    dev = torch.device("cuda" if device is None else device)
+    dev = _resolve("cuda" if device is None else device)
     sp = _stream_ptr(stream)
     ws = _WS.get(dev, stream, 4096)
     _check(lib().cr_sync_status(ws.data_ptr(), sp), "cr_sync_status")
@@ -296,5 +308,28 @@ def measure_add_peak(dtype=torch.float64, device="cuda", stream=None):
     return rate.value, lat.value
 
 
+def add_pairs_int(a: torch.Tensor, b: torch.Tensor, stream=None) -> torch.Tensor:
+    """Elementwise binary64 a + b through libcr's integer-pipe add."""
+    if a.dtype != torch.float64 or b.dtype != torch.float64 or a.shape != b.shape:
+        raise TypeError("float64 tensors of one shape")
+    a, b = a.contiguous(), b.contiguous()
+    out = torch.empty_like(a)
+    _check(lib().cr_add_pairs_int(a.data_ptr(), b.data_ptr(), out.data_ptr(), a.numel(),
+                                  _stream_ptr(stream)), "cr_add_pairs_int")
+    return out
+
+
+def measure_int_add_rate(device="cuda", stream=None) -> float:
+    """Adds per second of the integer-pipe binary64 add over the GPU."""
+    with torch.cuda.device(torch.device(device)):
+        nb = lib().cr_measure_add_peak_scratch_bytes()
+        scratch = torch.empty(max(int(nb), 256), dtype=torch.uint8, device=device)
+        rate = ctypes.c_double(0)
+        _check(lib().cr_measure_int_add_rate(scratch.data_ptr(), scratch.numel(),
+                                             _stream_ptr(stream), ctypes.byref(rate)),
+               "cr_measure_int_add_rate")
+    return rate.value
+
+
 __all__ = ["reduce", "reduce_batched", "inclusive_scan", "inclusive_scan_batched",
-           "sync_status", "lib", "workspace", "launch_count", "profile_enable", "profile_collect", "measure_add_peak", "CrError", "POLICIES", "SIGNATURES"]
+           "sync_status", "lib", "workspace", "launch_count", "profile_enable", "profile_collect", "measure_add_peak", "add_pairs_int", "measure_int_add_rate", "CrError", "POLICIES", "SIGNATURES"]

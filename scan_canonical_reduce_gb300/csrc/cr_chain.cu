@@ -201,22 +201,29 @@ __device__ __forceinline__ bool in_binade(__int128 A, bool neg, uint32_t fcls) {
   return (fz ? A <= -LO : A <= -LO - 1) && (fz ? A >= -HI + 1 : A >= -HI);
 }
 
-// A rise by d binades: M (old unit) -> RNE((M + q + f) / 2^d) in the new
-// unit, with the in-binade test of the new sum. False if the test fails.
 template <class T>
-__device__ __forceinline__ bool up_step(uint64_t& M, int64_t q, uint32_t fcls, int d, bool neg) {
-  const int64_t A = (int64_t)M + q;   // |M| <= 2^54, |q| < 2^62
-  const int64_t hi = A >> d;          // floor
+__device__ __forceinline__ bool in_binade64(int64_t A, bool neg, bool fz) {
+  constexpr int64_t LO = int64_t(1) << FP<T>::P, HI = int64_t(1) << (FP<T>::P + 1);
+  if (!neg) return A >= LO && A <= HI - 1;
+  return (fz ? A <= -LO : A <= -LO - 1) && (fz ? A >= -HI + 1 : A >= -HI);
+}
+
+// A rise by d binades: M (old unit) -> RNE((M + q + f) / 2^d) in the new
+// unit. s / u_new = hi + F with hi = floor(A / 2^d), F = (lo + f) / 2^d;
+// round up when F > 1/2, or F == 1/2 and hi is odd. `ok` records whether the
+// new sum really lies in the predicted binade and sign (kept off the path
+// that computes M, which the walk's next step depends on).
+template <class T>
+__device__ __forceinline__ uint64_t up_step(uint64_t M, int64_t q, uint32_t fcls, int d,
+                                            bool neg, bool& ok) {
+  const int64_t A = (int64_t)M + q;  // |M| <= 2^54, |q| < 2^62
+  const int64_t hi = A >> d;         // floor
   const uint64_t lo = (uint64_t)A & ((uint64_t(1) << d) - 1);
   const uint64_t half = uint64_t(1) << (d - 1);
-  uint32_t f2;
-  if (lo == 0 && fcls == kFZero) f2 = kFZero;
-  else if (lo < half) f2 = kFLow;
-  else if (lo == half && fcls == kFZero) f2 = kFHalf;
-  else f2 = kFHigh;
-  if (!in_binade<T>(hi, neg, f2)) return false;
-  M = (uint64_t)(hi + (int64_t)delta(f2, (uint64_t)hi & 1));
-  return true;
+  const bool fpos = fcls != kFZero;
+  const bool rup = lo > half || (lo == half && (fpos || (hi & 1)));
+  ok = ok && in_binade64<T>(hi, neg, lo == 0 && !fpos);
+  return (uint64_t)(hi + (rup ? 1 : 0));
 }
 
 // ---------------------------------------------------------------- pass 1
@@ -408,6 +415,7 @@ struct SegRec {
   int64_t start;
   Map map;
   int64_t q;        // up: T split in the old unit
+  double tval;      // start or fp break: T at the start step (exact in double)
   uint32_t meta;    // meta word of the start step (type kMap marks a continuation)
   int32_t e_prev;   // fp break: binade of the previous step (if certain)
   int32_t prev_certain;
@@ -444,8 +452,8 @@ __device__ __forceinline__ void thread_scan(const int64_t* qv, const uint32_t* m
 
 template <class T>
 __global__ void __launch_bounds__(kCT) chain_segments_kernel(
-    const int64_t* qv, const uint32_t* meta, int64_t K, const int64_t* seg_base, SegRec* segs,
-    int64_t seg_cap, int* fail) {
+    const T* src, const int64_t* qv, const uint32_t* meta, int64_t K, const int64_t* seg_base,
+    SegRec* segs, int64_t seg_cap, int* fail) {
   __shared__ Summ sh[kCT];
   const int t = threadIdx.x;
   const int64_t tile0 = (int64_t)blockIdx.x * kCTile;
@@ -486,6 +494,7 @@ __global__ void __launch_bounds__(kCT) chain_segments_kernel(
         r.start = k;
         r.meta = m;
         r.q = qv[k];
+        r.tval = (double)src[k];
         const uint32_t pm = meta[k > 0 ? k - 1 : 0];
         r.e_prev = m_e(pm);
         r.prev_certain = (k > 0 && m_certain(pm)) ? 1 : 0;
@@ -516,7 +525,6 @@ __global__ void __launch_bounds__(32) chain_walk_kernel(const T* src, T* dst, co
                                                         int64_t seg_cap, int64_t* m_in,
                                                         int* fail) {
   __shared__ SegRec buf[2][32];
-  __shared__ T tval[2][32];
   const int lane = threadIdx.x;
   const int64_t nseg = *nseg_total;
   if (*fail || nseg > seg_cap) {
@@ -524,55 +532,44 @@ __global__ void __launch_bounds__(32) chain_walk_kernel(const T* src, T* dst, co
     return;
   }
   SegRec nr{};
-  T nt = T(0);
-  if (lane < nseg) {
-    nr = segs[lane];
-    nt = src[nr.start];
-  }
+  if (lane < nseg) nr = segs[lane];
   uint64_t M = 0;
   T C = T(0);
   bool cval = false;  // C holds the current chain value
-  int ecur = 0;       // binade of M's unit
   bool bad = false;
   for (int64_t b0 = 0, it = 0; b0 < nseg; b0 += 32, ++it) {
     const int slot = (int)(it & 1);
     buf[slot][lane] = nr;  // loaded one batch ago
-    tval[slot][lane] = nt;
     __syncwarp();
     const int64_t nb = b0 + 32 + lane;
-    if (nb < nseg) {
-      nr = segs[nb];
-      nt = src[nr.start];
-    }
-    if (lane == 0 && !bad) {
+    if (nb < nseg) nr = segs[nb];
+    if (lane == 0) {
       const int cnt = (int)(nseg - b0 < 32 ? nseg - b0 : 32);
+      bool ok = true;
       for (int j = 0; j < cnt; ++j) {
         const SegRec& r = buf[slot][j];
         const uint32_t m = r.meta;
         const uint32_t type = m_type(m);
-        const int e = m_e(m);
-        if (type == kStart || type == kFp) {  // the real add
+        if (type == kUp) {  // the common break: integers only
+          M = up_step<T>(M, r.q, m_fcls(m), m_d(m), m_neg(m), ok);
+          cval = false;
+        } else if (type != kMap) {  // start or uncertain step: the real add
           if (type == kStart) {
-            C = tval[slot][j];
+            C = (T)r.tval;
           } else {
             if (!cval) {
-              if (!r.prev_certain) { bad = true; break; }
+              ok = ok && r.prev_certain;
               C = m_to_value<T>((int64_t)M, r.e_prev);
             }
-            C = add_rn(C, tval[slot][j]);
+            C = add_rn(C, (T)r.tval);
           }
           dst[r.start] = C;
           cval = true;
           if (m_certain(m)) {
-            int64_t Mi;
-            if (!value_to_m<T>(C, e, Mi)) { bad = true; break; }
+            int64_t Mi = 0;
+            ok = ok && value_to_m<T>(C, m_e(m), Mi);
             M = (uint64_t)Mi;
-            ecur = e;
           }
-        } else if (type == kUp) {
-          if (!up_step<T>(M, r.q, m_fcls(m), m_d(m), m_neg(m))) { bad = true; break; }
-          ecur = e;
-          cval = false;
         }
         m_in[b0 + j] = (int64_t)M;
         if (r.nsteps > 0) {
@@ -580,7 +577,7 @@ __global__ void __launch_bounds__(32) chain_walk_kernel(const T* src, T* dst, co
           cval = false;
         }
       }
-      (void)ecur;
+      bad = bad || !ok;
     }
     __syncwarp();
   }
@@ -696,8 +693,8 @@ cudaError_t run_chain(const ChainPlan& p, const T* src, T* dst, char* ws, cudaSt
   CR_LAUNCH(kKChainOffsets, s,
             exclusive_scan_1block<int64_t><<<1, 1024, 0, s>>>(nseg, segbase, p.ntiles, total));
   CR_LAUNCH(kKChainSegments, s,
-            chain_segments_kernel<T><<<g, kCT, 0, s>>>(qv, meta, p.K, segbase, segs, p.seg_cap,
-                                                       fail));
+            chain_segments_kernel<T><<<g, kCT, 0, s>>>(src, qv, meta, p.K, segbase, segs,
+                                                       p.seg_cap, fail));
   CR_LAUNCH(kKChainWalk, s,
             chain_walk_kernel<T><<<1, 32, 0, s>>>(src, dst, segs, total, p.seg_cap, m_in, fail));
   CR_LAUNCH(kKChainFill, s,

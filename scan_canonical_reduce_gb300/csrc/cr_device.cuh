@@ -23,6 +23,60 @@ __device__ __forceinline__ float add_rn(float a, float b) { return __fadd_rn(a, 
 template <class T>
 __device__ __forceinline__ T ldg(const T* p) { return __ldg(p); }
 
+// Binary64 addition, round to nearest even, evaluated on the integer pipes
+// (written from the IEEE-754 definition of the operation). GB300 executes
+// only about 1.7 fp64 adds per clock per SM while its integer pipes idle in
+// the fp64 kernels; this add was measured as a second add unit: alone it
+// runs at half the FP64 pipe's rate, and mixed into the fp64-bound loops it
+// cost more issue slots, registers and divergence than it added, so the
+// kernels do not use it (it is exposed through cr_add_pairs_int). Operands are
+// ordered by magnitude, the smaller significand is aligned with 9 guard bits
+// and a sticky bit, added or subtracted, normalised and rounded to nearest
+// even. Zero, subnormal, infinite or NaN operands and results that would be
+// subnormal or overflow take the hardware add, so every input gives exactly
+// the IEEE result.
+__device__ __forceinline__ double add_rn_int(double a, double b) {
+  constexpr uint64_t kAbs = 0x7FFFFFFFFFFFFFFFull, kFrac = 0x000FFFFFFFFFFFFFull;
+  constexpr uint64_t kHid = 0x0010000000000000ull;
+  uint64_t ua = (uint64_t)__double_as_longlong(a), ub = (uint64_t)__double_as_longlong(b);
+  uint64_t xa = ua & kAbs, xb = ub & kAbs;
+  if (xb > xa) {  // |a| >= |b| from here on
+    const uint64_t t = ua; ua = ub; ub = t;
+    const uint64_t tx = xa; xa = xb; xb = tx;
+  }
+  const int ea = (int)(xa >> 52), eb = (int)(xb >> 52);
+  if (ea == 0x7FF || eb == 0) return __dadd_rn(a, b);  // inf/nan, zero or subnormal
+  const uint64_t A = ((xa & kFrac) | kHid) << 9;        // leading one at bit 61
+  const uint64_t Bv = ((xb & kFrac) | kHid) << 9;
+  const int d = ea - eb;
+  uint64_t Bs;
+  if (d == 0) Bs = Bv;
+  else if (d < 63) Bs = (Bv >> d) | ((Bv << (64 - d)) != 0 ? 1u : 0u);
+  else Bs = 1;  // everything below the guard bits: sticky only
+  uint64_t S = ((ua ^ ub) >> 63) ? A - Bs : A + Bs;
+  int e = ea;
+  if (S >> 62) {  // carry out of the addition
+    S = (S >> 1) | (S & 1);
+    e += 1;
+  } else if (!(S >> 61)) {  // cancellation
+    if (S == 0) return 0.0;  // x + (-x) = +0 under round to nearest
+    const int sh = __clzll((long long)S) - 2;
+    S <<= sh;
+    e -= sh;
+    if (e <= 0) return __dadd_rn(a, b);  // subnormal result
+  }
+  const uint64_t low = S & 0x1FF;
+  S >>= 9;
+  if (low > 0x100 || (low == 0x100 && (S & 1))) S += 1;
+  if (S >> 53) {
+    S >>= 1;
+    e += 1;
+  }
+  if (e >= 0x7FF) return __dadd_rn(a, b);  // overflow
+  return __longlong_as_double(
+      (long long)((ua & ~kAbs) | ((uint64_t)e << 52) | (S & kFrac)));
+}
+
 // Perfect tree over U (a power of two) register values, operands in index
 // order: ((v0 op v1) op (v2 op v3)) op ...
 template <class T, int U>

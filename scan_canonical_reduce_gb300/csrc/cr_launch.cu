@@ -40,7 +40,8 @@ const char* kernel_name(int id) {
       "scan_down_kernel",      "carry_chain_kernel",    "scan_seq_kernel",
       "chain_tile_sum_kernel", "chain_offsets_kernel",  "chain_prefix_kernel",
       "chain_classify_kernel", "chain_segments_kernel", "chain_walk_kernel",
-      "chain_fill_kernel",     "chain_fallback_kernel"};
+      "chain_fill_kernel",     "chain_fallback_kernel", "scan_onepass_kernel",
+      "scan_local_kernel",     "carry_fixup_kernel"};
   return (id >= 0 && id < kKernelCount) ? names[id] : "unknown";
 }
 

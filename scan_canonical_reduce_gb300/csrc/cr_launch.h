@@ -25,6 +25,9 @@ enum KernelId : int {
   kKChainWalk,
   kKChainFill,
   kKChainFallback,
+  kKScanOnePass,
+  kKScanLocal,
+  kKCarryFixup,
   kKernelCount
 };
 

@@ -27,6 +27,7 @@
 // adjacent in memory) run one thread per sequence with a register
 // shift-reduce stack.
 #include <algorithm>
+#include <atomic>
 #include <vector>
 
 #include "cr_device.cuh"
@@ -95,17 +96,82 @@ __device__ __forceinline__ void local_scan(const T (&v)[E], T (&w)[E], T (&agg)[
   }
 }
 
+// w[e] = nd op w[e] for the thread's elements (nd is the left operand).
+template <class T>
+__device__ __forceinline__ void apply_node(T nd, T (&w)[kE]) {
+#pragma unroll
+  for (int e = 0; e < kE; ++e) w[e] = add_rn(nd, w[e]);
+}
+
+// A thread's 8 consecutive elements: 16-byte vector accesses when the
+// address allows it (the common case), else scalar ones; tails are bounded.
+template <class T>
+__device__ __forceinline__ void load8(const T* p, int64_t cnt, T (&v)[kE]) {
+  if (cnt == kE && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
+    if (sizeof(T) == 8) {
+      const double2* q = reinterpret_cast<const double2*>(p);
+#pragma unroll
+      for (int k = 0; k < kE / 2; ++k) {
+        const double2 d = q[k];
+        v[2 * k] = (T)d.x;
+        v[2 * k + 1] = (T)d.y;
+      }
+    } else {
+      const float4* q = reinterpret_cast<const float4*>(p);
+#pragma unroll
+      for (int k = 0; k < kE / 4; ++k) {
+        const float4 d = q[k];
+        v[4 * k] = (T)d.x; v[4 * k + 1] = (T)d.y; v[4 * k + 2] = (T)d.z; v[4 * k + 3] = (T)d.w;
+      }
+    }
+    return;
+  }
+#pragma unroll
+  for (int e = 0; e < kE; ++e) v[e] = (e < cnt) ? p[e] : T(0);
+}
+template <class T>
+__device__ __forceinline__ void store8(T* p, int64_t cnt, const T (&v)[kE]) {
+  if (cnt == kE && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
+    if (sizeof(T) == 8) {
+      double2* q = reinterpret_cast<double2*>(p);
+#pragma unroll
+      for (int k = 0; k < kE / 2; ++k) q[k] = make_double2((double)v[2 * k], (double)v[2 * k + 1]);
+    } else {
+      float4* q = reinterpret_cast<float4*>(p);
+#pragma unroll
+      for (int k = 0; k < kE / 4; ++k)
+        q[k] = make_float4((float)v[4 * k], (float)v[4 * k + 1], (float)v[4 * k + 2],
+                           (float)v[4 * k + 3]);
+    }
+    return;
+  }
+  for (int e = 0; e < cnt; ++e) p[e] = v[e];
+}
+
 // In-block pyramid over the 256 thread aggregates, all levels kept:
 // level p (p = 0..8) holds 256 >> p nodes at lvl[lvl_base(p) + q].
 __device__ __forceinline__ int lvl_base(int p) {
   return 2 * kScanThreads - ((2 * kScanThreads) >> p);
 }
 
+// Levels 1-5 of a warp's nodes depend only on that warp's threads, so they
+// are built with warp barriers; levels 6-8 combine warps.
 template <class T>
-__device__ __forceinline__ void build_tile_pyramid(T* lvl, int t, int full_threads) {
+__device__ __forceinline__ void build_tile_pyramid(T* lvl, int t, int full_threads,
+                                                   int top = 8) {
+  const int lane = t & 31, wp = t >> 5;
+  __syncwarp();
+  for (int p = 1; p <= (top < 5 ? top : 5); ++p) {
+    const int per = 32 >> p;  // level-p nodes per warp
+    const int q = wp * per + lane;
+    if (lane < per && q < (full_threads >> p))  // complete nodes only
+      lvl[lvl_base(p) + q] =
+          add_rn(lvl[lvl_base(p - 1) + 2 * q], lvl[lvl_base(p - 1) + 2 * q + 1]);
+    __syncwarp();
+  }
   __syncthreads();
-  for (int p = 1; p <= 8; ++p) {
-    const int c = full_threads >> p;  // complete nodes only
+  for (int p = 6; p <= top; ++p) {
+    const int c = full_threads >> p;
     if (t < c)
       lvl[lvl_base(p) + t] =
           add_rn(lvl[lvl_base(p - 1) + 2 * t], lvl[lvl_base(p - 1) + 2 * t + 1]);
@@ -200,13 +266,7 @@ scan_down_kernel(const T* x, T* out, const T* __restrict__ pyr, const T* __restr
   }
 
   T v[kE];
-  if (cnt == kE) {
-#pragma unroll
-    for (int e = 0; e < kE; ++e) v[e] = x[i0 + e];
-  } else {
-#pragma unroll
-    for (int e = 0; e < kE; ++e) v[e] = (e < cnt) ? x[i0 + e] : T(0);
-  }
+  load8(x + i0, cnt, v);
   T w[kE], agg[NS];
   local_scan<T, kE, S>(v, w, agg);
   T tagg;
@@ -226,16 +286,14 @@ scan_down_kernel(const T* x, T* out, const T* __restrict__ pyr, const T* __restr
   for (int p = 0; p < thread_bits; ++p) {
     if ((t >> p) & 1) {
       const T nd = lvl[lvl_base(p) + (t >> p) - 1];
-#pragma unroll
-      for (int e = 0; e < kE; ++e) w[e] = add_rn(nd, w[e]);
+      apply_node(nd, w);
     }
   }
   // tile-level prefix nodes, lowest bit first
   for (int p = 0; p < tile_bits; ++p) {
     if ((b >> p) & 1) {
       const T nd = tile_nodes[p];
-#pragma unroll
-      for (int e = 0; e < kE; ++e) w[e] = add_rn(nd, w[e]);
+      apply_node(nd, w);
     }
   }
   // block carry: out[i] = C_{k-1} op P(i) for blocks k >= 1
@@ -254,11 +312,144 @@ scan_down_kernel(const T* x, T* out, const T* __restrict__ pyr, const T* __restr
       }
     }
   }
-  if (cnt == kE) {
+  store8(out + i0, cnt, w);
+}
+
+// ------------------------------------------- iterated_pairwise, one pass
+// Tiles take indices in the order they start (a counter), publish their
+// aggregate, climb the node pyramid by arrival tickets (the second of two
+// siblings to arrive computes the parent, left op right, and publishes it
+// with a ready flag), and only then wait for the nodes of earlier tiles that
+// their own prefix needs. Every wait is on tiles that started earlier and
+// never wait before publishing, so the waits end; each is still bounded and,
+// if it gives up, records CR_ERR_TIMEOUT in the workspace status word.
+template <class T>
+__global__ void __launch_bounds__(kScanThreads)
+scan_onepass_kernel(const T* x, T* out, T* pyr, int* counters, int* ready, int* tile_ctr,
+                    int* status, ScanArgs a, int64_t skip_publish) {
+  __shared__ T lvl[2 * kScanThreads];
+  __shared__ T tile_nodes[64];
+  __shared__ int64_t s_tile;
+  const int t = threadIdx.x;
+  if (t == 0) s_tile = atomicAdd(tile_ctr, 1);
+  __syncthreads();
+  const int64_t b = s_tile;
+  const int64_t i0 = b * kTile + (int64_t)t * kE;
+  const int64_t cnt = imax(0, imin(kE, a.n - i0));
+  const int full_threads = (int)imin(kScanThreads, (a.n - b * kTile) / kE);
+
+  T v[kE];
+  load8(x + i0, cnt, v);
+  T w[kE], agg[1];
+  local_scan<T, kE, kE>(v, w, agg);
+  if (t < full_threads) lvl[t] = agg[0];
+  build_tile_pyramid(lvl, t, full_threads);
+
+  // publish this tile's aggregate, then climb as long as we arrive second
+  if (t == 0 && b < a.full_tiles && a.pyr_levels > 0 && b != skip_publish) {
+    T node = lvl[lvl_base(8)];
+    pyr[a.pyr_off[0] + b] = node;
+    __threadfence();
+    atomicExch(ready + a.pyr_off[0] + b, 1);
+    int64_t q = b;
+    for (int p = 1; p < a.pyr_levels; ++p) {
+      const int64_t parent = q >> 1;
+      if (parent >= (a.full_tiles >> p)) break;
+      const int ticket = atomicAdd(counters + a.cnt_off[p] + parent, 1);
+      if (ticket == 0) break;
+      __threadfence();
+      const T left = __ldcg(pyr + a.pyr_off[p - 1] + 2 * parent);
+      const T right = __ldcg(pyr + a.pyr_off[p - 1] + 2 * parent + 1);
+      node = add_rn(left, right);
+      pyr[a.pyr_off[p] + parent] = node;
+      __threadfence();
+      atomicExch(ready + a.pyr_off[p] + parent, 1);
+      q = parent;
+    }
+  }
+
+  // thread-level prefix nodes (all bits of t), lowest first
+  for (int p = 0; p < 8; ++p) {
+    if (((t >> p) & 1) && cnt > 0) apply_node(lvl[lvl_base(p) + (t >> p) - 1], w);
+  }
+  // wait for the tile-level nodes this tile needs (bits of b)
+  const int tile_bits = a.pyr_levels;
+  if (t < tile_bits && ((b >> t) & 1)) {
+    const int64_t q = (b >> t) - 1;
+    const volatile int* f = ready + a.pyr_off[t] + q;
+    uint32_t spins = 0;
+    while (*f == 0) {
+      if (++spins > kSpinLimit) {
+        raise_status(status, CR_ERR_TIMEOUT);
+        break;
+      }
+      __nanosleep(64);
+    }
+    __threadfence();
+    tile_nodes[t] = __ldcg(pyr + a.pyr_off[t] + q);
+  }
+  __syncthreads();
+  if (cnt == 0) return;
+  for (int p = 0; p < tile_bits; ++p) {
+    if ((b >> p) & 1) apply_node(tile_nodes[p], w);
+  }
+  store8(out + i0, cnt, w);
+}
+
+// ------------------------------- block_dyadic, blocks inside a tile (B <= 2048)
+// Pass 1: the in-block iterated_pairwise values P(i) and the block totals T_k.
+template <class T, int S>
+__global__ void __launch_bounds__(kScanThreads)
+scan_local_kernel(const T* x, T* out, T* __restrict__ totals, ScanArgs a) {
+  __shared__ T lvl[2 * kScanThreads];
+  constexpr int NS = kE / S;
+  constexpr int LS = Log2<S>::value;
+  const int t = threadIdx.x;
+  const int64_t b = blockIdx.x;
+  const int64_t i0 = b * kTile + (int64_t)t * kE;
+  const int64_t cnt = imax(0, imin(kE, a.n - i0));
+  const int full_threads = (int)imin(kScanThreads, (a.n - b * kTile) / kE);
+  T v[kE];
+  load8(x + i0, cnt, v);
+  T w[kE], agg[NS];
+  local_scan<T, kE, S>(v, w, agg);
+  if (a.totals_level == 0) {  // blocks inside a thread
 #pragma unroll
-    for (int e = 0; e < kE; ++e) out[i0 + e] = w[e];
-  } else {
-    for (int e = 0; e < cnt; ++e) out[i0 + e] = w[e];
+    for (int s = 0; s < NS; ++s)
+      if ((s + 1) * S <= cnt) totals[(i0 >> LS) + s] = agg[s];
+  }
+  if (a.logB > kLogE) {  // blocks span threads: build the tile pyramid
+    T tagg = agg[0];
+    if (t < full_threads) lvl[t] = tagg;
+    build_tile_pyramid(lvl, t, full_threads, a.logB - kLogE);  // levels inside a block
+    const int p = a.logB - kLogE;
+    if (t < (full_threads >> p)) totals[((b * kTile) >> a.logB) + t] = lvl[lvl_base(p) + t];
+    if (cnt > 0) {
+      for (int q = 0; q < p; ++q)
+        if ((t >> q) & 1) apply_node(lvl[lvl_base(q) + (t >> q) - 1], w);
+    }
+  }
+  store8(out + i0, cnt, w);
+}
+
+// Pass 2: out[i] = C_{k-1} op P(i) for every element of blocks k >= 1.
+template <class T>
+__global__ void __launch_bounds__(256)
+carry_fixup_kernel(T* out, const T* __restrict__ carries, int64_t n, int logB) {
+  const int64_t i0 = (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * kE) + ((int64_t)1 << logB);
+  if (i0 >= n) return;
+  if (i0 + kE <= n && logB >= kLogE) {  // one block for all 8 elements
+    const T c = ldg(carries + (i0 >> logB) - 1);
+    T v[kE];
+    load8(out + i0, kE, v);
+#pragma unroll
+    for (int e = 0; e < kE; ++e) v[e] = add_rn(c, v[e]);
+    store8(out + i0, kE, v);
+    return;
+  }
+  for (int e = 0; e < kE && i0 + e < n; ++e) {
+    const int64_t i = i0 + e;
+    out[i] = add_rn(ldg(carries + (i >> logB) - 1), out[i]);
   }
 }
 
@@ -341,6 +532,12 @@ scan_seq_kernel(const T* x, T* out, int64_t batch, int64_t n, int64_t es, int64_
 }
 
 // ---------------------------------------------------------------- planning
+namespace {
+std::atomic<int64_t> g_skip_publish{-1};
+}
+int64_t debug_skip_publish() { return g_skip_publish.load(); }
+void set_debug_skip_publish(int64_t tile) { g_skip_publish.store(tile); }
+
 bool scan_args_ok(cr_policy p, int64_t B) {
   switch (p) {
     case CR_LEFT_FOLD:
@@ -406,9 +603,13 @@ ScanPlan plan_scan(int64_t batch, int64_t n, cr_policy p, int64_t B, size_t esiz
   plan.logB = logB;
   plan.n_tiles = (n + kTile - 1) / kTile;
   plan.full_tiles = n / kTile;
-  // global pyramid levels: every level inside a block that has a complete node
+  if (!block) plan.mode = ScanPlan::kOnePass;
+  else if (logB <= kLogTile) plan.mode = ScanPlan::kLocalFixup;
+  else plan.mode = ScanPlan::kUpDown;
+  // global node pyramid over complete tiles (one pass, up/down): level l has
+  // full_tiles >> l nodes; up/down keeps only the levels inside a block
   int levels = 0;
-  if (plan.full_tiles >= 1) {
+  if (plan.mode != ScanPlan::kLocalFixup && plan.full_tiles >= 1) {
     levels = ilog2(plan.full_tiles) + 1;
     if (block) levels = std::min(levels, std::max(0, logB - kLogTile + 1));
   }
@@ -422,16 +623,24 @@ ScanPlan plan_scan(int64_t batch, int64_t n, cr_policy p, int64_t B, size_t esiz
   }
   plan.pyr_ws = off;
   off += round256((size_t)pyr_elems * esize);
+  // arrival counters, ready flags (one pass) and the tile counter: one
+  // region cleared by a single memset per call
+  plan.zero_ws = off;
   plan.cnt_ws = off;
   plan.cnt_bytes = (size_t)cnt_elems * sizeof(int);
   off += round256(plan.cnt_bytes);
+  if (plan.mode == ScanPlan::kOnePass) {
+    plan.ready_ws = off;
+    off += round256((size_t)pyr_elems * sizeof(int));
+    plan.tilectr_ws = off;
+    off += 256;
+  }
+  plan.zero_bytes = off - plan.zero_ws;
   if (block) {
     plan.K = (n + B - 1) / B;
-    // totals: inside a thread (level 0 flag), inside a tile (pyramid level p),
-    // or spanning tiles (a level of the global pyramid)
-    if (logB <= kLogE) plan.totals_level = 0;
-    else if (logB < kLogTile + 0) plan.totals_level = logB - kLogE;
-    else plan.totals_level = -1;  // read from the global pyramid
+    if (logB <= kLogE) plan.totals_level = 0;            // inside a thread
+    else if (logB <= kLogTile) plan.totals_level = logB - kLogE;  // tile pyramid level
+    else plan.totals_level = -1;                         // global pyramid level
     plan.totals_ws = off;
     off += round256((size_t)plan.K * esize);
     plan.carries_ws = off;
@@ -502,35 +711,60 @@ cudaError_t run_scan(const ScanPlan& plan, const T* x, T* out, int64_t es, int64
   int* counters = reinterpret_cast<int*>(ws + plan.cnt_ws);
   T* totals = block ? reinterpret_cast<T*>(ws + plan.totals_ws) : nullptr;
   T* carries = block ? reinterpret_cast<T*>(ws + plan.carries_ws) : nullptr;
-  if (plan.cnt_bytes > 0) {
-    if ((e = cudaMemsetAsync(counters, 0, plan.cnt_bytes, s)) != cudaSuccess) return e;
+  if (plan.zero_bytes > 0) {
+    if ((e = cudaMemsetAsync(ws + plan.zero_ws, 0, plan.zero_bytes, s)) != cudaSuccess) return e;
   }
   if (plan.n_tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  const int S = block ? (int)(plan.B < kE ? plan.B : kE) : kE;
   const unsigned grid = (unsigned)plan.n_tiles;
-  const bool up_needed = plan.pyr_levels > 0 || (block && plan.totals_level >= 0);
-  if (up_needed) {
-    CR_LAUNCH(kKScanUp, s, {
-      if (S == 8) scan_up_kernel<T, 8><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
-      else if (S == 4) scan_up_kernel<T, 4><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
-      else scan_up_kernel<T, 2><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
+  const int S = block ? (int)(plan.B < kE ? plan.B : kE) : kE;
+
+  if (plan.mode == ScanPlan::kOnePass) {
+    int* ready = reinterpret_cast<int*>(ws + plan.ready_ws);
+    int* tctr = reinterpret_cast<int*>(ws + plan.tilectr_ws);
+    int* status = reinterpret_cast<int*>(ws);
+    CR_LAUNCH(kKScanOnePass, s,
+              scan_onepass_kernel<T><<<grid, kScanThreads, 0, s>>>(
+                  x, out, pyr, counters, ready, tctr, status, a, debug_skip_publish()));
+    return cudaGetLastError();
+  }
+
+  // block carries: C_0..C_{K-2} from the block totals
+  auto chain = [&](const T* src) -> cudaError_t {
+    if (plan.K < 2) return cudaSuccess;
+    if (plan.parallel_chain) return run_chain<T>(plan.chain, src, carries, ws + plan.chain_ws, s);
+    CR_LAUNCH(kKCarryChain, s, carry_chain_kernel<T><<<1, 32, 0, s>>>(src, carries, plan.K - 1));
+    return cudaGetLastError();
+  };
+
+  if (plan.mode == ScanPlan::kLocalFixup) {
+    CR_LAUNCH(kKScanLocal, s, {
+      if (S == 8) scan_local_kernel<T, 8><<<grid, kScanThreads, 0, s>>>(x, out, totals, a);
+      else if (S == 4) scan_local_kernel<T, 4><<<grid, kScanThreads, 0, s>>>(x, out, totals, a);
+      else scan_local_kernel<T, 2><<<grid, kScanThreads, 0, s>>>(x, out, totals, a);
     });
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  if (block && plan.K >= 2) {
-    // blocks 1..K-1 need C_0..C_{K-2}; those blocks are all complete
-    const T* src = (plan.totals_level >= 0)
-                       ? totals
-                       : pyr + plan.pyr_off[plan.logB - kLogTile];
-    if (plan.parallel_chain) {
-      e = run_chain<T>(plan.chain, src, carries, ws + plan.chain_ws, s);
-    } else {
-      CR_LAUNCH(kKCarryChain, s,
-                carry_chain_kernel<T><<<1, 32, 0, s>>>(src, carries, plan.K - 1));
+    if ((e = chain(totals)) != cudaSuccess) return e;
+    if (plan.K >= 2) {
+      const int64_t nfix = plan.n - plan.B;  // elements of blocks k >= 1
+      const int64_t threads = (nfix + kE - 1) / kE;
+      const int64_t blocks = (threads + 255) / 256;
+      if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+      CR_LAUNCH(kKCarryFixup, s,
+                carry_fixup_kernel<T><<<(unsigned)blocks, 256, 0, s>>>(out, carries, plan.n,
+                                                                        plan.logB));
       e = cudaGetLastError();
     }
-    if (e != cudaSuccess) return e;
+    return e;
   }
+
+  // up/down: blocks spanning tiles (B > 2048)
+  CR_LAUNCH(kKScanUp, s, {
+    if (S == 8) scan_up_kernel<T, 8><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
+    else if (S == 4) scan_up_kernel<T, 4><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
+    else scan_up_kernel<T, 2><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
+  });
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = chain(pyr + plan.pyr_off[plan.logB - kLogTile])) != cudaSuccess) return e;
   CR_LAUNCH(kKScanDown, s, {
     if (S == 8) scan_down_kernel<T, 8><<<grid, kScanThreads, 0, s>>>(x, out, pyr, carries, a);
     else if (S == 4) scan_down_kernel<T, 4><<<grid, kScanThreads, 0, s>>>(x, out, pyr, carries, a);

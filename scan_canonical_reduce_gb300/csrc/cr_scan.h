@@ -28,6 +28,10 @@ struct ScanArgs {
 
 struct ScanPlan {
   enum Kind { kEmpty, kPerSequence, kChainOnly, kTiled };
+  // tiled 1-D scans: one pass (iterated_pairwise), local scan + carry
+  // fix-up (block_dyadic, B <= 2048), up/down passes (block_dyadic, B > 2048)
+  enum Mode { kOnePass, kLocalFixup, kUpDown };
+  Mode mode = kOnePass;
   bool supported = false;
   Kind kind = kEmpty;
   int64_t batch = 0, n = 0;
@@ -40,6 +44,8 @@ struct ScanPlan {
   int64_t pyr_off[kMaxLevels] = {};
   int64_t cnt_off[kMaxLevels] = {};
   size_t pyr_ws = 0, cnt_ws = 0, cnt_bytes = 0;
+  size_t ready_ws = 0, tilectr_ws = 0;  // one pass: node ready flags, tile counter
+  size_t zero_ws = 0, zero_bytes = 0;   // cleared once per call
   int64_t K = 0;             // blocks (block_dyadic)
   int totals_level = -1;
   size_t totals_ws = 0, carries_ws = 0;
@@ -53,6 +59,12 @@ struct ScanPlan {
 };
 
 bool scan_args_ok(cr_policy p, int64_t B);
+
+// Test hook: the one-pass scan's tile with this index does not publish its
+// aggregate, so the tiles that need it exhaust their bounded waits and report
+// CR_ERR_TIMEOUT (-1 = off).
+int64_t debug_skip_publish();
+void set_debug_skip_publish(int64_t tile);
 ScanPlan plan_scan(int64_t batch, int64_t n, cr_policy p, int64_t B, size_t esize);
 
 template <class T>
