@@ -103,6 +103,37 @@ __device__ __forceinline__ void apply_node(T nd, T (&w)[kE]) {
   for (int e = 0; e < kE; ++e) w[e] = add_rn(nd, w[e]);
 }
 
+// The node of lane-index bit q (q < 5) for every lane of the warp. Only the
+// lanes whose bit q is set need it (8 adds each); done per lane, half of each
+// warp instruction would idle. Instead the lanes pair up across bit q: the
+// lane with the bit does its elements 0-3, its partner does elements 4-7 of
+// it (operands and results travel by shuffles) - the same adds, in the same
+// order, on all 32 lanes. `lvl_node(t_hi)` is the level-q node needed by the
+// pair's lane with the bit set. Every lane of the warp must call this.
+template <class T, class NodeOf>
+__device__ __forceinline__ void apply_lane_bit(int q, int t, NodeOf lvl_node, T (&w)[kE]) {
+  const unsigned full = 0xffffffffu;
+  const int m = 1 << q;
+  const bool hi = (t >> q) & 1;
+  const T nd = lvl_node(t | m);
+  T x[kE / 2];
+#pragma unroll
+  for (int e = 0; e < kE / 2; ++e) {
+    const T other = __shfl_xor_sync(full, w[kE / 2 + e], m);  // partner's upper half
+    x[e] = hi ? w[e] : other;
+  }
+#pragma unroll
+  for (int e = 0; e < kE / 2; ++e) x[e] = add_rn(nd, x[e]);
+#pragma unroll
+  for (int e = 0; e < kE / 2; ++e) {
+    const T back = __shfl_xor_sync(full, x[e], m);  // my upper half, done by the partner
+    if (hi) {
+      w[e] = x[e];
+      w[kE / 2 + e] = back;
+    }
+  }
+}
+
 // A thread's 8 consecutive elements: 16-byte vector accesses when the
 // address allows it (the common case), else scalar ones; tails are bounded.
 template <class T>
@@ -368,8 +399,11 @@ scan_onepass_kernel(const T* x, T* out, T* pyr, int* counters, int* ready, int* 
     }
   }
 
-  // thread-level prefix nodes (all bits of t), lowest first
-  for (int p = 0; p < 8; ++p) {
+  // thread-level prefix nodes (all bits of t), lowest first; lane bits by
+  // pairs of lanes, warp bits (uniform across the warp) directly
+  auto node_of = [&](int p) { return [&, p](int th) { return lvl[lvl_base(p) + (th >> p) - 1]; }; };
+  for (int p = 0; p < 5; ++p) apply_lane_bit(p, t, node_of(p), w);
+  for (int p = 5; p < 8; ++p) {
     if (((t >> p) & 1) && cnt > 0) apply_node(lvl[lvl_base(p) + (t >> p) - 1], w);
   }
   // wait for the tile-level nodes this tile needs (bits of b)
@@ -424,10 +458,10 @@ scan_local_kernel(const T* x, T* out, T* __restrict__ totals, ScanArgs a) {
     build_tile_pyramid(lvl, t, full_threads, a.logB - kLogE);  // levels inside a block
     const int p = a.logB - kLogE;
     if (t < (full_threads >> p)) totals[((b * kTile) >> a.logB) + t] = lvl[lvl_base(p) + t];
-    if (cnt > 0) {
-      for (int q = 0; q < p; ++q)
-        if ((t >> q) & 1) apply_node(lvl[lvl_base(q) + (t >> q) - 1], w);
-    }
+    auto node_of = [&](int q) { return [&, q](int th) { return lvl[lvl_base(q) + (th >> q) - 1]; }; };
+    for (int q = 0; q < p && q < 5; ++q) apply_lane_bit(q, t, node_of(q), w);
+    for (int q = 5; q < p; ++q)
+      if (((t >> q) & 1) && cnt > 0) apply_node(lvl[lvl_base(q) + (t >> q) - 1], w);
   }
   store8(out + i0, cnt, w);
 }
