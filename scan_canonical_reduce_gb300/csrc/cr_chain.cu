@@ -516,15 +516,38 @@ __global__ void __launch_bounds__(kCT) chain_segments_kernel(
 }
 
 // ---------------------------------------------------------------- pass 7
-// Breaks in order, in one thread. Records are staged through shared memory by
-// the whole warp one batch ahead, so the sequential part never waits on
-// global memory.
+// The walk's compact record: everything one break and its segment's map need,
+// in 32 bytes (two 16-byte shared-memory loads).
+struct alignas(16) Hot {
+  int64_t q;        // up: T split in the old unit (0 for a continuation)
+  uint64_t b0, b1;  // the segment map's offsets
+  uint32_t ctrl;    // d (6 bits) | shift (7) << 6 | fpos << 13 | neg << 14 | type << 15 | steps << 17
+  uint32_t idx;     // record index within the batch (unused padding)
+};
+__device__ __forceinline__ Hot make_hot(const SegRec& r) {
+  Hot h;
+  const uint32_t m = r.meta, type = m_type(m);
+  const bool up = type == kUp;
+  h.q = up ? r.q : 0;
+  h.b0 = r.map.b0;
+  h.b1 = r.map.b1;
+  const uint32_t shift = r.map.a == 0 ? 64u : (uint32_t)(__ffsll((long long)r.map.a) - 1);
+  h.ctrl = (up ? (uint32_t)m_d(m) : 0u) | (shift << 6) | ((m_fcls(m) != kFZero) ? 1u << 13 : 0u) |
+           (m_neg(m) ? 1u << 14 : 0u) | (type << 15) | (r.nsteps > 0 ? 1u << 17 : 0u);
+  h.idx = 0;
+  return h;
+}
+
+// Breaks in order, in one thread. The whole warp loads the next 32 records
+// while lane 0 runs the current 32 from shared memory; rises and
+// continuations (nearly all records) take a branch-free integer path.
 template <class T>
 __global__ void __launch_bounds__(32) chain_walk_kernel(const T* src, T* dst, const SegRec* segs,
                                                         const int64_t* nseg_total,
                                                         int64_t seg_cap, int64_t* m_in,
                                                         int* fail) {
-  __shared__ SegRec buf[2][32];
+  __shared__ Hot hot[2][32];
+  __shared__ SegRec cold[2][32];
   const int lane = threadIdx.x;
   const int64_t nseg = *nseg_total;
   if (*fail || nseg > seg_cap) {
@@ -539,21 +562,42 @@ __global__ void __launch_bounds__(32) chain_walk_kernel(const T* src, T* dst, co
   bool bad = false;
   for (int64_t b0 = 0, it = 0; b0 < nseg; b0 += 32, ++it) {
     const int slot = (int)(it & 1);
-    buf[slot][lane] = nr;  // loaded one batch ago
+    hot[slot][lane] = make_hot(nr);  // loaded one batch ago
+    cold[slot][lane] = nr;
     __syncwarp();
     const int64_t nb = b0 + 32 + lane;
     if (nb < nseg) nr = segs[nb];
     if (lane == 0) {
       const int cnt = (int)(nseg - b0 < 32 ? nseg - b0 : 32);
       bool ok = true;
+      uint32_t okw = 1u;
       for (int j = 0; j < cnt; ++j) {
-        const SegRec& r = buf[slot][j];
-        const uint32_t m = r.meta;
-        const uint32_t type = m_type(m);
-        if (type == kUp) {  // the common break: integers only
-          M = up_step<T>(M, r.q, m_fcls(m), m_d(m), m_neg(m), ok);
-          cval = false;
-        } else if (type != kMap) {  // start or uncertain step: the real add
+        const Hot h = hot[slot][j];
+        const uint32_t c = h.ctrl;
+        const uint32_t type = (c >> 15) & 3u;
+        uint64_t M1;
+        if (type <= kUp) {  // kMap (continuation, d = 0) or kUp: branch-free
+          const int d = (int)(c & 63u);
+          const int64_t A = (int64_t)M + h.q;
+          const int64_t hi = A >> d;
+          const uint64_t mask = (uint64_t(1) << d) - 1;  // d = 0: 0
+          const uint64_t lo = (uint64_t)A & mask;
+          const uint64_t half = (mask >> 1) + (d > 0 ? 1u : 0u);  // 2^(d-1); d = 0: 0
+          const uint32_t fpos = (c >> 13) & 1u;
+          const uint32_t gt = lo > half, eq = (lo == half) & (d > 0);
+          const uint32_t rup = gt | (eq & (fpos | (uint32_t)(hi & 1)));
+          M1 = (uint64_t)hi + rup;
+          // in-binade test of a rise, as integer comparisons on hi
+          constexpr int64_t LO = int64_t(1) << FP<T>::P, HI = int64_t(1) << (FP<T>::P + 1);
+          const uint32_t fz = (lo == 0) & (fpos ^ 1u);
+          const uint32_t pos_ok = (hi >= LO) & (hi <= HI - 1);
+          const uint32_t neg_ok = (fz ? (hi <= -LO) & (hi >= -HI + 1) : (hi <= -LO - 1) & (hi >= -HI));
+          const uint32_t in_ok = ((c >> 14) & 1u) ? neg_ok : pos_ok;
+          okw &= (type == kUp) ? in_ok : 1u;
+          cval = cval & (type != kUp);
+        } else {  // start or uncertain step: the real add
+          const SegRec& r = cold[slot][j];
+          const uint32_t m = r.meta;
           if (type == kStart) {
             C = (T)r.tval;
           } else {
@@ -565,19 +609,23 @@ __global__ void __launch_bounds__(32) chain_walk_kernel(const T* src, T* dst, co
           }
           dst[r.start] = C;
           cval = true;
+          M1 = M;
           if (m_certain(m)) {
             int64_t Mi = 0;
             ok = ok && value_to_m<T>(C, m_e(m), Mi);
-            M = (uint64_t)Mi;
+            M1 = (uint64_t)Mi;
           }
         }
-        m_in[b0 + j] = (int64_t)M;
-        if (r.nsteps > 0) {
-          M = apply(r.map, M);
-          cval = false;
-        }
+        m_in[b0 + j] = (int64_t)M1;
+        // the segment's composed map (identity when it has no steps)
+        const uint32_t steps = (c >> 17) & 1u;
+        const uint32_t sh = (c >> 6) & 127u;
+        const uint64_t aM = sh >= 64 ? 0 : (M1 << sh);
+        const uint64_t mapped = aM + ((M1 & 1) ? h.b1 : h.b0);
+        M = steps ? mapped : M1;
+        cval = cval & !steps;
       }
-      bad = bad || !ok;
+      bad = bad || !ok || !okw;
     }
     __syncwarp();
   }
