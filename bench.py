@@ -330,15 +330,52 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "note": "fallback"}
 
 
+# DRAM bytes per launch from ncu captures (profiles/), scaled from the captured
+# size to the benchmark's n = 2^28 by elements processed (traffic grows in
+# proportion); None when the kernel changed after the capture.
+NCU_TRAFFIC = {
+    # profiles/scan_onepass_kernel_iterated_pairwise_n2e25.md: 269.18 MB read +
+    # 218.79 MB written at n = 2^25, x 8
+    "scan_onepass_kernel": (269.18e6 + 218.79e6) * 8,
+    # profiles/lane_pass_kernel_reduce_f64_L16_n2e25.md: level-0 pass, x 8
+    "lane_pass_kernel": (268.48e6 + 4.03e6) * 8,
+}
+
+
 def dominant_roofline(kernels, prof, row_stats, dadd_rate, dadd_lat, hbm_peak, steps):
-    """Roofline of the kernel with the largest share of device time."""
+    """Roofline of the kernel with the largest share of device time:
+    achieved = algorithmic work per launch / its average launch duration
+    (CUDA events recorded by libcr around each launch in the timed region)."""
     if not kernels:
         return None
     top = next(iter(kernels))
     launches = kernels[top]["launches"]
     avg_ms = kernels[top]["ms_total"] / max(1, launches)
+    if top == "scan_onepass_kernel":
+        # one launch = the whole iterated_pairwise scan of n = 2^28 fp64
+        adds = row_stats["scan_iterated_pairwise"]["adds"]
+        nbytes = row_stats["scan_iterated_pairwise"]["bytes"]
+        achieved = adds / (avg_ms * 1e-3)
+        return {"kernel": top, "bound": "alu", "achieved": achieved, "peak": dadd_rate,
+                "unit": "fp64 adds/s", "frac": round(achieved / dadd_rate, 4),
+                "traffic": NCU_TRAFFIC.get(top),
+                "work_per_launch": {"adds": adds, "bytes": nbytes},
+                "hbm": {"achieved_gbs": round(nbytes / (avg_ms * 1e-3) / 1e9, 1),
+                        "peak_gbs": hbm_peak,
+                        "frac": round(nbytes / (avg_ms * 1e-3) / 1e9 / hbm_peak, 4)},
+                "note": "peak = fp64 adds/s measured live by libcr's calibration kernel "
+                        "(independent round-to-nearest adds on all SMs); traffic from an "
+                        "ncu capture at n = 2^25 scaled by 8"}
+    if top == "lane_pass_kernel":
+        r = row_stats["reduce_f64_L16"]
+        achieved = r["bytes"] / (r["ms"] * 1e-3) / 1e9
+        return {"kernel": top, "bound": "alu", "achieved": r["adds"] / (r["ms"] * 1e-3),
+                "peak": dadd_rate, "unit": "fp64 adds/s",
+                "frac": round(r["adds"] / (r["ms"] * 1e-3) / dadd_rate, 4),
+                "traffic": NCU_TRAFFIC.get(top),
+                "hbm": {"achieved_gbs": round(achieved, 1), "peak_gbs": hbm_peak,
+                        "frac": round(achieved / hbm_peak, 4)}}
     if top == "carry_chain_kernel":
-        # the serial chain of block_dyadic<16>: bound by dependent-add latency
         K = N // 16 - 1
         chains = [ms for nm, ms in prof if nm == top]
         ms = max(chains) if chains else avg_ms
@@ -346,19 +383,7 @@ def dominant_roofline(kernels, prof, row_stats, dadd_rate, dadd_lat, hbm_peak, s
         peak = 1e9 / dadd_lat
         return {"kernel": top, "bound": "alu", "achieved": achieved, "peak": peak,
                 "unit": "dependent adds/s", "frac": round(achieved / peak, 4),
-                "traffic": None, "note": "serial carry chain of block_dyadic<16>, "
-                                         "K = 2^24 - 1 dependent fp64 adds; peak = 1 / "
-                                         "measured dependent-add latency"}
-    if top == "scan_down_kernel":
-        r = row_stats["scan_iterated_pairwise"]
-        achieved = r["adds"] / (r["ms"] * 1e-3)
-        return {"kernel": top, "bound": "alu", "achieved": achieved, "peak": dadd_rate,
-                "unit": "fp64 adds/s", "frac": round(achieved / dadd_rate, 4), "traffic": None}
-    if top == "lane_pass_kernel":
-        r = row_stats["reduce_f64_L16"]
-        achieved = r["bytes"] / (r["ms"] * 1e-3) / 1e9
-        return {"kernel": top, "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
-                "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": None}
+                "traffic": None}
     return {"kernel": top, "bound": "alu", "achieved": None, "peak": dadd_rate,
             "unit": "fp64 adds/s", "frac": None, "traffic": None}
 
