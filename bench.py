@@ -67,6 +67,20 @@ def adds_block_dyadic(n: int, B: int) -> int:
     return a + max(0, n - B) + max(0, -(-n // B) - 2)  # carries applied + chain
 
 
+def adds_pairwise(n: int) -> int:
+    """Adds of a pairwise scan: every complete aligned node (n - popcount(n))
+    plus one left-nested combination per prefix length that is not a power
+    of two."""
+    return (n - bin(n).count("1")) + (n - n.bit_length())
+
+
+def extra_rows():
+    """Rows beyond the headline step (the next policies), timed on their own
+    after it and reported under "extras"; not part of value."""
+    return [("scan_pairwise", "scan", {"policy": "pairwise", "B": 1}, 16 * N,
+             adds_pairwise(N), "f64")]
+
+
 def rows_spec():
     """(name, kind, params, algorithmic bytes, algorithmic adds, dtype)."""
     rs = []
@@ -293,6 +307,8 @@ def run_native(args):
     roofline = dominant_roofline(kernels, prof, row_stats, dadd_rate, dadd_lat, hbm_peak,
                                  args.steps)
 
+    extras = run_extras(args, scr, torch, dev, stream, run_row, dadd_rate, fadd_rate, hbm_peak)
+
     # ---- e2e through the public API with pinned host buffers
     e2e = run_e2e(args, scr, torch, dev, hin, rows, world, dist)
 
@@ -312,7 +328,7 @@ def run_native(args):
                                    "row reduce + 90x200000 fp64 column scans",
                        "n": N, "l2": "every input larger than L2 (>=144 MB); no flush",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
-            "rows": row_stats, "kernels": kernels, "roofline": roofline,
+            "rows": row_stats, "kernels": kernels, "roofline": roofline, "extras": extras,
             "peaks": {"hbm_gbs": hbm_peak, "dadd_per_s": dadd_rate, "dadd_latency_ns": dadd_lat,
                       "fadd_per_s": fadd_rate},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
@@ -320,6 +336,41 @@ def run_native(args):
         print(json.dumps(line))
     if dist:
         dist.destroy_process_group()
+
+
+def run_extras(args, scr, torch, dev, stream, run_row, dadd_rate, fadd_rate, hbm_peak):
+    """Each extra row timed alone: W warm-up calls, then K calls bracketed by
+    CUDA events on the launching stream (inputs larger than L2)."""
+    out = {}
+    for r in extra_rows():
+        for _ in range(args.warmup):
+            run_row(r)
+        torch.cuda.synchronize(dev)
+        scr.profile_enable(True)
+        evs = []
+        for _ in range(args.steps):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            run_row(r)
+            b.record(stream)
+            evs.append((a, b))
+        torch.cuda.synchronize(dev)
+        scr.profile_enable(False)
+        prof = scr.profile_collect()
+        ms = statistics.median([a.elapsed_time(b) for a, b in evs])
+        gbs = r[3] / (ms * 1e-3) / 1e9
+        add_rate = r[4] / (ms * 1e-3)
+        peak_add = dadd_rate if r[5] == "f64" else fadd_rate
+        kms = {}
+        for name, t in prof:
+            kms[name] = kms.get(name, 0.0) + t / args.steps
+        out[r[0]] = {"ms": round(ms, 4), "gb_s": round(gbs, 1),
+                     "hbm_frac": round(gbs / hbm_peak, 4) if hbm_peak else None,
+                     "adds_per_s": add_rate, "alu_frac": round(add_rate / peak_add, 4),
+                     "bytes": r[3], "adds": r[4], "dtype": r[5],
+                     "kernels_ms": {k: round(v, 4) for k, v in kms.items()}}
+    return out
 
 
 def measured_peaks():

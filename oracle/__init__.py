@@ -61,6 +61,14 @@ def _declare(L: ctypes.CDLL) -> None:
         "cro_scan_modp": (I32, [P, P, I64, I32, I64]),
         "cro_scan_batched_f64": (I32, [P, P, I64, I64, I64, I64, I32, I64]),
         "cro_scan_batched_f32": (I32, [P, P, I64, I64, I64, I64, I32, I64]),
+        "cro_scan_ex_f64": (I32, [P, I64, P, I64, I64, I32, I64, D, I32]),
+        "cro_scan_ex_f32": (I32, [P, I64, P, I64, I64, I32, I64, F, I32]),
+        "cro_scan_ex_modp": (I32, [P, P, I64, I32, I64, U64, I32]),
+        "cro_scan_ex_batched_f64": (I32, [P, P, I64, I64, I64, I64, I64, I64, I32, I64, D,
+                                          I32]),
+        "cro_scan_ex_batched_f32": (I32, [P, P, I64, I64, I64, I64, I64, I64, I32, I64, F,
+                                          I32]),
+        "cro_sym_scan_ex": (I64, [I64, I32, I64, I32, I64, P, I64]),
         "cro_reduce_policy_f64": (I32, [P, I64, I32, I64, P]),
         "cro_reduce_policy_f32": (I32, [P, I64, I32, I64, P]),
         "cro_reduce_policy_modp": (I32, [P, I64, I32, I64, P]),
@@ -165,6 +173,46 @@ def scan_batched(buf: np.ndarray, batch: int, n: int, elem_stride: int,
     return y
 
 
+SCAN_MODES = {"exclusive": 0, "include_initial": 1}
+
+
+def _mode(mode) -> int:
+    return SCAN_MODES[mode] if isinstance(mode, str) else int(mode)
+
+
+def scan_ex(x: np.ndarray, policy, B: int = 1, init=0.0, mode="exclusive") -> np.ndarray:
+    """Exclusive scan (n outputs) or include_initial (n + 1 outputs) of a 1-D
+    array: out[0] = init, out[k] = init + inclusive[k - 1]."""
+    x = np.ascontiguousarray(x)
+    k = _kind(x)
+    md = _mode(mode)
+    y = np.empty(x.size + (1 if md == 1 else 0), dtype=x.dtype)
+    rc = getattr(lib(), "cro_scan_ex_" + k)(_ptr(x), 1, _ptr(y), 1, x.size, _policy(policy),
+                                            int(B), x.dtype.type(init), md)
+    if rc:
+        raise ValueError("bad policy, block size or mode")
+    return y
+
+
+def scan_ex_batched(buf: np.ndarray, batch: int, n: int, elem_stride: int, batch_stride: int,
+                    policy, B: int, init, mode, out: np.ndarray, out_elem_stride: int,
+                    out_batch_stride: int) -> np.ndarray:
+    """Batched exclusive / include_initial scans into ``out`` (1-D, its own
+    strides); returns ``out``."""
+    assert buf.flags.c_contiguous and buf.ndim == 1
+    assert out.flags.c_contiguous and out.ndim == 1 and out.dtype == buf.dtype
+    k = _kind(buf)
+    md = _mode(mode)
+    _check_extent(buf, batch, n, elem_stride, batch_stride)
+    _check_extent(out, batch, n + (1 if md == 1 else 0), out_elem_stride, out_batch_stride)
+    rc = getattr(lib(), "cro_scan_ex_batched_" + k)(
+        _ptr(buf), _ptr(out), batch, n, elem_stride, batch_stride, out_elem_stride,
+        out_batch_stride, _policy(policy), int(B), buf.dtype.type(init), md)
+    if rc:
+        raise ValueError("bad policy, block size or mode")
+    return out
+
+
 def reduce_policy(x: np.ndarray, policy, B: int = 1) -> np.floating:
     """reduce<E>(x): the root of the named expression, from its own definition."""
     x = np.ascontiguousarray(x)
@@ -188,6 +236,15 @@ def scan_modp(x: np.ndarray, policy, B: int = 1) -> np.ndarray:
     y = np.empty_like(x)
     if lib().cro_scan_modp(_ptr(x), _ptr(y), x.size, _policy(policy), int(B)):
         raise ValueError("bad policy or block size")
+    return y
+
+
+def scan_ex_modp(x: np.ndarray, policy, B: int, init: int, mode) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.uint64)
+    md = _mode(mode)
+    y = np.empty(x.size + (1 if md == 1 else 0), dtype=np.uint64)
+    if lib().cro_scan_ex_modp(_ptr(x), _ptr(y), x.size, _policy(policy), int(B), int(init), md):
+        raise ValueError("bad policy, block size or mode")
     return y
 
 
@@ -219,6 +276,10 @@ def sym_reduce(n: int, L: int) -> str:
 
 def sym_scan(n: int, policy, B: int, i: int) -> str:
     return _text(lib().cro_sym_scan, n, _policy(policy), B, i)
+
+
+def sym_scan_ex(n: int, policy, B: int, mode, k: int) -> str:
+    return _text(lib().cro_sym_scan_ex, n, _policy(policy), B, _mode(mode), k)
 
 
 def sym_reduce_policy(n: int, policy, B: int = 1) -> str:

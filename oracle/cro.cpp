@@ -31,6 +31,11 @@
 //     operands, blocks chained left to right by a running carry.
 //   * block_dyadic_alt<B> (reading B, kept for comparison only): left fold
 //     inside each block, tree() across the block results.
+//   * exclusive scan and include_initial (the inclusive/exclusive duality of
+//     the page "Vertical scan redesign: research notes", section B.2; init
+//     placement of P4016R0): with y the inclusive scan, out[0] = init and
+//     out[k] = op(init, y[k-1]); exclusive has n outputs, include_initial
+//     n + 1.
 //
 // Arithmetic: op is IEEE-754 addition in the element type, round to nearest
 // even; build with -ffp-contract=off and without fast-math (the page's
@@ -233,6 +238,22 @@ int scan(const V* x, int64_t xs, V* y, int64_t ys, int64_t n, int policy, int64_
   }
 }
 
+// Exclusive scan (m = n outputs) or include_initial (m = n + 1 outputs):
+// out[0] = init, out[k] = op(init, y[k-1]) for 1 <= k < m, where y is the
+// inclusive scan of the policy. init is combined once, as the left operand,
+// after the expression, as the reduction combines it with its root.
+template <class V, class Op>
+int scan_with_init(const V* x, int64_t xs, V* out, int64_t os, int64_t n, int policy,
+                   int64_t B, const V& init, bool include_initial, const Op& op) {
+  std::vector<V> y((size_t)n);
+  if (scan(x, xs, y.data(), 1, n, policy, B, op)) return -1;
+  const int64_t m = include_initial ? n + 1 : n;
+  if (m == 0) return 0;
+  out[0] = init;
+  for (int64_t k = 1; k < m; ++k) out[k * os] = op(init, y[(size_t)(k - 1)]);
+  return 0;
+}
+
 // reduce<E>(x): the root of the named expression, evaluated directly from
 // its definition (not from a scan), for n >= 1.
 template <class V, class Op>
@@ -365,6 +386,50 @@ int cro_scan_batched_f32(const float* x, float* y, int64_t batch, int64_t n,
   return 0;
 }
 
+// ---- exclusive scan (mode 0, n outputs) and include_initial (mode 1,
+// n + 1 outputs), output element k at out[k * out_stride]; batched forms
+// take the output's own strides (sequence b, element k at
+// out[b * out_batch_stride + k * out_elem_stride]).
+int cro_scan_ex_f64(const double* x, int64_t xs, double* out, int64_t os, int64_t n,
+                    int policy, int64_t B, double init, int mode) {
+  if (mode != 0 && mode != 1) return -1;
+  return scan_with_init(x, xs, out, os, n, policy, B, init, mode == 1, AddF64{});
+}
+int cro_scan_ex_f32(const float* x, int64_t xs, float* out, int64_t os, int64_t n,
+                    int policy, int64_t B, float init, int mode) {
+  if (mode != 0 && mode != 1) return -1;
+  return scan_with_init(x, xs, out, os, n, policy, B, init, mode == 1, AddF32{});
+}
+int cro_scan_ex_modp(const uint64_t* x, uint64_t* out, int64_t n, int policy, int64_t B,
+                     uint64_t init, int mode) {
+  if (mode != 0 && mode != 1) return -1;
+  return scan_with_init(x, 1, out, 1, n, policy, B, init, mode == 1, ModP{});
+}
+int cro_scan_ex_batched_f64(const double* x, double* out, int64_t batch, int64_t n,
+                            int64_t elem_stride, int64_t batch_stride,
+                            int64_t out_elem_stride, int64_t out_batch_stride, int policy,
+                            int64_t B, double init, int mode) {
+  if (mode != 0 && mode != 1) return -1;
+  for (int64_t b = 0; b < batch; ++b) {
+    const int rc = scan_with_init(x + b * batch_stride, elem_stride, out + b * out_batch_stride,
+                                  out_elem_stride, n, policy, B, init, mode == 1, AddF64{});
+    if (rc) return rc;
+  }
+  return 0;
+}
+int cro_scan_ex_batched_f32(const float* x, float* out, int64_t batch, int64_t n,
+                            int64_t elem_stride, int64_t batch_stride,
+                            int64_t out_elem_stride, int64_t out_batch_stride, int policy,
+                            int64_t B, float init, int mode) {
+  if (mode != 0 && mode != 1) return -1;
+  for (int64_t b = 0; b < batch; ++b) {
+    const int rc = scan_with_init(x + b * batch_stride, elem_stride, out + b * out_batch_stride,
+                                  out_elem_stride, n, policy, B, init, mode == 1, AddF32{});
+    if (rc) return rc;
+  }
+  return 0;
+}
+
 // ---- reduce<E>, computed from the expression's own definition
 int cro_reduce_policy_f64(const double* x, int64_t n, int policy, int64_t B, double* out) {
   return reduce_policy(x, 1, n, policy, B, AddF64{}, out);
@@ -396,6 +461,17 @@ int64_t cro_sym_scan(int64_t n, int policy, int64_t B, int64_t i, char* buf, int
   std::vector<std::string> y((size_t)n);
   if (scan(v.data(), 1, y.data(), 1, n, policy, B, Sym{})) return -1;
   return put_text(y[(size_t)i], buf, cap);
+}
+int64_t cro_sym_scan_ex(int64_t n, int policy, int64_t B, int mode, int64_t k, char* buf,
+                        int64_t cap) {
+  const int64_t m = (mode == 1) ? n + 1 : n;
+  if (n < 0 || (mode != 0 && mode != 1) || k < 0 || k >= m) return -1;
+  const auto v = leaves(n);
+  std::vector<std::string> y((size_t)m);
+  if (scan_with_init(v.data(), 1, y.data(), 1, n, policy, B, std::string("I"), mode == 1,
+                     Sym{}))
+    return -1;
+  return put_text(y[(size_t)k], buf, cap);
 }
 int64_t cro_sym_reduce_policy(int64_t n, int policy, int64_t B, char* buf, int64_t cap) {
   const auto v = leaves(n);

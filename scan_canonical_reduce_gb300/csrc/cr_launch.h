@@ -28,6 +28,7 @@ enum KernelId : int {
   kKScanOnePass,
   kKScanLocal,
   kKCarryFixup,
+  kKScanPairwise,
   kKernelCount
 };
 

@@ -10,6 +10,9 @@
 // with w[e] the thread-local scan of its 8 elements and each level folded
 // from its lowest set bit up (right-nested). A node at level p starting at
 // q*2^p is the perfect tree over aligned thread (tile) aggregates.
+// pairwise: out[i] = ((N_1 op N_2) op ...) op N_m, the same nodes folded from
+// the left (largest first): the up pass builds the node pyramid, then a
+// down-sweep (scan_pairwise_kernel) writes every output.
 // block_dyadic<B>: the same restricted to the position inside the block (only
 // the bits below log2 B), then out[i] = C_{k-1} op P(i) for blocks k >= 1,
 // where C_0 = T_0 and C_k = C_{k-1} op T_k over the block totals T_k.
@@ -176,7 +179,9 @@ __device__ __forceinline__ void store8(T* p, int64_t cnt, const T (&v)[kE]) {
     }
     return;
   }
-  for (int e = 0; e < cnt; ++e) p[e] = v[e];
+#pragma unroll
+  for (int e = 0; e < kE; ++e)  // unrolled: v stays in registers
+    if (e < cnt) p[e] = v[e];
 }
 
 // In-block pyramid over the 256 thread aggregates, all levels kept:
@@ -346,7 +351,7 @@ scan_down_kernel(const T* x, T* out, const T* __restrict__ pyr, const T* __restr
   store8(out + i0, cnt, w);
 }
 
-// ------------------------------------------- iterated_pairwise, one pass
+// ------------------------------------------- one-pass tile protocol
 // Tiles take indices in the order they start (a counter), publish their
 // aggregate, climb the node pyramid by arrival tickets (the second of two
 // siblings to arrive computes the parent, left op right, and publishes it
@@ -354,6 +359,50 @@ scan_down_kernel(const T* x, T* out, const T* __restrict__ pyr, const T* __restr
 // their own prefix needs. Every wait is on tiles that started earlier and
 // never wait before publishing, so the waits end; each is still bounded and,
 // if it gives up, records CR_ERR_TIMEOUT in the workspace status word.
+
+// Publishes tile b's aggregate as level-0 node b and climbs while this tile
+// arrives second (one thread).
+template <class T>
+__device__ __forceinline__ void publish_and_climb(T node, int64_t b, T* pyr, int* counters,
+                                                  int* ready, const ScanArgs& a) {
+  pyr[a.pyr_off[0] + b] = node;
+  __threadfence();
+  atomicExch(ready + a.pyr_off[0] + b, 1);
+  int64_t q = b;
+  for (int p = 1; p < a.pyr_levels; ++p) {
+    const int64_t parent = q >> 1;
+    if (parent >= (a.full_tiles >> p)) break;  // the parent is not a complete node
+    const int ticket = atomicAdd(counters + a.cnt_off[p] + parent, 1);
+    if (ticket == 0) break;  // the sibling is still running; it will climb
+    __threadfence();
+    const T left = __ldcg(pyr + a.pyr_off[p - 1] + 2 * parent);
+    const T right = __ldcg(pyr + a.pyr_off[p - 1] + 2 * parent + 1);
+    node = add_rn(left, right);
+    pyr[a.pyr_off[p] + parent] = node;
+    __threadfence();
+    atomicExch(ready + a.pyr_off[p] + parent, 1);
+    q = parent;
+  }
+}
+
+// The published pyramid node q of level p, after a bounded wait for its flag.
+template <class T>
+__device__ __forceinline__ T wait_node(const T* pyr, const int* ready, int* status,
+                                       const ScanArgs& a, int p, int64_t q) {
+  const volatile int* f = ready + a.pyr_off[p] + q;
+  uint32_t spins = 0;
+  while (*f == 0) {
+    if (++spins > kSpinLimit) {
+      raise_status(status, CR_ERR_TIMEOUT);
+      break;
+    }
+    __nanosleep(64);
+  }
+  __threadfence();
+  return __ldcg(pyr + a.pyr_off[p] + q);
+}
+
+// ------------------------------------------- iterated_pairwise, one pass
 template <class T>
 __global__ void __launch_bounds__(kScanThreads)
 scan_onepass_kernel(const T* x, T* out, T* pyr, int* counters, int* ready, int* tile_ctr,
@@ -376,28 +425,8 @@ scan_onepass_kernel(const T* x, T* out, T* pyr, int* counters, int* ready, int* 
   if (t < full_threads) lvl[t] = agg[0];
   build_tile_pyramid(lvl, t, full_threads);
 
-  // publish this tile's aggregate, then climb as long as we arrive second
-  if (t == 0 && b < a.full_tiles && a.pyr_levels > 0 && b != skip_publish) {
-    T node = lvl[lvl_base(8)];
-    pyr[a.pyr_off[0] + b] = node;
-    __threadfence();
-    atomicExch(ready + a.pyr_off[0] + b, 1);
-    int64_t q = b;
-    for (int p = 1; p < a.pyr_levels; ++p) {
-      const int64_t parent = q >> 1;
-      if (parent >= (a.full_tiles >> p)) break;
-      const int ticket = atomicAdd(counters + a.cnt_off[p] + parent, 1);
-      if (ticket == 0) break;
-      __threadfence();
-      const T left = __ldcg(pyr + a.pyr_off[p - 1] + 2 * parent);
-      const T right = __ldcg(pyr + a.pyr_off[p - 1] + 2 * parent + 1);
-      node = add_rn(left, right);
-      pyr[a.pyr_off[p] + parent] = node;
-      __threadfence();
-      atomicExch(ready + a.pyr_off[p] + parent, 1);
-      q = parent;
-    }
-  }
+  if (t == 0 && b < a.full_tiles && a.pyr_levels > 0 && b != skip_publish)
+    publish_and_climb(lvl[lvl_base(8)], b, pyr, counters, ready, a);
 
   // thread-level prefix nodes (all bits of t), lowest first; lane bits by
   // pairs of lanes, warp bits (uniform across the warp) directly
@@ -408,25 +437,121 @@ scan_onepass_kernel(const T* x, T* out, T* pyr, int* counters, int* ready, int* 
   }
   // wait for the tile-level nodes this tile needs (bits of b)
   const int tile_bits = a.pyr_levels;
-  if (t < tile_bits && ((b >> t) & 1)) {
-    const int64_t q = (b >> t) - 1;
-    const volatile int* f = ready + a.pyr_off[t] + q;
-    uint32_t spins = 0;
-    while (*f == 0) {
-      if (++spins > kSpinLimit) {
-        raise_status(status, CR_ERR_TIMEOUT);
-        break;
-      }
-      __nanosleep(64);
-    }
-    __threadfence();
-    tile_nodes[t] = __ldcg(pyr + a.pyr_off[t] + q);
-  }
+  if (t < tile_bits && ((b >> t) & 1))
+    tile_nodes[t] = wait_node(pyr, ready, status, a, t, (b >> t) - 1);
   __syncthreads();
   if (cnt == 0) return;
   for (int p = 0; p < tile_bits; ++p) {
     if ((b >> p) & 1) apply_node(tile_nodes[p], w);
   }
+  store8(out + i0, cnt, w);
+}
+
+// ------------------------------------------------------ pairwise, down pass
+// out[i] = W(i + 1), where W(m) folds the perfect subtrees over the aligned
+// blocks of the binary decomposition of m from the LEFT:
+// W(m) = ((N_1 op N_2) op ...) op N_k, largest block first. Equivalently
+// W(m) = W(m - lowbit(m)) op N(lowbit(m), m - lowbit(m)), with W(0) empty:
+// one add per output given the node tree (a down-sweep). Per tile b:
+// Y_b = W(2048 b) and Y_{b+1} from the tile-level nodes; per warp the thread
+// prefixes E_{32w} = W(2048 b + 256 w) from the warp-level nodes; per lane
+// E_t = W(2048 b + 8 t) by a down-sweep over the lane bits; per thread
+// W(8t + r), r = 1..7, from E_t and its own pairs and quads, and
+// W(8t + 8) = E_{t+1}.
+// Y_b is the innermost (left-most) operand of every output of tile b, so no
+// later fix-up can apply it: the node pyramid over complete tiles is built
+// first by the up pass (scan_up_kernel), and this pass only reads it. (A
+// single pass that waits for the nodes measured 2.5x slower here: a tile's
+// own add work is too short to hide the pyramid's completion latency.)
+template <class T>
+__global__ void __launch_bounds__(kScanThreads)
+scan_pairwise_kernel(const T* x, T* out, const T* __restrict__ pyr, ScanArgs a) {
+  __shared__ T lvl[2 * kScanThreads];
+  __shared__ T nodes_b[32], nodes_b1[32];  // tile-level nodes of b and of b + 1
+  __shared__ T s_base[kScanThreads / 32 + 1];  // E_{32 w}, w = 0..8 (E_256 = Y_{b+1})
+  const unsigned full = 0xffffffffu;
+  const int t = threadIdx.x, lane = t & 31, wp = t >> 5;
+  const int64_t b = blockIdx.x;
+  const int64_t i0 = b * kTile + (int64_t)t * kE;
+  const int64_t cnt = imax(0, imin(kE, a.n - i0));
+  const int full_threads = (int)imin(kScanThreads, (a.n - b * kTile) / kE);
+  const int64_t b1 = b + 1;
+  const bool complete = (b1 <= a.full_tiles);  // its last output is W(2048 (b + 1))
+  const int tile_bits = a.pyr_levels;
+
+  // tile-level nodes of b (threads 0..31) and of b + 1 (threads 32..63)
+  if (t < tile_bits && ((b >> t) & 1)) nodes_b[t] = pyr[a.pyr_off[t] + (b >> t) - 1];
+  if (complete && t >= 32 && t < 32 + tile_bits && ((b1 >> (t - 32)) & 1))
+    nodes_b1[t - 32] = pyr[a.pyr_off[t - 32] + (b1 >> (t - 32)) - 1];
+
+  T v[kE];
+  load8(x + i0, cnt, v);
+  // the thread's nodes: pairs, quads, its aggregate
+  const T p01 = add_rn(v[0], v[1]), p23 = add_rn(v[2], v[3]);
+  const T p45 = add_rn(v[4], v[5]), p67 = add_rn(v[6], v[7]);
+  const T q03 = add_rn(p01, p23), q47 = add_rn(p45, p67);
+  if (t < full_threads) lvl[t] = add_rn(q03, q47);
+  build_tile_pyramid(lvl, t, full_threads);  // ends with a block barrier
+
+  // warp prefixes: lane w of warp 0 folds Y_b (or Y_{b+1}) and the warp bits
+  if (t <= kScanThreads / 32) {
+    const bool next = (t == kScanThreads / 32);
+    const int64_t bb = next ? b1 : b;
+    T acc = T(0);
+    bool has = false;
+    if (!next || complete) {
+      for (int p = tile_bits - 1; p >= 0; --p) {
+        if ((bb >> p) & 1) {
+          const T nd = next ? nodes_b1[p] : nodes_b[p];
+          acc = has ? add_rn(acc, nd) : nd;
+          has = true;
+        }
+      }
+    }
+    if (!next) {
+      const int th = t * 32;  // first thread of warp t
+      for (int p = 7; p >= 5; --p) {
+        if ((th >> p) & 1) {
+          const T nd = lvl[lvl_base(p) + (th >> p) - 1];
+          acc = has ? add_rn(acc, nd) : nd;
+          has = true;
+        }
+      }
+    }
+    s_base[t] = acc;  // W(0) is empty; s_base[8] is used only when complete
+  }
+  __syncthreads();
+  // no early exit: every lane takes part in the shuffles; lanes past the end
+  // compute on values they never store
+
+  // lane down-sweep: E_t = E_{t - lowbit} op node(lowbit), highest lane bit first
+  T E = s_base[wp];
+#pragma unroll
+  for (int p = 4; p >= 0; --p) {
+    const T src = __shfl_sync(full, E, (lane - (1 << p)) & 31);
+    if ((lane & ((2 << p) - 1)) == (1 << p)) {  // lowbit(lane) == 2^p
+      const T nd = lvl[lvl_base(p) + (t >> p) - 1];
+      E = (b == 0 && t == (1 << p)) ? nd : add_rn(src, nd);  // W(0) is empty
+    }
+  }
+  const T E_down = __shfl_down_sync(full, E, 1);
+  const T E1 = (lane == 31) ? s_base[wp + 1] : E_down;
+
+  T w[kE];
+  if (b == 0 && t == 0) {  // W(0) is empty
+    w[0] = v[0];
+    w[1] = p01;
+    w[3] = q03;
+  } else {
+    w[0] = add_rn(E, v[0]);
+    w[1] = add_rn(E, p01);
+    w[3] = add_rn(E, q03);
+  }
+  w[2] = add_rn(w[1], v[2]);
+  w[4] = add_rn(w[3], v[4]);
+  w[5] = add_rn(w[3], p45);
+  w[6] = add_rn(w[5], v[6]);
+  w[7] = E1;
   store8(out + i0, cnt, w);
 }
 
@@ -626,18 +751,13 @@ ScanPlan plan_scan(int64_t batch, int64_t n, cr_policy p, int64_t B, size_t esiz
     plan.ws_bytes = off;
     return plan;
   }
-  if (p == CR_PAIRWISE) {  // 1-D pairwise: not in this build yet
-    plan.kind = ScanPlan::kEmpty;
-    plan.supported = false;
-    plan.ws_bytes = off;
-    return plan;
-  }
   plan.kind = ScanPlan::kTiled;
   const int logB = block ? ilog2(B) : 62;
   plan.logB = logB;
   plan.n_tiles = (n + kTile - 1) / kTile;
   plan.full_tiles = n / kTile;
-  if (!block) plan.mode = ScanPlan::kOnePass;
+  if (p == CR_PAIRWISE) plan.mode = ScanPlan::kUpDown;
+  else if (!block) plan.mode = ScanPlan::kOnePass;
   else if (logB <= kLogTile) plan.mode = ScanPlan::kLocalFixup;
   else plan.mode = ScanPlan::kUpDown;
   // global node pyramid over complete tiles (one pass, up/down): level l has
@@ -648,6 +768,7 @@ ScanPlan plan_scan(int64_t batch, int64_t n, cr_policy p, int64_t B, size_t esiz
     if (block) levels = std::min(levels, std::max(0, logB - kLogTile + 1));
   }
   plan.pyr_levels = levels;
+  if (p == CR_PAIRWISE && levels > 32) plan.supported = false;  // 2^43 elements and more
   int64_t pyr_elems = 0, cnt_elems = 0;
   for (int l = 0; l < levels; ++l) {
     plan.pyr_off[l] = pyr_elems;
@@ -789,6 +910,15 @@ cudaError_t run_scan(const ScanPlan& plan, const T* x, T* out, int64_t es, int64
       e = cudaGetLastError();
     }
     return e;
+  }
+
+  if (plan.policy == CR_PAIRWISE) {  // node pyramid first, then the down-sweep
+    CR_LAUNCH(kKScanUp, s,
+              scan_up_kernel<T, 8><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a));
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    CR_LAUNCH(kKScanPairwise, s,
+              scan_pairwise_kernel<T><<<grid, kScanThreads, 0, s>>>(x, out, pyr, a));
+    return cudaGetLastError();
   }
 
   // up/down: blocks spanning tiles (B > 2048)

@@ -44,8 +44,8 @@ SIZES = [1, 2, 3, 7, 8, 9, 15, 16, 17, 100, 255, 256, 257, 2047, 2048, 2049, 409
 
 
 @pytest.mark.parametrize("dtype", [np.float64, np.float32])
-@pytest.mark.parametrize("policy,B", [("iterated_pairwise", 1), ("left_fold", 1),
-                                      ("block_dyadic", 1), ("block_dyadic", 2),
+@pytest.mark.parametrize("policy,B", [("iterated_pairwise", 1), ("pairwise", 1),
+                                      ("left_fold", 1), ("block_dyadic", 1), ("block_dyadic", 2),
                                       ("block_dyadic", 4), ("block_dyadic", 8),
                                       ("block_dyadic", 16), ("block_dyadic", 32),
                                       ("block_dyadic", 256), ("block_dyadic", 2048),
@@ -58,12 +58,14 @@ def test_scan_sizes(scr, dtype, policy, B):
 
 def test_scan_empty(scr):
     x = torch.empty(0, dtype=torch.float64, device=DEV)
-    for policy, B in (("iterated_pairwise", 1), ("block_dyadic", 16), ("left_fold", 1)):
+    for policy, B in (("iterated_pairwise", 1), ("pairwise", 1), ("block_dyadic", 16),
+                      ("left_fold", 1)):
         assert scr.inclusive_scan(x, policy, B).numel() == 0
 
 
-@pytest.mark.parametrize("policy,B", [("iterated_pairwise", 1), ("block_dyadic", 16),
-                                      ("block_dyadic", 4096), ("left_fold", 1)])
+@pytest.mark.parametrize("policy,B", [("iterated_pairwise", 1), ("pairwise", 1),
+                                      ("block_dyadic", 16), ("block_dyadic", 4096),
+                                      ("left_fold", 1)])
 def test_scan_in_place(scr, policy, B):
     x = W.family3(2048 * 5 + 77)
     t = torch.from_numpy(x).to(DEV)
@@ -134,3 +136,29 @@ def test_scan_reduce_consistency_on_gpu(scr):
     for i in list(rng.choice(x.size, 40, replace=False)) + [0, x.size - 1]:
         r = scr.reduce(xd[: i + 1], 1, -0.0).cpu().numpy()[0]
         assert bits(y[i]) == bits(r), i
+
+
+def test_pairwise_full_size(scr):
+    """1-D pairwise at the benchmark sizes: every element against the oracle.
+    Its back element is the tree of the whole input when n is a power of two
+    (one maximal subtree), and it equals iterated_pairwise wherever the
+    prefix length has at most two set bits (two subtrees fold the same way
+    from either side) - checked GPU against GPU at every such index."""
+    for n in (1 << 24, (1 << 28) + 37):
+        x = W.family3(n)
+        xd = torch.from_numpy(x).to(DEV)
+        got = scr.inclusive_scan(xd, "pairwise").cpu().numpy()
+        want = oracle.scan(x, "pairwise")
+        assert bits(got) == bits(want), (n, first_diff(got, want))
+        it = scr.inclusive_scan(xd, "iterated_pairwise").cpu().numpy()
+        m = np.arange(1, n + 1, dtype=np.uint64)
+        low = m & (~m + np.uint64(1))
+        rest = m - low
+        two = (rest & (rest - np.uint64(1))) == 0  # popcount(i + 1) <= 2
+        assert bits(got[two]) == bits(it[two])
+        del it, m, low, rest, two
+    x = W.family3(1 << 24)
+    xd = torch.from_numpy(x).to(DEV)
+    y = scr.inclusive_scan(xd, "pairwise").cpu().numpy()
+    r = scr.reduce(xd, 1, -0.0).cpu().numpy()[0]
+    assert bits(y[-1]) == bits(r)

@@ -14,19 +14,20 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
 
-def test_timeout_is_reported_and_cleared():
+@pytest.mark.parametrize("policy", ["iterated_pairwise"])
+def test_timeout_is_reported_and_cleared(policy):
     import scan_canonical_reduce_gb300 as scr
     lib = scr.lib()
     x = W.family3(2048 * 16 + 5)
     xd = torch.from_numpy(x).to(DEV)
     lib.cr_debug_skip_publish(2)  # tile 3 waits on tile 2's aggregate
     try:
-        scr.inclusive_scan(xd, "iterated_pairwise")
+        scr.inclusive_scan(xd, policy)
         with pytest.raises(scr.CrError) as ei:
             scr.sync_status()
         assert ei.value.code == 5  # CR_ERR_TIMEOUT
     finally:
         lib.cr_debug_skip_publish(-1)
-    y = scr.inclusive_scan(xd, "iterated_pairwise")
+    y = scr.inclusive_scan(xd, policy)
     scr.sync_status()  # CR_OK: the status word is cleared by every call
-    assert y.cpu().numpy().tobytes() == oracle.scan(x, "iterated_pairwise").tobytes()
+    assert y.cpu().numpy().tobytes() == oracle.scan(x, policy).tobytes()

@@ -56,6 +56,8 @@ def test_golden_expressions():
             got = oracle.sym_scan(int(f[3]), f[1], int(f[2]), int(f[4]))
         elif f[0] == "reduce_policy":
             got = oracle.sym_reduce_policy(int(f[3]), f[1], int(f[2]))
+        elif f[0] == "scan_ex":
+            got = oracle.sym_scan_ex(int(f[4]), f[2], int(f[3]), f[1], int(f[5]))
         else:
             raise AssertionError(line)
         assert got == rhs, line
@@ -83,6 +85,10 @@ def test_golden_worked_values():
             assert got.tobytes() == dt(float(exp)).tobytes(), (line, got)
         elif h[0] == "scan":
             got = oracle.scan(x, h[2], int(h[3]))
+            want = np.array([float(t) for t in exp.split()], dtype=dt)
+            assert got.tobytes() == want.tobytes(), (line, got)
+        elif h[0] == "scan_ex":
+            got = oracle.scan_ex(x, h[3], int(h[4]), dt(float(h[5])), h[2])
             want = np.array([float(t) for t in exp.split()], dtype=dt)
             assert got.tobytes() == want.tobytes(), (line, got)
         else:
@@ -193,7 +199,7 @@ def test_reduce_bruteforce_modp(n, L):
                                       ("pairwise", 1), ("block_dyadic", 2),
                                       ("block_dyadic", 4), ("block_dyadic_alt", 2)])
 def test_scan_bruteforce_modp(policy, B):
-    rng = random.Random(hash(policy) % 1000 + B)
+    rng = random.Random("%s-%d" % (policy, B))
     for n in range(1, 8):
         x = [rng.randrange(MODP) for _ in range(n)]
         y = oracle.scan_modp(np.array(x, dtype=np.uint64), policy, B)
