@@ -78,7 +78,14 @@ def extra_rows():
     """Rows beyond the headline step (the next policies), timed on their own
     after it and reported under "extras"; not part of value."""
     return [("scan_pairwise", "scan", {"policy": "pairwise", "B": 1}, 16 * N,
-             adds_pairwise(N), "f64")]
+             adds_pairwise(N), "f64"),
+            # init combined once with each of the n - 1 (n) observations
+            ("scan_iterated_pairwise_exclusive", "scan_ex",
+             {"policy": "iterated_pairwise", "B": 1, "mode": "exclusive"}, 16 * N,
+             adds_iterated(N) - 1 + (N - 1), "f64"),
+            ("scan_block_dyadic_16_include_initial", "scan_ex",
+             {"policy": "block_dyadic", "B": 16, "mode": "include_initial"}, 16 * N + 8,
+             adds_block_dyadic(N, 16) + N, "f64")]
 
 
 def rows_spec():
@@ -196,6 +203,7 @@ def run_native(args):
     x4 = torch.from_numpy(hin["f4"]).to(dev)
     x5 = torch.from_numpy(hin["f5"]).to(dev).view(COLS_LEVELS, COLS_N)
     y_scan = torch.empty_like(x3)
+    y_scan1 = torch.empty(N + 1, dtype=x3.dtype, device=dev)  # include_initial: n + 1
     y_cols = torch.empty_like(x5)
     r_out = torch.empty(1, dtype=torch.float64, device=dev)
     rows_out = torch.empty(ROWS_R, dtype=torch.float32, device=dev)
@@ -207,6 +215,11 @@ def run_native(args):
             scr.reduce(x2, p["L"], 0.0, out=r_out)
         elif kind == "scan":
             scr.inclusive_scan(x3, p["policy"], p["B"], out=y_scan)
+        elif kind == "scan_ex":
+            if p["mode"] == "exclusive":
+                scr.exclusive_scan(x3, p["policy"], p["B"], 0.5, out=y_scan)
+            else:
+                scr.scan_include_initial(x3, p["policy"], p["B"], 0.5, out=y_scan1)
         elif kind == "rows":
             scr.reduce_batched(x4, p["L"], 0.0, dim=-1, out=rows_out)
         elif kind == "cols":

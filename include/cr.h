@@ -140,6 +140,48 @@ cr_status cr_inclusive_scan_batched(const void* x, void* out, int64_t batch, int
                                     int64_t B, cr_dtype dt, void* ws, size_t ws_bytes,
                                     void* stream);
 
+/* Exclusive scan and the include_initial form (the inclusive/exclusive
+ * duality of the page "Vertical scan redesign: research notes", section B.2,
+ * with init placed as in P4016R0: combined once, as the left operand, after
+ * the named expression). With y the inclusive scan of the same policy:
+ *   CR_EXCLUSIVE        m = n outputs:     out[0] = init,
+ *                                          out[k] = init op y[k-1], 0 < k < n
+ *   CR_INCLUDE_INITIAL  m = n + 1 outputs: out[0] = init,
+ *                                          out[k] = init op y[k-1], 0 < k <= n
+ * (init = -0.0 gives exactly the inclusive scan moved one place right). */
+typedef enum { CR_EXCLUSIVE = 1, CR_INCLUDE_INITIAL = 2 } cr_scan_mode;
+
+/* Workspace bytes for cr_scan_ex(n, p, B, mode, dt); 0 for bad arguments. */
+size_t cr_scan_ex_workspace_bytes(int64_t n, cr_policy p, int64_t B, cr_scan_mode mode,
+                                  cr_dtype dt);
+
+/* 1-D exclusive / include_initial scan. x: device, n contiguous elements;
+ * out: device, m contiguous elements (see above); init_host: host pointer to
+ * one element of dt. out == x (in place; for CR_INCLUDE_INITIAL the buffer
+ * must hold n + 1 elements) is allowed, any other overlap is INVALID_ARG.
+ * n == 0 writes nothing (CR_EXCLUSIVE) or out[0] = init
+ * (CR_INCLUDE_INITIAL). Policies and B as for cr_inclusive_scan. */
+cr_status cr_scan_ex(const void* x, void* out, int64_t n, cr_policy p, int64_t B,
+                     cr_scan_mode mode, const void* init_host, cr_dtype dt, void* ws,
+                     size_t ws_bytes, void* stream);
+
+/* Workspace bytes for cr_scan_ex_batched with these sizes. */
+size_t cr_scan_ex_batched_workspace_bytes(int64_t batch, int64_t n, cr_policy p, int64_t B,
+                                          cr_scan_mode mode, cr_dtype dt);
+
+/* A batch of independent exclusive / include_initial scans: sequence b is
+ * x[b*batch_stride + i*elem_stride], i < n; its m outputs go to
+ * out[b*out_batch_stride + k*out_elem_stride], k < m. Typical use: the n
+ * levels of each column of a level-major array give n + 1 interface values
+ * (CR_INCLUDE_INITIAL, out_elem_stride = ncols, out_batch_stride = 1). If
+ * out == x the output strides must equal the input strides; otherwise the
+ * output must not overlap the input or itself across sequences. */
+cr_status cr_scan_ex_batched(const void* x, void* out, int64_t batch, int64_t n,
+                             int64_t elem_stride, int64_t batch_stride,
+                             int64_t out_elem_stride, int64_t out_batch_stride, cr_policy p,
+                             int64_t B, cr_scan_mode mode, const void* init_host, cr_dtype dt,
+                             void* ws, size_t ws_bytes, void* stream);
+
 /* Allocation-free canonical reduction. The paper has no counterpart: this
  * serves callers that cannot allocate device memory, such as a plugin whose
  * host framework owns all device memory through its own pool, or a
@@ -215,10 +257,11 @@ cr_status cr_measure_add_peak(cr_dtype dt, void* scratch_dev, size_t scratch_byt
                               void* stream, double* adds_per_second,
                               double* dependent_latency_ns);
 
-/* out[i] = a[i] + b[i] (binary64, round to nearest even) computed by the
- * integer-pipe add that libcr's fp64 kernels use for part of their adds
- * (device pointers, n elements, enqueued on `stream`). Exposed so that the
- * add can be checked bit for bit against the hardware add. */
+/* out[i] = a[i] + b[i] (binary64, round to nearest even) computed by libcr's
+ * integer-pipe add, written from the IEEE-754 definition of the operation
+ * (device pointers, n elements, enqueued on `stream`). A measured
+ * alternative to the FP64 pipe that the kernels do not use; exposed so that
+ * it can be checked bit for bit against the hardware add. */
 cr_status cr_add_pairs_int(const double* a, const double* b, double* out, int64_t n,
                            void* stream);
 

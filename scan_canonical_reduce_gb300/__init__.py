@@ -30,6 +30,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libcr.so")
 
 CR_F32, CR_F64 = 1, 2
 POLICIES = {"left_fold": 0, "pairwise": 1, "iterated_pairwise": 2, "block_dyadic": 3}
+MODES = {"exclusive": 1, "include_initial": 2}  # cr_scan_mode
 STATUS = {0: "CR_OK", 1: "CR_ERR_INVALID_ARG", 2: "CR_ERR_UNSUPPORTED",
           3: "CR_ERR_WORKSPACE", 4: "CR_ERR_CUDA", 5: "CR_ERR_TIMEOUT"}
 
@@ -47,6 +48,11 @@ SIGNATURES = {
     "cr_scan_batched_workspace_bytes": (_SZ, [_I64, _I64, _INT, _I64, _INT]),
     "cr_inclusive_scan_batched": (_INT, [_P, _P, _I64, _I64, _I64, _I64, _INT, _I64, _INT, _P,
                                          _SZ, _P]),
+    "cr_scan_ex_workspace_bytes": (_SZ, [_I64, _INT, _I64, _INT, _INT]),
+    "cr_scan_ex": (_INT, [_P, _P, _I64, _INT, _I64, _INT, _P, _INT, _P, _SZ, _P]),
+    "cr_scan_ex_batched_workspace_bytes": (_SZ, [_I64, _I64, _INT, _I64, _INT, _INT]),
+    "cr_scan_ex_batched": (_INT, [_P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _INT, _I64, _INT,
+                                  _P, _INT, _P, _SZ, _P]),
     "cr_sync_status": (_INT, [_P, _P]),
     "cr_status_string": (ctypes.c_char_p, [_INT]),
     "cr_version": (_INT, []),
@@ -265,6 +271,90 @@ def inclusive_scan_batched(x: torch.Tensor, policy="left_fold", B: int = 1, dim:
     return o.to("cpu") if host else o
 
 
+def _scan_ex(x, policy, B, init, mode, out, stream, what):
+    if x.dim() != 1:
+        raise ValueError("%s expects a 1-D tensor" % what)
+    xd, host = _on_device(x)
+    xd = xd.contiguous()
+    dt = _dtype_code(xd)
+    n = xd.numel()
+    md = MODES[mode]
+    m = n + (1 if md == 2 else 0)
+    o = out if out is not None else torch.empty(m, dtype=xd.dtype, device=xd.device)
+    if o.dim() != 1 or not o.is_contiguous() or o.numel() < m or o.dtype != xd.dtype:
+        raise ValueError("out must be a contiguous 1-D tensor of %d elements of x's dtype" % m)
+    p = _policy(policy)
+    sp = _stream_ptr(stream)
+    nb = lib().cr_scan_ex_workspace_bytes(n, p, int(B), md, dt)
+    if nb == 0:
+        raise ValueError("invalid scan arguments (policy=%s, B=%d)" % (policy, B))
+    ws = _WS.get(xd.device, stream, nb)
+    ini = _init_buffer(init, dt)
+    _check(lib().cr_scan_ex(xd.data_ptr() if n else None, o.data_ptr(), n, p, int(B), md,
+                            ctypes.byref(ini), dt, ws.data_ptr(), ws.numel(), sp), "cr_scan_ex")
+    return o.to("cpu") if host else o
+
+
+def exclusive_scan(x: torch.Tensor, policy="iterated_pairwise", B: int = 1, init=0.0,
+                   out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Exclusive scan of a 1-D tensor: out[0] = init, out[k] = init op y[k-1]
+    with y the inclusive scan of the policy (n outputs; ``out`` may be ``x``)."""
+    return _scan_ex(x, policy, B, init, "exclusive", out, stream, "exclusive_scan")
+
+
+def scan_include_initial(x: torch.Tensor, policy="iterated_pairwise", B: int = 1, init=0.0,
+                         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The include_initial form: n + 1 outputs, out[0] = init and
+    out[k] = init op y[k-1] for k = 1..n."""
+    return _scan_ex(x, policy, B, init, "include_initial", out, stream, "scan_include_initial")
+
+
+def _scan_ex_batched(x, policy, B, init, dim, mode, out, stream, what):
+    if x.dim() != 2:
+        raise ValueError("%s expects a 2-D tensor" % what)
+    xd, host = _on_device(x)
+    dt = _dtype_code(xd)
+    d = dim % 2
+    n, batch = xd.shape[d], xd.shape[1 - d]
+    es, bs = xd.stride(d), xd.stride(1 - d)
+    md = MODES[mode]
+    m = n + (1 if md == 2 else 0)
+    shape = (m, batch) if d == 0 else (batch, m)
+    o = out if out is not None else torch.empty(shape, dtype=xd.dtype, device=xd.device)
+    if tuple(o.shape) != shape or o.dtype != xd.dtype:
+        raise ValueError("out must have shape %s and x's dtype" % (shape,))
+    oes, obs = o.stride(d), o.stride(1 - d)
+    p = _policy(policy)
+    sp = _stream_ptr(stream)
+    nb = lib().cr_scan_ex_batched_workspace_bytes(batch, n, p, int(B), md, dt)
+    if nb == 0:
+        raise ValueError("invalid scan arguments")
+    ws = _WS.get(xd.device, stream, nb)
+    ini = _init_buffer(init, dt)
+    _check(lib().cr_scan_ex_batched(xd.data_ptr() if xd.numel() else None, o.data_ptr(), batch,
+                                    n, es, bs, oes, obs, p, int(B), md, ctypes.byref(ini), dt,
+                                    ws.data_ptr(), ws.numel(), sp), "cr_scan_ex_batched")
+    return o.to("cpu") if host else o
+
+
+def exclusive_scan_batched(x: torch.Tensor, policy="left_fold", B: int = 1, init=0.0,
+                           dim: int = 0, out: torch.Tensor | None = None,
+                           stream=None) -> torch.Tensor:
+    """Independent exclusive scans along ``dim`` of a 2-D tensor."""
+    return _scan_ex_batched(x, policy, B, init, dim, "exclusive", out, stream,
+                            "exclusive_scan_batched")
+
+
+def scan_include_initial_batched(x: torch.Tensor, policy="left_fold", B: int = 1, init=0.0,
+                                 dim: int = 0, out: torch.Tensor | None = None,
+                                 stream=None) -> torch.Tensor:
+    """Independent include_initial scans along ``dim``: n levels give n + 1
+    values (e.g. cell values to interface values of a level-major column
+    array, the first being init)."""
+    return _scan_ex_batched(x, policy, B, init, dim, "include_initial", out, stream,
+                            "scan_include_initial_batched")
+
+
 def sync_status(device=None, stream=None) -> None:
     """Synchronise the stream and raise if the last call on its workspace
     reported a device-side timeout."""
@@ -332,4 +422,5 @@ def measure_int_add_rate(device="cuda", stream=None) -> float:
 
 
 __all__ = ["reduce", "reduce_batched", "inclusive_scan", "inclusive_scan_batched",
-           "sync_status", "lib", "workspace", "launch_count", "profile_enable", "profile_collect", "measure_add_peak", "add_pairs_int", "measure_int_add_rate", "CrError", "POLICIES", "SIGNATURES"]
+           "exclusive_scan", "scan_include_initial", "exclusive_scan_batched",
+           "scan_include_initial_batched", "MODES", "sync_status", "lib", "workspace", "launch_count", "profile_enable", "profile_collect", "measure_add_peak", "add_pairs_int", "measure_int_add_rate", "CrError", "POLICIES", "SIGNATURES"]

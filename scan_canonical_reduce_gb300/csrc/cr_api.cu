@@ -102,20 +102,43 @@ size_t cr_scan_batched_workspace_bytes(int64_t batch, int64_t n, cr_policy p, in
   return cr::plan_scan(batch, n, p, B, esize(dt)).ws_bytes;
 }
 
+static bool mode_ok(int mode) { return mode == CR_EXCLUSIVE || mode == CR_INCLUDE_INITIAL; }
+
+size_t cr_scan_ex_workspace_bytes(int64_t n, cr_policy p, int64_t B, cr_scan_mode mode,
+                                  cr_dtype dt) {
+  if (esize(dt) == 0 || n < 0 || !mode_ok(mode) || !cr::scan_args_ok(p, B)) return 0;
+  return cr::plan_scan(1, n, p, B, esize(dt), mode).ws_bytes;
+}
+
+size_t cr_scan_ex_batched_workspace_bytes(int64_t batch, int64_t n, cr_policy p, int64_t B,
+                                          cr_scan_mode mode, cr_dtype dt) {
+  if (esize(dt) == 0 || n < 0 || batch < 0 || !mode_ok(mode) || !cr::scan_args_ok(p, B))
+    return 0;
+  return cr::plan_scan(batch, n, p, B, esize(dt), mode).ws_bytes;
+}
+
+// Shared by every scan entry point. mode 0 = inclusive (out uses x's
+// strides, no init); 1-D calls (contiguous) reject partial overlap of the
+// input and output ranges; batched calls with out == x need equal strides.
 static cr_status scan_impl(const void* x, void* out, int64_t batch, int64_t n, int64_t es,
-                           int64_t bs, cr_policy p, int64_t B, cr_dtype dt, void* ws,
+                           int64_t bs, int64_t oes, int64_t obs, cr_policy p, int64_t B,
+                           int mode, const void* init_host, cr_dtype dt, void* ws,
                            size_t ws_bytes, void* stream, bool contiguous) {
   const size_t sz = esize(dt);
   if (sz == 0 || n < 0 || batch < 0 || !cr::scan_args_ok(p, B)) return CR_ERR_INVALID_ARG;
-  if (batch > 0 && n > 0 && (x == nullptr || out == nullptr)) return CR_ERR_INVALID_ARG;
+  if (mode != 0 && (!mode_ok(mode) || init_host == nullptr)) return CR_ERR_INVALID_ARG;
+  const int64_t m = n + (mode == CR_INCLUDE_INITIAL ? 1 : 0);
+  if (batch > 0 && m > 0 && out == nullptr) return CR_ERR_INVALID_ARG;
+  if (batch > 0 && n > 0 && x == nullptr) return CR_ERR_INVALID_ARG;
   if ((x && !aligned(x, sz)) || (out && !aligned(out, sz))) return CR_ERR_INVALID_ARG;
-  if (contiguous && x != out && n > 0) {
+  if (contiguous && x != out && n > 0 && m > 0) {
     const char* a = static_cast<const char*>(x);
     const char* o = static_cast<const char*>(out);
-    const size_t bytes = (size_t)n * sz;
-    if (a < o + bytes && o < a + bytes) return CR_ERR_INVALID_ARG;  // partial overlap
+    if (a < o + (size_t)m * sz && o < a + (size_t)n * sz) return CR_ERR_INVALID_ARG;
   }
-  const cr::ScanPlan plan = cr::plan_scan(batch, n, p, B, sz);
+  if (!contiguous && x == out && x != nullptr && (oes != es || obs != bs))
+    return CR_ERR_INVALID_ARG;
+  const cr::ScanPlan plan = cr::plan_scan(batch, n, p, B, sz, mode);
   const cr_status ws_ok = check_ws(ws, ws_bytes, plan.ws_bytes);
   if (ws_ok != CR_OK) return ws_ok;
   if (!plan.supported) return CR_ERR_UNSUPPORTED;
@@ -123,26 +146,50 @@ static cr_status scan_impl(const void* x, void* out, int64_t batch, int64_t n, i
   cudaError_t e = clear_status(ws, s);
   if (e != cudaSuccess) return CR_ERR_CUDA;
   char* w = static_cast<char*>(ws);
-  if (dt == CR_F64)
+  if (dt == CR_F64) {
+    double init = 0.0;
+    if (mode != 0) std::memcpy(&init, init_host, sizeof(init));
     e = cr::run_scan<double>(plan, static_cast<const double*>(x), static_cast<double*>(out),
-                             es, bs, w, s);
-  else
+                             es, bs, oes, obs, init, w, s);
+  } else {
+    float init = 0.0f;
+    if (mode != 0) std::memcpy(&init, init_host, sizeof(init));
     e = cr::run_scan<float>(plan, static_cast<const float*>(x), static_cast<float*>(out), es,
-                            bs, w, s);
+                            bs, oes, obs, init, w, s);
+  }
   return from_cuda(e);
 }
 
 cr_status cr_inclusive_scan(const void* x, void* out, int64_t n, cr_policy p, int64_t B,
                             cr_dtype dt, void* ws, size_t ws_bytes, void* stream) {
-  return scan_impl(x, out, 1, n, 1, n, p, B, dt, ws, ws_bytes, stream, true);
+  return scan_impl(x, out, 1, n, 1, n, 1, n, p, B, 0, nullptr, dt, ws, ws_bytes, stream, true);
 }
 
 cr_status cr_inclusive_scan_batched(const void* x, void* out, int64_t batch, int64_t n,
                                     int64_t elem_stride, int64_t batch_stride, cr_policy p,
                                     int64_t B, cr_dtype dt, void* ws, size_t ws_bytes,
                                     void* stream) {
-  return scan_impl(x, out, batch, n, elem_stride, batch_stride, p, B, dt, ws, ws_bytes, stream,
-                   false);
+  return scan_impl(x, out, batch, n, elem_stride, batch_stride, elem_stride, batch_stride, p,
+                   B, 0, nullptr, dt, ws, ws_bytes, stream, false);
+}
+
+cr_status cr_scan_ex(const void* x, void* out, int64_t n, cr_policy p, int64_t B,
+                     cr_scan_mode mode, const void* init_host, cr_dtype dt, void* ws,
+                     size_t ws_bytes, void* stream) {
+  if (!mode_ok(mode)) return CR_ERR_INVALID_ARG;
+  const int64_t m = n + (mode == CR_INCLUDE_INITIAL ? 1 : 0);
+  return scan_impl(x, out, 1, n, 1, n, 1, m, p, B, mode, init_host, dt, ws, ws_bytes, stream,
+                   true);
+}
+
+cr_status cr_scan_ex_batched(const void* x, void* out, int64_t batch, int64_t n,
+                             int64_t elem_stride, int64_t batch_stride,
+                             int64_t out_elem_stride, int64_t out_batch_stride, cr_policy p,
+                             int64_t B, cr_scan_mode mode, const void* init_host, cr_dtype dt,
+                             void* ws, size_t ws_bytes, void* stream) {
+  if (!mode_ok(mode)) return CR_ERR_INVALID_ARG;
+  return scan_impl(x, out, batch, n, elem_stride, batch_stride, out_elem_stride,
+                   out_batch_stride, p, B, mode, init_host, dt, ws, ws_bytes, stream, false);
 }
 
 cr_status cr_sync_status(void* ws, void* stream) {

@@ -29,6 +29,9 @@ enum KernelId : int {
   kKScanLocal,
   kKCarryFixup,
   kKScanPairwise,
+  kKApplyInit,
+  kKFillInit,
+  kKCarryFixupShift,
   kKernelCount
 };
 

@@ -184,6 +184,47 @@ __device__ __forceinline__ void store8(T* p, int64_t cnt, const T (&v)[kE]) {
     if (e < cnt) p[e] = v[e];
 }
 
+// The last valid one of a thread's values (cnt >= 1), without dynamic
+// indexing so that the values stay in registers.
+template <class T>
+__device__ __forceinline__ T last_of(const T (&w)[kE], int64_t cnt) {
+  T r = w[0];
+#pragma unroll
+  for (int e = 1; e < kE; ++e)
+    if (e == cnt - 1) r = w[e];
+  return r;
+}
+
+// Shifted write of a thread's results y[i0 .. i0+cnt) for the exclusive and
+// include_initial forms: out[i] = f(y[i - 1]) at the thread's own positions
+// (so in-place scans stay correct and vector stores stay aligned), and
+// out[0] = init, where f(v) = init op v (kInit) or v (in-block values that a
+// fix-up pass completes). y[i0 - 1] is the previous lane's last value
+// (shuffle), the previous warp's (shared memory) or, for the tile's first
+// thread, tile_prev. With a.emit_last the thread holding y[n - 1] also
+// writes out[n] = f(y[n - 1]). Every thread of the block must call this: it
+// synchronises the block.
+template <class T, bool kInit>
+__device__ __forceinline__ void emit_shifted(T* out, int64_t i0, int64_t cnt, const T (&w)[kE],
+                                             T tile_prev, T init, const ScanArgs& a,
+                                             T* s_last) {
+  const unsigned full = 0xffffffffu;
+  const int t = threadIdx.x, lane = t & 31, wp = t >> 5;
+  const T up = __shfl_up_sync(full, w[kE - 1], 1);
+  if (lane == 31) s_last[wp] = w[kE - 1];
+  __syncthreads();
+  const T prev = lane ? up : (wp ? s_last[wp - 1] : tile_prev);
+  T o[kE];
+  o[0] = (i0 == 0) ? init : (kInit ? add_rn(init, prev) : prev);
+#pragma unroll
+  for (int e = 1; e < kE; ++e) o[e] = kInit ? add_rn(init, w[e - 1]) : w[e - 1];
+  store8(out + i0, cnt, o);
+  if (a.emit_last && cnt > 0 && i0 + cnt == a.n) {
+    const T yl = last_of(w, cnt);
+    out[a.n] = kInit ? add_rn(init, yl) : yl;
+  }
+}
+
 // In-block pyramid over the 256 thread aggregates, all levels kept:
 // level p (p = 0..8) holds 256 >> p nodes at lvl[lvl_base(p) + q].
 __device__ __forceinline__ int lvl_base(int p) {
@@ -278,13 +319,14 @@ scan_up_kernel(const T* __restrict__ x, T* __restrict__ pyr, int* __restrict__ c
 }
 
 // ---------------------------------------------------------------- down pass
-template <class T, int S>
+template <class T, int S, bool kShift>
 __global__ void __launch_bounds__(kScanThreads)
 scan_down_kernel(const T* x, T* out, const T* __restrict__ pyr, const T* __restrict__ carries,
-                 ScanArgs a) {
+                 ScanArgs a, T init) {
   __shared__ T lvl[2 * kScanThreads];
   __shared__ T tile_nodes[64];
   __shared__ T tile_carry;
+  __shared__ T s_last[kScanThreads / 32];
   constexpr int NS = kE / S;
   const int t = threadIdx.x;
   const int64_t b = blockIdx.x;
@@ -316,24 +358,24 @@ scan_down_kernel(const T* x, T* out, const T* __restrict__ pyr, const T* __restr
   }
   if (t < full_threads) lvl[t] = tagg;
   build_tile_pyramid(lvl, t, full_threads);  // also publishes tile_nodes/tile_carry
-  if (cnt == 0) return;
+  if (!kShift && cnt == 0) return;
 
   // thread-level prefix nodes, lowest bit first (right-nested)
   for (int p = 0; p < thread_bits; ++p) {
-    if ((t >> p) & 1) {
+    if (((t >> p) & 1) && cnt > 0) {
       const T nd = lvl[lvl_base(p) + (t >> p) - 1];
       apply_node(nd, w);
     }
   }
   // tile-level prefix nodes, lowest bit first
   for (int p = 0; p < tile_bits; ++p) {
-    if ((b >> p) & 1) {
+    if (((b >> p) & 1) && cnt > 0) {
       const T nd = tile_nodes[p];
       apply_node(nd, w);
     }
   }
   // block carry: out[i] = C_{k-1} op P(i) for blocks k >= 1
-  if (a.carry) {
+  if (a.carry && cnt > 0) {
     if (a.logB >= kLogTile) {
       if (((b * kTile) >> a.logB) >= 1) {
         const T c = tile_carry;
@@ -348,7 +390,30 @@ scan_down_kernel(const T* x, T* out, const T* __restrict__ pyr, const T* __restr
       }
     }
   }
-  store8(out + i0, cnt, w);
+  if (!kShift) {
+    store8(out + i0, cnt, w);
+    return;
+  }
+  // y[2048 b - 1]: blocks span tiles here (B > 2048). At a block start it is
+  // C_{k-1}; else C_{k-1} op P with P = tree(x[kB .. 2048 b)), the in-block
+  // tile-level nodes folded right-nested (no carry in block 0).
+  T tile_prev = T(0);
+  if (t == 0 && b > 0) {
+    const int64_t k = (b * kTile) >> a.logB;
+    if (((b * kTile) & (((int64_t)1 << a.logB) - 1)) == 0) {
+      tile_prev = carries[k - 1];
+    } else {
+      bool has = false;
+      for (int p = 0; p < tile_bits; ++p) {
+        if ((b >> p) & 1) {
+          tile_prev = has ? add_rn(tile_nodes[p], tile_prev) : tile_nodes[p];
+          has = true;
+        }
+      }
+      if (k >= 1) tile_prev = add_rn(tile_carry, tile_prev);
+    }
+  }
+  emit_shifted<T, true>(out, i0, cnt, w, tile_prev, init, a, s_last);
 }
 
 // ------------------------------------------- one-pass tile protocol
@@ -403,12 +468,13 @@ __device__ __forceinline__ T wait_node(const T* pyr, const int* ready, int* stat
 }
 
 // ------------------------------------------- iterated_pairwise, one pass
-template <class T>
+template <class T, bool kShift>
 __global__ void __launch_bounds__(kScanThreads)
 scan_onepass_kernel(const T* x, T* out, T* pyr, int* counters, int* ready, int* tile_ctr,
-                    int* status, ScanArgs a, int64_t skip_publish) {
+                    int* status, ScanArgs a, int64_t skip_publish, T init) {
   __shared__ T lvl[2 * kScanThreads];
   __shared__ T tile_nodes[64];
+  __shared__ T s_last[kScanThreads / 32];
   __shared__ int64_t s_tile;
   const int t = threadIdx.x;
   if (t == 0) s_tile = atomicAdd(tile_ctr, 1);
@@ -440,11 +506,28 @@ scan_onepass_kernel(const T* x, T* out, T* pyr, int* counters, int* ready, int* 
   if (t < tile_bits && ((b >> t) & 1))
     tile_nodes[t] = wait_node(pyr, ready, status, a, t, (b >> t) - 1);
   __syncthreads();
-  if (cnt == 0) return;
-  for (int p = 0; p < tile_bits; ++p) {
-    if ((b >> p) & 1) apply_node(tile_nodes[p], w);
+  if (!kShift && cnt == 0) return;
+  if (cnt > 0) {
+    for (int p = 0; p < tile_bits; ++p) {
+      if ((b >> p) & 1) apply_node(tile_nodes[p], w);
+    }
   }
-  store8(out + i0, cnt, w);
+  if (!kShift) {
+    store8(out + i0, cnt, w);
+    return;
+  }
+  // y[2048 b - 1] = tree(x[0 .. 2048 b)): the tile-level nodes, right-nested
+  T tile_prev = T(0);
+  if (t == 0 && b > 0) {
+    bool has = false;
+    for (int p = 0; p < tile_bits; ++p) {
+      if ((b >> p) & 1) {
+        tile_prev = has ? add_rn(tile_nodes[p], tile_prev) : tile_nodes[p];
+        has = true;
+      }
+    }
+  }
+  emit_shifted<T, true>(out, i0, cnt, w, tile_prev, init, a, s_last);
 }
 
 // ------------------------------------------------------ pairwise, down pass
@@ -463,10 +546,11 @@ scan_onepass_kernel(const T* x, T* out, T* pyr, int* counters, int* ready, int* 
 // first by the up pass (scan_up_kernel), and this pass only reads it. (A
 // single pass that waits for the nodes measured 2.5x slower here: a tile's
 // own add work is too short to hide the pyramid's completion latency.)
-template <class T>
+template <class T, bool kShift>
 __global__ void __launch_bounds__(kScanThreads)
-scan_pairwise_kernel(const T* x, T* out, const T* __restrict__ pyr, ScanArgs a) {
+scan_pairwise_kernel(const T* x, T* out, const T* __restrict__ pyr, ScanArgs a, T init) {
   __shared__ T lvl[2 * kScanThreads];
+  __shared__ T s_last[kScanThreads / 32];
   __shared__ T nodes_b[32], nodes_b1[32];  // tile-level nodes of b and of b + 1
   __shared__ T s_base[kScanThreads / 32 + 1];  // E_{32 w}, w = 0..8 (E_256 = Y_{b+1})
   const unsigned full = 0xffffffffu;
@@ -552,15 +636,19 @@ scan_pairwise_kernel(const T* x, T* out, const T* __restrict__ pyr, ScanArgs a) 
   w[5] = add_rn(w[3], p45);
   w[6] = add_rn(w[5], v[6]);
   w[7] = E1;
-  store8(out + i0, cnt, w);
+  if (kShift)  // y[2048 b - 1] = W(2048 b) = Y_b
+    emit_shifted<T, true>(out, i0, cnt, w, s_base[0], init, a, s_last);
+  else
+    store8(out + i0, cnt, w);
 }
 
 // ------------------------------- block_dyadic, blocks inside a tile (B <= 2048)
 // Pass 1: the in-block iterated_pairwise values P(i) and the block totals T_k.
-template <class T, int S>
+template <class T, int S, bool kShift>
 __global__ void __launch_bounds__(kScanThreads)
 scan_local_kernel(const T* x, T* out, T* __restrict__ totals, ScanArgs a) {
   __shared__ T lvl[2 * kScanThreads];
+  __shared__ T s_last[kScanThreads / 32];
   constexpr int NS = kE / S;
   constexpr int LS = Log2<S>::value;
   const int t = threadIdx.x;
@@ -588,7 +676,10 @@ scan_local_kernel(const T* x, T* out, T* __restrict__ totals, ScanArgs a) {
     for (int q = 5; q < p; ++q)
       if (((t >> q) & 1) && cnt > 0) apply_node(lvl[lvl_base(q) + (t >> q) - 1], w);
   }
-  store8(out + i0, cnt, w);
+  if (kShift)  // out[i + 1] = P(i); a tile starts a block, whose start the fix-up writes
+    emit_shifted<T, false>(out, i0, cnt, w, T(0), T(0), a, s_last);
+  else
+    store8(out + i0, cnt, w);
 }
 
 // Pass 2: out[i] = C_{k-1} op P(i) for every element of blocks k >= 1.
@@ -610,6 +701,61 @@ carry_fixup_kernel(T* out, const T* __restrict__ carries, int64_t n, int logB) {
     const int64_t i = i0 + e;
     out[i] = add_rn(ldg(carries + (i >> logB) - 1), out[i]);
   }
+}
+
+// Pass 2 of the shifted forms: out holds P(j - 1) at j (the local pass wrote
+// it one place right). For 0 <= j < m: out[0] = init; at a block start
+// j = kB < n, out[j] = init op C_{k-1} (the end of block k - 1); otherwise
+// j - 1 lies in block k = (j - 1) >> logB and
+// out[j] = init op (C_{k-1} op P(j - 1)), or init op P(j - 1) in block 0.
+template <class T>
+__global__ void __launch_bounds__(256)
+carry_fixup_shift_kernel(T* out, const T* __restrict__ carries, int64_t n, int64_t m, int logB,
+                         T init) {
+  const int64_t j0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * kE;
+  if (j0 >= m) return;
+  const int64_t bmask = ((int64_t)1 << logB) - 1;
+  if (j0 + kE <= n && logB >= kLogE) {  // j0 .. j0+7 in one block, j0 the only possible start
+    const int64_t k = j0 >> logB;
+    const T c = k >= 1 ? ldg(carries + k - 1) : T(0);
+    T v[kE];
+    load8(out + j0, kE, v);
+#pragma unroll
+    for (int e = 0; e < kE; ++e) v[e] = add_rn(init, k >= 1 ? add_rn(c, v[e]) : v[e]);
+    if ((j0 & bmask) == 0) v[0] = (j0 == 0) ? init : add_rn(init, ldg(carries + k - 1));
+    store8(out + j0, kE, v);
+    return;
+  }
+  for (int e = 0; e < kE && j0 + e < m; ++e) {
+    const int64_t j = j0 + e;
+    if (j == 0) {
+      out[0] = init;
+    } else if ((j & bmask) == 0 && j < n) {
+      out[j] = add_rn(init, ldg(carries + (j >> logB) - 1));
+    } else {
+      const int64_t k = (j - 1) >> logB;
+      const T v = out[j];
+      out[j] = add_rn(init, k >= 1 ? add_rn(ldg(carries + k - 1), v) : v);
+    }
+  }
+}
+
+// out[0] = init, out[k] = init op out[k] for 0 < k < m (the shifted left
+// fold: the chain wrote y[k - 1] to out[k]).
+template <class T>
+__global__ void __launch_bounds__(256)
+apply_init_kernel(T* out, int64_t m, T init) {
+  const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (k >= m) return;
+  out[k] = (k == 0) ? init : add_rn(init, out[k]);
+}
+
+// out[q * stride] = init for q < count (include_initial of empty sequences).
+template <class T>
+__global__ void __launch_bounds__(256)
+fill_init_kernel(T* out, int64_t count, int64_t stride, T init) {
+  const int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (q < count) out[q * stride] = init;
 }
 
 // --------------------------------------------------------------- carry chain
@@ -641,21 +787,32 @@ __global__ void carry_chain_kernel(const T* src, T* carries, int64_t K) {
 }
 
 // ------------------------------------------------ batched: thread per sequence
-// Sequence q: element k at x[q*bs + k*es]; its result at out[q*bs + k*es].
+// Sequence q: element k at x[q*bs + k*es]; inclusive results go to
+// out[q*obs + k*oes]. Shifted forms (shift = 1): out[q*obs] = init and
+// y[k] goes to position k + 1 as init op y[k], for k + 1 < m. The next
+// element is loaded before the current result is stored, so that an
+// in-place call (out == x, same strides) reads every element first.
 template <class T, int LV>
 __global__ void __launch_bounds__(256)
 scan_seq_kernel(const T* x, T* out, int64_t batch, int64_t n, int64_t es, int64_t bs,
-                int policy, int64_t B) {
+                int64_t oes, int64_t obs, int policy, int64_t B, int shift, int64_t m, T init) {
   const int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (q >= batch) return;
   const T* xp = x + q * bs;
-  T* yp = out + q * bs;
+  T* yp = out + q * obs;
+  auto put = [&](int64_t k, T v) {  // the result y[k]
+    if (!shift) yp[k * oes] = v;
+    else if (k + 1 < m) yp[(k + 1) * oes] = add_rn(init, v);
+  };
+  T cur = xp[0];
+  if (shift) yp[0] = init;
   if (policy == CR_LEFT_FOLD) {
-    T acc = xp[0];
-    yp[0] = acc;
-    for (int64_t k = 1; k < n; ++k) {
-      acc = add_rn(acc, xp[k * es]);
-      yp[k * es] = acc;
+    T acc = cur;
+    for (int64_t k = 0; k < n; ++k) {
+      const T nxt = (k + 1 < n) ? xp[(k + 1) * es] : T(0);
+      if (k > 0) acc = add_rn(acc, cur);
+      put(k, acc);
+      cur = nxt;
     }
     return;
   }
@@ -666,7 +823,10 @@ scan_seq_kernel(const T* x, T* out, int64_t batch, int64_t n, int64_t es, int64_
     RegStack<T, LV> st;
     st.reset();
     for (int64_t e = 0; e < len; ++e) {
-      st.push(xp[(k0 + e) * es], 0);
+      const int64_t k = k0 + e;
+      const T nxt = (k + 1 < n) ? xp[(k + 1) * es] : T(0);
+      st.push(cur, 0);
+      cur = nxt;
       T acc = T(0);
       if (policy == CR_PAIRWISE) {  // maximal subtrees folded from the left
         bool has = false;
@@ -680,7 +840,7 @@ scan_seq_kernel(const T* x, T* out, int64_t batch, int64_t n, int64_t es, int64_
       } else {  // tree(prefix): folded from the top down (right-nested)
         st.fold_onto(acc, false);
       }
-      yp[(k0 + e) * es] = (k0 == 0) ? acc : add_rn(carry, acc);
+      put(k, (k0 == 0) ? acc : add_rn(carry, acc));
     }
     if (policy == CR_BLOCK_DYADIC && k0 + blk < n) {
       T tk = T(0);
@@ -716,16 +876,25 @@ int ilog2(int64_t v) {
 size_t round256(size_t v) { return (v + 255) & ~size_t(255); }
 }  // namespace
 
-ScanPlan plan_scan(int64_t batch, int64_t n, cr_policy p, int64_t B, size_t esize) {
+ScanPlan plan_scan(int64_t batch, int64_t n, cr_policy p, int64_t B, size_t esize,
+                   int out_mode) {
   ScanPlan plan;
   plan.batch = batch;
   plan.n = n;
   plan.policy = p;
   plan.B = (p == CR_BLOCK_DYADIC) ? B : 0;
+  plan.out_mode = out_mode;
+  const bool shift = out_mode != 0;
+  plan.m = n + (out_mode == CR_INCLUDE_INITIAL ? 1 : 0);
   size_t off = kHeaderBytes;
   plan.supported = true;
-  if (n == 0 || batch == 0) {
+  if (batch == 0 || plan.m == 0) {
     plan.kind = ScanPlan::kEmpty;
+    plan.ws_bytes = off;
+    return plan;
+  }
+  if (n == 0) {  // include_initial of empty sequences
+    plan.kind = ScanPlan::kInitOnly;
     plan.ws_bytes = off;
     return plan;
   }
@@ -739,14 +908,19 @@ ScanPlan plan_scan(int64_t batch, int64_t n, cr_policy p, int64_t B, size_t esiz
     return plan;
   }
   if (p == CR_LEFT_FOLD || (block && B == 1)) {
-    plan.kind = ScanPlan::kChainOnly;  // every element is its own block
-    if (n >= kParallelChainMin) {
+    // every element is its own block: the left-fold chain (into out + 1 for
+    // the shifted forms, then init applied)
+    plan.kind = ScanPlan::kChainOnly;
+    plan.chain_n = shift ? plan.m - 1 : n;
+    if (plan.chain_n >= kParallelChainMin) {
       plan.parallel_chain = true;
-      plan.chain = plan_chain(n);
+      plan.chain = plan_chain(plan.chain_n);
       plan.chain_ws = off;
       off += round256(plan.chain.bytes);
-      plan.copy_ws = off;  // used only when out == x
-      off += round256((size_t)n * esize);
+    }
+    if (plan.chain_n > 0 && (plan.parallel_chain || shift)) {
+      plan.copy_ws = off;  // used only in place (out == x)
+      off += round256((size_t)plan.chain_n * esize);
     }
     plan.ws_bytes = off;
     return plan;
@@ -815,18 +989,28 @@ ScanPlan plan_scan(int64_t batch, int64_t n, cr_policy p, int64_t B, size_t esiz
 
 template <class T>
 cudaError_t run_scan(const ScanPlan& plan, const T* x, T* out, int64_t es, int64_t bs,
-                     char* ws, cudaStream_t s) {
+                     int64_t oes, int64_t obs, T init, char* ws, cudaStream_t s) {
   cudaError_t e = cudaSuccess;
+  const bool shift = plan.out_mode != 0;
   switch (plan.kind) {
     case ScanPlan::kEmpty: return cudaSuccess;
+    case ScanPlan::kInitOnly: {
+      if ((plan.batch + 255) / 256 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+      CR_LAUNCH(kKFillInit, s,
+                fill_init_kernel<T><<<(unsigned)((plan.batch + 255) / 256), 256, 0, s>>>(
+                    out, plan.batch, obs, init));
+      return cudaGetLastError();
+    }
     case ScanPlan::kPerSequence: {
       if ((plan.batch + 255) / 256 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
       const unsigned grid = (unsigned)((plan.batch + 255) / 256);
       const int LV = plan.stack_levels;
-#define CR_SEQ(LVV)                                                                  \
-  CR_LAUNCH(kKScanSeq, s,                                                            \
-            scan_seq_kernel<T, LVV><<<grid, 256, 0, s>>>(x, out, plan.batch, plan.n, \
-                                                         es, bs, (int)plan.policy, plan.B))
+#define CR_SEQ(LVV)                                                                      \
+  CR_LAUNCH(kKScanSeq, s,                                                                \
+            scan_seq_kernel<T, LVV><<<grid, 256, 0, s>>>(x, out, plan.batch, plan.n, es, \
+                                                         bs, oes, obs, (int)plan.policy, \
+                                                         plan.B, shift ? 1 : 0, plan.m,  \
+                                                         init))
       if (LV <= 5) CR_SEQ(5);
       else if (LV <= 9) CR_SEQ(9);
       else if (LV <= 17) CR_SEQ(17);
@@ -835,18 +1019,36 @@ cudaError_t run_scan(const ScanPlan& plan, const T* x, T* out, int64_t es, int64
       return cudaGetLastError();
     }
     case ScanPlan::kChainOnly: {
-      if (!plan.parallel_chain) {
-        CR_LAUNCH(kKCarryChain, s, carry_chain_kernel<T><<<1, 32, 0, s>>>(x, out, plan.n));
-        return cudaGetLastError();
+      // inclusive: out[k] = y[k]; shifted: y[k] into out[k + 1], then init
+      T* dst = shift ? out + 1 : out;
+      const int64_t K = plan.chain_n;
+      if (K > 0) {
+        const T* src = x;
+        // in place, the chain must not overwrite input it has still to read:
+        // the parallel chain's fallback re-reads all of it, and a shifted
+        // output runs one element ahead of the input. Keep a copy then.
+        if (out == x && (plan.parallel_chain || shift)) {
+          T* copy = reinterpret_cast<T*>(ws + plan.copy_ws);
+          e = cudaMemcpyAsync(copy, x, (size_t)K * sizeof(T), cudaMemcpyDeviceToDevice, s);
+          if (e != cudaSuccess) return e;
+          src = copy;
+        }
+        if (!plan.parallel_chain) {
+          CR_LAUNCH(kKCarryChain, s, carry_chain_kernel<T><<<1, 32, 0, s>>>(src, dst, K));
+          if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        } else if ((e = run_chain<T>(plan.chain, src, dst, ws + plan.chain_ws, s)) !=
+                   cudaSuccess) {
+          return e;
+        }
       }
-      const T* src = x;
-      if (x == out) {  // the chain's fallback re-reads its input: keep a copy
-        T* copy = reinterpret_cast<T*>(ws + plan.copy_ws);
-        e = cudaMemcpyAsync(copy, x, (size_t)plan.n * sizeof(T), cudaMemcpyDeviceToDevice, s);
-        if (e != cudaSuccess) return e;
-        src = copy;
+      if (shift) {
+        const int64_t blocks = (plan.m + 255) / 256;
+        if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+        CR_LAUNCH(kKApplyInit, s,
+                  apply_init_kernel<T><<<(unsigned)blocks, 256, 0, s>>>(out, plan.m, init));
+        e = cudaGetLastError();
       }
-      return run_chain<T>(plan.chain, src, out, ws + plan.chain_ws, s);
+      return e;
     }
     case ScanPlan::kTiled: break;
   }
@@ -858,6 +1060,7 @@ cudaError_t run_scan(const ScanPlan& plan, const T* x, T* out, int64_t es, int64
   a.pyr_levels = plan.pyr_levels;
   a.carry = block ? 1 : 0;
   a.totals_level = block ? plan.totals_level : -1;
+  a.emit_last = plan.out_mode == CR_INCLUDE_INITIAL ? 1 : 0;
   for (int l = 0; l < kMaxLevels; ++l) {
     a.pyr_off[l] = plan.pyr_off[l];
     a.cnt_off[l] = plan.cnt_off[l];
@@ -877,9 +1080,14 @@ cudaError_t run_scan(const ScanPlan& plan, const T* x, T* out, int64_t es, int64
     int* ready = reinterpret_cast<int*>(ws + plan.ready_ws);
     int* tctr = reinterpret_cast<int*>(ws + plan.tilectr_ws);
     int* status = reinterpret_cast<int*>(ws);
-    CR_LAUNCH(kKScanOnePass, s,
-              scan_onepass_kernel<T><<<grid, kScanThreads, 0, s>>>(
-                  x, out, pyr, counters, ready, tctr, status, a, debug_skip_publish()));
+    CR_LAUNCH(kKScanOnePass, s, {
+      if (shift)
+        scan_onepass_kernel<T, true><<<grid, kScanThreads, 0, s>>>(
+            x, out, pyr, counters, ready, tctr, status, a, debug_skip_publish(), init);
+      else
+        scan_onepass_kernel<T, false><<<grid, kScanThreads, 0, s>>>(
+            x, out, pyr, counters, ready, tctr, status, a, debug_skip_publish(), init);
+    });
     return cudaGetLastError();
   }
 
@@ -892,13 +1100,31 @@ cudaError_t run_scan(const ScanPlan& plan, const T* x, T* out, int64_t es, int64
   };
 
   if (plan.mode == ScanPlan::kLocalFixup) {
+#define CR_LOCAL(SS, SH) \
+  scan_local_kernel<T, SS, SH><<<grid, kScanThreads, 0, s>>>(x, out, totals, a)
     CR_LAUNCH(kKScanLocal, s, {
-      if (S == 8) scan_local_kernel<T, 8><<<grid, kScanThreads, 0, s>>>(x, out, totals, a);
-      else if (S == 4) scan_local_kernel<T, 4><<<grid, kScanThreads, 0, s>>>(x, out, totals, a);
-      else scan_local_kernel<T, 2><<<grid, kScanThreads, 0, s>>>(x, out, totals, a);
+      if (shift) {
+        if (S == 8) CR_LOCAL(8, true);
+        else if (S == 4) CR_LOCAL(4, true);
+        else CR_LOCAL(2, true);
+      } else {
+        if (S == 8) CR_LOCAL(8, false);
+        else if (S == 4) CR_LOCAL(4, false);
+        else CR_LOCAL(2, false);
+      }
     });
+#undef CR_LOCAL
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if ((e = chain(totals)) != cudaSuccess) return e;
+    if (shift) {  // every output: init, carries and the shifted in-block values
+      const int64_t threads = (plan.m + kE - 1) / kE;
+      const int64_t blocks = (threads + 255) / 256;
+      if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+      CR_LAUNCH(kKCarryFixupShift, s,
+                carry_fixup_shift_kernel<T><<<(unsigned)blocks, 256, 0, s>>>(
+                    out, carries, plan.n, plan.m, plan.logB, init));
+      return cudaGetLastError();
+    }
     if (plan.K >= 2) {
       const int64_t nfix = plan.n - plan.B;  // elements of blocks k >= 1
       const int64_t threads = (nfix + kE - 1) / kE;
@@ -916,8 +1142,12 @@ cudaError_t run_scan(const ScanPlan& plan, const T* x, T* out, int64_t es, int64
     CR_LAUNCH(kKScanUp, s,
               scan_up_kernel<T, 8><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    CR_LAUNCH(kKScanPairwise, s,
-              scan_pairwise_kernel<T><<<grid, kScanThreads, 0, s>>>(x, out, pyr, a));
+    CR_LAUNCH(kKScanPairwise, s, {
+      if (shift)
+        scan_pairwise_kernel<T, true><<<grid, kScanThreads, 0, s>>>(x, out, pyr, a, init);
+      else
+        scan_pairwise_kernel<T, false><<<grid, kScanThreads, 0, s>>>(x, out, pyr, a, init);
+    });
     return cudaGetLastError();
   }
 
@@ -929,17 +1159,26 @@ cudaError_t run_scan(const ScanPlan& plan, const T* x, T* out, int64_t es, int64
   });
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if ((e = chain(pyr + plan.pyr_off[plan.logB - kLogTile])) != cudaSuccess) return e;
+#define CR_DOWN(SS, SH) \
+  scan_down_kernel<T, SS, SH><<<grid, kScanThreads, 0, s>>>(x, out, pyr, carries, a, init)
   CR_LAUNCH(kKScanDown, s, {
-    if (S == 8) scan_down_kernel<T, 8><<<grid, kScanThreads, 0, s>>>(x, out, pyr, carries, a);
-    else if (S == 4) scan_down_kernel<T, 4><<<grid, kScanThreads, 0, s>>>(x, out, pyr, carries, a);
-    else scan_down_kernel<T, 2><<<grid, kScanThreads, 0, s>>>(x, out, pyr, carries, a);
+    if (shift) {
+      if (S == 8) CR_DOWN(8, true);
+      else if (S == 4) CR_DOWN(4, true);
+      else CR_DOWN(2, true);
+    } else {
+      if (S == 8) CR_DOWN(8, false);
+      else if (S == 4) CR_DOWN(4, false);
+      else CR_DOWN(2, false);
+    }
   });
+#undef CR_DOWN
   return cudaGetLastError();
 }
 
 template cudaError_t run_scan<double>(const ScanPlan&, const double*, double*, int64_t,
-                                      int64_t, char*, cudaStream_t);
+                                      int64_t, int64_t, int64_t, double, char*, cudaStream_t);
 template cudaError_t run_scan<float>(const ScanPlan&, const float*, float*, int64_t, int64_t,
-                                     char*, cudaStream_t);
+                                     int64_t, int64_t, float, char*, cudaStream_t);
 
 }  // namespace cr

@@ -22,16 +22,22 @@ struct ScanArgs {
   int32_t pyr_levels;        // global pyramid levels kept (level 0: tile aggregates)
   int32_t carry;             // block_dyadic: apply C_{k-1}
   int32_t totals_level;      // block totals: 0 in-thread, p > 0 tile pyramid level, -1 global
+  int32_t emit_last;         // shifted output of n + 1 entries: also write out[n]
   int64_t pyr_off[kMaxLevels];  // element offset of each pyramid level
   int64_t cnt_off[kMaxLevels];  // offset of each level's arrival counters
 };
 
 struct ScanPlan {
-  enum Kind { kEmpty, kPerSequence, kChainOnly, kTiled };
+  // kInitOnly: include_initial of empty sequences (out[0] = init only)
+  enum Kind { kEmpty, kInitOnly, kPerSequence, kChainOnly, kTiled };
   // tiled 1-D scans: one pass (iterated_pairwise), local scan + carry
   // fix-up (block_dyadic, B <= 2048), up/down passes (block_dyadic, B > 2048)
   enum Mode { kOnePass, kLocalFixup, kUpDown };
   Mode mode = kOnePass;
+  // 0: inclusive; CR_EXCLUSIVE / CR_INCLUDE_INITIAL: out[0] = init,
+  // out[k] = init op y[k-1] for k < m (m = n or n + 1)
+  int out_mode = 0;
+  int64_t m = 0;             // outputs per sequence
   bool supported = false;
   Kind kind = kEmpty;
   int64_t batch = 0, n = 0;
@@ -54,7 +60,8 @@ struct ScanPlan {
   bool parallel_chain = false;
   ChainPlan chain;
   size_t chain_ws = 0;
-  size_t copy_ws = 0;        // 1-D left_fold in place: private copy of x
+  size_t copy_ws = 0;        // 1-D left_fold in place (or shifted): private copy of x
+  int64_t chain_n = 0;       // 1-D left_fold: elements the chain folds
   size_t ws_bytes = kHeaderBytes;
 };
 
@@ -65,10 +72,16 @@ bool scan_args_ok(cr_policy p, int64_t B);
 // CR_ERR_TIMEOUT (-1 = off).
 int64_t debug_skip_publish();
 void set_debug_skip_publish(int64_t tile);
-ScanPlan plan_scan(int64_t batch, int64_t n, cr_policy p, int64_t B, size_t esize);
+// out_mode: 0 inclusive, CR_EXCLUSIVE or CR_INCLUDE_INITIAL.
+ScanPlan plan_scan(int64_t batch, int64_t n, cr_policy p, int64_t B, size_t esize,
+                   int out_mode = 0);
 
+// Batched scans read x[b*batch_stride + i*elem_stride] and write
+// out[b*out_batch_stride + k*out_elem_stride]; init is used by the shifted
+// modes only.
 template <class T>
 cudaError_t run_scan(const ScanPlan& plan, const T* x, T* out, int64_t elem_stride,
-                     int64_t batch_stride, char* ws, cudaStream_t s);
+                     int64_t batch_stride, int64_t out_elem_stride, int64_t out_batch_stride,
+                     T init, char* ws, cudaStream_t s);
 
 }  // namespace cr

@@ -86,6 +86,37 @@ def test_host_side_argument_errors(scr):
                                1 << 20, None) == 1
 
 
+def test_scan_ex_host_side_argument_errors(scr):
+    """Exclusive / include_initial: bad mode, missing init, an output range
+    that partially overlaps the input (the include_initial output is one
+    element longer), in-place batched calls with other output strides."""
+    L = scr.lib()
+    one = ctypes.c_double(0.0)
+    fake = ctypes.c_void_p(0x10000)
+    assert L.cr_scan_ex_workspace_bytes(100, 2, 1, 0, 2) == 0   # mode 0 is not a mode here
+    assert L.cr_scan_ex_workspace_bytes(100, 2, 1, 3, 2) == 0
+    assert L.cr_scan_ex_workspace_bytes(100, 3, 6, 1, 2) == 0   # B not a power of two
+    for mode in (1, 2):
+        assert L.cr_scan_ex_workspace_bytes(100, 3, 16, mode, 2) >= 256
+        assert L.cr_scan_ex_workspace_bytes(0, 0, 1, mode, 1) >= 256
+        assert L.cr_scan_ex_batched_workspace_bytes(7, 90, 3, 16, mode, 2) >= 256
+    assert L.cr_scan_ex(fake, fake, 10, 2, 1, 5, ctypes.byref(one), 2, fake, 1 << 20,
+                        None) == 1
+    assert L.cr_scan_ex(fake, fake, 10, 2, 1, 1, None, 2, fake, 1 << 20, None) == 1
+    # out starts one element before x: overlaps, not in place
+    assert L.cr_scan_ex(ctypes.c_void_p(0x10008), fake, 10, 2, 1, 2, ctypes.byref(one), 2,
+                        fake, 1 << 20, None) == 1
+    # include_initial writes n + 1 elements: out ending inside x overlaps
+    assert L.cr_scan_ex(fake, ctypes.c_void_p(0x10000 - 8 * 5), 10, 2, 1, 2, ctypes.byref(one),
+                        2, fake, 1 << 20, None) == 1
+    # in place batched with different output strides
+    assert L.cr_scan_ex_batched(fake, fake, 4, 10, 4, 1, 5, 1, 0, 1, 2, ctypes.byref(one), 2,
+                                fake, 1 << 20, None) == 1
+    # workspace too small
+    assert L.cr_scan_ex(fake, ctypes.c_void_p(0x10000000), 1 << 20, 3, 16, 1, ctypes.byref(one),
+                        2, fake, 256, None) == 3
+
+
 def test_binding_fails_loudly_without_library(tmp_path, scr):
     """The binding has no CPU fallback: with the library absent it raises."""
     import importlib.util
