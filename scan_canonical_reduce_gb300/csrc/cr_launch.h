@@ -32,6 +32,8 @@ enum KernelId : int {
   kKApplyInit,
   kKFillInit,
   kKCarryFixupShift,
+  kKScanSeqBlock,
+  kKRowReduce,
   kKernelCount
 };
 

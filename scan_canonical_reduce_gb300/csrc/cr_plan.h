@@ -53,6 +53,12 @@ struct ReducePlan {
   int64_t batch = 0;
   std::vector<PassPlan> passes;
   size_t ws_bytes = 0;
+  // Many contiguous rows whose lane count is one warp's 16-byte vector
+  // width (L = 32 * 16 / sizeof(T)) and a multiple of it as length: one warp
+  // per row (row_reduce_kernel) when the rows are 16-byte aligned; else the
+  // passes above. rows_lv = register-stack levels, 0 = not applicable.
+  int rows_lv = 0;
+  int64_t rows_P = 0, rows_bs = 0;
 };
 
 ReducePlan plan_reduce(int64_t batch, int64_t n, int64_t L, int64_t elem_stride,

@@ -28,6 +28,7 @@
 // No value is ever combined with an atomic; the grid shape changes which
 // block evaluates a node, never the node.
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 #include <vector>
 
@@ -178,6 +179,77 @@ __global__ void write_init_kernel(T* out, int64_t batch, T init) {
   if (i < batch) out[i] = init;
 }
 
+// ------------------------------------------------- rows: one warp per row
+template <class T>
+struct Vec16;
+template <>
+struct Vec16<double> {
+  using type = double2;
+  __device__ static double get(const double2& d, int v) { return v == 0 ? d.x : d.y; }
+};
+template <>
+struct Vec16<float> {
+  using type = float4;
+  __device__ static float get(const float4& d, int v) {
+    return v == 0 ? d.x : (v == 1 ? d.y : (v == 2 ? d.z : d.w));
+  }
+};
+
+// Batched canonical reduce of contiguous rows with L = 32 V lanes
+// (V = 16 / sizeof(T)) and n = P L: lane j of a row holds the columns
+// j + L t, t < P, so the V components of a thread's 16-byte loads are V
+// consecutive lanes and one warp's load is one row of the (P x L) lane
+// matrix. One warp per row: per lane the P-operand tree in a register
+// binary-counter stack (perfect trees of 8 positions pushed at level 3, the
+// rest one by one), then the perfect tree over the L lane results (in the
+// thread, then across lanes by shuffles, lower lane on the left), then
+// op(init, root).
+template <class T, int LV>
+__global__ void __launch_bounds__(256)
+row_reduce_kernel(const T* x, T* out, int64_t batch, int64_t P, int64_t bs, T init) {
+  constexpr int V = 16 / sizeof(T);
+  using Vec = typename Vec16<T>::type;
+  const unsigned full = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (row >= batch) return;  // whole warps
+  const Vec* p = reinterpret_cast<const Vec*>(x + row * bs) + lane;  // position t at p[32 t]
+  RegStack<T, LV> st[V];
+#pragma unroll
+  for (int v = 0; v < V; ++v) st[v].reset();
+  int64_t t = 0;
+  for (; t + 8 <= P; t += 8) {
+    Vec d[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) d[u] = __ldcs(p + (t + u) * 32);
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      T a[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) a[u] = Vec16<T>::get(d[u], v);
+      st[v].push(perfect_tree<T, 8>(a), 3);
+    }
+  }
+  for (; t < P; ++t) {
+    const Vec d = __ldcs(p + t * 32);
+#pragma unroll
+    for (int v = 0; v < V; ++v) st[v].push(Vec16<T>::get(d, v), 0);
+  }
+  T r[V];
+#pragma unroll
+  for (int v = 0; v < V; ++v) {
+    r[v] = T(0);
+    st[v].fold_onto(r[v], false);
+  }
+  T val = perfect_tree<T, V>(r);
+#pragma unroll
+  for (int sh = 1; sh < 32; sh *= 2) {
+    const T other = __shfl_down_sync(full, val, sh);
+    if ((lane & (2 * sh - 1)) == 0) val = add_rn(val, other);
+  }
+  if (lane == 0) out[row] = add_rn(init, val);
+}
+
 // ------------------------------------------------------------------ planning
 namespace {
 
@@ -291,6 +363,18 @@ ReducePlan plan_reduce(int64_t batch, int64_t n, int64_t L, int64_t elem_stride,
   MatRef x_in{false, 0, batch_stride, Leff * elem_stride, elem_stride};
   plan_tree(plan, ws, batch, R, r, Leff, m, x_in, esize);
   plan.ws_bytes = ws.off;
+  const int64_t Lrow = 32 * (16 / (int64_t)esize);
+  if (batch >= 2048 && elem_stride == 1 && L == Lrow && n >= L && n % L == 0 &&
+      (batch_stride * (int64_t)esize) % 16 == 0) {
+    const int64_t P = n / L;
+    const int need = (int)std::log2((double)P) + 1;  // stack levels for P operands
+    const int lv = need <= 6 ? 6 : need <= 11 ? 11 : need <= 16 ? 16 : need <= 21 ? 21 : 0;
+    if (lv && P < (int64_t(1) << 21)) {
+      plan.rows_lv = lv;
+      plan.rows_P = P;
+      plan.rows_bs = batch_stride;
+    }
+  }
   return plan;
 }
 
@@ -302,6 +386,21 @@ cudaError_t run_reduce(const ReducePlan& plan, const T* x, T* out, T init, char*
       CR_LAUNCH(kKWriteInit, s,
                 write_init_kernel<T><<<(unsigned)((plan.batch + 255) / 256), 256, 0, s>>>(
                     out, plan.batch, init));
+    return cudaGetLastError();
+  }
+  if (plan.rows_lv && (reinterpret_cast<uintptr_t>(x) & 15) == 0) {
+    const int64_t blocks = (plan.batch + 7) / 8;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+#define CR_ROWS(LVV)                                                                       \
+  CR_LAUNCH(kKRowReduce, s,                                                                \
+            (row_reduce_kernel<T, LVV><<<(unsigned)blocks, 256, 0, s>>>(x, out, plan.batch, \
+                                                                      plan.rows_P,         \
+                                                                      plan.rows_bs, init)))
+    if (plan.rows_lv == 6) CR_ROWS(6);
+    else if (plan.rows_lv == 11) CR_ROWS(11);
+    else if (plan.rows_lv == 16) CR_ROWS(16);
+    else CR_ROWS(21);
+#undef CR_ROWS
     return cudaGetLastError();
   }
   for (const PassPlan& pp : plan.passes) {

@@ -850,6 +850,62 @@ scan_seq_kernel(const T* x, T* out, int64_t batch, int64_t n, int64_t es, int64_
   }
 }
 
+// Batched block_dyadic with B = BB <= 16 (BB > 1) and left_fold (BB = 16,
+// kLeft): one thread per sequence, one block of BB levels per step. The BB
+// loads of a block are issued together (consecutive threads read
+// consecutive columns, so each is a coalesced row), the in-block values come
+// from the compile-time tree of local_scan (only its adds, none predicated
+// off), then the carry. Outputs as in scan_seq_kernel; in the shifted forms
+// the first element of the next block is loaded before this block's stores
+// (which reach one position further), so in-place calls stay correct.
+template <class T, int BB, bool kLeft>
+__global__ void __launch_bounds__(256)
+scan_seq_block_kernel(const T* x, T* out, int64_t batch, int64_t n, int64_t es, int64_t bs,
+                      int64_t oes, int64_t obs, int shift, int64_t m, T init) {
+  const int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (q >= batch) return;
+  const T* xp = x + q * bs;
+  T* yp = out + q * obs;
+  T v[BB];
+  v[0] = xp[0];
+  if (shift) yp[0] = init;
+  T carry = T(0);
+  for (int64_t k0 = 0; k0 < n; k0 += BB) {
+    const int64_t len = imin(BB, n - k0);
+#pragma unroll
+    for (int e = 1; e < BB; ++e) v[e] = (e < len) ? xp[(k0 + e) * es] : T(0);
+    const T nxt0 = (k0 + BB < n) ? xp[(k0 + BB) * es] : T(0);
+    T w[BB];
+    if (kLeft) {
+      T acc = (k0 == 0) ? v[0] : add_rn(carry, v[0]);
+      w[0] = acc;
+#pragma unroll
+      for (int e = 1; e < BB; ++e) {
+        acc = add_rn(acc, v[e]);
+        w[e] = acc;
+      }
+      carry = acc;  // read only when a full block follows
+    } else {
+      T agg[1];
+      local_scan<T, BB, BB>(v, w, agg);
+      if (k0 > 0) {
+#pragma unroll
+        for (int e = 0; e < BB; ++e) w[e] = add_rn(carry, w[e]);
+      }
+      carry = (k0 == 0) ? agg[0] : add_rn(carry, agg[0]);
+    }
+#pragma unroll
+    for (int e = 0; e < BB; ++e) {
+      if (e < len) {
+        const int64_t k = k0 + e;
+        if (!shift) yp[k * oes] = w[e];
+        else if (k + 1 < m) yp[(k + 1) * oes] = add_rn(init, w[e]);
+      }
+    }
+    v[0] = nxt0;
+  }
+}
+
 // ---------------------------------------------------------------- planning
 namespace {
 std::atomic<int64_t> g_skip_publish{-1};
@@ -1011,10 +1067,21 @@ cudaError_t run_scan(const ScanPlan& plan, const T* x, T* out, int64_t es, int64
                                                          bs, oes, obs, (int)plan.policy, \
                                                          plan.B, shift ? 1 : 0, plan.m,  \
                                                          init))
-      if (LV <= 5) CR_SEQ(5);
+#define CR_SEQB(BBV, LEFT)                                                                 \
+  CR_LAUNCH(kKScanSeqBlock, s,                                                             \
+            (scan_seq_block_kernel<T, BBV, LEFT><<<grid, 256, 0, s>>>(                     \
+                x, out, plan.batch, plan.n, es, bs, oes, obs, shift ? 1 : 0, plan.m, init)))
+      const bool bd = plan.policy == CR_BLOCK_DYADIC;
+      if (plan.policy == CR_LEFT_FOLD || (bd && plan.B == 1)) CR_SEQB(16, true);
+      else if (bd && plan.B == 16) CR_SEQB(16, false);
+      else if (bd && plan.B == 8) CR_SEQB(8, false);
+      else if (bd && plan.B == 4) CR_SEQB(4, false);
+      else if (bd && plan.B == 2) CR_SEQB(2, false);
+      else if (LV <= 5) CR_SEQ(5);
       else if (LV <= 9) CR_SEQ(9);
       else if (LV <= 17) CR_SEQ(17);
       else CR_SEQ(32);
+#undef CR_SEQB
 #undef CR_SEQ
       return cudaGetLastError();
     }

@@ -141,3 +141,29 @@ def test_reduce_exact_integers_two_to_thirty(scr):
     for L in (16, 1024):
         got = scr.reduce(x, L, 7.0).item()
         assert got == float(exact + 7)
+
+
+@pytest.mark.parametrize("dtype,L", [(np.float32, 128), (np.float64, 64)])
+def test_reduce_rows_one_warp_per_row(scr, dtype, L):
+    """Many contiguous rows with L = one warp's 16-byte vector width and
+    n = P L take the one-warp-per-row kernel: every row against the oracle,
+    for lane lengths P around the register blocks of 8 and the stack depths;
+    a misaligned start, a padded row stride and a row stride that breaks
+    16-byte alignment (general passes) give the same results."""
+    rows = 2048
+    for P in (1, 7, 8, 9, 32, 63, 64, 100, 1100, 2100):
+        cols = P * L
+        x = W.signed_pow2(rows * cols, W.seed_for(4, P), dtype, -20, 20).reshape(rows, cols)
+        got = scr.reduce_batched(torch.from_numpy(x).to(DEV), L, 0.25).cpu().numpy()
+        want = oracle.reduce_batched(x.reshape(-1), rows, cols, 1, cols, L, dtype(0.25))
+        assert bits(got) == bits(want), P
+    P = 9
+    cols = P * L
+    x = W.signed_pow2(rows * (cols + 8) + 1, W.seed_for(4, 99), dtype, -20, 20)
+    base = torch.from_numpy(x).to(DEV)
+    for pad, off in ((0, 1), (8, 0), (1, 0)):
+        stride = cols + pad
+        view = base[off:off + rows * stride].view(rows, stride)[:, :cols]
+        got = scr.reduce_batched(view, L, -1.0).cpu().numpy()
+        want = oracle.reduce_batched(x[off:].copy(), rows, cols, 1, stride, L, dtype(-1.0))
+        assert bits(got) == bits(want), (pad, off)

@@ -82,11 +82,13 @@ def test_scan_rejects_bad_block_and_overlap(scr):
 
 
 @pytest.mark.parametrize("dtype", [np.float64, np.float32])
-@pytest.mark.parametrize("policy,B", [("left_fold", 1), ("block_dyadic", 16),
-                                      ("block_dyadic", 4), ("block_dyadic", 256),
+@pytest.mark.parametrize("policy,B", [("left_fold", 1), ("block_dyadic", 1),
+                                      ("block_dyadic", 2), ("block_dyadic", 4),
+                                      ("block_dyadic", 8), ("block_dyadic", 16),
+                                      ("block_dyadic", 32), ("block_dyadic", 256),
                                       ("iterated_pairwise", 1), ("pairwise", 1)])
 def test_scan_batched_columns_and_rows(scr, dtype, policy, B):
-    levels, cols = 90, 1001
+    levels, cols = 90, 1001  # 90 = 5 blocks of 16 + 10: a ragged last block
     buf = W.signed_pow2(levels * cols, W.seed_for(5, 3), dtype)
     t = torch.from_numpy(buf).to(DEV).view(levels, cols)
     got = scr.inclusive_scan_batched(t, policy, B, dim=0).cpu().numpy().reshape(-1)

@@ -103,8 +103,9 @@ def test_minus_zero_init_is_the_shifted_inclusive_scan(scr, policy, B):
 @pytest.mark.parametrize("dtype", [np.float64, np.float32])
 @pytest.mark.parametrize("mode", ["exclusive", "include_initial"])
 @pytest.mark.parametrize("policy,B", [("left_fold", 1), ("block_dyadic", 16),
-                                      ("block_dyadic", 4), ("iterated_pairwise", 1),
-                                      ("pairwise", 1)])
+                                      ("block_dyadic", 8), ("block_dyadic", 4),
+                                      ("block_dyadic", 2), ("block_dyadic", 64),
+                                      ("iterated_pairwise", 1), ("pairwise", 1)])
 def test_batched(scr, dtype, mode, policy, B):
     """Columns of a level-major (levels x cols) array, written to a
     (levels + extra) x cols array; rows of a (cols x levels) array."""
@@ -170,3 +171,18 @@ def test_left_fold_chain_size(scr):
         f = scr.exclusive_scan if mode == "exclusive" else scr.scan_include_initial
         got = f(xd, "left_fold", 1, 0.125).cpu().numpy()
         assert bits(got) == bits(oracle.scan_ex(x, "left_fold", 1, 0.125, mode)), mode
+
+
+@pytest.mark.parametrize("policy,B", [("left_fold", 1), ("block_dyadic", 16),
+                                      ("block_dyadic", 4), ("iterated_pairwise", 1)])
+def test_batched_exclusive_in_place(scr, policy, B):
+    """out == x with the same strides: every element is read before the
+    store one level further down overwrites it."""
+    levels, cols = 90, 777
+    buf = W.signed_pow2(levels * cols, W.seed_for(5, 9))
+    t = torch.from_numpy(buf).to(DEV).view(levels, cols)
+    scr.exclusive_scan_batched(t, policy, B, 0.5, dim=0, out=t)
+    want = np.empty(levels * cols)
+    oracle.scan_ex_batched(buf, cols, levels, cols, 1, policy, B, 0.5, "exclusive", want, cols,
+                           1)
+    assert bits(t.cpu().numpy().reshape(-1)) == bits(want)
