@@ -516,31 +516,67 @@ __global__ void __launch_bounds__(kCT) chain_segments_kernel(
 }
 
 // ---------------------------------------------------------------- pass 7
-// The walk's compact record: everything one break and its segment's map need,
-// in 32 bytes (two 16-byte shared-memory loads).
+// The walk carries A = M + q, the integer to be rounded at the next break,
+// instead of M: the next record's q is folded into this record's map
+// offsets, which takes one 64-bit add off the sequential path. A rise by d
+// binades rounds A / 2^d half to even in one step,
+//   M1 = (A + 2^(d-1) - 1 + x) >> d,   x = fpos | (bit d of A),
+// which rounds up exactly when the remainder exceeds half, or equals it and
+// either the exact sum lies above A (fpos) or the quotient is odd.
 struct alignas(16) Hot {
-  int64_t q;        // up: T split in the old unit (0 for a continuation)
-  uint64_t b0, b1;  // the segment map's offsets
-  uint32_t ctrl;    // d (6 bits) | shift (7) << 6 | fpos << 13 | neg << 14 | type << 15 | steps << 17
-  uint32_t idx;     // record index within the batch (unused padding)
+  int64_t c;        // 2^(d-1) - 1 for a rise, 0 for a continuation
+  uint64_t b0, b1;  // the segment map's offsets, plus the next record's q when
+                    // that record is a rise or a continuation
+  uint32_t ctrl;    // d (6 bits) | sh (7) << 6 | rise << 13 | fpos << 14 | neg << 15 |
+                    // type (2) << 16 | steps << 18
+  uint32_t pad;
 };
-__device__ __forceinline__ Hot make_hot(const SegRec& r) {
+__device__ __forceinline__ bool is_fast(uint32_t meta) { return m_type(meta) <= kUp; }
+__device__ __forceinline__ Hot make_hot(const SegRec& r, int64_t q_next) {
   Hot h;
   const uint32_t m = r.meta, type = m_type(m);
   const bool up = type == kUp;
-  h.q = up ? r.q : 0;
-  h.b0 = r.map.b0;
-  h.b1 = r.map.b1;
+  const int d = up ? m_d(m) : 0;
+  h.c = d > 0 ? (int64_t(1) << (d - 1)) - 1 : 0;
+  h.b0 = r.map.b0 + (uint64_t)q_next;
+  h.b1 = r.map.b1 + (uint64_t)q_next;
   const uint32_t shift = r.map.a == 0 ? 64u : (uint32_t)(__ffsll((long long)r.map.a) - 1);
-  h.ctrl = (up ? (uint32_t)m_d(m) : 0u) | (shift << 6) | ((m_fcls(m) != kFZero) ? 1u << 13 : 0u) |
-           (m_neg(m) ? 1u << 14 : 0u) | (type << 15) | (r.nsteps > 0 ? 1u << 17 : 0u);
-  h.idx = 0;
+  h.ctrl = (uint32_t)d | (shift << 6) | (d > 0 ? 1u << 13 : 0u) |
+           ((m_fcls(m) != kFZero) ? 1u << 14 : 0u) | (m_neg(m) ? 1u << 15 : 0u) |
+           (type << 16) | (r.nsteps > 0 ? 1u << 18 : 0u);
+  h.pad = 0;
   return h;
 }
 
-// Breaks in order, in one thread. The whole warp loads the next 32 records
-// while lane 0 runs the current 32 from shared memory; rises and
-// continuations (nearly all records) take a branch-free integer path.
+// One break (rise or continuation) from A: writes m_in, returns the next A.
+template <class T>
+__device__ __forceinline__ int64_t walk_fast(const Hot& h, int64_t A, int64_t* m_in_j,
+                                             uint32_t& okw, bool& cval) {
+  const uint32_t c = h.ctrl;
+  const int d = (int)(c & 63u);
+  const uint32_t sh = (c >> 6) & 127u;
+  const uint32_t rise = (c >> 13) & 1u, fpos = (c >> 14) & 1u;
+  const int64_t hi = A >> d;
+  const int64_t x = (int64_t)(((uint32_t)hi & rise) | (fpos & rise));
+  const int64_t M1 = (A + h.c + x) >> d;
+  *m_in_j = M1;
+  // in-binade test of a rise, as integer comparisons on hi (off the chain)
+  constexpr int64_t LO = int64_t(1) << FP<T>::P, HI = int64_t(1) << (FP<T>::P + 1);
+  const uint64_t mask = (uint64_t(1) << d) - 1;  // d = 0: 0
+  const uint32_t fz = (((uint64_t)A & mask) == 0) & (fpos ^ 1u);
+  const uint32_t pos_ok = (hi >= LO) & (hi <= HI - 1);
+  const uint32_t neg_ok = fz ? (hi <= -LO) & (hi >= -HI + 1) : (hi <= -LO - 1) & (hi >= -HI);
+  const uint32_t in_ok = ((c >> 15) & 1u) ? neg_ok : pos_ok;
+  okw &= rise ? in_ok : 1u;
+  cval = cval & !rise & !((c >> 18) & 1u);
+  const uint64_t aM = sh >= 64 ? 0 : ((uint64_t)M1 << sh);
+  return (int64_t)(aM + ((M1 & 1) ? h.b1 : h.b0));
+}
+
+// Breaks in order, in one thread. The whole warp converts the next 32
+// records to compact form while lane 0 runs the current 32 from shared
+// memory; batches with no start or uncertain step run an unrolled loop of
+// the integer path alone.
 template <class T>
 __global__ void __launch_bounds__(32) chain_walk_kernel(const T* src, T* dst, const SegRec* segs,
                                                         const int64_t* nseg_total,
@@ -548,54 +584,62 @@ __global__ void __launch_bounds__(32) chain_walk_kernel(const T* src, T* dst, co
                                                         int* fail) {
   __shared__ Hot hot[2][32];
   __shared__ SegRec cold[2][32];
+  __shared__ int cold_batch[2];
+  const unsigned full = 0xffffffffu;
   const int lane = threadIdx.x;
   const int64_t nseg = *nseg_total;
   if (*fail || nseg > seg_cap) {
     if (lane == 0) atomicExch(fail, 2);
     return;
   }
-  SegRec nr{};
-  if (lane < nseg) nr = segs[lane];
-  uint64_t M = 0;
+  SegRec cur{}, nxt{};
+  if (lane < nseg) cur = segs[lane];
+  if (32 + lane < nseg) nxt = segs[32 + lane];
+  // A = M + q of the next record: M = 0 before the first (in practice a start)
+  int64_t A = __shfl_sync(full, (lane == 0 && nseg > 0 && m_type(cur.meta) == kUp) ? cur.q : 0, 0);
   T C = T(0);
   bool cval = false;  // C holds the current chain value
   bool bad = false;
   for (int64_t b0 = 0, it = 0; b0 < nseg; b0 += 32, ++it) {
     const int slot = (int)(it & 1);
-    hot[slot][lane] = make_hot(nr);  // loaded one batch ago
-    cold[slot][lane] = nr;
+    // q of the record after mine (lane 31: the next batch's first record)
+    const int64_t q_mine = (b0 + lane < nseg && m_type(cur.meta) == kUp) ? cur.q : 0;
+    const int64_t q_nb = (b0 + 32 < nseg && m_type(nxt.meta) == kUp) ? nxt.q : 0;
+    int64_t q_next = __shfl_down_sync(full, q_mine, 1);
+    const int64_t q_nb0 = __shfl_sync(full, q_nb, 0);
+    if (lane == 31) q_next = q_nb0;
+    hot[slot][lane] = make_hot(cur, q_next);
+    cold[slot][lane] = cur;
+    const bool is_cold = b0 + lane < nseg && !is_fast(cur.meta);
+    const unsigned any_cold = __ballot_sync(full, is_cold);
+    if (lane == 0) cold_batch[slot] = any_cold != 0;
     __syncwarp();
-    const int64_t nb = b0 + 32 + lane;
-    if (nb < nseg) nr = segs[nb];
+    cur = nxt;
+    const int64_t nb = b0 + 64 + lane;
+    if (nb < nseg) nxt = segs[nb];
     if (lane == 0) {
       const int cnt = (int)(nseg - b0 < 32 ? nseg - b0 : 32);
       bool ok = true;
       uint32_t okw = 1u;
-      for (int j = 0; j < cnt; ++j) {
-        const Hot h = hot[slot][j];
-        const uint32_t c = h.ctrl;
-        const uint32_t type = (c >> 15) & 3u;
-        uint64_t M1;
-        if (type <= kUp) {  // kMap (continuation, d = 0) or kUp: branch-free
-          const int d = (int)(c & 63u);
-          const int64_t A = (int64_t)M + h.q;
-          const int64_t hi = A >> d;
-          const uint64_t mask = (uint64_t(1) << d) - 1;  // d = 0: 0
-          const uint64_t lo = (uint64_t)A & mask;
-          const uint64_t half = (mask >> 1) + (d > 0 ? 1u : 0u);  // 2^(d-1); d = 0: 0
-          const uint32_t fpos = (c >> 13) & 1u;
-          const uint32_t gt = lo > half, eq = (lo == half) & (d > 0);
-          const uint32_t rup = gt | (eq & (fpos | (uint32_t)(hi & 1)));
-          M1 = (uint64_t)hi + rup;
-          // in-binade test of a rise, as integer comparisons on hi
-          constexpr int64_t LO = int64_t(1) << FP<T>::P, HI = int64_t(1) << (FP<T>::P + 1);
-          const uint32_t fz = (lo == 0) & (fpos ^ 1u);
-          const uint32_t pos_ok = (hi >= LO) & (hi <= HI - 1);
-          const uint32_t neg_ok = (fz ? (hi <= -LO) & (hi >= -HI + 1) : (hi <= -LO - 1) & (hi >= -HI));
-          const uint32_t in_ok = ((c >> 14) & 1u) ? neg_ok : pos_ok;
-          okw &= (type == kUp) ? in_ok : 1u;
-          cval = cval & (type != kUp);
-        } else {  // start or uncertain step: the real add
+      if (!cold_batch[slot]) {
+        if (cnt == 32) {
+#pragma unroll 8
+          for (int j = 0; j < 32; ++j)
+            A = walk_fast<T>(hot[slot][j], A, m_in + b0 + j, okw, cval);
+        } else {
+          for (int j = 0; j < cnt; ++j)
+            A = walk_fast<T>(hot[slot][j], A, m_in + b0 + j, okw, cval);
+        }
+      } else {
+        for (int j = 0; j < cnt; ++j) {
+          const Hot h = hot[slot][j];
+          const uint32_t type = (h.ctrl >> 16) & 3u;
+          if (type <= kUp) {
+            A = walk_fast<T>(h, A, m_in + b0 + j, okw, cval);
+            continue;
+          }
+          // start or uncertain step: the real add. The previous record folded
+          // no q into A for this one, so A is the entering M.
           const SegRec& r = cold[slot][j];
           const uint32_t m = r.meta;
           if (type == kStart) {
@@ -603,27 +647,24 @@ __global__ void __launch_bounds__(32) chain_walk_kernel(const T* src, T* dst, co
           } else {
             if (!cval) {
               ok = ok && r.prev_certain;
-              C = m_to_value<T>((int64_t)M, r.e_prev);
+              C = m_to_value<T>(A, r.e_prev);
             }
             C = add_rn(C, (T)r.tval);
           }
           dst[r.start] = C;
           cval = true;
-          M1 = M;
+          int64_t M1 = A;
           if (m_certain(m)) {
             int64_t Mi = 0;
             ok = ok && value_to_m<T>(C, m_e(m), Mi);
-            M1 = (uint64_t)Mi;
+            M1 = Mi;
           }
+          m_in[b0 + j] = M1;
+          const uint32_t sh = (h.ctrl >> 6) & 127u;
+          const uint64_t aM = sh >= 64 ? 0 : ((uint64_t)M1 << sh);
+          A = (int64_t)(aM + ((M1 & 1) ? h.b1 : h.b0));
+          cval = cval & !((h.ctrl >> 18) & 1u);
         }
-        m_in[b0 + j] = (int64_t)M1;
-        // the segment's composed map (identity when it has no steps)
-        const uint32_t steps = (c >> 17) & 1u;
-        const uint32_t sh = (c >> 6) & 127u;
-        const uint64_t aM = sh >= 64 ? 0 : (M1 << sh);
-        const uint64_t mapped = aM + ((M1 & 1) ? h.b1 : h.b0);
-        M = steps ? mapped : M1;
-        cval = cval & !steps;
       }
       bad = bad || !ok || !okw;
     }
