@@ -23,12 +23,16 @@
 // whose binade is uncertain (a real add). These are "breaks", evaluated in
 // order by one thread from integers only (real adds only when uncertain).
 //
-// Passes (tile = 4096 steps, 16 per thread):
-//   1 tile sums, 2 tile offsets (one block), 3 prefix P~_k and max|P~|;
-//   4 classify: the binade and sign of s_k from P~_k, certain when the whole
-//     interval P~_k +- mu (mu = K ulp(2 max|P~|) bounds both |C_k - P_k| and
-//     |P~_k - P_k|) lies inside one binade; step types MAP (same or lower
-//     binade), UP (higher binade, integer break), FP (uncertain: real add);
+// Passes (tile = 4096 steps, 16 consecutive steps per thread):
+//   1 tile sums and the largest |T| of each tile (coalesced);
+//   2 tile offsets and a bound B >= max |P_k| (one block);
+//   3 classify: the approximate prefix P~_k (in registers) and the binade
+//     and sign of s_k from it, certain when the whole interval P~_k +- mu
+//     (mu = K ulp(2B) bounds both |C_k - P_k| and |P~_k - P_k|) lies inside
+//     one binade, decided on the bits with integers only; step types MAP
+//     (same or lower binade), UP (higher binade, integer break), FP
+//     (uncertain: real add); each thread's composed map after its last
+//     break, scanned across the tile;
 //   5 segment bases (one block), 6 segment records: each break (or tile
 //     start) and the composed map of the MAP steps that follow it;
 //   7 walk: the breaks in order, from integers; M entering every segment;
@@ -226,24 +230,89 @@ __device__ __forceinline__ uint64_t up_step(uint64_t M, int64_t q, uint32_t fcls
   return (uint64_t)(hi + (rup ? 1 : 0));
 }
 
+// ---------------------------------------------------------------- runs
+// N consecutive elements of a thread's run: 16-byte vector accesses when
+// whole and aligned, bounded scalar ones at the tail.
+template <class E, int N>
+__device__ __forceinline__ void load_run(const E* p, int64_t cnt, E (&v)[N]) {
+  constexpr int PER = 16 / sizeof(E);
+  if (cnt >= N && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
+    const uint4* q = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+    for (int k = 0; k < N / PER; ++k) {
+      const uint4 d = q[k];
+#pragma unroll
+      for (int j = 0; j < PER; ++j) v[k * PER + j] = reinterpret_cast<const E*>(&d)[j];
+    }
+    return;
+  }
+#pragma unroll
+  for (int e = 0; e < N; ++e) v[e] = (e < cnt) ? p[e] : E(0);
+}
+template <class E, int N>
+__device__ __forceinline__ void store_run(E* p, int64_t cnt, const E (&v)[N]) {
+  constexpr int PER = 16 / sizeof(E);
+  if (cnt >= N && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
+    uint4* q = reinterpret_cast<uint4*>(p);
+#pragma unroll
+    for (int k = 0; k < N / PER; ++k) {
+      uint4 d;
+#pragma unroll
+      for (int j = 0; j < PER; ++j) reinterpret_cast<E*>(&d)[j] = v[k * PER + j];
+      q[k] = d;
+    }
+    return;
+  }
+#pragma unroll
+  for (int e = 0; e < N; ++e)
+    if (e < cnt) p[e] = v[e];
+}
+
 // ---------------------------------------------------------------- pass 1
+// Coalesced: thread t reads steps t, t + 256, ... of the tile. The tile sum
+// feeds the approximate prefix; the largest |T| (compared as bit patterns,
+// no floating-point work) feeds the bound of pass 2.
 template <class T>
 __global__ void __launch_bounds__(kCT) chain_tile_sum_kernel(const T* src, int64_t K,
-                                                             double* tsum) {
-  __shared__ double sh[kCT];
-  const int t = threadIdx.x;
-  const int64_t k0 = (int64_t)blockIdx.x * kCTile + (int64_t)t * kCE;
-  double s = 0.0;
+                                                             double* tsum, double* tmax) {
+  __shared__ double sh_s[kCT / 32];
+  __shared__ uint64_t sh_m[kCT / 32];
+  const unsigned full = 0xffffffffu;
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const int64_t tile0 = (int64_t)blockIdx.x * kCTile;
+  double sum = 0.0;
+  uint64_t mx = 0;
 #pragma unroll
-  for (int i = 0; i < kCE; ++i)
-    if (k0 + i < K) s += (double)src[k0 + i];
-  sh[t] = s;
-  __syncthreads();
-  for (int w = kCT / 2; w > 0; w >>= 1) {
-    if (t < w) sh[t] += sh[t + w];
-    __syncthreads();
+  for (int j = 0; j < kCE; ++j) {
+    const int64_t k = tile0 + (int64_t)j * kCT + t;
+    if (k < K) {
+      const double v = (double)src[k];
+      sum += v;
+      const uint64_t a = (uint64_t)__double_as_longlong(v) & 0x7FFFFFFFFFFFFFFFull;
+      mx = a > mx ? a : mx;
+    }
   }
-  if (t == 0) tsum[blockIdx.x] = sh[0];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    sum += __shfl_down_sync(full, sum, off);
+    const uint64_t o = __shfl_down_sync(full, mx, off);
+    mx = o > mx ? o : mx;
+  }
+  if (lane == 0) {
+    sh_s[w] = sum;
+    sh_m[w] = mx;
+  }
+  __syncthreads();
+  if (t == 0) {
+    double S = 0.0;
+    uint64_t M = 0;
+    for (int i = 0; i < kCT / 32; ++i) {
+      S += sh_s[i];
+      M = sh_m[i] > M ? sh_m[i] : M;
+    }
+    tsum[blockIdx.x] = S;
+    tmax[blockIdx.x] = __longlong_as_double((long long)M);  // NaN patterns stay NaN
+  }
 }
 
 // ---------------------------------------------------------------- pass 2 / 5
@@ -274,133 +343,112 @@ __global__ void __launch_bounds__(1024) exclusive_scan_1block(const V* in, V* ou
   if (t == 0 && total) *total = carry;
 }
 
-// ---------------------------------------------------------------- pass 3
-template <class T>
-__global__ void __launch_bounds__(kCT) chain_prefix_kernel(const T* src, int64_t K,
-                                                           const double* toff, double* pre,
-                                                           unsigned long long* maxabs) {
-  __shared__ double sh[kCT];
+// Tile offsets (exclusive prefix of the tile sums) and the bound
+// B = max over tiles of |offset| + 4096 max|T| >= every |P~_k| (one block).
+__global__ void __launch_bounds__(1024) chain_offsets_kernel(const double* tsum,
+                                                             const double* tmax, int64_t n,
+                                                             double* toff, double* bound) {
+  __shared__ double sh[1024];
+  __shared__ double carry, bmax;
   const int t = threadIdx.x;
-  const int64_t k0 = (int64_t)blockIdx.x * kCTile + (int64_t)t * kCE;
-  double v[kCE];
-  double s = 0.0;
-#pragma unroll
-  for (int i = 0; i < kCE; ++i) {
-    v[i] = (k0 + i < K) ? (double)src[k0 + i] : 0.0;
-    s += v[i];
+  if (t == 0) {
+    carry = 0.0;
+    bmax = 0.0;
   }
-  sh[t] = s;
   __syncthreads();
-  for (int off = 1; off < kCT; off <<= 1) {  // inclusive scan of thread sums
-    const double a = t >= off ? sh[t - off] : 0.0;
+  for (int64_t base = 0; base < n; base += 1024) {
+    const int64_t i = base + t;
+    const double v = i < n ? tsum[i] : 0.0;
+    sh[t] = v;
     __syncthreads();
-    sh[t] += a;
-    __syncthreads();
-  }
-  double run = toff[blockIdx.x] + (sh[t] - s);
-  double mx = 0.0;
-#pragma unroll
-  for (int i = 0; i < kCE; ++i) {
-    if (k0 + i < K) {
-      run += v[i];
-      pre[k0 + i] = run;
-      mx = fmax(mx, fabs(run));
+    for (int off = 1; off < 1024; off <<= 1) {
+      const double a = t >= off ? sh[t - off] : 0.0;
+      __syncthreads();
+      sh[t] += a;
+      __syncthreads();
     }
-  }
-  if (!(mx <= 1.7e308)) mx = 1.7e308;  // non-finite: those steps are uncertain anyway
-  __syncthreads();
-  sh[t] = mx;
-  __syncthreads();
-  for (int w = kCT / 2; w > 0; w >>= 1) {
-    if (t < w) sh[t] = fmax(sh[t], sh[t + w]);
+    const double o = carry + sh[t] - v;
+    double b = 0.0;
+    if (i < n) {
+      toff[i] = o;
+      b = fabs(o) + (double)kCTile * tmax[i];
+      if (!(b <= 1.7e308)) b = 1.7e308;  // non-finite: every step uncertain
+    }
+    __syncthreads();
+    sh[t] = b;
+    __syncthreads();
+    for (int w = 512; w > 0; w >>= 1) {
+      if (t < w) sh[t] = fmax(sh[t], sh[t + w]);
+      __syncthreads();
+    }
+    if (t == 0) bmax = fmax(bmax, sh[0]);
+    __syncthreads();
+    sh[t] = v;
+    __syncthreads();
+    for (int w = 512; w > 0; w >>= 1) {
+      if (t < w) sh[t] += sh[t + w];
+      __syncthreads();
+    }
+    if (t == 0) carry += sh[0];
     __syncthreads();
   }
-  if (t == 0) atomicMax(maxabs, (unsigned long long)__double_as_longlong(sh[0]));
+  if (t == 0) *bound = bmax * (1.0 + 0x1p-40);  // covers the rounding of the bound itself
 }
 
-// ---------------------------------------------------------------- pass 4
-// Binade exponent of a positive finite double from its bits.
-__device__ __forceinline__ int dexp(double a) {
-  return (int)((FP<double>::bits(a) >> 52) & 0x7FF) - 1023;
-}
-__device__ __forceinline__ double dpow2(int e) {  // 2^e, normal range
-  return FP<double>::from_bits((uint64_t)(e + 1023) << 52);
-}
-
+// ---------------------------------------------------------------- pass 3
+// mu = Kmu 2^emu as an integer and a power of two, from the bound of pass 2.
+struct MuInt {
+  int64_t K;
+  int em;
+  int all_uncertain;
+};
 template <class T>
-__device__ __forceinline__ void classify(double p, double mu, bool& certain, bool& neg, int& e) {
+__device__ __forceinline__ MuInt mu_from_bound(double bound, int64_t K) {
+  const double m2 = 2.0 * bound;
+  if (!(m2 < 1e300)) return MuInt{0, 0, 1};
+  if (m2 <= 1e-290) return MuInt{1, -930, 0};
+  const int e = (int)((FP<double>::bits(m2) >> 52) & 0x7FF) - 1023;
+  return MuInt{K, e - FP<T>::P, 0};
+}
+
+// The binade e and sign of s from p = P~, certain when [|p| - mu,
+// |p| + mu + ulp_T(e)) lies inside [2^e, 2^(e+1)) (and e is well inside T's
+// normal range). On the bits of p: |p| = (2^52 + f) 2^(e-52), and with
+// mu' = mu / 2^(e-52) = Kmu 2^s the test is f >= ceil(mu') and
+// 2^52 - f - ulp_T / 2^(e-52) > floor(mu'): integers only.
+template <class T>
+__device__ __forceinline__ void classify(double p, const MuInt& mu, bool& certain, bool& neg,
+                                         int& e) {
+  constexpr int kEMin = FP<T>::EMIN + 2 > -960 ? FP<T>::EMIN + 2 : -960;
+  constexpr int kEMax = FP<T>::EMAX - 2 < 996 ? FP<T>::EMAX - 2 : 996;
+  const uint64_t b = FP<double>::bits(p);
+  neg = (b >> 63) != 0;
   certain = false;
-  neg = p < 0;
   e = 0;
-  const double a = fabs(p);
-  if (!(a <= 1e300)) return;  // non-finite
-  if (a <= mu || a < 1e-290) return;  // sign, zero or the subnormal range uncertain
-  const int ee = dexp(a);
-  if (ee < FP<T>::EMIN + 2 || ee > FP<T>::EMAX - 2) return;
-  const double lo = dpow2(ee), hi = dpow2(ee + 1), ulp = dpow2(ee - FP<T>::P);
-  if (a - mu < lo || a + mu + ulp >= hi) return;  // interval crosses a binade edge
+  if (mu.all_uncertain) return;
+  const int ef = (int)((b >> 52) & 0x7FF);
+  const int ee = ef - 1023;
+  if (ef == 0x7FF || ee < kEMin || ee > kEMax) return;  // also zero and subnormals
+  const int64_t f = (int64_t)(b & ((uint64_t(1) << 52) - 1));
+  const int sft = mu.em + 52 - ee;
+  int64_t t1, t2;  // ceil(mu'), floor(mu')
+  if (sft >= 0) {
+    if (sft >= 52 || (mu.K >> (52 - sft)) != 0) return;  // mu' = Kmu 2^sft >= 2^52 > f
+    t1 = t2 = mu.K << sft;
+  } else if (-sft >= 62) {
+    t2 = 0;
+    t1 = mu.K > 0 ? 1 : 0;
+  } else {
+    const int r = -sft;
+    t2 = mu.K >> r;
+    t1 = t2 + ((mu.K & ((int64_t(1) << r) - 1)) != 0 ? 1 : 0);
+  }
+  constexpr int64_t c = int64_t(1) << (52 - FP<T>::P);  // ulp_T(e) / 2^(e-52)
+  if (f < t1 || (int64_t(1) << 52) - f - c <= t2) return;
   certain = true;
   e = ee;
 }
 
-template <class T>
-__global__ void __launch_bounds__(kCT) chain_classify_kernel(
-    const T* src, int64_t K, const double* pre, const unsigned long long* maxabs, int64_t* qv,
-    uint32_t* meta, int64_t* tile_nseg) {
-  __shared__ int cnt[kCT];
-  const int t = threadIdx.x;
-  const int64_t k0 = (int64_t)blockIdx.x * kCTile + (int64_t)t * kCE;
-  double mu;
-  {
-    const double m2 = 2.0 * __longlong_as_double((long long)*maxabs);
-    mu = m2 > 1e-290 && m2 < 1e300 ? (double)K * dpow2(dexp(m2) - FP<T>::P) : 1e300;
-    if (m2 <= 1e-290) mu = 1e-280;
-  }
-  int nbrk = 0;
-  bool pc = false, pn = false;
-  int pe = 0;
-  if (k0 > 0 && k0 < K) classify<T>(pre[k0 - 1], mu, pc, pn, pe);
-  for (int i = 0; i < kCE; ++i) {
-    const int64_t k = k0 + i;
-    if (k >= K) break;
-    bool c, n;
-    int e;
-    classify<T>(pre[k], mu, c, n, e);
-    uint32_t type;
-    int d = 0;
-    int64_t q = 0;
-    uint32_t f = 0;
-    const T tv = src[k];
-    if (k == 0) {
-      type = kStart;
-    } else if (!c || !pc) {
-      type = kFp;
-    } else if (e <= pe) {  // same or lower binade: a composable step
-      d = pe - e;
-      type = (d <= 63 && split_unit<T>(tv, e, q, f)) ? kMap : kFp;
-    } else {  // rise: integer break, T split in the old (finer) unit
-      d = e - pe;
-      type = (d <= 8 && split_unit<T>(tv, pe, q, f)) ? kUp : kFp;
-    }
-    if (type == kFp) d = 0;
-    meta[k] = make_meta(type, c, n, f, d, e);
-    qv[k] = q;
-    nbrk += type != kMap ? 1 : 0;
-    pc = c; pn = n; pe = e;
-  }
-  cnt[t] = nbrk;
-  __syncthreads();
-  for (int w = kCT / 2; w > 0; w >>= 1) {
-    if (t < w) cnt[t] += cnt[t + w];
-    __syncthreads();
-  }
-  if (t == 0) {  // one segment per break, plus one if the tile starts inside a run
-    const int64_t first = (int64_t)blockIdx.x * kCTile;
-    tile_nseg[blockIdx.x] = cnt[0] + (m_type(meta[first]) == kMap ? 1 : 0);
-  }
-}
-
-// ---------------------------------------------------------------- pass 6
 struct Summ {  // composition after the last break of a thread's steps
   Map map;
   int brk;
@@ -408,6 +456,139 @@ struct Summ {  // composition after the last break of a thread's steps
 __device__ __forceinline__ Summ combine(const Summ& l, const Summ& r) {
   return r.brk ? Summ{r.map, l.brk + r.brk} : Summ{compose(l.map, r.map), l.brk};
 }
+
+// Exclusive segmented scan of the threads' summaries across the tile.
+__device__ __forceinline__ Summ block_summ_scan(Summ me, Summ* sh) {
+  const int t = threadIdx.x;
+  sh[t] = me;
+  __syncthreads();
+  for (int off = 1; off < kCT; off <<= 1) {  // inclusive
+    Summ a = sh[t];
+    if (t >= off) a = combine(sh[t - off], a);
+    __syncthreads();
+    sh[t] = a;
+    __syncthreads();
+  }
+  const Summ r = t > 0 ? sh[t - 1] : Summ{map_id(), 0};
+  __syncthreads();
+  return r;
+}
+
+// Exclusive sum of one double per thread across the block (warp shuffles).
+__device__ __forceinline__ double block_excl_sum(double v, double* sh_w) {
+  const unsigned full = 0xffffffffu;
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  double incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const double o = __shfl_up_sync(full, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) sh_w[w] = incl;
+  __syncthreads();
+  double base = 0.0;
+  for (int i = 0; i < w; ++i) base += sh_w[i];
+  __syncthreads();
+  return base + incl - v;
+}
+
+template <class T>
+__global__ void __launch_bounds__(kCT) chain_classify_kernel(
+    const T* src, int64_t K, const double* toff, const double* bound, int64_t* qv,
+    uint32_t* meta, int64_t* tile_nseg, Summ* thr_in) {
+  __shared__ Summ sh[kCT];
+  __shared__ double sh_w[kCT / 32];
+  __shared__ int cnt[kCT / 32];
+  __shared__ int first_cont;
+  const unsigned full = 0xffffffffu;
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const int64_t tile0 = (int64_t)blockIdx.x * kCTile;
+  const int64_t k0 = tile0 + (int64_t)t * kCE;
+  const int64_t n = k0 < K ? (K - k0 < kCE ? K - k0 : kCE) : 0;
+  const MuInt mu = mu_from_bound<T>(*bound, K);
+  T tv[kCE];
+  load_run(src + (k0 < K ? k0 : 0), n, tv);
+  double tsum = 0.0;
+#pragma unroll
+  for (int i = 0; i < kCE; ++i) tsum += (double)tv[i];  // zero past the end
+  double run = toff[blockIdx.x] + block_excl_sum(tsum, sh_w);  // P~ just before k0
+  bool pc = false, pn = false;
+  int pe = 0;
+  if (k0 > 0 && n > 0) classify<T>(run, mu, pc, pn, pe);
+  int nbrk = 0;
+  Summ me{map_id(), 0};
+  constexpr int H = kCE / 2;  // outputs written in two halves: fewer live registers
+  int first_type = -1;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+  int64_t q_out[H];
+  uint32_t m_out[H];
+#pragma unroll
+  for (int j = 0; j < H; ++j) {
+    const int i = h * H + j;
+    q_out[j] = 0;
+    m_out[j] = 0;
+    if (i < n) {
+      const int64_t k = k0 + i;
+      run += (double)tv[i];
+      bool c, ng;
+      int e;
+      classify<T>(run, mu, c, ng, e);
+      uint32_t type;
+      int d = 0;
+      int64_t q = 0;
+      uint32_t f = 0;
+      if (k == 0) {
+        type = kStart;
+      } else if (!c || !pc) {
+        type = kFp;
+      } else if (e <= pe) {  // same or lower binade: a composable step
+        d = pe - e;
+        type = (d <= 63 && split_unit<T>(tv[i], e, q, f)) ? kMap : kFp;
+      } else {  // rise: integer break, T split in the old (finer) unit
+        d = e - pe;
+        type = (d <= 8 && split_unit<T>(tv[i], pe, q, f)) ? kUp : kFp;
+      }
+      if (type == kFp) {
+        d = 0;
+        q = 0;
+      }
+      m_out[j] = make_meta(type, c, ng, f, d, e);
+      q_out[j] = q;
+      if (i == 0) first_type = (int)type;
+      if (type != kMap) {
+        me.map = map_id();
+        me.brk += 1;
+        nbrk += 1;
+      } else {
+        me.map = compose(me.map, step_map(d, q, f));
+      }
+      pc = c;
+      pn = ng;
+      pe = e;
+    }
+  }
+  const int64_t nh = n - h * H;
+  if (nh > 0) {
+    store_run(qv + k0 + h * H, nh, q_out);
+    store_run(meta + k0 + h * H, nh, m_out);
+  }
+  }
+  (void)pn;
+  if (t == 0) first_cont = (first_type == (int)kMap) ? 1 : 0;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) nbrk += __shfl_down_sync(full, nbrk, off);
+  if (lane == 0) cnt[w] = nbrk;
+  const Summ in = block_summ_scan(me, sh);  // synchronises: cnt and first_cont visible
+  thr_in[blockIdx.x * kCT + t] = in;
+  if (t == 0) {  // one segment per break, plus one if the tile starts inside a run
+    int total = 0;
+    for (int i = 0; i < kCT / 32; ++i) total += cnt[i];
+    tile_nseg[blockIdx.x] = total + first_cont;
+  }
+}
+
+// ---------------------------------------------------------------- pass 6
 
 // Segment record: a break (or a tile start inside a run) and the composed
 // map of the MAP steps after it, up to the next break or the tile end.
@@ -422,45 +603,20 @@ struct SegRec {
   int32_t nsteps;   // MAP steps in the map
 };
 
-__device__ __forceinline__ void thread_scan(const int64_t* qv, const uint32_t* meta,
-                                            int64_t k0, int64_t K, Summ& in_excl, Summ* sh) {
-  Summ me{map_id(), 0};
-  for (int i = 0; i < kCE; ++i) {
-    const int64_t k = k0 + i;
-    if (k >= K) break;
-    const uint32_t m = meta[k];
-    if (m_type(m) != kMap) {
-      me.map = map_id();
-      me.brk += 1;
-    } else {
-      me.map = compose(me.map, step_map(m_d(m), qv[k], m_fcls(m)));
-    }
-  }
-  const int t = threadIdx.x;
-  sh[t] = me;
-  __syncthreads();
-  for (int off = 1; off < kCT; off <<= 1) {  // inclusive segmented scan
-    Summ a = sh[t];
-    if (t >= off) a = combine(sh[t - off], a);
-    __syncthreads();
-    sh[t] = a;
-    __syncthreads();
-  }
-  in_excl = t > 0 ? sh[t - 1] : Summ{map_id(), 0};
-  __syncthreads();
-}
-
 template <class T>
 __global__ void __launch_bounds__(kCT) chain_segments_kernel(
     const T* src, const int64_t* qv, const uint32_t* meta, int64_t K, const int64_t* seg_base,
-    SegRec* segs, int64_t seg_cap, int* fail) {
-  __shared__ Summ sh[kCT];
+    const Summ* thr_in, SegRec* segs, int64_t seg_cap, int* fail) {
   const int t = threadIdx.x;
   const int64_t tile0 = (int64_t)blockIdx.x * kCTile;
   const int64_t k0 = tile0 + (int64_t)t * kCE;
-  Summ in;
-  thread_scan(qv, meta, k0, K, in, sh);
+  const int64_t n = k0 < K ? (K - k0 < kCE ? K - k0 : kCE) : 0;
+  const Summ in = thr_in[blockIdx.x * kCT + t];
   const bool cont = m_type(meta[tile0]) == kMap;
+  int64_t qr[kCE];
+  uint32_t mr[kCE];
+  load_run(qv + (k0 < K ? k0 : 0), n, qr);
+  load_run(meta + (k0 < K ? k0 : 0), n, mr);
   int64_t ord = (cont ? 1 : 0) + in.brk - 1;  // segment open at my first step
   Map cur = in.map;
   int steps = 0;  // MAP steps of the open segment seen by this thread
@@ -477,10 +633,11 @@ __global__ void __launch_bounds__(kCT) chain_segments_kernel(
       atomicExch(fail, 2);
     }
   }
+#pragma unroll
   for (int i = 0; i < kCE; ++i) {
+    if (i >= n) break;
     const int64_t k = k0 + i;
-    if (k >= K) break;
-    const uint32_t m = meta[k];
+    const uint32_t m = mr[i];
     if (m_type(m) != kMap) {
       if (ord >= 0 && base + ord < seg_cap) {  // close the open segment
         segs[base + ord].map = cur;
@@ -493,16 +650,16 @@ __global__ void __launch_bounds__(kCT) chain_segments_kernel(
         SegRec& r = segs[base + ord];
         r.start = k;
         r.meta = m;
-        r.q = qv[k];
+        r.q = qr[i];
         r.tval = (double)src[k];
-        const uint32_t pm = meta[k > 0 ? k - 1 : 0];
+        const uint32_t pm = i > 0 ? mr[i > 0 ? i - 1 : 0] : meta[k > 0 ? k - 1 : 0];
         r.e_prev = m_e(pm);
         r.prev_certain = (k > 0 && m_certain(pm)) ? 1 : 0;
       } else {
         atomicExch(fail, 2);
       }
     } else {
-      cur = compose(cur, step_map(m_d(m), qv[k], m_fcls(m)));
+      cur = compose(cur, step_map(m_d(m), qr[i], m_fcls(m)));
       steps += 1;
     }
   }
@@ -674,43 +831,75 @@ __global__ void __launch_bounds__(32) chain_walk_kernel(const T* src, T* dst, co
 }
 
 // ---------------------------------------------------------------- pass 8
+// M u_e as T from its bits, for M in [2^P, 2^(P+1)] in magnitude (a value of
+// binade e, or 2^(e+1) after rounding up at the binade's top) with e well
+// inside T's normal range, as every validated step has: integers only.
+template <class T>
+__device__ __forceinline__ T m_to_value_normal(int64_t M, int e) {
+  using F = FP<T>;
+  using U = typename F::U;
+  const uint64_t mag = M < 0 ? (uint64_t)(-M) : (uint64_t)M;
+  U b;
+  if (mag >> (F::P + 1)) b = (U)(e + 1 + F::BIAS) << F::P;
+  else b = ((U)(e + F::BIAS) << F::P) | (U)(mag - (uint64_t(1) << F::P));
+  if (M < 0) b |= (U)1 << (F::W - 1);
+  return F::from_bits(b);
+}
+
 template <class T>
 __global__ void __launch_bounds__(kCT) chain_fill_kernel(const int64_t* qv, const uint32_t* meta,
                                                          int64_t K, const int64_t* seg_base,
-                                                         const SegRec* segs, int64_t seg_cap,
+                                                         const Summ* thr_in, int64_t seg_cap,
                                                          const int64_t* m_in, T* dst, int* fail) {
-  __shared__ Summ sh[kCT];
   const int t = threadIdx.x;
   const int64_t tile0 = (int64_t)blockIdx.x * kCTile;
   const int64_t k0 = tile0 + (int64_t)t * kCE;
-  Summ in;
-  thread_scan(qv, meta, k0, K, in, sh);
-  if (*fail) return;
+  if (*fail || k0 >= K) return;
+  const int64_t n = K - k0 < kCE ? K - k0 : kCE;
+  const Summ in = thr_in[blockIdx.x * kCT + t];
   const bool cont = m_type(meta[tile0]) == kMap;
   int64_t seg = seg_base[blockIdx.x] + (cont ? 1 : 0) + in.brk - 1;
+  int64_t qr[kCE];
+  uint32_t mr[kCE];
+  load_run(qv + k0, n, qr);
+  load_run(meta + k0, n, mr);
   uint64_t M = 0;
-  if (k0 < K && seg >= 0 && seg < seg_cap) M = apply(in.map, (uint64_t)m_in[seg]);
+  if (seg >= 0 && seg < seg_cap) M = apply(in.map, (uint64_t)m_in[seg]);
   bool ok = true;
+  T out[kCE];
+#pragma unroll
   for (int i = 0; i < kCE; ++i) {
-    const int64_t k = k0 + i;
-    if (k >= K) break;
-    const uint32_t m = meta[k];
-    const uint32_t type = m_type(m);
-    if (type != kMap) {  // enter the next segment
-      seg += 1;
-      if (seg >= seg_cap) { ok = false; break; }
-      M = (uint64_t)m_in[seg];
-      if (type == kUp) dst[k] = m_to_value<T>((int64_t)M, m_e(m));  // walk wrote fp breaks
-      continue;
+    out[i] = T(0);
+    if (i < n) {
+      const uint32_t m = mr[i];
+      const uint32_t type = m_type(m);
+      if (type != kMap) {  // enter the next segment
+        seg += 1;
+        if (seg >= seg_cap) {
+          ok = false;
+        } else {
+          M = (uint64_t)m_in[seg];
+          // the walk wrote start and uncertain steps; keep them
+          out[i] = type == kUp ? m_to_value_normal<T>((int64_t)M, m_e(m)) : dst[k0 + i];
+        }
+        continue;
+      }
+      const int d = m_d(m);
+      const uint32_t f = m_fcls(m);
+      int64_t A64;
+      if (d <= 9) {  // |M 2^d| <= 2^63 / 2 and |q| < 2^62: no overflow
+        A64 = (int64_t)(M << d) + qr[i];
+        if (!in_binade64<T>(A64, m_neg(m), f == kFZero)) ok = false;
+      } else {
+        const __int128 A = (__int128)(int64_t)M * ((__int128)1 << d) + (__int128)qr[i];
+        if (!in_binade<T>(A, m_neg(m), f)) ok = false;
+        A64 = (int64_t)A;
+      }
+      M = (uint64_t)(A64 + (int64_t)delta(f, (uint64_t)A64 & 1));
+      out[i] = m_to_value_normal<T>((int64_t)M, m_e(m));
     }
-    const int d = m_d(m);
-    const __int128 A = (__int128)(int64_t)M * ((__int128)1 << d) + (__int128)qv[k];
-    const uint32_t f = m_fcls(m);
-    if (!in_binade<T>(A, m_neg(m), f)) { ok = false; break; }
-    const int64_t A64 = (int64_t)A;
-    M = (uint64_t)(A64 + (int64_t)delta(f, (uint64_t)A64 & 1));
-    dst[k] = m_to_value<T>((int64_t)M, m_e(m));
   }
+  store_run(dst + k0, n, out);
   if (!ok) atomicExch(fail, 1);
 }
 
@@ -738,14 +927,15 @@ ChainPlan plan_chain(int64_t K) {
   size_t off = 0;
   p.tsum_off = off; off += r256(p.ntiles * sizeof(double));
   p.toff_off = off; off += r256(p.ntiles * sizeof(double));
-  p.pre_off = off; off += r256(K * sizeof(double));
+  p.tmax_off = off; off += r256(p.ntiles * sizeof(double));
+  p.thr_off = off; off += r256(p.ntiles * kCT * sizeof(Summ));
   p.q_off = off; off += r256(K * sizeof(int64_t));
   p.meta_off = off; off += r256(K * sizeof(uint32_t));
   p.nseg_off = off; off += r256(p.ntiles * sizeof(int64_t));
   p.segbase_off = off; off += r256(p.ntiles * sizeof(int64_t));
   p.segs_off = off; off += r256(p.seg_cap * sizeof(SegRec));
   p.min_off = off; off += r256(p.seg_cap * sizeof(int64_t));
-  p.misc_off = off; off += 256;  // maxabs (8), total segments (8), fail (4)
+  p.misc_off = off; off += 256;  // bound (8), total segments (8), fail (4)
   p.bytes = off;
   return p;
 }
@@ -755,14 +945,15 @@ cudaError_t run_chain(const ChainPlan& p, const T* src, T* dst, char* ws, cudaSt
   if (p.K <= 0) return cudaSuccess;
   double* tsum = reinterpret_cast<double*>(ws + p.tsum_off);
   double* toff = reinterpret_cast<double*>(ws + p.toff_off);
-  double* pre = reinterpret_cast<double*>(ws + p.pre_off);
+  double* tmax = reinterpret_cast<double*>(ws + p.tmax_off);
+  Summ* thr_in = reinterpret_cast<Summ*>(ws + p.thr_off);
   int64_t* qv = reinterpret_cast<int64_t*>(ws + p.q_off);
   uint32_t* meta = reinterpret_cast<uint32_t*>(ws + p.meta_off);
   int64_t* nseg = reinterpret_cast<int64_t*>(ws + p.nseg_off);
   int64_t* segbase = reinterpret_cast<int64_t*>(ws + p.segbase_off);
   SegRec* segs = reinterpret_cast<SegRec*>(ws + p.segs_off);
   int64_t* m_in = reinterpret_cast<int64_t*>(ws + p.min_off);
-  unsigned long long* maxabs = reinterpret_cast<unsigned long long*>(ws + p.misc_off);
+  double* bound = reinterpret_cast<double*>(ws + p.misc_off);
   int64_t* total = reinterpret_cast<int64_t*>(ws + p.misc_off + 8);
   int* fail = reinterpret_cast<int*>(ws + p.misc_off + 16);
   cudaError_t e = cudaMemsetAsync(ws + p.misc_off, 0, 256, s);
@@ -772,23 +963,23 @@ cudaError_t run_chain(const ChainPlan& p, const T* src, T* dst, char* ws, cudaSt
   if (e != cudaSuccess) return e;
   if (p.ntiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const unsigned g = (unsigned)p.ntiles;
-  CR_LAUNCH(kKChainTileSum, s, chain_tile_sum_kernel<T><<<g, kCT, 0, s>>>(src, p.K, tsum));
+  CR_LAUNCH(kKChainTileSum, s,
+            chain_tile_sum_kernel<T><<<g, kCT, 0, s>>>(src, p.K, tsum, tmax));
   CR_LAUNCH(kKChainOffsets, s,
-            exclusive_scan_1block<double><<<1, 1024, 0, s>>>(tsum, toff, p.ntiles, nullptr));
-  CR_LAUNCH(kKChainPrefix, s,
-            chain_prefix_kernel<T><<<g, kCT, 0, s>>>(src, p.K, toff, pre, maxabs));
+            chain_offsets_kernel<<<1, 1024, 0, s>>>(tsum, tmax, p.ntiles, toff, bound));
   CR_LAUNCH(kKChainClassify, s,
-            chain_classify_kernel<T><<<g, kCT, 0, s>>>(src, p.K, pre, maxabs, qv, meta, nseg));
+            chain_classify_kernel<T><<<g, kCT, 0, s>>>(src, p.K, toff, bound, qv, meta, nseg,
+                                                       thr_in));
   CR_LAUNCH(kKChainOffsets, s,
             exclusive_scan_1block<int64_t><<<1, 1024, 0, s>>>(nseg, segbase, p.ntiles, total));
   CR_LAUNCH(kKChainSegments, s,
-            chain_segments_kernel<T><<<g, kCT, 0, s>>>(src, qv, meta, p.K, segbase, segs,
+            chain_segments_kernel<T><<<g, kCT, 0, s>>>(src, qv, meta, p.K, segbase, thr_in, segs,
                                                        p.seg_cap, fail));
   CR_LAUNCH(kKChainWalk, s,
             chain_walk_kernel<T><<<1, 32, 0, s>>>(src, dst, segs, total, p.seg_cap, m_in, fail));
   CR_LAUNCH(kKChainFill, s,
-            chain_fill_kernel<T><<<g, kCT, 0, s>>>(qv, meta, p.K, segbase, segs, p.seg_cap, m_in,
-                                                   dst, fail));
+            chain_fill_kernel<T><<<g, kCT, 0, s>>>(qv, meta, p.K, segbase, thr_in, p.seg_cap,
+                                                   m_in, dst, fail));
   CR_LAUNCH(kKChainFallback, s, chain_fallback_kernel<T><<<1, 32, 0, s>>>(src, dst, p.K, fail));
   return cudaGetLastError();
 }
