@@ -33,8 +33,10 @@
 //     (same or lower binade), UP (higher binade, integer break), FP
 //     (uncertain: real add); each thread's composed map after its last
 //     break, scanned across the tile;
-//   5 segment bases (one block), 6 segment records: each break (or tile
-//     start) and the composed map of the MAP steps that follow it;
+//   5 segment bases (one block), 6 segment records: each break and the
+//     composed map of the MAP steps that follow it in its tile; the steps
+//     before a tile's first break are folded into the previous tile's last
+//     segment by a small link pass, so the walk sees breaks only;
 //   7 walk: the breaks in order, from integers; M entering every segment;
 //   8 fill: every MAP step recomputed from its segment's entry value with an
 //     exact 128-bit test that s_k lies in the predicted binade and sign;
@@ -316,31 +318,56 @@ __global__ void __launch_bounds__(kCT) chain_tile_sum_kernel(const T* src, int64
 }
 
 // ---------------------------------------------------------------- pass 2 / 5
+// One block of 1024 threads; thread t owns the contiguous chunk
+// [t per, (t + 1) per): its sum, an exclusive scan of the sums across the
+// block (warp shuffles, then the warp totals), then its outputs.
+template <class V>
+__device__ __forceinline__ V block1024_excl(V v, V* sh_w, V& total) {
+  const unsigned full = 0xffffffffu;
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  V incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const V o = __shfl_up_sync(full, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) sh_w[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    const V x = sh_w[lane];
+    V xi = x;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const V o = __shfl_up_sync(full, xi, off);
+      if (lane >= off) xi += o;
+    }
+    sh_w[lane] = xi - x;  // exclusive warp offsets
+    if (lane == 31) sh_w[32] = xi;
+  }
+  __syncthreads();
+  total = sh_w[32];
+  const V r = sh_w[w] + incl - v;
+  __syncthreads();
+  return r;
+}
+
 template <class V>
 __global__ void __launch_bounds__(1024) exclusive_scan_1block(const V* in, V* out, int64_t n,
                                                               V* total) {
-  __shared__ V sh[1024];
-  __shared__ V carry;
+  __shared__ V sh_w[33];
   const int t = threadIdx.x;
-  if (t == 0) carry = V(0);
-  __syncthreads();
-  for (int64_t base = 0; base < n; base += 1024) {
-    const int64_t i = base + t;
-    const V v = i < n ? in[i] : V(0);
-    sh[t] = v;
-    __syncthreads();
-    for (int off = 1; off < 1024; off <<= 1) {
-      const V a = t >= off ? sh[t - off] : V(0);
-      __syncthreads();
-      sh[t] += a;
-      __syncthreads();
-    }
-    if (i < n) out[i] = carry + sh[t] - v;
-    __syncthreads();
-    if (t == 0) carry += sh[1023];
-    __syncthreads();
+  const int64_t per = (n + 1023) / 1024;
+  const int64_t a = t * per, b = a + per < n ? a + per : n;
+  V s = V(0);
+  for (int64_t i = a; i < b; ++i) s += in[i];
+  V tot;
+  V run = block1024_excl(s, sh_w, tot);
+  for (int64_t i = a; i < b; ++i) {
+    const V v = in[i];
+    out[i] = run;
+    run += v;
   }
-  if (t == 0 && total) *total = carry;
+  if (t == 0 && total) *total = tot;
 }
 
 // Tile offsets (exclusive prefix of the tile sums) and the bound
@@ -348,51 +375,33 @@ __global__ void __launch_bounds__(1024) exclusive_scan_1block(const V* in, V* ou
 __global__ void __launch_bounds__(1024) chain_offsets_kernel(const double* tsum,
                                                              const double* tmax, int64_t n,
                                                              double* toff, double* bound) {
-  __shared__ double sh[1024];
-  __shared__ double carry, bmax;
-  const int t = threadIdx.x;
-  if (t == 0) {
-    carry = 0.0;
-    bmax = 0.0;
+  __shared__ double sh_w[33];
+  __shared__ double sh_b[32];
+  const unsigned full = 0xffffffffu;
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const int64_t per = (n + 1023) / 1024;
+  const int64_t a = t * per, b = a + per < n ? a + per : n;
+  double s = 0.0;
+  for (int64_t i = a; i < b; ++i) s += tsum[i];
+  double tot;
+  double run = block1024_excl(s, sh_w, tot);
+  double bm = 0.0;
+  for (int64_t i = a; i < b; ++i) {
+    toff[i] = run;
+    double bb = fabs(run) + (double)kCTile * tmax[i];
+    if (!(bb <= 1.7e308)) bb = 1.7e308;  // non-finite: every step uncertain
+    bm = fmax(bm, bb);
+    run += tsum[i];
   }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) bm = fmax(bm, __shfl_down_sync(full, bm, off));
+  if (lane == 0) sh_b[w] = bm;
   __syncthreads();
-  for (int64_t base = 0; base < n; base += 1024) {
-    const int64_t i = base + t;
-    const double v = i < n ? tsum[i] : 0.0;
-    sh[t] = v;
-    __syncthreads();
-    for (int off = 1; off < 1024; off <<= 1) {
-      const double a = t >= off ? sh[t - off] : 0.0;
-      __syncthreads();
-      sh[t] += a;
-      __syncthreads();
-    }
-    const double o = carry + sh[t] - v;
-    double b = 0.0;
-    if (i < n) {
-      toff[i] = o;
-      b = fabs(o) + (double)kCTile * tmax[i];
-      if (!(b <= 1.7e308)) b = 1.7e308;  // non-finite: every step uncertain
-    }
-    __syncthreads();
-    sh[t] = b;
-    __syncthreads();
-    for (int w = 512; w > 0; w >>= 1) {
-      if (t < w) sh[t] = fmax(sh[t], sh[t + w]);
-      __syncthreads();
-    }
-    if (t == 0) bmax = fmax(bmax, sh[0]);
-    __syncthreads();
-    sh[t] = v;
-    __syncthreads();
-    for (int w = 512; w > 0; w >>= 1) {
-      if (t < w) sh[t] += sh[t + w];
-      __syncthreads();
-    }
-    if (t == 0) carry += sh[0];
-    __syncthreads();
+  if (t == 0) {
+    double m = 0.0;
+    for (int i = 0; i < 32; ++i) m = fmax(m, sh_b[i]);
+    *bound = m * (1.0 + 0x1p-40);  // covers the rounding of the bound itself
   }
-  if (t == 0) *bound = bmax * (1.0 + 0x1p-40);  // covers the rounding of the bound itself
 }
 
 // ---------------------------------------------------------------- pass 3
@@ -499,7 +508,6 @@ __global__ void __launch_bounds__(kCT) chain_classify_kernel(
   __shared__ Summ sh[kCT];
   __shared__ double sh_w[kCT / 32];
   __shared__ int cnt[kCT / 32];
-  __shared__ int first_cont;
   const unsigned full = 0xffffffffu;
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   const int64_t tile0 = (int64_t)blockIdx.x * kCTile;
@@ -518,7 +526,7 @@ __global__ void __launch_bounds__(kCT) chain_classify_kernel(
   int nbrk = 0;
   Summ me{map_id(), 0};
   constexpr int H = kCE / 2;  // outputs written in two halves: fewer live registers
-  int first_type = -1;
+  int first_type = -1;  // (kept for symmetry with the segment pass)
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
   int64_t q_out[H];
@@ -575,16 +583,16 @@ __global__ void __launch_bounds__(kCT) chain_classify_kernel(
   }
   }
   (void)pn;
-  if (t == 0) first_cont = (first_type == (int)kMap) ? 1 : 0;
+  (void)first_type;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) nbrk += __shfl_down_sync(full, nbrk, off);
   if (lane == 0) cnt[w] = nbrk;
-  const Summ in = block_summ_scan(me, sh);  // synchronises: cnt and first_cont visible
+  const Summ in = block_summ_scan(me, sh);  // synchronises: cnt visible
   thr_in[blockIdx.x * kCT + t] = in;
-  if (t == 0) {  // one segment per break, plus one if the tile starts inside a run
+  if (t == 0) {  // one segment per break
     int total = 0;
     for (int i = 0; i < kCT / 32; ++i) total += cnt[i];
-    tile_nseg[blockIdx.x] = total + first_cont;
+    tile_nseg[blockIdx.x] = total;
   }
 }
 
@@ -603,36 +611,28 @@ struct SegRec {
   int32_t nsteps;   // MAP steps in the map
 };
 
+// The steps of a tile before its first break (all of them if it has none)
+// form no record of their own: their composed map goes to lead[tile] (and
+// whether there are any to lead_steps), and the link pass folds it into the
+// previous tile's last segment.
 template <class T>
 __global__ void __launch_bounds__(kCT) chain_segments_kernel(
     const T* src, const int64_t* qv, const uint32_t* meta, int64_t K, const int64_t* seg_base,
-    const Summ* thr_in, SegRec* segs, int64_t seg_cap, int* fail) {
+    const Summ* thr_in, SegRec* segs, int64_t seg_cap, Map* lead, int* lead_steps,
+    int* fail) {
   const int t = threadIdx.x;
   const int64_t tile0 = (int64_t)blockIdx.x * kCTile;
   const int64_t k0 = tile0 + (int64_t)t * kCE;
   const int64_t n = k0 < K ? (K - k0 < kCE ? K - k0 : kCE) : 0;
   const Summ in = thr_in[blockIdx.x * kCT + t];
-  const bool cont = m_type(meta[tile0]) == kMap;
   int64_t qr[kCE];
   uint32_t mr[kCE];
   load_run(qv + (k0 < K ? k0 : 0), n, qr);
   load_run(meta + (k0 < K ? k0 : 0), n, mr);
-  int64_t ord = (cont ? 1 : 0) + in.brk - 1;  // segment open at my first step
+  int64_t ord = in.brk - 1;  // segment open at my first step (-1: the leading run)
   Map cur = in.map;
   int steps = 0;  // MAP steps of the open segment seen by this thread
   const int64_t base = seg_base[blockIdx.x];
-  if (t == 0 && cont) {
-    if (base < seg_cap) {
-      SegRec& r = segs[base];
-      r.start = tile0;
-      r.meta = meta[tile0];
-      r.q = 0;
-      r.e_prev = 0;
-      r.prev_certain = 0;
-    } else {
-      atomicExch(fail, 2);
-    }
-  }
 #pragma unroll
   for (int i = 0; i < kCE; ++i) {
     if (i >= n) break;
@@ -642,6 +642,9 @@ __global__ void __launch_bounds__(kCT) chain_segments_kernel(
       if (ord >= 0 && base + ord < seg_cap) {  // close the open segment
         segs[base + ord].map = cur;
         if (steps) atomicAdd(&segs[base + ord].nsteps, steps);
+      } else if (ord < 0) {  // the tile's leading run ends here
+        lead[blockIdx.x] = cur;
+        if (steps) atomicAdd(&lead_steps[blockIdx.x], steps);
       }
       ord += 1;
       cur = map_id();
@@ -663,12 +666,94 @@ __global__ void __launch_bounds__(kCT) chain_segments_kernel(
       steps += 1;
     }
   }
+  // my trailing MAP steps belong to the segment still open; the thread
+  // holding the tile's last step closes it
+  const int64_t last = (tile0 + kCTile < K ? tile0 + kCTile : K) - 1;
+  const bool closer = k0 <= last && last < k0 + kCE;
   if (ord >= 0 && base + ord < seg_cap) {
-    // my trailing MAP steps belong to the segment still open; the thread
-    // holding the tile's last step closes it
     if (steps) atomicAdd(&segs[base + ord].nsteps, steps);
-    const int64_t last = (tile0 + kCTile < K ? tile0 + kCTile : K) - 1;
-    if (k0 <= last && last < k0 + kCE) segs[base + ord].map = cur;
+    if (closer) segs[base + ord].map = cur;
+  } else if (ord < 0 && n > 0) {  // no break in the tile up to here
+    if (steps) atomicAdd(&lead_steps[blockIdx.x], steps);
+    if (closer) lead[blockIdx.x] = cur;
+  }
+}
+
+// Link pass (one block): a segmented scan over the tiles. State after tile
+// u: the last segment r that starts at or before it and the composed map
+// from r's start to the end of u. A tile with breaks resets it to (its last
+// segment, that segment's map); a tile without composes its leading run on.
+// Then entry[u] = the state entering tile u (the fill pass starts u's
+// leading run from it), and the segment r whose chain tile u (with breaks)
+// ends gets the map up to u's first break: the walk sees breaks only.
+struct LinkSt {
+  Map map;
+  int64_t r;
+  int steps;
+  int reset;
+};
+__device__ __forceinline__ LinkSt link_combine(const LinkSt& a, const LinkSt& b) {
+  if (b.reset) return b;
+  return LinkSt{compose(a.map, b.map), a.r, a.steps + b.steps, a.reset};
+}
+
+// Segment maps are read (scan phases) before any is written (last phase, after
+// a barrier); a tile's lead slots, touched by one thread only, hold the new
+// map in between.
+__global__ void __launch_bounds__(1024) chain_link_kernel(const int64_t* tile_nseg,
+                                                          const int64_t* seg_base,
+                                                          int64_t ntiles, SegRec* segs,
+                                                          int64_t seg_cap, Map* lead,
+                                                          int* lead_steps, Map* entry,
+                                                          int64_t* entry_rec) {
+  __shared__ LinkSt sh[1024];
+  __shared__ LinkSt last_st;
+  const int t = threadIdx.x;
+  const int64_t per = (ntiles + 1023) / 1024;
+  const int64_t a = t * per, b = a + per < ntiles ? a + per : ntiles;
+  auto elem = [&](int64_t u) -> LinkSt {
+    const int64_t nb = tile_nseg[u];
+    if (nb > 0) {
+      const int64_t r = seg_base[u] + nb - 1;
+      if (r >= seg_cap) return LinkSt{map_id(), -1, 0, 1};  // overflow: the walk fails
+      return LinkSt{segs[r].map, r, segs[r].nsteps, 1};
+    }
+    return LinkSt{lead[u], -1, lead_steps[u], 0};
+  };
+  LinkSt agg{map_id(), -1, 0, 0};
+  for (int64_t u = a; u < b; ++u) agg = link_combine(agg, elem(u));
+  sh[t] = agg;
+  __syncthreads();
+  for (int off = 1; off < 1024; off <<= 1) {  // inclusive
+    LinkSt v = sh[t];
+    if (t >= off) v = link_combine(sh[t - off], v);
+    __syncthreads();
+    sh[t] = v;
+    __syncthreads();
+  }
+  LinkSt st = t > 0 ? sh[t - 1] : LinkSt{map_id(), -1, 0, 0};
+  for (int64_t u = a; u < b; ++u) {
+    entry[u] = st.map;
+    entry_rec[u] = st.r;
+    const LinkSt e = elem(u);
+    if (e.reset) {  // the chain of segment st.r ends at u's first break
+      lead[u] = compose(st.map, lead[u]);
+      lead_steps[u] = st.steps + lead_steps[u];
+    }
+    st = link_combine(st, e);
+  }
+  if (t == 1023) last_st = sh[1023];
+  __syncthreads();
+  for (int64_t u = a; u < b; ++u) {
+    const int64_t r = entry_rec[u];
+    if (tile_nseg[u] > 0 && r >= 0 && r < seg_cap) {
+      segs[r].map = lead[u];
+      segs[r].nsteps = lead_steps[u];
+    }
+  }
+  if (t == 0 && last_st.r >= 0 && last_st.r < seg_cap) {  // the last chain runs to the end
+    segs[last_st.r].map = last_st.map;
+    segs[last_st.r].nsteps = last_st.steps;
   }
 }
 
@@ -849,22 +934,28 @@ __device__ __forceinline__ T m_to_value_normal(int64_t M, int e) {
 template <class T>
 __global__ void __launch_bounds__(kCT) chain_fill_kernel(const int64_t* qv, const uint32_t* meta,
                                                          int64_t K, const int64_t* seg_base,
-                                                         const Summ* thr_in, int64_t seg_cap,
-                                                         const int64_t* m_in, T* dst, int* fail) {
+                                                         const Summ* thr_in, const Map* entry,
+                                                         const int64_t* entry_rec,
+                                                         int64_t seg_cap, const int64_t* m_in,
+                                                         T* dst, int* fail) {
   const int t = threadIdx.x;
   const int64_t tile0 = (int64_t)blockIdx.x * kCTile;
   const int64_t k0 = tile0 + (int64_t)t * kCE;
   if (*fail || k0 >= K) return;
   const int64_t n = K - k0 < kCE ? K - k0 : kCE;
   const Summ in = thr_in[blockIdx.x * kCT + t];
-  const bool cont = m_type(meta[tile0]) == kMap;
-  int64_t seg = seg_base[blockIdx.x] + (cont ? 1 : 0) + in.brk - 1;
+  int64_t seg = seg_base[blockIdx.x] + in.brk - 1;
   int64_t qr[kCE];
   uint32_t mr[kCE];
   load_run(qv + k0, n, qr);
   load_run(meta + k0, n, mr);
   uint64_t M = 0;
-  if (seg >= 0 && seg < seg_cap) M = apply(in.map, (uint64_t)m_in[seg]);
+  if (in.brk > 0) {
+    if (seg < seg_cap) M = apply(in.map, (uint64_t)m_in[seg]);
+  } else if (blockIdx.x > 0) {  // the tile's leading run: enters from an earlier tile
+    const int64_t r = entry_rec[blockIdx.x];
+    if (r >= 0 && r < seg_cap) M = apply(in.map, apply(entry[blockIdx.x], (uint64_t)m_in[r]));
+  }
   bool ok = true;
   T out[kCE];
 #pragma unroll
@@ -929,6 +1020,10 @@ ChainPlan plan_chain(int64_t K) {
   p.toff_off = off; off += r256(p.ntiles * sizeof(double));
   p.tmax_off = off; off += r256(p.ntiles * sizeof(double));
   p.thr_off = off; off += r256(p.ntiles * kCT * sizeof(Summ));
+  p.lead_off = off; off += r256(p.ntiles * sizeof(Map));
+  p.leadsteps_off = off; off += r256(p.ntiles * sizeof(int));
+  p.entry_off = off; off += r256(p.ntiles * sizeof(Map));
+  p.entryrec_off = off; off += r256(p.ntiles * sizeof(int64_t));
   p.q_off = off; off += r256(K * sizeof(int64_t));
   p.meta_off = off; off += r256(K * sizeof(uint32_t));
   p.nseg_off = off; off += r256(p.ntiles * sizeof(int64_t));
@@ -947,6 +1042,10 @@ cudaError_t run_chain(const ChainPlan& p, const T* src, T* dst, char* ws, cudaSt
   double* toff = reinterpret_cast<double*>(ws + p.toff_off);
   double* tmax = reinterpret_cast<double*>(ws + p.tmax_off);
   Summ* thr_in = reinterpret_cast<Summ*>(ws + p.thr_off);
+  Map* lead = reinterpret_cast<Map*>(ws + p.lead_off);
+  int* lead_steps = reinterpret_cast<int*>(ws + p.leadsteps_off);
+  Map* entry = reinterpret_cast<Map*>(ws + p.entry_off);
+  int64_t* entry_rec = reinterpret_cast<int64_t*>(ws + p.entryrec_off);
   int64_t* qv = reinterpret_cast<int64_t*>(ws + p.q_off);
   uint32_t* meta = reinterpret_cast<uint32_t*>(ws + p.meta_off);
   int64_t* nseg = reinterpret_cast<int64_t*>(ws + p.nseg_off);
@@ -961,6 +1060,8 @@ cudaError_t run_chain(const ChainPlan& p, const T* src, T* dst, char* ws, cudaSt
   // per-segment MAP step counts are accumulated with atomics: clear them
   e = cudaMemsetAsync(segs, 0, (size_t)p.seg_cap * sizeof(SegRec), s);
   if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(lead_steps, 0, (size_t)p.ntiles * sizeof(int), s);
+  if (e != cudaSuccess) return e;
   if (p.ntiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const unsigned g = (unsigned)p.ntiles;
   CR_LAUNCH(kKChainTileSum, s,
@@ -974,12 +1075,15 @@ cudaError_t run_chain(const ChainPlan& p, const T* src, T* dst, char* ws, cudaSt
             exclusive_scan_1block<int64_t><<<1, 1024, 0, s>>>(nseg, segbase, p.ntiles, total));
   CR_LAUNCH(kKChainSegments, s,
             chain_segments_kernel<T><<<g, kCT, 0, s>>>(src, qv, meta, p.K, segbase, thr_in, segs,
-                                                       p.seg_cap, fail));
+                                                       p.seg_cap, lead, lead_steps, fail));
+  CR_LAUNCH(kKChainLink, s,
+            chain_link_kernel<<<1, 1024, 0, s>>>(nseg, segbase, p.ntiles, segs, p.seg_cap, lead,
+                                                 lead_steps, entry, entry_rec));
   CR_LAUNCH(kKChainWalk, s,
             chain_walk_kernel<T><<<1, 32, 0, s>>>(src, dst, segs, total, p.seg_cap, m_in, fail));
   CR_LAUNCH(kKChainFill, s,
-            chain_fill_kernel<T><<<g, kCT, 0, s>>>(qv, meta, p.K, segbase, thr_in, p.seg_cap,
-                                                   m_in, dst, fail));
+            chain_fill_kernel<T><<<g, kCT, 0, s>>>(qv, meta, p.K, segbase, thr_in, entry,
+                                                   entry_rec, p.seg_cap, m_in, dst, fail));
   CR_LAUNCH(kKChainFallback, s, chain_fallback_kernel<T><<<1, 32, 0, s>>>(src, dst, p.K, fail));
   return cudaGetLastError();
 }

@@ -10,7 +10,8 @@ namespace cr {
 
 struct ChainPlan {
   int64_t K = 0, ntiles = 0, seg_cap = 0;
-  size_t tsum_off = 0, toff_off = 0, tmax_off = 0, thr_off = 0, q_off = 0, meta_off = 0,
+  size_t tsum_off = 0, toff_off = 0, tmax_off = 0, thr_off = 0, lead_off = 0,
+         leadsteps_off = 0, entry_off = 0, entryrec_off = 0, q_off = 0, meta_off = 0,
          nseg_off = 0, segbase_off = 0, segs_off = 0, min_off = 0, misc_off = 0;
   size_t bytes = 0;  // workspace bytes (offsets are relative to the chain's base)
 };

@@ -43,7 +43,8 @@ const char* kernel_name(int id) {
       "chain_fill_kernel",     "chain_fallback_kernel", "scan_onepass_kernel",
       "scan_local_kernel",     "carry_fixup_kernel",    "scan_pairwise_kernel",
       "apply_init_kernel",     "fill_init_kernel",      "carry_fixup_shift_kernel",
-      "scan_seq_block_kernel", "row_reduce_kernel"};
+      "scan_seq_block_kernel", "row_reduce_kernel",
+      "chain_link_kernel"};
   return (id >= 0 && id < kKernelCount) ? names[id] : "unknown";
 }
 

@@ -34,6 +34,7 @@ enum KernelId : int {
   kKCarryFixupShift,
   kKScanSeqBlock,
   kKRowReduce,
+  kKChainLink,
   kKernelCount
 };
 

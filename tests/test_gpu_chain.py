@@ -58,6 +58,10 @@ CASES = {
     * (np.arange(n) // 2 % 7 + 1),
     "big_small_mix": lambda n, dt: np.where(np.arange(n) % 97 == 0, 1e12, 1.0).astype(dt)
     * u(n, 17).astype(dt),
+    # one large first value, then small steps that never change its binade:
+    # long runs of tiles without any break
+    "big_then_small": lambda n, dt: np.where(np.arange(n) == 0, 2.0 ** 30,
+                                             np.abs(u(n, 18)) * 1e-3).astype(dt),
 }
 
 
