@@ -159,11 +159,25 @@ def _init_buffer(init, dt_code):
     return ctypes.c_float(float(init))
 
 
-def _on_device(x: torch.Tensor):
-    """Host tensors are copied in (the result is copied back by the caller)."""
+def _on_device(x: torch.Tensor, stream=None):
+    """Host tensors are copied in on the call's stream (asynchronously from
+    pinned memory); the caller copies the result back with _to_host."""
     if x.is_cuda:
         return x, False
-    return x.to("cuda", non_blocking=True), True
+    s = torch.cuda.current_stream() if stream is None else stream
+    with torch.cuda.stream(s):
+        return x.to("cuda", non_blocking=True), True
+
+
+def _to_host(o: torch.Tensor, stream=None) -> torch.Tensor:
+    """Device result -> a pinned host tensor, copied on the call's stream,
+    which is then synchronised."""
+    s = torch.cuda.current_stream(o.device) if stream is None else stream
+    h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    with torch.cuda.stream(s):
+        h.copy_(o, non_blocking=True)
+    s.synchronize()
+    return h
 
 
 # ---------------------------------------------------------------- reduce
@@ -175,7 +189,7 @@ def reduce(x: torch.Tensor, L: int, init=0.0, out: torch.Tensor | None = None,
     gives a host tensor back, through pinned-memory copies)."""
     if x.dim() != 1:
         raise ValueError("reduce expects a 1-D tensor; use reduce_batched for 2-D")
-    xd, host = _on_device(x.contiguous() if x.is_cuda else x)
+    xd, host = _on_device(x.contiguous() if x.is_cuda else x, stream)
     xd = xd.contiguous()
     dt = _dtype_code(xd)
     n = xd.numel()
@@ -188,7 +202,7 @@ def reduce(x: torch.Tensor, L: int, init=0.0, out: torch.Tensor | None = None,
     ini = _init_buffer(init, dt)
     _check(lib().cr_reduce(xd.data_ptr() if n else None, n, int(L), ctypes.byref(ini), dt,
                            o.data_ptr(), ws.data_ptr(), ws.numel(), sp), "cr_reduce")
-    return o.to("cpu") if host else o
+    return _to_host(o, stream) if host else o
 
 
 def reduce_batched(x: torch.Tensor, L: int, init=0.0, dim: int = -1,
@@ -197,7 +211,7 @@ def reduce_batched(x: torch.Tensor, L: int, init=0.0, dim: int = -1,
     strides): dim=-1 reduces rows, dim=0 reduces columns."""
     if x.dim() != 2:
         raise ValueError("reduce_batched expects a 2-D tensor")
-    xd, host = _on_device(x)
+    xd, host = _on_device(x, stream)
     dt = _dtype_code(xd)
     d = dim % 2
     n = xd.shape[d]
@@ -213,7 +227,7 @@ def reduce_batched(x: torch.Tensor, L: int, init=0.0, dim: int = -1,
     _check(lib().cr_reduce_batched(xd.data_ptr(), o.data_ptr(), batch, n, es, bs, int(L),
                                    ctypes.byref(ini), dt, ws.data_ptr(), ws.numel(), sp),
            "cr_reduce_batched")
-    return o.to("cpu") if host else o
+    return _to_host(o, stream) if host else o
 
 
 # ------------------------------------------------------------------ scan
@@ -227,7 +241,7 @@ def inclusive_scan(x: torch.Tensor, policy="iterated_pairwise", B: int = 1,
     ``out`` may be ``x`` itself (in place)."""
     if x.dim() != 1:
         raise ValueError("inclusive_scan expects a 1-D tensor")
-    xd, host = _on_device(x)
+    xd, host = _on_device(x, stream)
     xd = xd.contiguous()
     dt = _dtype_code(xd)
     n = xd.numel()
@@ -240,7 +254,7 @@ def inclusive_scan(x: torch.Tensor, policy="iterated_pairwise", B: int = 1,
     ws = _WS.get(xd.device, stream, nb)
     _check(lib().cr_inclusive_scan(xd.data_ptr(), o.data_ptr(), n, p, int(B), dt,
                                    ws.data_ptr(), ws.numel(), sp), "cr_inclusive_scan")
-    return o.to("cpu") if host else o
+    return _to_host(o, stream) if host else o
 
 
 def inclusive_scan_batched(x: torch.Tensor, policy="left_fold", B: int = 1, dim: int = 0,
@@ -250,7 +264,7 @@ def inclusive_scan_batched(x: torch.Tensor, policy="left_fold", B: int = 1, dim:
     strides."""
     if x.dim() != 2:
         raise ValueError("inclusive_scan_batched expects a 2-D tensor")
-    xd, host = _on_device(x)
+    xd, host = _on_device(x, stream)
     dt = _dtype_code(xd)
     d = dim % 2
     n, batch = xd.shape[d], xd.shape[1 - d]
@@ -268,13 +282,13 @@ def inclusive_scan_batched(x: torch.Tensor, policy="left_fold", B: int = 1, dim:
     _check(lib().cr_inclusive_scan_batched(xd.data_ptr(), o.data_ptr(), batch, n, es, bs, p,
                                            int(B), dt, ws.data_ptr(), ws.numel(), sp),
            "cr_inclusive_scan_batched")
-    return o.to("cpu") if host else o
+    return _to_host(o, stream) if host else o
 
 
 def _scan_ex(x, policy, B, init, mode, out, stream, what):
     if x.dim() != 1:
         raise ValueError("%s expects a 1-D tensor" % what)
-    xd, host = _on_device(x)
+    xd, host = _on_device(x, stream)
     xd = xd.contiguous()
     dt = _dtype_code(xd)
     n = xd.numel()
@@ -292,7 +306,7 @@ def _scan_ex(x, policy, B, init, mode, out, stream, what):
     ini = _init_buffer(init, dt)
     _check(lib().cr_scan_ex(xd.data_ptr() if n else None, o.data_ptr(), n, p, int(B), md,
                             ctypes.byref(ini), dt, ws.data_ptr(), ws.numel(), sp), "cr_scan_ex")
-    return o.to("cpu") if host else o
+    return _to_host(o, stream) if host else o
 
 
 def exclusive_scan(x: torch.Tensor, policy="iterated_pairwise", B: int = 1, init=0.0,
@@ -312,7 +326,7 @@ def scan_include_initial(x: torch.Tensor, policy="iterated_pairwise", B: int = 1
 def _scan_ex_batched(x, policy, B, init, dim, mode, out, stream, what):
     if x.dim() != 2:
         raise ValueError("%s expects a 2-D tensor" % what)
-    xd, host = _on_device(x)
+    xd, host = _on_device(x, stream)
     dt = _dtype_code(xd)
     d = dim % 2
     n, batch = xd.shape[d], xd.shape[1 - d]
@@ -334,7 +348,7 @@ def _scan_ex_batched(x, policy, B, init, dim, mode, out, stream, what):
     _check(lib().cr_scan_ex_batched(xd.data_ptr() if xd.numel() else None, o.data_ptr(), batch,
                                     n, es, bs, oes, obs, p, int(B), md, ctypes.byref(ini), dt,
                                     ws.data_ptr(), ws.numel(), sp), "cr_scan_ex_batched")
-    return o.to("cpu") if host else o
+    return _to_host(o, stream) if host else o
 
 
 def exclusive_scan_batched(x: torch.Tensor, policy="left_fold", B: int = 1, init=0.0,

@@ -790,27 +790,20 @@ __device__ __forceinline__ Hot make_hot(const SegRec& r, int64_t q_next) {
   return h;
 }
 
-// One break (rise or continuation) from A: writes m_in, returns the next A.
+// One rise from A: writes m_in, returns the next A. (Whether the rise really
+// lands in its predicted binade is checked afterwards, in parallel, by
+// chain_verify_kernel, which recomputes A from the previous record.)
 template <class T>
 __device__ __forceinline__ int64_t walk_fast(const Hot& h, int64_t A, int64_t* m_in_j,
-                                             uint32_t& okw, bool& cval) {
+                                             bool& cval) {
   const uint32_t c = h.ctrl;
   const int d = (int)(c & 63u);
   const uint32_t sh = (c >> 6) & 127u;
-  const uint32_t rise = (c >> 13) & 1u, fpos = (c >> 14) & 1u;
-  const int64_t hi = A >> d;
-  const int64_t x = (int64_t)(((uint32_t)hi & rise) | (fpos & rise));
+  const int64_t rise = (c >> 13) & 1u, fpos = (c >> 14) & 1u;
+  const int64_t x = rise & ((A >> d) | fpos);
   const int64_t M1 = (A + h.c + x) >> d;
   *m_in_j = M1;
-  // in-binade test of a rise, as integer comparisons on hi (off the chain)
-  constexpr int64_t LO = int64_t(1) << FP<T>::P, HI = int64_t(1) << (FP<T>::P + 1);
-  const uint64_t mask = (uint64_t(1) << d) - 1;  // d = 0: 0
-  const uint32_t fz = (((uint64_t)A & mask) == 0) & (fpos ^ 1u);
-  const uint32_t pos_ok = (hi >= LO) & (hi <= HI - 1);
-  const uint32_t neg_ok = fz ? (hi <= -LO) & (hi >= -HI + 1) : (hi <= -LO - 1) & (hi >= -HI);
-  const uint32_t in_ok = ((c >> 15) & 1u) ? neg_ok : pos_ok;
-  okw &= rise ? in_ok : 1u;
-  cval = cval & !rise & !((c >> 18) & 1u);
+  cval = cval & ((c & ((1u << 13) | (1u << 18))) == 0);
   const uint64_t aM = sh >= 64 ? 0 : ((uint64_t)M1 << sh);
   return (int64_t)(aM + ((M1 & 1) ? h.b1 : h.b0));
 }
@@ -862,22 +855,19 @@ __global__ void __launch_bounds__(32) chain_walk_kernel(const T* src, T* dst, co
     if (lane == 0) {
       const int cnt = (int)(nseg - b0 < 32 ? nseg - b0 : 32);
       bool ok = true;
-      uint32_t okw = 1u;
       if (!cold_batch[slot]) {
         if (cnt == 32) {
-#pragma unroll 8
-          for (int j = 0; j < 32; ++j)
-            A = walk_fast<T>(hot[slot][j], A, m_in + b0 + j, okw, cval);
+#pragma unroll 16
+          for (int j = 0; j < 32; ++j) A = walk_fast<T>(hot[slot][j], A, m_in + b0 + j, cval);
         } else {
-          for (int j = 0; j < cnt; ++j)
-            A = walk_fast<T>(hot[slot][j], A, m_in + b0 + j, okw, cval);
+          for (int j = 0; j < cnt; ++j) A = walk_fast<T>(hot[slot][j], A, m_in + b0 + j, cval);
         }
       } else {
         for (int j = 0; j < cnt; ++j) {
           const Hot h = hot[slot][j];
           const uint32_t type = (h.ctrl >> 16) & 3u;
           if (type <= kUp) {
-            A = walk_fast<T>(h, A, m_in + b0 + j, okw, cval);
+            A = walk_fast<T>(h, A, m_in + b0 + j, cval);
             continue;
           }
           // start or uncertain step: the real add. The previous record folded
@@ -908,11 +898,34 @@ __global__ void __launch_bounds__(32) chain_walk_kernel(const T* src, T* dst, co
           cval = cval & !((h.ctrl >> 18) & 1u);
         }
       }
-      bad = bad || !ok || !okw;
+      bad = bad || !ok;
     }
     __syncwarp();
   }
   if (lane == 0 && bad) atomicExch(fail, 1);
+}
+
+// Every rise of the walk, checked in parallel: A = (previous record's map
+// applied to its M) + q must round into the predicted binade and sign
+// (integer comparisons on hi = floor(A / 2^d)). A failure sends the chain
+// to the serial fallback.
+template <class T>
+__global__ void __launch_bounds__(256) chain_verify_kernel(const SegRec* segs,
+                                                           const int64_t* nseg_total,
+                                                           int64_t seg_cap, const int64_t* m_in,
+                                                           int* fail) {
+  const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t nseg = *nseg_total;
+  if (j == 0 || j >= nseg || j >= seg_cap || *fail) return;
+  const uint32_t m = segs[j].meta;
+  if (m_type(m) != kUp) return;
+  const Map g = segs[j - 1].map;
+  const int64_t A = (int64_t)apply(g, (uint64_t)m_in[j - 1]) + segs[j].q;
+  const int d = m_d(m);
+  const int64_t hi = A >> d;
+  const uint64_t lo = (uint64_t)A & ((uint64_t(1) << d) - 1);
+  const bool fpos = m_fcls(m) != kFZero;
+  if (!in_binade64<T>(hi, m_neg(m), lo == 0 && !fpos)) atomicExch(fail, 1);
 }
 
 // ---------------------------------------------------------------- pass 8
@@ -1081,6 +1094,10 @@ cudaError_t run_chain(const ChainPlan& p, const T* src, T* dst, char* ws, cudaSt
                                                  lead_steps, entry, entry_rec));
   CR_LAUNCH(kKChainWalk, s,
             chain_walk_kernel<T><<<1, 32, 0, s>>>(src, dst, segs, total, p.seg_cap, m_in, fail));
+  if ((p.seg_cap + 255) / 256 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  CR_LAUNCH(kKChainVerify, s,
+            chain_verify_kernel<T><<<(unsigned)((p.seg_cap + 255) / 256), 256, 0, s>>>(
+                segs, total, p.seg_cap, m_in, fail));
   CR_LAUNCH(kKChainFill, s,
             chain_fill_kernel<T><<<g, kCT, 0, s>>>(qv, meta, p.K, segbase, thr_in, entry,
                                                    entry_rec, p.seg_cap, m_in, dst, fail));

@@ -35,6 +35,7 @@ enum KernelId : int {
   kKScanSeqBlock,
   kKRowReduce,
   kKChainLink,
+  kKChainVerify,
   kKernelCount
 };
 
