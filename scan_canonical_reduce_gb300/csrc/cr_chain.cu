@@ -42,6 +42,10 @@
 //     exact 128-bit test that s_k lies in the predicted binade and sign;
 //   9 if any test failed (or the segment buffer overflowed), the serial chain
 //     recomputes everything on the device (no host sync).
+// mu is a rigorous bound, so the evaluation pays only where K ulp is small
+// against the values: binary64 chains of any practical length, binary32
+// chains of a few thousand steps. Longer binary32 chains use the serial
+// chain directly (run_serial_chain).
 // Every add of the chain is therefore the real add or proven equal to it.
 #include <cstdint>
 
@@ -1008,14 +1012,70 @@ __global__ void __launch_bounds__(kCT) chain_fill_kernel(const int64_t* qv, cons
 }
 
 // ---------------------------------------------------------------- pass 9
+// The left fold in one warp, streamed: the warp moves the steps through
+// shared memory in buffers of 1024 (coalesced loads and stores) while lane 0
+// folds the current buffer; the next buffer's loads are in flight meanwhile.
+// With only_if non-null it runs only when *only_if is set (the fallback of
+// the parallel evaluation). A buffer is read before any of its results is
+// stored, and the next buffer is read before this one's results are stored,
+// so dst may equal src.
 template <class T>
-__global__ void chain_fallback_kernel(const T* src, T* dst, int64_t K, const int* fail) {
-  if (threadIdx.x != 0 || blockIdx.x != 0 || *fail == 0) return;
-  T c = src[0];
-  dst[0] = c;
-  for (int64_t k = 1; k < K; ++k) {
-    c = add_rn(c, src[k]);
-    dst[k] = c;
+__global__ void __launch_bounds__(32) chain_serial_kernel(const T* src, T* dst, int64_t K,
+                                                          const int* only_if) {
+  constexpr int kBuf = 1024, kPer = kBuf / 32;
+  __shared__ __align__(16) T buf[kBuf];
+  const int lane = threadIdx.x;
+  if (only_if != nullptr && *only_if == 0) return;
+  T nxt[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int64_t k = lane + 32 * i;
+    nxt[i] = k < K ? src[k] : T(0);
+  }
+  T c = T(0);
+  for (int64_t base = 0; base < K; base += kBuf) {
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) buf[lane + 32 * i] = nxt[i];
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {  // the next buffer, in flight during the fold
+      const int64_t k = base + kBuf + lane + 32 * i;
+      nxt[i] = k < K ? src[k] : T(0);
+    }
+    if (lane == 0) {  // 32 steps at a time through registers (16-byte smem moves)
+      const int cnt = (int)(K - base < kBuf ? K - base : kBuf);
+      constexpr int G = 32, PER = 16 / sizeof(T);
+      for (int j0 = 0; j0 < cnt; j0 += G) {
+        T v[G];
+#pragma unroll
+        for (int u = 0; u < G / PER; ++u) {
+          const uint4 d = reinterpret_cast<const uint4*>(buf + j0)[u];
+#pragma unroll
+          for (int w = 0; w < PER; ++w) v[u * PER + w] = reinterpret_cast<const T*>(&d)[w];
+        }
+        c = (base == 0 && j0 == 0) ? v[0] : add_rn(c, v[0]);  // the chain starts at C_0 = T_0
+        v[0] = c;
+#pragma unroll
+        for (int u = 1; u < G; ++u) {
+          c = add_rn(c, v[u]);
+          v[u] = c;
+        }
+#pragma unroll
+        for (int u = 0; u < G / PER; ++u) {
+          uint4 d;
+#pragma unroll
+          for (int w = 0; w < PER; ++w) reinterpret_cast<T*>(&d)[w] = v[u * PER + w];
+          reinterpret_cast<uint4*>(buf + j0)[u] = d;
+        }
+      }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int64_t k = base + lane + 32 * i;
+      if (k < K) dst[k] = buf[lane + 32 * i];
+    }
+    __syncwarp();
   }
 }
 
@@ -1101,10 +1161,19 @@ cudaError_t run_chain(const ChainPlan& p, const T* src, T* dst, char* ws, cudaSt
   CR_LAUNCH(kKChainFill, s,
             chain_fill_kernel<T><<<g, kCT, 0, s>>>(qv, meta, p.K, segbase, thr_in, entry,
                                                    entry_rec, p.seg_cap, m_in, dst, fail));
-  CR_LAUNCH(kKChainFallback, s, chain_fallback_kernel<T><<<1, 32, 0, s>>>(src, dst, p.K, fail));
+  CR_LAUNCH(kKChainFallback, s, chain_serial_kernel<T><<<1, 32, 0, s>>>(src, dst, p.K, fail));
   return cudaGetLastError();
 }
 
+template <class T>
+cudaError_t run_serial_chain(const T* src, T* dst, int64_t K, cudaStream_t s) {
+  if (K <= 0) return cudaSuccess;
+  CR_LAUNCH(kKCarryChain, s, chain_serial_kernel<T><<<1, 32, 0, s>>>(src, dst, K, nullptr));
+  return cudaGetLastError();
+}
+
+template cudaError_t run_serial_chain<double>(const double*, double*, int64_t, cudaStream_t);
+template cudaError_t run_serial_chain<float>(const float*, float*, int64_t, cudaStream_t);
 template cudaError_t run_chain<double>(const ChainPlan&, const double*, double*, char*,
                                        cudaStream_t);
 template cudaError_t run_chain<float>(const ChainPlan&, const float*, float*, char*,

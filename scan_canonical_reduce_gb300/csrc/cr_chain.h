@@ -23,4 +23,14 @@ ChainPlan plan_chain(int64_t K);
 template <class T>
 cudaError_t run_chain(const ChainPlan& plan, const T* src, T* dst, char* ws, cudaStream_t s);
 
+// The same fold evaluated one step after the other by one warp (steps
+// streamed through shared memory): for short chains, and for binary32 chains
+// too long for the parallel evaluation's error bound. dst may equal src.
+template <class T>
+cudaError_t run_serial_chain(const T* src, T* dst, int64_t K, cudaStream_t s);
+
+// Longest binary32 chain the parallel evaluation is used for (K ulp must stay
+// small against the chain's values for its binade tests to be decisive).
+constexpr int64_t kMaxParallelChainF32 = 4096;
+
 }  // namespace cr

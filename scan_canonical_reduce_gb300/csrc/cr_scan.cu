@@ -758,34 +758,6 @@ fill_init_kernel(T* out, int64_t count, int64_t stride, T init) {
   if (q < count) out[q * stride] = init;
 }
 
-// --------------------------------------------------------------- carry chain
-// carries[0] = src[0], carries[k] = carries[k-1] op src[k], k < K. A serial
-// chain by definition of the expression; one thread, loads issued ahead of
-// the dependent adds. Also the whole 1-D left_fold scan (src = x, carries =
-// out, possibly the same array: plain loads, each read before its write).
-template <class T>
-__global__ void carry_chain_kernel(const T* src, T* carries, int64_t K) {
-  if (threadIdx.x != 0 || blockIdx.x != 0 || K <= 0) return;
-  T c = src[0];
-  carries[0] = c;
-  int64_t k = 1;
-  constexpr int D = 32;
-  for (; k + D <= K; k += D) {
-    T tv[D];
-#pragma unroll
-    for (int d = 0; d < D; ++d) tv[d] = src[k + d];
-#pragma unroll
-    for (int d = 0; d < D; ++d) {
-      c = add_rn(c, tv[d]);
-      carries[k + d] = c;
-    }
-  }
-  for (; k < K; ++k) {
-    c = add_rn(c, src[k]);
-    carries[k] = c;
-  }
-}
-
 // ------------------------------------------------ batched: thread per sequence
 // Sequence q: element k at x[q*bs + k*es]; inclusive results go to
 // out[q*obs + k*oes]. Shifted forms (shift = 1): out[q*obs] = init and
@@ -968,7 +940,8 @@ ScanPlan plan_scan(int64_t batch, int64_t n, cr_policy p, int64_t B, size_t esiz
     // the shifted forms, then init applied)
     plan.kind = ScanPlan::kChainOnly;
     plan.chain_n = shift ? plan.m - 1 : n;
-    if (plan.chain_n >= kParallelChainMin) {
+    if (plan.chain_n >= kParallelChainMin &&
+        (esize == 8 || plan.chain_n <= kMaxParallelChainF32)) {
       plan.parallel_chain = true;
       plan.chain = plan_chain(plan.chain_n);
       plan.chain_ws = off;
@@ -986,7 +959,10 @@ ScanPlan plan_scan(int64_t batch, int64_t n, cr_policy p, int64_t B, size_t esiz
   plan.logB = logB;
   plan.n_tiles = (n + kTile - 1) / kTile;
   plan.full_tiles = n / kTile;
-  if (p == CR_PAIRWISE) plan.mode = ScanPlan::kUpDown;
+  // one pass for binary64 iterated_pairwise, whose adds hide the waits for
+  // earlier tiles' pyramid nodes; binary32 (adds far cheaper) and pairwise
+  // (2 adds per element) would expose them: node pyramid first instead
+  if (p == CR_PAIRWISE || (!block && esize == 4)) plan.mode = ScanPlan::kUpDown;
   else if (!block) plan.mode = ScanPlan::kOnePass;
   else if (logB <= kLogTile) plan.mode = ScanPlan::kLocalFixup;
   else plan.mode = ScanPlan::kUpDown;
@@ -1030,7 +1006,7 @@ ScanPlan plan_scan(int64_t batch, int64_t n, cr_policy p, int64_t B, size_t esiz
     off += round256((size_t)plan.K * esize);
     plan.carries_ws = off;
     off += round256((size_t)plan.K * esize);
-    if (plan.K - 1 >= kParallelChainMin) {
+    if (plan.K - 1 >= kParallelChainMin && (esize == 8 || plan.K - 1 <= kMaxParallelChainF32)) {
       plan.parallel_chain = true;
       plan.chain = plan_chain(plan.K - 1);
       plan.chain_ws = off;
@@ -1101,8 +1077,7 @@ cudaError_t run_scan(const ScanPlan& plan, const T* x, T* out, int64_t es, int64
           src = copy;
         }
         if (!plan.parallel_chain) {
-          CR_LAUNCH(kKCarryChain, s, carry_chain_kernel<T><<<1, 32, 0, s>>>(src, dst, K));
-          if ((e = cudaGetLastError()) != cudaSuccess) return e;
+          if ((e = run_serial_chain<T>(src, dst, K, s)) != cudaSuccess) return e;
         } else if ((e = run_chain<T>(plan.chain, src, dst, ws + plan.chain_ws, s)) !=
                    cudaSuccess) {
           return e;
@@ -1162,8 +1137,7 @@ cudaError_t run_scan(const ScanPlan& plan, const T* x, T* out, int64_t es, int64
   auto chain = [&](const T* src) -> cudaError_t {
     if (plan.K < 2) return cudaSuccess;
     if (plan.parallel_chain) return run_chain<T>(plan.chain, src, carries, ws + plan.chain_ws, s);
-    CR_LAUNCH(kKCarryChain, s, carry_chain_kernel<T><<<1, 32, 0, s>>>(src, carries, plan.K - 1));
-    return cudaGetLastError();
+    return run_serial_chain<T>(src, carries, plan.K - 1, s);
   };
 
   if (plan.mode == ScanPlan::kLocalFixup) {
@@ -1218,14 +1192,14 @@ cudaError_t run_scan(const ScanPlan& plan, const T* x, T* out, int64_t es, int64
     return cudaGetLastError();
   }
 
-  // up/down: blocks spanning tiles (B > 2048)
+  // up/down: blocks spanning tiles (B > 2048), binary32 iterated_pairwise
   CR_LAUNCH(kKScanUp, s, {
     if (S == 8) scan_up_kernel<T, 8><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
     else if (S == 4) scan_up_kernel<T, 4><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
     else scan_up_kernel<T, 2><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
   });
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if ((e = chain(pyr + plan.pyr_off[plan.logB - kLogTile])) != cudaSuccess) return e;
+  if (block && (e = chain(pyr + plan.pyr_off[plan.logB - kLogTile])) != cudaSuccess) return e;
 #define CR_DOWN(SS, SH) \
   scan_down_kernel<T, SS, SH><<<grid, kScanThreads, 0, s>>>(x, out, pyr, carries, a, init)
   CR_LAUNCH(kKScanDown, s, {

@@ -164,3 +164,16 @@ def test_pairwise_full_size(scr):
     y = scr.inclusive_scan(xd, "pairwise").cpu().numpy()
     r = scr.reduce(xd, 1, -0.0).cpu().numpy()[0]
     assert bits(y[-1]) == bits(r)
+
+
+@pytest.mark.parametrize("policy,B", [("iterated_pairwise", 1), ("pairwise", 1),
+                                      ("left_fold", 1), ("block_dyadic", 16),
+                                      ("block_dyadic", 256), ("block_dyadic", 4096)])
+def test_scan_f32_large(scr, policy, B):
+    """binary32 at 2^26 + 5: iterated_pairwise through the up/down passes,
+    long carry chains through the streamed serial fold (the parallel
+    evaluation's error bound is too coarse for 24-bit chains this long)."""
+    x = W.family3((1 << 26) + 5).astype(np.float32)
+    got = scr.inclusive_scan(torch.from_numpy(x).to(DEV), policy, B).cpu().numpy()
+    want = oracle.scan(x, policy, B)
+    assert bits(got) == bits(want), first_diff(got, want)
