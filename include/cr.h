@@ -140,6 +140,25 @@ cr_status cr_inclusive_scan_batched(const void* x, void* out, int64_t batch, int
                                     int64_t B, cr_dtype dt, void* ws, size_t ws_bytes,
                                     void* stream);
 
+/* reduce<E>: the root of the named expression whose prefixes
+ * cr_inclusive_scan observes (P4229R0, Key Design Points: "reduce observes
+ * the root"):
+ *   CR_LEFT_FOLD                        ((x0 op x1) op x2) op ...
+ *   CR_PAIRWISE, CR_ITERATED_PAIRWISE   tree(x[0..n))  (= cr_reduce with L = 1
+ *                                       without init)
+ *   CR_BLOCK_DYADIC                     C_{K-1}: C_0 = T_0, C_k = C_{k-1} op T_k
+ *                                       over the block trees T_k, K = ceil(n/B)
+ * For the policies that are consistent (left_fold, iterated_pairwise,
+ * block_dyadic) it equals the inclusive scan's last element; pairwise's last
+ * element folds the maximal subtrees from the left instead.
+ *   x        device, n >= 1 contiguous elements (an empty expression has no
+ *            root: n == 0 is INVALID_ARG)
+ *   out_dev  device pointer to one element of dt
+ * Workspace from cr_reduce_policy_workspace_bytes (0 for bad arguments). */
+size_t cr_reduce_policy_workspace_bytes(int64_t n, cr_policy p, int64_t B, cr_dtype dt);
+cr_status cr_reduce_policy(const void* x, int64_t n, cr_policy p, int64_t B, cr_dtype dt,
+                           void* out_dev, void* ws, size_t ws_bytes, void* stream);
+
 /* Exclusive scan and the include_initial form (the inclusive/exclusive
  * duality of the page "Vertical scan redesign: research notes", section B.2,
  * with init placed as in P4016R0: combined once, as the left operand, after

@@ -48,6 +48,8 @@ SIGNATURES = {
     "cr_scan_batched_workspace_bytes": (_SZ, [_I64, _I64, _INT, _I64, _INT]),
     "cr_inclusive_scan_batched": (_INT, [_P, _P, _I64, _I64, _I64, _I64, _INT, _I64, _INT, _P,
                                          _SZ, _P]),
+    "cr_reduce_policy_workspace_bytes": (_SZ, [_I64, _INT, _I64, _INT]),
+    "cr_reduce_policy": (_INT, [_P, _I64, _INT, _I64, _INT, _P, _P, _SZ, _P]),
     "cr_scan_ex_workspace_bytes": (_SZ, [_I64, _INT, _I64, _INT, _INT]),
     "cr_scan_ex": (_INT, [_P, _P, _I64, _INT, _I64, _INT, _P, _INT, _P, _SZ, _P]),
     "cr_scan_ex_batched_workspace_bytes": (_SZ, [_I64, _I64, _INT, _I64, _INT, _INT]),
@@ -285,6 +287,29 @@ def inclusive_scan_batched(x: torch.Tensor, policy="left_fold", B: int = 1, dim:
     return _to_host(o, stream) if host else o
 
 
+def reduce_policy(x: torch.Tensor, policy="iterated_pairwise", B: int = 1,
+                  out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """reduce<E>(x): the root of the named expression whose prefixes
+    inclusive_scan observes (1-element tensor; x must not be empty)."""
+    if x.dim() != 1:
+        raise ValueError("reduce_policy expects a 1-D tensor")
+    xd, host = _on_device(x, stream)
+    xd = xd.contiguous()
+    dt = _dtype_code(xd)
+    n = xd.numel()
+    p = _policy(policy)
+    o = out if out is not None else torch.empty(1, dtype=xd.dtype, device=xd.device)
+    sp = _stream_ptr(stream)
+    nb = lib().cr_reduce_policy_workspace_bytes(n, p, int(B), dt)
+    if nb == 0:
+        raise ValueError("invalid reduce_policy arguments (n=%d, policy=%s, B=%d)" %
+                         (n, policy, B))
+    ws = _WS.get(xd.device, stream, nb)
+    _check(lib().cr_reduce_policy(xd.data_ptr(), n, p, int(B), dt, o.data_ptr(), ws.data_ptr(),
+                                  ws.numel(), sp), "cr_reduce_policy")
+    return _to_host(o, stream) if host else o
+
+
 def _scan_ex(x, policy, B, init, mode, out, stream, what):
     if x.dim() != 1:
         raise ValueError("%s expects a 1-D tensor" % what)
@@ -435,6 +460,7 @@ def measure_int_add_rate(device="cuda", stream=None) -> float:
     return rate.value
 
 
-__all__ = ["reduce", "reduce_batched", "inclusive_scan", "inclusive_scan_batched",
+__all__ = ["reduce", "reduce_batched", "reduce_policy", "inclusive_scan",
+           "inclusive_scan_batched",
            "exclusive_scan", "scan_include_initial", "exclusive_scan_batched",
            "scan_include_initial_batched", "MODES", "sync_status", "lib", "workspace", "launch_count", "profile_enable", "profile_collect", "measure_add_peak", "add_pairs_int", "measure_int_add_rate", "CrError", "POLICIES", "SIGNATURES"]

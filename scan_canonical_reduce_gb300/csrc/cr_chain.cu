@@ -816,11 +816,15 @@ __device__ __forceinline__ int64_t walk_fast(const Hot& h, int64_t A, int64_t* m
 // records to compact form while lane 0 runs the current 32 from shared
 // memory; batches with no start or uncertain step run an unrolled loop of
 // the integer path alone.
+// dst == nullptr: the chain's outputs are not wanted (a reduction); with
+// final_out, lane 0 also writes C_{K-1}, taken from the last segment's map
+// (e_last: binade of the last step) or from the last real add.
 template <class T>
 __global__ void __launch_bounds__(32) chain_walk_kernel(const T* src, T* dst, const SegRec* segs,
                                                         const int64_t* nseg_total,
                                                         int64_t seg_cap, int64_t* m_in,
-                                                        int* fail) {
+                                                        int* fail, const uint32_t* meta,
+                                                        int64_t K, T* final_out) {
   __shared__ Hot hot[2][32];
   __shared__ SegRec cold[2][32];
   __shared__ int cold_batch[2];
@@ -887,7 +891,7 @@ __global__ void __launch_bounds__(32) chain_walk_kernel(const T* src, T* dst, co
             }
             C = add_rn(C, (T)r.tval);
           }
-          dst[r.start] = C;
+          if (dst != nullptr) dst[r.start] = C;
           cval = true;
           int64_t M1 = A;
           if (m_certain(m)) {
@@ -907,6 +911,8 @@ __global__ void __launch_bounds__(32) chain_walk_kernel(const T* src, T* dst, co
     __syncwarp();
   }
   if (lane == 0 && bad) atomicExch(fail, 1);
+  if (lane == 0 && final_out != nullptr && !bad)  // A = M after the last segment's map
+    *final_out = cval ? C : m_to_value<T>(A, m_e(meta[K - 1]));
 }
 
 // Every rise of the walk, checked in parallel: A = (previous record's map
@@ -988,7 +994,8 @@ __global__ void __launch_bounds__(kCT) chain_fill_kernel(const int64_t* qv, cons
         } else {
           M = (uint64_t)m_in[seg];
           // the walk wrote start and uncertain steps; keep them
-          out[i] = type == kUp ? m_to_value_normal<T>((int64_t)M, m_e(m)) : dst[k0 + i];
+          if (dst != nullptr)
+            out[i] = type == kUp ? m_to_value_normal<T>((int64_t)M, m_e(m)) : dst[k0 + i];
         }
         continue;
       }
@@ -1007,7 +1014,7 @@ __global__ void __launch_bounds__(kCT) chain_fill_kernel(const int64_t* qv, cons
       out[i] = m_to_value_normal<T>((int64_t)M, m_e(m));
     }
   }
-  store_run(dst + k0, n, out);
+  if (dst != nullptr) store_run(dst + k0, n, out);  // else: validation only
   if (!ok) atomicExch(fail, 1);
 }
 
@@ -1021,7 +1028,7 @@ __global__ void __launch_bounds__(kCT) chain_fill_kernel(const int64_t* qv, cons
 // so dst may equal src.
 template <class T>
 __global__ void __launch_bounds__(32) chain_serial_kernel(const T* src, T* dst, int64_t K,
-                                                          const int* only_if) {
+                                                          const int* only_if, T* final_out) {
   constexpr int kBuf = 1024, kPer = kBuf / 32;
   __shared__ __align__(16) T buf[kBuf];
   const int lane = threadIdx.x;
@@ -1070,13 +1077,16 @@ __global__ void __launch_bounds__(32) chain_serial_kernel(const T* src, T* dst, 
       }
     }
     __syncwarp();
+    if (dst != nullptr) {
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int64_t k = base + lane + 32 * i;
-      if (k < K) dst[k] = buf[lane + 32 * i];
+      for (int i = 0; i < kPer; ++i) {
+        const int64_t k = base + lane + 32 * i;
+        if (k < K) dst[k] = buf[lane + 32 * i];
+      }
     }
     __syncwarp();
   }
+  if (lane == 0 && final_out != nullptr) *final_out = c;
 }
 
 size_t r256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -1109,7 +1119,8 @@ ChainPlan plan_chain(int64_t K) {
 }
 
 template <class T>
-cudaError_t run_chain(const ChainPlan& p, const T* src, T* dst, char* ws, cudaStream_t s) {
+cudaError_t run_chain(const ChainPlan& p, const T* src, T* dst, char* ws, cudaStream_t s,
+                      T* final_out) {
   if (p.K <= 0) return cudaSuccess;
   double* tsum = reinterpret_cast<double*>(ws + p.tsum_off);
   double* toff = reinterpret_cast<double*>(ws + p.toff_off);
@@ -1153,7 +1164,8 @@ cudaError_t run_chain(const ChainPlan& p, const T* src, T* dst, char* ws, cudaSt
             chain_link_kernel<<<1, 1024, 0, s>>>(nseg, segbase, p.ntiles, segs, p.seg_cap, lead,
                                                  lead_steps, entry, entry_rec));
   CR_LAUNCH(kKChainWalk, s,
-            chain_walk_kernel<T><<<1, 32, 0, s>>>(src, dst, segs, total, p.seg_cap, m_in, fail));
+            chain_walk_kernel<T><<<1, 32, 0, s>>>(src, dst, segs, total, p.seg_cap, m_in, fail,
+                                                  meta, p.K, final_out));
   if ((p.seg_cap + 255) / 256 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   CR_LAUNCH(kKChainVerify, s,
             chain_verify_kernel<T><<<(unsigned)((p.seg_cap + 255) / 256), 256, 0, s>>>(
@@ -1161,22 +1173,26 @@ cudaError_t run_chain(const ChainPlan& p, const T* src, T* dst, char* ws, cudaSt
   CR_LAUNCH(kKChainFill, s,
             chain_fill_kernel<T><<<g, kCT, 0, s>>>(qv, meta, p.K, segbase, thr_in, entry,
                                                    entry_rec, p.seg_cap, m_in, dst, fail));
-  CR_LAUNCH(kKChainFallback, s, chain_serial_kernel<T><<<1, 32, 0, s>>>(src, dst, p.K, fail));
+  CR_LAUNCH(kKChainFallback, s,
+            chain_serial_kernel<T><<<1, 32, 0, s>>>(src, dst, p.K, fail, final_out));
   return cudaGetLastError();
 }
 
 template <class T>
-cudaError_t run_serial_chain(const T* src, T* dst, int64_t K, cudaStream_t s) {
+cudaError_t run_serial_chain(const T* src, T* dst, int64_t K, cudaStream_t s, T* final_out) {
   if (K <= 0) return cudaSuccess;
-  CR_LAUNCH(kKCarryChain, s, chain_serial_kernel<T><<<1, 32, 0, s>>>(src, dst, K, nullptr));
+  CR_LAUNCH(kKCarryChain, s,
+            chain_serial_kernel<T><<<1, 32, 0, s>>>(src, dst, K, nullptr, final_out));
   return cudaGetLastError();
 }
 
-template cudaError_t run_serial_chain<double>(const double*, double*, int64_t, cudaStream_t);
-template cudaError_t run_serial_chain<float>(const float*, float*, int64_t, cudaStream_t);
+template cudaError_t run_serial_chain<double>(const double*, double*, int64_t, cudaStream_t,
+                                              double*);
+template cudaError_t run_serial_chain<float>(const float*, float*, int64_t, cudaStream_t,
+                                             float*);
 template cudaError_t run_chain<double>(const ChainPlan&, const double*, double*, char*,
-                                       cudaStream_t);
+                                       cudaStream_t, double*);
 template cudaError_t run_chain<float>(const ChainPlan&, const float*, float*, char*,
-                                      cudaStream_t);
+                                      cudaStream_t, float*);
 
 }  // namespace cr

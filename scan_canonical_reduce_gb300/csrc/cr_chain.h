@@ -19,15 +19,20 @@ struct ChainPlan {
 ChainPlan plan_chain(int64_t K);
 
 // dst[k] = C_k for k < K. src and dst must not overlap (the fallback re-reads
-// src). ws: plan.bytes of 256-byte aligned device memory.
+// src). ws: plan.bytes of 256-byte aligned device memory. With final_out
+// (device, one element) C_{K-1} is also written there; dst may then be
+// nullptr (a reduction: every step is still validated, no output written).
 template <class T>
-cudaError_t run_chain(const ChainPlan& plan, const T* src, T* dst, char* ws, cudaStream_t s);
+cudaError_t run_chain(const ChainPlan& plan, const T* src, T* dst, char* ws, cudaStream_t s,
+                      T* final_out = nullptr);
 
 // The same fold evaluated one step after the other by one warp (steps
 // streamed through shared memory): for short chains, and for binary32 chains
-// too long for the parallel evaluation's error bound. dst may equal src.
+// too long for the parallel evaluation's error bound. dst may equal src or
+// be nullptr when final_out is given.
 template <class T>
-cudaError_t run_serial_chain(const T* src, T* dst, int64_t K, cudaStream_t s);
+cudaError_t run_serial_chain(const T* src, T* dst, int64_t K, cudaStream_t s,
+                             T* final_out = nullptr);
 
 // Longest binary32 chain the parallel evaluation is used for (K ulp must stay
 // small against the chain's values for its binade tests to be decisive).

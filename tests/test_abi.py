@@ -128,3 +128,17 @@ def test_binding_fails_loudly_without_library(tmp_path, scr):
     mod = importlib.util.module_from_spec(spec)
     with pytest.raises(ImportError):
         spec.loader.exec_module(mod)
+
+
+def test_reduce_policy_host_side_argument_errors(scr):
+    """reduce<E> of an empty input has no root; bad policy or block size."""
+    L = scr.lib()
+    fake = ctypes.c_void_p(0x10000)
+    assert L.cr_reduce_policy_workspace_bytes(0, 2, 1, 2) == 0
+    assert L.cr_reduce_policy_workspace_bytes(10, 3, 6, 2) == 0
+    for p, B in ((0, 1), (1, 1), (2, 1), (3, 16), (3, 1 << 20)):
+        assert L.cr_reduce_policy_workspace_bytes(1 << 20, p, B, 2) >= 256
+    assert L.cr_reduce_policy(fake, 0, 2, 1, 2, fake, fake, 1 << 20, None) == 1
+    assert L.cr_reduce_policy(fake, 10, 9, 1, 2, fake, fake, 1 << 20, None) == 1
+    assert L.cr_reduce_policy(fake, 10, 2, 1, 2, None, fake, 1 << 20, None) == 1
+    assert L.cr_reduce_policy(fake, 1 << 20, 3, 16, 2, fake, fake, 256, None) == 3
