@@ -41,7 +41,7 @@ namespace cr {
 constexpr int kThreads = 256;
 constexpr int kLV = 10;  // stack levels: a run of up to 512 operands
 
-template <class T, int U>
+template <class T, int U, bool kContig>
 __global__ void __launch_bounds__(kThreads)
 lane_pass_kernel(const T* __restrict__ in_base, int64_t in_seg, int64_t in_row,
                  int64_t in_lane, T* __restrict__ next, T* __restrict__ acc,
@@ -88,6 +88,21 @@ lane_pass_kernel(const T* __restrict__ in_base, int64_t in_seg, int64_t in_row,
   if (cnt > 0) {
     const T* p = in_base + b * in_seg + run0 * in_row + j * in_lane;
     int64_t k = 0;
+    constexpr int VW = 16 / sizeof(T);  // elements per 16-byte vector
+    if (kContig && U % VW == 0 && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
+      // one lane (L = 1 and the lane-result passes): the run is contiguous
+      for (; k + U <= cnt; k += U) {
+        T v[U];
+        const uint4* q = reinterpret_cast<const uint4*>(p + k);
+#pragma unroll
+        for (int u = 0; u < U / VW; ++u) {
+          const uint4 d = __ldg(q + u);
+#pragma unroll
+          for (int e = 0; e < VW; ++e) v[u * VW + e] = reinterpret_cast<const T*>(&d)[e];
+        }
+        st.push(perfect_tree<T, U>(v), LOGU);
+      }
+    }
     for (; k + U <= cnt; k += U) {
       T v[U];
 #pragma unroll
@@ -409,17 +424,21 @@ cudaError_t run_reduce(const ReducePlan& plan, const T* x, T* out, T init, char*
     T* acc = reinterpret_cast<T*>(ws + pp.acc_off);
     int* has = reinterpret_cast<int*>(ws + pp.has_off);
     if (pp.grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    // runs shorter than 16 rows use smaller register blocks
-    if (pp.a.P >= 16)
-      CR_LAUNCH(kKLanePass, s,
-                lane_pass_kernel<T, 16><<<(unsigned)pp.grid, kThreads, 0, s>>>(
-                    in_base, pp.in.seg, pp.in.row, pp.in.lane, next, acc, has, out, init,
-                    pp.a));
-    else
-      CR_LAUNCH(kKLanePass, s,
-                lane_pass_kernel<T, 4><<<(unsigned)pp.grid, kThreads, 0, s>>>(
-                    in_base, pp.in.seg, pp.in.row, pp.in.lane, next, acc, has, out, init,
-                    pp.a));
+    // runs shorter than 16 rows use smaller register blocks; one-lane passes
+    // (contiguous runs, 16-byte aligned) load with vector accesses
+    const bool contig = pp.in.row == 1 && (reinterpret_cast<uintptr_t>(in_base) & 15) == 0 &&
+                        (pp.in.seg * (int64_t)sizeof(T)) % 16 == 0;
+#define CR_LANE(UU, CC)                                                                   \
+  CR_LAUNCH(kKLanePass, s,                                                                \
+            (lane_pass_kernel<T, UU, CC><<<(unsigned)pp.grid, kThreads, 0, s>>>(          \
+                in_base, pp.in.seg, pp.in.row, pp.in.lane, next, acc, has, out, init, pp.a)))
+    if (pp.a.P >= 16) {
+      if (contig) CR_LANE(16, true);
+      else CR_LANE(16, false);
+    } else {
+      CR_LANE(4, false);
+    }
+#undef CR_LANE
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

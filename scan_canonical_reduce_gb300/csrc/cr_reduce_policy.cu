@@ -6,10 +6,10 @@
 //   block_dyadic<B>      C_{K-1}, C_0 = T_0, C_k = C_{k-1} op T_k over the
 //                        block trees T_k = tree(x[kB .. kB+B))
 // The tree is the canonical reduction with one lane and init -0.0 (the exact
-// identity of IEEE addition, so op(-0.0, R) = R); the block trees are one
-// batched reduction over the full blocks plus one for a ragged last block;
-// the folds are the carry chain in its reduce-only form (every step still
-// validated, no prefix written).
+// identity of IEEE addition, so op(-0.0, R) = R); the block trees come from
+// the block_dyadic scan's up pass (without its outputs) plus one reduction
+// for a ragged last block; the folds are the carry chain in its reduce-only
+// form (every step still validated, no prefix written).
 #include <cstdint>
 #include <cstring>
 
@@ -27,10 +27,11 @@ constexpr int64_t kParallelChainMinR = 1024;  // shorter folds: the serial chain
 struct PolicyReducePlan {
   int kind = 0;  // 0 tree, 1 fold of x, 2 block trees then their fold
   ReducePlan tree, tail;
+  ScanPlan blocks;  // kind 2: the up pass that yields the block trees
   int64_t n = 0, B = 0, K = 0, Kf = 0;
   bool parallel = false;
   ChainPlan chain;
-  size_t tree_ws = 0, tail_ws = 0, totals_ws = 0, chain_ws = 0, ws_bytes = 0;
+  size_t tree_ws = 0, tail_ws = 0, blocks_ws = 0, chain_ws = 0, ws_bytes = 0;
 };
 
 size_t r256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -60,16 +61,14 @@ PolicyReducePlan plan_policy_reduce(int64_t n, cr_policy p, int64_t B, size_t es
     plan.B = B;
     plan.K = (n + B - 1) / B;
     plan.Kf = n / B;
-    plan.tree = plan_reduce(plan.Kf, B, 1, 1, B, esize);
-    plan.tree_ws = off;
-    off += r256(plan.tree.ws_bytes);
+    plan.blocks = plan_scan(1, n, CR_BLOCK_DYADIC, B, esize);
+    plan.blocks_ws = off;
+    off += r256(plan.blocks.ws_bytes);
     if (plan.K > plan.Kf) {
       plan.tail = plan_reduce(1, n - plan.Kf * B, 1, 1, n - plan.Kf * B, esize);
       plan.tail_ws = off;
       off += r256(plan.tail.ws_bytes);
     }
-    plan.totals_ws = off;
-    off += r256((size_t)plan.K * esize);
     chain_for(plan.K);
   }
   plan.ws_bytes = off;
@@ -92,10 +91,9 @@ cudaError_t run_policy_reduce(const PolicyReducePlan& plan, const T* x, T* out, 
     case 1:
       return fold(x, plan.n);
     default: {
-      T* totals = reinterpret_cast<T*>(ws + plan.totals_ws);
-      if (plan.Kf > 0 &&
-          (e = run_reduce<T>(plan.tree, x, totals, minus_zero, ws + plan.tree_ws, s)) !=
-              cudaSuccess)
+      T* totals = nullptr;
+      if ((e = run_block_totals<T>(plan.blocks, x, ws + plan.blocks_ws, s, &totals)) !=
+          cudaSuccess)
         return e;
       if (plan.K > plan.Kf &&
           (e = run_reduce<T>(plan.tail, x + plan.Kf * plan.B, totals + plan.Kf, minus_zero,

@@ -1217,6 +1217,51 @@ cudaError_t run_scan(const ScanPlan& plan, const T* x, T* out, int64_t es, int64
   return cudaGetLastError();
 }
 
+template <class T>
+cudaError_t run_block_totals(const ScanPlan& plan, const T* x, char* ws, cudaStream_t s,
+                             T** totals_out) {
+  ScanArgs a{};
+  a.n = plan.n;
+  a.full_tiles = plan.full_tiles;
+  a.logB = plan.logB;
+  // blocks inside a tile need no node pyramid across tiles
+  a.pyr_levels = plan.mode == ScanPlan::kLocalFixup ? 0 : plan.pyr_levels;
+  a.carry = 0;
+  a.totals_level = plan.totals_level;
+  for (int l = 0; l < kMaxLevels; ++l) {
+    a.pyr_off[l] = plan.pyr_off[l];
+    a.cnt_off[l] = plan.cnt_off[l];
+  }
+  T* pyr = reinterpret_cast<T*>(ws + plan.pyr_ws);
+  int* counters = reinterpret_cast<int*>(ws + plan.cnt_ws);
+  T* totals = reinterpret_cast<T*>(ws + plan.totals_ws);
+  cudaError_t e;
+  if (plan.zero_bytes > 0 && a.pyr_levels > 0 &&
+      (e = cudaMemsetAsync(ws + plan.zero_ws, 0, plan.zero_bytes, s)) != cudaSuccess)
+    return e;
+  if (plan.n_tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const unsigned grid = (unsigned)plan.n_tiles;
+  const int S = (int)(plan.B < kE ? plan.B : kE);
+  CR_LAUNCH(kKScanUp, s, {
+    if (S == 8) scan_up_kernel<T, 8><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
+    else if (S == 4) scan_up_kernel<T, 4><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
+    else scan_up_kernel<T, 2><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
+  });
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const int64_t Kf = plan.n / plan.B;
+  if (plan.logB > kLogTile && Kf > 0) {  // the pyramid level of whole blocks
+    e = cudaMemcpyAsync(totals, pyr + plan.pyr_off[plan.logB - kLogTile], (size_t)Kf * sizeof(T),
+                        cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return e;
+  }
+  *totals_out = totals;
+  return cudaSuccess;
+}
+
+template cudaError_t run_block_totals<double>(const ScanPlan&, const double*, char*,
+                                              cudaStream_t, double**);
+template cudaError_t run_block_totals<float>(const ScanPlan&, const float*, char*, cudaStream_t,
+                                             float**);
 template cudaError_t run_scan<double>(const ScanPlan&, const double*, double*, int64_t,
                                       int64_t, int64_t, int64_t, double, char*, cudaStream_t);
 template cudaError_t run_scan<float>(const ScanPlan&, const float*, float*, int64_t, int64_t,

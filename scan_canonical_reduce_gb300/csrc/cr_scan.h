@@ -84,4 +84,13 @@ cudaError_t run_scan(const ScanPlan& plan, const T* x, T* out, int64_t elem_stri
                      int64_t batch_stride, int64_t out_elem_stride, int64_t out_batch_stride,
                      T init, char* ws, cudaStream_t s);
 
+// The trees T_k = tree(x[kB .. (k+1)B)) of the n / B complete blocks, for
+// reduce<block_dyadic>: the scan's up pass without its outputs. plan =
+// plan_scan(1, n, CR_BLOCK_DYADIC, B, sizeof(T)) with n >= B > 1; the values
+// land in the plan's totals buffer (K = ceil(n / B) slots, the last one left
+// for a ragged block), whose address goes to *totals_out.
+template <class T>
+cudaError_t run_block_totals(const ScanPlan& plan, const T* x, char* ws, cudaStream_t s,
+                             T** totals_out);
+
 }  // namespace cr
