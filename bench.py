@@ -402,7 +402,7 @@ NCU_TRAFFIC = {
     # 218.27 MB written at n = 2^25, x 8
     "scan_onepass_kernel": (268.94e6 + 218.27e6) * 8,
     # profiles/lane_pass_kernel_reduce_f64_L16_n2e25.md: level-0 pass, x 8
-    "lane_pass_kernel": (268.48e6 + 4.03e6) * 8,
+    "lane_pass_kernel": (268.48e6 + 3.10e6) * 8,
 }
 
 
