@@ -201,6 +201,25 @@ cr_status cr_scan_ex_batched(const void* x, void* out, int64_t batch, int64_t n,
                              int64_t B, cr_scan_mode mode, const void* init_host, cr_dtype dt,
                              void* ws, size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------------- host buffers
+ * The same operations with x and out in HOST memory (page-locked memory
+ * gives the full host link bandwidth; pageable memory works, slower). The
+ * call copies in, computes and copies out, and returns when out is
+ * written. For the tiled 1-D scans the copies and the passes are pipelined
+ * in chunks over three streams (copy in, compute on `stream`, copy out),
+ * so that the transfers overlap the kernels. dev_buf: caller-owned device
+ * memory of at least the bytes the query returns (256-byte aligned); it
+ * holds device copies of x and out and the workspace. Errors as for the
+ * device forms. */
+size_t cr_inclusive_scan_host_workspace_bytes(int64_t n, cr_policy p, int64_t B, cr_dtype dt);
+cr_status cr_inclusive_scan_host(const void* x_host, void* out_host, int64_t n, cr_policy p,
+                                 int64_t B, cr_dtype dt, void* dev_buf, size_t dev_bytes,
+                                 void* stream);
+size_t cr_reduce_host_workspace_bytes(int64_t n, int32_t L, cr_dtype dt);
+cr_status cr_reduce_host(const void* x_host, int64_t n, int32_t L, const void* init_host,
+                         cr_dtype dt, void* out_host, void* dev_buf, size_t dev_bytes,
+                         void* stream);
+
 /* Allocation-free canonical reduction. The paper has no counterpart: this
  * serves callers that cannot allocate device memory, such as a plugin whose
  * host framework owns all device memory through its own pool, or a

@@ -55,6 +55,10 @@ SIGNATURES = {
     "cr_scan_ex_batched_workspace_bytes": (_SZ, [_I64, _I64, _INT, _I64, _INT, _INT]),
     "cr_scan_ex_batched": (_INT, [_P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _INT, _I64, _INT,
                                   _P, _INT, _P, _SZ, _P]),
+    "cr_inclusive_scan_host_workspace_bytes": (_SZ, [_I64, _INT, _I64, _INT]),
+    "cr_inclusive_scan_host": (_INT, [_P, _P, _I64, _INT, _I64, _INT, _P, _SZ, _P]),
+    "cr_reduce_host_workspace_bytes": (_SZ, [_I64, _I32, _INT]),
+    "cr_reduce_host": (_INT, [_P, _I64, _I32, _P, _INT, _P, _P, _SZ, _P]),
     "cr_sync_status": (_INT, [_P, _P]),
     "cr_status_string": (ctypes.c_char_p, [_INT]),
     "cr_version": (_INT, []),
@@ -191,6 +195,21 @@ def reduce(x: torch.Tensor, L: int, init=0.0, out: torch.Tensor | None = None,
     gives a host tensor back, through pinned-memory copies)."""
     if x.dim() != 1:
         raise ValueError("reduce expects a 1-D tensor; use reduce_batched for 2-D")
+    if not x.is_cuda:  # host buffers: one C call copies in, reduces, copies out
+        xc = x.contiguous()
+        dt = _dtype_code(xc)
+        n = xc.numel()
+        o = out if out is not None else torch.empty(1, dtype=xc.dtype, pin_memory=True)
+        nb = lib().cr_reduce_host_workspace_bytes(n, int(L), dt)
+        if nb == 0:
+            raise ValueError("invalid reduce arguments (n=%d, L=%d)" % (n, L))
+        dev = torch.device("cuda", torch.cuda.current_device())
+        ws = _WS.get(dev, stream, nb)
+        ini = _init_buffer(init, dt)
+        _check(lib().cr_reduce_host(xc.data_ptr() if n else None, n, int(L), ctypes.byref(ini),
+                                    dt, o.data_ptr(), ws.data_ptr(), ws.numel(),
+                                    _stream_ptr(stream)), "cr_reduce_host")
+        return o
     xd, host = _on_device(x.contiguous() if x.is_cuda else x, stream)
     xd = xd.contiguous()
     dt = _dtype_code(xd)
@@ -243,6 +262,23 @@ def inclusive_scan(x: torch.Tensor, policy="iterated_pairwise", B: int = 1,
     ``out`` may be ``x`` itself (in place)."""
     if x.dim() != 1:
         raise ValueError("inclusive_scan expects a 1-D tensor")
+    if not x.is_cuda:  # host buffers: one C call, transfers pipelined with the passes
+        xc = x.contiguous()
+        dt = _dtype_code(xc)
+        n = xc.numel()
+        o = out if out is not None else torch.empty(n, dtype=xc.dtype, pin_memory=True)
+        if o.is_cuda or o.numel() != n or o.dtype != xc.dtype or not o.is_contiguous():
+            raise ValueError("out must be a contiguous host tensor like x")
+        p = _policy(policy)
+        nb = lib().cr_inclusive_scan_host_workspace_bytes(n, p, int(B), dt)
+        if nb == 0:
+            raise ValueError("invalid scan arguments (policy=%s, B=%d)" % (policy, B))
+        dev = torch.device("cuda", torch.cuda.current_device())
+        ws = _WS.get(dev, stream, nb)
+        _check(lib().cr_inclusive_scan_host(xc.data_ptr(), o.data_ptr(), n, p, int(B), dt,
+                                            ws.data_ptr(), ws.numel(), _stream_ptr(stream)),
+               "cr_inclusive_scan_host")
+        return o
     xd, host = _on_device(x, stream)
     xd = xd.contiguous()
     dt = _dtype_code(xd)

@@ -192,6 +192,71 @@ cr_status cr_scan_ex_batched(const void* x, void* out, int64_t batch, int64_t n,
                    out_batch_stride, p, B, mode, init_host, dt, ws, ws_bytes, stream, false);
 }
 
+static size_t r256(size_t v) { return (v + 255) & ~size_t(255); }
+
+size_t cr_inclusive_scan_host_workspace_bytes(int64_t n, cr_policy p, int64_t B, cr_dtype dt) {
+  const size_t sz = esize(dt);
+  if (sz == 0 || n < 0 || !cr::scan_args_ok(p, B)) return 0;
+  return 2 * r256((size_t)n * sz) + cr::plan_scan(1, n, p, B, sz).ws_bytes;
+}
+
+cr_status cr_inclusive_scan_host(const void* x_host, void* out_host, int64_t n, cr_policy p,
+                                 int64_t B, cr_dtype dt, void* dev_buf, size_t dev_bytes,
+                                 void* stream) {
+  const size_t sz = esize(dt);
+  if (sz == 0 || n < 0 || !cr::scan_args_ok(p, B)) return CR_ERR_INVALID_ARG;
+  if (n > 0 && (x_host == nullptr || out_host == nullptr)) return CR_ERR_INVALID_ARG;
+  const cr::ScanPlan plan = cr::plan_scan(1, n, p, B, sz);
+  const size_t arr = r256((size_t)n * sz);
+  const cr_status ws_ok = check_ws(dev_buf, dev_bytes, 2 * arr + plan.ws_bytes);
+  if (ws_ok != CR_OK) return ws_ok;
+  if (!plan.supported) return CR_ERR_UNSUPPORTED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* base = static_cast<char*>(dev_buf);
+  char* ws = base + 2 * arr;
+  if (clear_status(ws, s) != cudaSuccess) return CR_ERR_CUDA;
+  cudaError_t e;
+  if (dt == CR_F64)
+    e = cr::run_scan_host<double>(plan, static_cast<const double*>(x_host),
+                                  static_cast<double*>(out_host), reinterpret_cast<double*>(base),
+                                  reinterpret_cast<double*>(base + arr), ws, s);
+  else
+    e = cr::run_scan_host<float>(plan, static_cast<const float*>(x_host),
+                                 static_cast<float*>(out_host), reinterpret_cast<float*>(base),
+                                 reinterpret_cast<float*>(base + arr), ws, s);
+  return from_cuda(e);
+}
+
+size_t cr_reduce_host_workspace_bytes(int64_t n, int32_t L, cr_dtype dt) {
+  const size_t sz = esize(dt);
+  if (sz == 0 || n < 0 || L < 1) return 0;
+  return r256((size_t)n * sz) + 256 + cr::plan_reduce(1, n, L, 1, n, sz).ws_bytes;
+}
+
+cr_status cr_reduce_host(const void* x_host, int64_t n, int32_t L, const void* init_host,
+                         cr_dtype dt, void* out_host, void* dev_buf, size_t dev_bytes,
+                         void* stream) {
+  const size_t sz = esize(dt);
+  if (sz == 0 || n < 0 || L < 1 || init_host == nullptr || out_host == nullptr)
+    return CR_ERR_INVALID_ARG;
+  if (n > 0 && x_host == nullptr) return CR_ERR_INVALID_ARG;
+  const size_t arr = r256((size_t)n * sz);
+  const size_t need = arr + 256 + cr::plan_reduce(1, n, L, 1, n, sz).ws_bytes;
+  const cr_status ws_ok = check_ws(dev_buf, dev_bytes, need);
+  if (ws_ok != CR_OK) return ws_ok;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* base = static_cast<char*>(dev_buf);
+  if (n > 0 && cudaMemcpyAsync(base, x_host, (size_t)n * sz, cudaMemcpyHostToDevice, s) !=
+                   cudaSuccess)
+    return CR_ERR_CUDA;
+  const cr_status st = reduce_impl(n > 0 ? base : nullptr, base + arr, 1, n, 1, n, L, init_host,
+                                   dt, base + arr + 256, dev_bytes - arr - 256, stream);
+  if (st != CR_OK) return st;
+  if (cudaMemcpyAsync(out_host, base + arr, sz, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return CR_ERR_CUDA;
+  return cudaStreamSynchronize(s) == cudaSuccess ? CR_OK : CR_ERR_CUDA;
+}
+
 cr_status cr_sync_status(void* ws, void* stream) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return CR_ERR_CUDA;

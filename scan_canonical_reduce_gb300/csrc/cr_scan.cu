@@ -31,6 +31,7 @@
 // shift-reduce stack.
 #include <algorithm>
 #include <atomic>
+#include <mutex>
 #include <vector>
 
 #include "cr_device.cuh"
@@ -265,7 +266,7 @@ scan_up_kernel(const T* __restrict__ x, T* __restrict__ pyr, int* __restrict__ c
   constexpr int NS = kE / S;
   constexpr int LS = Log2<S>::value;
   const int t = threadIdx.x;
-  const int64_t b = blockIdx.x;
+  const int64_t b = a.tile_base + blockIdx.x;
   const int64_t i0 = b * kTile + (int64_t)t * kE;
   const int64_t cnt = imax(0, imin(kE, a.n - i0));
   const int full_threads = (int)imin(kScanThreads, (a.n - b * kTile) / kE);
@@ -329,7 +330,7 @@ scan_down_kernel(const T* x, T* out, const T* __restrict__ pyr, const T* __restr
   __shared__ T s_last[kScanThreads / 32];
   constexpr int NS = kE / S;
   const int t = threadIdx.x;
-  const int64_t b = blockIdx.x;
+  const int64_t b = a.tile_base + blockIdx.x;
   const int64_t i0 = b * kTile + (int64_t)t * kE;
   const int64_t cnt = imax(0, imin(kE, a.n - i0));
   const int full_threads = (int)imin(kScanThreads, (a.n - b * kTile) / kE);
@@ -555,7 +556,7 @@ scan_pairwise_kernel(const T* x, T* out, const T* __restrict__ pyr, ScanArgs a, 
   __shared__ T s_base[kScanThreads / 32 + 1];  // E_{32 w}, w = 0..8 (E_256 = Y_{b+1})
   const unsigned full = 0xffffffffu;
   const int t = threadIdx.x, lane = t & 31, wp = t >> 5;
-  const int64_t b = blockIdx.x;
+  const int64_t b = a.tile_base + blockIdx.x;
   const int64_t i0 = b * kTile + (int64_t)t * kE;
   const int64_t cnt = imax(0, imin(kE, a.n - i0));
   const int full_threads = (int)imin(kScanThreads, (a.n - b * kTile) / kE);
@@ -652,7 +653,7 @@ scan_local_kernel(const T* x, T* out, T* __restrict__ totals, ScanArgs a) {
   constexpr int NS = kE / S;
   constexpr int LS = Log2<S>::value;
   const int t = threadIdx.x;
-  const int64_t b = blockIdx.x;
+  const int64_t b = a.tile_base + blockIdx.x;
   const int64_t i0 = b * kTile + (int64_t)t * kE;
   const int64_t cnt = imax(0, imin(kE, a.n - i0));
   const int full_threads = (int)imin(kScanThreads, (a.n - b * kTile) / kE);
@@ -683,10 +684,11 @@ scan_local_kernel(const T* x, T* out, T* __restrict__ totals, ScanArgs a) {
 }
 
 // Pass 2: out[i] = C_{k-1} op P(i) for every element of blocks k >= 1.
+// Elements [start, end) with start >= B (block 0 has no carry).
 template <class T>
 __global__ void __launch_bounds__(256)
-carry_fixup_kernel(T* out, const T* __restrict__ carries, int64_t n, int logB) {
-  const int64_t i0 = (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * kE) + ((int64_t)1 << logB);
+carry_fixup_kernel(T* out, const T* __restrict__ carries, int64_t start, int64_t n, int logB) {
+  const int64_t i0 = (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * kE) + start;
   if (i0 >= n) return;
   if (i0 + kE <= n && logB >= kLogE) {  // one block for all 8 elements
     const T c = ldg(carries + (i0 >> logB) - 1);
@@ -1019,6 +1021,194 @@ ScanPlan plan_scan(int64_t batch, int64_t n, cr_policy p, int64_t B, size_t esiz
   return plan;
 }
 
+// Streams and events of the host-buffer pipeline, one set per device,
+// created on first use and kept.
+struct HostPipe {
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr;
+  std::vector<cudaEvent_t> ev_in, ev_out;
+  cudaError_t ensure(int chunks) {
+    cudaError_t e;
+    if (in == nullptr) {
+      if ((e = cudaStreamCreateWithFlags(&in, cudaStreamNonBlocking)) != cudaSuccess) return e;
+      if ((e = cudaStreamCreateWithFlags(&out, cudaStreamNonBlocking)) != cudaSuccess) return e;
+      if ((e = cudaEventCreateWithFlags(&start, cudaEventDisableTiming)) != cudaSuccess) return e;
+    }
+    while ((int)ev_in.size() < chunks) {
+      cudaEvent_t a, b;
+      if ((e = cudaEventCreateWithFlags(&a, cudaEventDisableTiming)) != cudaSuccess) return e;
+      if ((e = cudaEventCreateWithFlags(&b, cudaEventDisableTiming)) != cudaSuccess) return e;
+      ev_in.push_back(a);
+      ev_out.push_back(b);
+    }
+    return cudaSuccess;
+  }
+};
+namespace {
+std::mutex g_pipe_mu;
+HostPipe g_pipes[64];
+}
+// The device's pipeline (callers hold g_pipe_mu for the whole call).
+HostPipe& host_pipe() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return g_pipes[(dev >= 0 && dev < 64) ? dev : 0];
+}
+
+template <class T>
+cudaError_t launch_fixup(const ScanPlan& plan, T* out, const T* carries, int64_t start,
+                         int64_t end, cudaStream_t s);
+
+// The passes of a tiled 1-D scan, each over a range of tiles [t0, t1):
+// first (one pass / local / up), middle (the carry chain, once), second
+// (fix-up / down / pairwise down-sweep; none for the one pass).
+template <class T>
+struct Tiled {
+  const ScanPlan& plan;
+  char* ws;
+  T init;
+  bool block, shift;
+  int S;
+  ScanArgs a{};
+  T *pyr, *totals, *carries;
+  int* counters;
+  Tiled(const ScanPlan& p, char* w, T i) : plan(p), ws(w), init(i) {
+    block = plan.policy == CR_BLOCK_DYADIC;
+    shift = plan.out_mode != 0;
+    S = block ? (int)(plan.B < kE ? plan.B : kE) : kE;
+    a.n = plan.n;
+    a.full_tiles = plan.full_tiles;
+    a.logB = plan.logB;
+    a.pyr_levels = plan.pyr_levels;
+    a.carry = block ? 1 : 0;
+    a.totals_level = block ? plan.totals_level : -1;
+    a.emit_last = plan.out_mode == CR_INCLUDE_INITIAL ? 1 : 0;
+    for (int l = 0; l < kMaxLevels; ++l) {
+      a.pyr_off[l] = plan.pyr_off[l];
+      a.cnt_off[l] = plan.cnt_off[l];
+    }
+    pyr = reinterpret_cast<T*>(ws + plan.pyr_ws);
+    counters = reinterpret_cast<int*>(ws + plan.cnt_ws);
+    totals = block ? reinterpret_cast<T*>(ws + plan.totals_ws) : nullptr;
+    carries = block ? reinterpret_cast<T*>(ws + plan.carries_ws) : nullptr;
+  }
+  bool has_second() const { return plan.mode != ScanPlan::kOnePass; }
+  cudaError_t prepare(cudaStream_t s) {
+    if (plan.n_tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    if (plan.zero_bytes > 0) return cudaMemsetAsync(ws + plan.zero_ws, 0, plan.zero_bytes, s);
+    return cudaSuccess;
+  }
+  cudaError_t first(const T* x, T* out, int64_t t0, int64_t t1, cudaStream_t s) {
+    if (t1 <= t0) return cudaSuccess;
+    const unsigned grid = (unsigned)(t1 - t0);
+    a.tile_base = t0;
+    if (plan.mode == ScanPlan::kOnePass) {  // tiles numbered by the counter, in launch order
+      int* ready = reinterpret_cast<int*>(ws + plan.ready_ws);
+      int* tctr = reinterpret_cast<int*>(ws + plan.tilectr_ws);
+      int* status = reinterpret_cast<int*>(ws);
+      CR_LAUNCH(kKScanOnePass, s, {
+        if (shift)
+          scan_onepass_kernel<T, true><<<grid, kScanThreads, 0, s>>>(
+              x, out, pyr, counters, ready, tctr, status, a, debug_skip_publish(), init);
+        else
+          scan_onepass_kernel<T, false><<<grid, kScanThreads, 0, s>>>(
+              x, out, pyr, counters, ready, tctr, status, a, debug_skip_publish(), init);
+      });
+      return cudaGetLastError();
+    }
+    if (plan.mode == ScanPlan::kLocalFixup) {
+#define CR_LOCAL(SS, SH) \
+  scan_local_kernel<T, SS, SH><<<grid, kScanThreads, 0, s>>>(x, out, totals, a)
+      CR_LAUNCH(kKScanLocal, s, {
+        if (shift) {
+          if (S == 8) CR_LOCAL(8, true);
+          else if (S == 4) CR_LOCAL(4, true);
+          else CR_LOCAL(2, true);
+        } else {
+          if (S == 8) CR_LOCAL(8, false);
+          else if (S == 4) CR_LOCAL(4, false);
+          else CR_LOCAL(2, false);
+        }
+      });
+#undef CR_LOCAL
+      return cudaGetLastError();
+    }
+    CR_LAUNCH(kKScanUp, s, {  // up pass: pairwise, blocks spanning tiles, binary32 iterated
+      if (S == 8) scan_up_kernel<T, 8><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
+      else if (S == 4) scan_up_kernel<T, 4><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
+      else scan_up_kernel<T, 2><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
+    });
+    return cudaGetLastError();
+  }
+  // block carries: C_0..C_{K-2} from the block totals
+  cudaError_t middle(cudaStream_t s) {
+    if (!block || plan.K < 2) return cudaSuccess;
+    const T* src = plan.mode == ScanPlan::kLocalFixup ? totals
+                                                       : pyr + plan.pyr_off[plan.logB - kLogTile];
+    if (plan.parallel_chain) return run_chain<T>(plan.chain, src, carries, ws + plan.chain_ws, s);
+    return run_serial_chain<T>(src, carries, plan.K - 1, s);
+  }
+  cudaError_t second(const T* x, T* out, int64_t t0, int64_t t1, cudaStream_t s) {
+    if (t1 <= t0 || plan.mode == ScanPlan::kOnePass) return cudaSuccess;
+    const unsigned grid = (unsigned)(t1 - t0);
+    a.tile_base = t0;
+    if (plan.mode == ScanPlan::kLocalFixup) {
+      if (shift) {  // every output: init, carries and the shifted in-block values (one range)
+        if (t0 != 0 || t1 != plan.n_tiles) return cudaErrorInvalidValue;
+        const int64_t threads = (plan.m + kE - 1) / kE;
+        const int64_t blocks = (threads + 255) / 256;
+        if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+        CR_LAUNCH(kKCarryFixupShift, s,
+                  carry_fixup_shift_kernel<T><<<(unsigned)blocks, 256, 0, s>>>(
+                      out, carries, plan.n, plan.m, plan.logB, init));
+        return cudaGetLastError();
+      }
+      if (plan.K < 2) return cudaSuccess;
+      const int64_t e0 = t0 * kTile > plan.B ? t0 * kTile : plan.B;
+      const int64_t e1 = t1 * kTile < plan.n ? t1 * kTile : plan.n;
+      return launch_fixup<T>(plan, out, carries, e0, e1, s);
+    }
+    if (plan.policy == CR_PAIRWISE) {
+      CR_LAUNCH(kKScanPairwise, s, {
+        if (shift)
+          scan_pairwise_kernel<T, true><<<grid, kScanThreads, 0, s>>>(x, out, pyr, a, init);
+        else
+          scan_pairwise_kernel<T, false><<<grid, kScanThreads, 0, s>>>(x, out, pyr, a, init);
+      });
+      return cudaGetLastError();
+    }
+#define CR_DOWN(SS, SH) \
+  scan_down_kernel<T, SS, SH><<<grid, kScanThreads, 0, s>>>(x, out, pyr, carries, a, init)
+    CR_LAUNCH(kKScanDown, s, {
+      if (shift) {
+        if (S == 8) CR_DOWN(8, true);
+        else if (S == 4) CR_DOWN(4, true);
+        else CR_DOWN(2, true);
+      } else {
+        if (S == 8) CR_DOWN(8, false);
+        else if (S == 4) CR_DOWN(4, false);
+        else CR_DOWN(2, false);
+      }
+    });
+#undef CR_DOWN
+    return cudaGetLastError();
+  }
+};
+
+// The carry fix-up of elements [start, end), start >= B.
+template <class T>
+cudaError_t launch_fixup(const ScanPlan& plan, T* out, const T* carries, int64_t start,
+                         int64_t end, cudaStream_t s) {
+  if (end <= start) return cudaSuccess;
+  const int64_t threads = (end - start + kE - 1) / kE;
+  const int64_t blocks = (threads + 255) / 256;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  CR_LAUNCH(kKCarryFixup, s,
+            carry_fixup_kernel<T><<<(unsigned)blocks, 256, 0, s>>>(out, carries, start, end,
+                                                                    plan.logB));
+  return cudaGetLastError();
+}
+
 template <class T>
 cudaError_t run_scan(const ScanPlan& plan, const T* x, T* out, int64_t es, int64_t bs,
                      int64_t oes, int64_t obs, T init, char* ws, cudaStream_t s) {
@@ -1094,127 +1284,83 @@ cudaError_t run_scan(const ScanPlan& plan, const T* x, T* out, int64_t es, int64
     }
     case ScanPlan::kTiled: break;
   }
-  const bool block = plan.policy == CR_BLOCK_DYADIC;
-  ScanArgs a{};
-  a.n = plan.n;
-  a.full_tiles = plan.full_tiles;
-  a.logB = plan.logB;
-  a.pyr_levels = plan.pyr_levels;
-  a.carry = block ? 1 : 0;
-  a.totals_level = block ? plan.totals_level : -1;
-  a.emit_last = plan.out_mode == CR_INCLUDE_INITIAL ? 1 : 0;
-  for (int l = 0; l < kMaxLevels; ++l) {
-    a.pyr_off[l] = plan.pyr_off[l];
-    a.cnt_off[l] = plan.cnt_off[l];
-  }
-  T* pyr = reinterpret_cast<T*>(ws + plan.pyr_ws);
-  int* counters = reinterpret_cast<int*>(ws + plan.cnt_ws);
-  T* totals = block ? reinterpret_cast<T*>(ws + plan.totals_ws) : nullptr;
-  T* carries = block ? reinterpret_cast<T*>(ws + plan.carries_ws) : nullptr;
-  if (plan.zero_bytes > 0) {
-    if ((e = cudaMemsetAsync(ws + plan.zero_ws, 0, plan.zero_bytes, s)) != cudaSuccess) return e;
-  }
-  if (plan.n_tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  const unsigned grid = (unsigned)plan.n_tiles;
-  const int S = block ? (int)(plan.B < kE ? plan.B : kE) : kE;
+  Tiled<T> tc(plan, ws, init);
+  if ((e = tc.prepare(s)) != cudaSuccess) return e;
+  if ((e = tc.first(x, out, 0, plan.n_tiles, s)) != cudaSuccess) return e;
+  if ((e = tc.middle(s)) != cudaSuccess) return e;
+  return tc.second(x, out, 0, plan.n_tiles, s);
+}
 
-  if (plan.mode == ScanPlan::kOnePass) {
-    int* ready = reinterpret_cast<int*>(ws + plan.ready_ws);
-    int* tctr = reinterpret_cast<int*>(ws + plan.tilectr_ws);
-    int* status = reinterpret_cast<int*>(ws);
-    CR_LAUNCH(kKScanOnePass, s, {
-      if (shift)
-        scan_onepass_kernel<T, true><<<grid, kScanThreads, 0, s>>>(
-            x, out, pyr, counters, ready, tctr, status, a, debug_skip_publish(), init);
-      else
-        scan_onepass_kernel<T, false><<<grid, kScanThreads, 0, s>>>(
-            x, out, pyr, counters, ready, tctr, status, a, debug_skip_publish(), init);
-    });
-    return cudaGetLastError();
+template <class T>
+cudaError_t run_scan_host(const ScanPlan& plan, const T* x_host, T* out_host, T* x_dev,
+                          T* out_dev, char* ws, cudaStream_t s) {
+  cudaError_t e;
+  const size_t bytes = (size_t)plan.n * sizeof(T);
+  if (plan.kind != ScanPlan::kTiled || plan.out_mode != 0) {  // not pipelined
+    if (plan.n > 0) {
+      if ((e = cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+        return e;
+    }
+    if ((e = run_scan<T>(plan, x_dev, out_dev, 1, plan.n, 1, plan.n, T(0), ws, s)) !=
+        cudaSuccess)
+      return e;
+    if (plan.n > 0 &&
+        (e = cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+      return e;
+    return cudaStreamSynchronize(s);
   }
-
-  // block carries: C_0..C_{K-2} from the block totals
-  auto chain = [&](const T* src) -> cudaError_t {
-    if (plan.K < 2) return cudaSuccess;
-    if (plan.parallel_chain) return run_chain<T>(plan.chain, src, carries, ws + plan.chain_ws, s);
-    return run_serial_chain<T>(src, carries, plan.K - 1, s);
+  // about 8 chunks of whole tiles (at least 256 tiles each)
+  const int64_t tiles = plan.n_tiles;
+  int64_t per = (tiles + 7) / 8;
+  if (per < 256) per = 256;
+  const int64_t nchunks = (tiles + per - 1) / per;
+  std::lock_guard<std::mutex> lock(g_pipe_mu);  // host-buffer calls share the streams
+  HostPipe& hp = host_pipe();
+  if ((e = hp.ensure((int)nchunks)) != cudaSuccess) return e;
+  cudaStream_t cin = hp.in, cout = hp.out;
+  // the caller's stream may hold earlier work on these buffers: start after it
+  if ((e = cudaEventRecord(hp.start, s)) != cudaSuccess) return e;
+  if ((e = cudaStreamWaitEvent(cin, hp.start, 0)) != cudaSuccess) return e;
+  if ((e = cudaStreamWaitEvent(cout, hp.start, 0)) != cudaSuccess) return e;
+  Tiled<T> tc(plan, ws, T(0));
+  if ((e = tc.prepare(s)) != cudaSuccess) return e;
+  auto range = [&](int64_t c, int64_t& t0, int64_t& t1, int64_t& e0, int64_t& e1) {
+    t0 = c * per;
+    t1 = t0 + per < tiles ? t0 + per : tiles;
+    e0 = t0 * kTile;
+    e1 = t1 * kTile < plan.n ? t1 * kTile : plan.n;
   };
-
-  if (plan.mode == ScanPlan::kLocalFixup) {
-#define CR_LOCAL(SS, SH) \
-  scan_local_kernel<T, SS, SH><<<grid, kScanThreads, 0, s>>>(x, out, totals, a)
-    CR_LAUNCH(kKScanLocal, s, {
-      if (shift) {
-        if (S == 8) CR_LOCAL(8, true);
-        else if (S == 4) CR_LOCAL(4, true);
-        else CR_LOCAL(2, true);
-      } else {
-        if (S == 8) CR_LOCAL(8, false);
-        else if (S == 4) CR_LOCAL(4, false);
-        else CR_LOCAL(2, false);
-      }
-    });
-#undef CR_LOCAL
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if ((e = chain(totals)) != cudaSuccess) return e;
-    if (shift) {  // every output: init, carries and the shifted in-block values
-      const int64_t threads = (plan.m + kE - 1) / kE;
-      const int64_t blocks = (threads + 255) / 256;
-      if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-      CR_LAUNCH(kKCarryFixupShift, s,
-                carry_fixup_shift_kernel<T><<<(unsigned)blocks, 256, 0, s>>>(
-                    out, carries, plan.n, plan.m, plan.logB, init));
-      return cudaGetLastError();
-    }
-    if (plan.K >= 2) {
-      const int64_t nfix = plan.n - plan.B;  // elements of blocks k >= 1
-      const int64_t threads = (nfix + kE - 1) / kE;
-      const int64_t blocks = (threads + 255) / 256;
-      if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-      CR_LAUNCH(kKCarryFixup, s,
-                carry_fixup_kernel<T><<<(unsigned)blocks, 256, 0, s>>>(out, carries, plan.n,
-                                                                        plan.logB));
-      e = cudaGetLastError();
-    }
-    return e;
+  for (int64_t c = 0; c < nchunks; ++c) {  // copy in, first pass per chunk
+    int64_t t0, t1, e0, e1;
+    range(c, t0, t1, e0, e1);
+    if ((e = cudaMemcpyAsync(x_dev + e0, x_host + e0, (size_t)(e1 - e0) * sizeof(T),
+                             cudaMemcpyHostToDevice, cin)) != cudaSuccess)
+      return e;
+    if ((e = cudaEventRecord(hp.ev_in[c], cin)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(s, hp.ev_in[c], 0)) != cudaSuccess) return e;
+    if ((e = tc.first(x_dev, out_dev, t0, t1, s)) != cudaSuccess) return e;
+    if (!tc.has_second() && (e = cudaEventRecord(hp.ev_out[c], s)) != cudaSuccess) return e;
   }
-
-  if (plan.policy == CR_PAIRWISE) {  // node pyramid first, then the down-sweep
-    CR_LAUNCH(kKScanUp, s,
-              scan_up_kernel<T, 8><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a));
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    CR_LAUNCH(kKScanPairwise, s, {
-      if (shift)
-        scan_pairwise_kernel<T, true><<<grid, kScanThreads, 0, s>>>(x, out, pyr, a, init);
-      else
-        scan_pairwise_kernel<T, false><<<grid, kScanThreads, 0, s>>>(x, out, pyr, a, init);
-    });
-    return cudaGetLastError();
-  }
-
-  // up/down: blocks spanning tiles (B > 2048), binary32 iterated_pairwise
-  CR_LAUNCH(kKScanUp, s, {
-    if (S == 8) scan_up_kernel<T, 8><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
-    else if (S == 4) scan_up_kernel<T, 4><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
-    else scan_up_kernel<T, 2><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
-  });
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (block && (e = chain(pyr + plan.pyr_off[plan.logB - kLogTile])) != cudaSuccess) return e;
-#define CR_DOWN(SS, SH) \
-  scan_down_kernel<T, SS, SH><<<grid, kScanThreads, 0, s>>>(x, out, pyr, carries, a, init)
-  CR_LAUNCH(kKScanDown, s, {
-    if (shift) {
-      if (S == 8) CR_DOWN(8, true);
-      else if (S == 4) CR_DOWN(4, true);
-      else CR_DOWN(2, true);
-    } else {
-      if (S == 8) CR_DOWN(8, false);
-      else if (S == 4) CR_DOWN(4, false);
-      else CR_DOWN(2, false);
+  if ((e = tc.middle(s)) != cudaSuccess) return e;
+  if (tc.has_second()) {
+    for (int64_t c = 0; c < nchunks; ++c) {
+      int64_t t0, t1, e0, e1;
+      range(c, t0, t1, e0, e1);
+      if ((e = tc.second(x_dev, out_dev, t0, t1, s)) != cudaSuccess) return e;
+      if ((e = cudaEventRecord(hp.ev_out[c], s)) != cudaSuccess) return e;
     }
-  });
-#undef CR_DOWN
-  return cudaGetLastError();
+  }
+  for (int64_t c = 0; c < nchunks; ++c) {  // copy out as each chunk completes
+    int64_t t0, t1, e0, e1;
+    range(c, t0, t1, e0, e1);
+    if ((e = cudaStreamWaitEvent(cout, hp.ev_out[c], 0)) != cudaSuccess) return e;
+    if ((e = cudaMemcpyAsync(out_host + e0, out_dev + e0, (size_t)(e1 - e0) * sizeof(T),
+                             cudaMemcpyDeviceToHost, cout)) != cudaSuccess)
+      return e;
+  }
+  if ((e = cudaStreamSynchronize(cout)) != cudaSuccess) return e;
+  if ((e = cudaStreamSynchronize(cin)) != cudaSuccess) return e;
+  return cudaStreamSynchronize(s);
 }
 
 template <class T>
@@ -1262,6 +1408,10 @@ template cudaError_t run_block_totals<double>(const ScanPlan&, const double*, ch
                                               cudaStream_t, double**);
 template cudaError_t run_block_totals<float>(const ScanPlan&, const float*, char*, cudaStream_t,
                                              float**);
+template cudaError_t run_scan_host<double>(const ScanPlan&, const double*, double*, double*,
+                                           double*, char*, cudaStream_t);
+template cudaError_t run_scan_host<float>(const ScanPlan&, const float*, float*, float*, float*,
+                                          char*, cudaStream_t);
 template cudaError_t run_scan<double>(const ScanPlan&, const double*, double*, int64_t,
                                       int64_t, int64_t, int64_t, double, char*, cudaStream_t);
 template cudaError_t run_scan<float>(const ScanPlan&, const float*, float*, int64_t, int64_t,

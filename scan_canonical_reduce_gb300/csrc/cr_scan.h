@@ -23,6 +23,7 @@ struct ScanArgs {
   int32_t carry;             // block_dyadic: apply C_{k-1}
   int32_t totals_level;      // block totals: 0 in-thread, p > 0 tile pyramid level, -1 global
   int32_t emit_last;         // shifted output of n + 1 entries: also write out[n]
+  int64_t tile_base;         // tile index of blockIdx.x == 0 (chunked launches)
   int64_t pyr_off[kMaxLevels];  // element offset of each pyramid level
   int64_t cnt_off[kMaxLevels];  // offset of each level's arrival counters
 };
@@ -83,6 +84,15 @@ template <class T>
 cudaError_t run_scan(const ScanPlan& plan, const T* x, T* out, int64_t elem_stride,
                      int64_t batch_stride, int64_t out_elem_stride, int64_t out_batch_stride,
                      T init, char* ws, cudaStream_t s);
+
+// The same inclusive 1-D scan with x and out in host memory: the copies and
+// the kernels are pipelined in chunks of tiles over three streams (copy in,
+// compute, copy out, ordered by events), so that the transfers overlap the
+// passes. x_dev and out_dev: device buffers of n elements; ws as for
+// run_scan. Returns when out is written (the streams are synchronised).
+template <class T>
+cudaError_t run_scan_host(const ScanPlan& plan, const T* x_host, T* out_host, T* x_dev,
+                          T* out_dev, char* ws, cudaStream_t s);
 
 // The trees T_k = tree(x[kB .. (k+1)B)) of the n / B complete blocks, for
 // reduce<block_dyadic>: the scan's up pass without its outputs. plan =
