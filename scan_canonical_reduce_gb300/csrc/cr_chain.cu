@@ -770,28 +770,41 @@ __global__ void __launch_bounds__(1024) chain_link_kernel(const int64_t* tile_ns
 // which rounds up exactly when the remainder exceeds half, or equals it and
 // either the exact sum lies above A (fpos) or the quotient is odd.
 struct alignas(16) Hot {
-  int64_t c;        // 2^(d-1) - 1 for a rise, 0 for a continuation
-  uint64_t b0, b1;  // the segment map's offsets, plus the next record's q when
-                    // that record is a rise or a continuation
-  uint32_t ctrl;    // d (6 bits) | sh (7) << 6 | rise << 13 | fpos << 14 | neg << 15 |
-                    // type (2) << 16 | steps << 18
-  uint32_t pad;
+  uint64_t b0;      // the segment map's offset for an even M, plus the next
+                    // record's q when that record is a rise
+  int64_t db;       // the offset for an odd M minus b0
+  uint32_t ctrl;    // d (4 bits) | sh (6) << 4 | zero map << 10 | fpos << 11 | neg << 12 |
+                    // type (2) << 13 | steps << 15
+  int32_t c;        // 2^(d-1) - 1 for a rise (d <= 8), 0 otherwise
+  uint32_t pad[2];
 };
 __device__ __forceinline__ bool is_fast(uint32_t meta) { return m_type(meta) <= kUp; }
 __device__ __forceinline__ Hot make_hot(const SegRec& r, int64_t q_next) {
   Hot h;
   const uint32_t m = r.meta, type = m_type(m);
-  const bool up = type == kUp;
-  const int d = up ? m_d(m) : 0;
-  h.c = d > 0 ? (int64_t(1) << (d - 1)) - 1 : 0;
+  const int d = type == kUp ? m_d(m) : 0;  // a rise spans at most 8 binades
+  h.c = d > 0 ? (1 << (d - 1)) - 1 : 0;
   h.b0 = r.map.b0 + (uint64_t)q_next;
-  h.b1 = r.map.b1 + (uint64_t)q_next;
-  const uint32_t shift = r.map.a == 0 ? 64u : (uint32_t)(__ffsll((long long)r.map.a) - 1);
-  h.ctrl = (uint32_t)d | (shift << 6) | (d > 0 ? 1u << 13 : 0u) |
-           ((m_fcls(m) != kFZero) ? 1u << 14 : 0u) | (m_neg(m) ? 1u << 15 : 0u) |
-           (type << 16) | (r.nsteps > 0 ? 1u << 18 : 0u);
-  h.pad = 0;
+  h.db = (int64_t)(r.map.b1 - r.map.b0);
+  const bool zero = r.map.a == 0;  // the map multiplies by 2^64 = 0 mod 2^64
+  const uint32_t shift = zero ? 0u : (uint32_t)(__ffsll((long long)r.map.a) - 1);
+  h.ctrl = (uint32_t)d | (shift << 4) | (zero ? 1u << 10 : 0u) |
+           ((m_fcls(m) != kFZero) ? 1u << 11 : 0u) | (m_neg(m) ? 1u << 12 : 0u) |
+           (type << 13) | (r.nsteps > 0 ? 1u << 15 : 0u);
+  h.pad[0] = h.pad[1] = 0;
   return h;
+}
+__device__ __forceinline__ uint32_t hot_type(const Hot& h) { return (h.ctrl >> 13) & 3u; }
+__device__ __forceinline__ bool hot_steps(const Hot& h) { return (h.ctrl >> 15) & 1u; }
+
+// The map of a record applied to M1, plus the next record's q:
+// (M1 2^sh (or 0 for a zero map)) + b0 + (M1 odd ? db : 0).
+__device__ __forceinline__ int64_t hot_map(const Hot& h, int64_t M1) {
+  const uint32_t ctl = h.ctrl;
+  const uint64_t amask = (ctl >> 10) & 1u ? 0ull : ~0ull;
+  const uint64_t odd = 0ull - ((uint64_t)M1 & 1ull);
+  return (int64_t)((((uint64_t)M1 << ((ctl >> 4) & 63u)) & amask) + h.b0 +
+                   (odd & (uint64_t)h.db));
 }
 
 // One rise from A: writes m_in, returns the next A. (Whether the rise really
@@ -800,16 +813,13 @@ __device__ __forceinline__ Hot make_hot(const SegRec& r, int64_t q_next) {
 template <class T>
 __device__ __forceinline__ int64_t walk_fast(const Hot& h, int64_t A, int64_t* m_in_j,
                                              bool& cval) {
-  const uint32_t c = h.ctrl;
-  const int d = (int)(c & 63u);
-  const uint32_t sh = (c >> 6) & 127u;
-  const int64_t rise = (c >> 13) & 1u, fpos = (c >> 14) & 1u;
-  const int64_t x = rise & ((A >> d) | fpos);
-  const int64_t M1 = (A + h.c + x) >> d;
+  const uint32_t ctl = h.ctrl;
+  const int d = (int)(ctl & 15u);  // 1..8: bit d of A lies in its low word
+  const uint32_t x = (((uint32_t)A >> d) | (ctl >> 11)) & 1u;
+  const int64_t M1 = (A + (int64_t)(h.c + (int32_t)x)) >> d;
   *m_in_j = M1;
-  cval = cval & ((c & ((1u << 13) | (1u << 18))) == 0);
-  const uint64_t aM = sh >= 64 ? 0 : ((uint64_t)M1 << sh);
-  return (int64_t)(aM + ((M1 & 1) ? h.b1 : h.b0));
+  cval = false;  // a rise leaves no real-add value current
+  return hot_map(h, M1);
 }
 
 // Breaks in order, in one thread. The whole warp converts the next 32
@@ -864,16 +874,30 @@ __global__ void __launch_bounds__(32) chain_walk_kernel(const T* src, T* dst, co
       const int cnt = (int)(nseg - b0 < 32 ? nseg - b0 : 32);
       bool ok = true;
       if (!cold_batch[slot]) {
-        if (cnt == 32) {
-#pragma unroll 16
-          for (int j = 0; j < 32; ++j) A = walk_fast<T>(hot[slot][j], A, m_in + b0 + j, cval);
+        if (cnt == 32) {  // the next 4 records are loaded while 4 are walked
+          Hot cur[4], nxt[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) cur[u] = hot[slot][u];
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            if (g < 7) {
+#pragma unroll
+              for (int u = 0; u < 4; ++u) nxt[u] = hot[slot][(g + 1) * 4 + u];
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) A = walk_fast<T>(cur[u], A, m_in + b0 + g * 4 + u, cval);
+            if (g < 7) {
+#pragma unroll
+              for (int u = 0; u < 4; ++u) cur[u] = nxt[u];
+            }
+          }
         } else {
           for (int j = 0; j < cnt; ++j) A = walk_fast<T>(hot[slot][j], A, m_in + b0 + j, cval);
         }
       } else {
         for (int j = 0; j < cnt; ++j) {
           const Hot h = hot[slot][j];
-          const uint32_t type = (h.ctrl >> 16) & 3u;
+          const uint32_t type = hot_type(h);
           if (type <= kUp) {
             A = walk_fast<T>(h, A, m_in + b0 + j, cval);
             continue;
@@ -900,10 +924,8 @@ __global__ void __launch_bounds__(32) chain_walk_kernel(const T* src, T* dst, co
             M1 = Mi;
           }
           m_in[b0 + j] = M1;
-          const uint32_t sh = (h.ctrl >> 6) & 127u;
-          const uint64_t aM = sh >= 64 ? 0 : ((uint64_t)M1 << sh);
-          A = (int64_t)(aM + ((M1 & 1) ? h.b1 : h.b0));
-          cval = cval & !((h.ctrl >> 18) & 1u);
+          A = hot_map(h, M1);
+          cval = cval && !hot_steps(h);
         }
       }
       bad = bad || !ok;
