@@ -278,6 +278,17 @@ int cr_profile_collect(int* kernel_ids, float* ms, int max_records);
  * (the output is then wrong). -1 turns it off. Process-wide. */
 void cr_debug_skip_publish(int64_t tile);
 
+/* Test hook for the block_dyadic scans with 2 <= B <= 2048 whose block
+ * carries take the parallel exact chain (inclusive, out != x). For B <= 16
+ * the chain's evaluation and the carry fix-up run as one cooperative pass
+ * by default; for larger B as separate passes. mode 0: that default; 1: the
+ * separate passes for every B; 2: the fused pass for every B, with a
+ * validation failure raised once the chain's walk is half-way, so that its
+ * recovery (the local pass again, the serial chain, the fix-up again) runs;
+ * 3: the fused pass for every B. Every mode gives the same, exact output.
+ * Process-wide. */
+void cr_debug_fused_fixup(int mode);
+
 /* Static name of a kernel id returned by cr_profile_collect(). */
 const char* cr_kernel_name(int id);
 

@@ -64,6 +64,7 @@ SIGNATURES = {
     "cr_version": (_INT, []),
     "cr_launch_count": (ctypes.c_uint64, []),
     "cr_debug_skip_publish": (None, [_I64]),
+    "cr_debug_fused_fixup": (None, [_INT]),
     "cr_profile_enable": (None, [_INT]),
     "cr_profile_collect": (_INT, [_P, _P, _INT]),
     "cr_kernel_name": (ctypes.c_char_p, [_INT]),

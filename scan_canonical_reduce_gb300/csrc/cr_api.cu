@@ -282,5 +282,6 @@ const char* cr_status_string(cr_status s) {
 int cr_version(void) { return 100; }
 
 void cr_debug_skip_publish(int64_t tile) { cr::set_debug_skip_publish(tile); }
+void cr_debug_fused_fixup(int mode) { cr::set_debug_fused_mode(mode); }
 
 }  // extern "C"

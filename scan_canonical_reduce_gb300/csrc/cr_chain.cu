@@ -59,6 +59,7 @@ namespace {
 constexpr int kCT = 256;           // threads per tile
 constexpr int kCE = 16;            // steps per thread
 constexpr int kCTile = kCT * kCE;  // 4096 steps per tile
+constexpr int kPublishBatches = 16;  // fused form: the walk's progress every 512 records
 
 template <class T>
 struct FP;
@@ -829,12 +830,17 @@ __device__ __forceinline__ int64_t walk_fast(const Hot& h, int64_t A, int64_t* m
 // dst == nullptr: the chain's outputs are not wanted (a reduction); with
 // final_out, lane 0 also writes C_{K-1}, taken from the last segment's map
 // (e_last: binade of the last step) or from the last real add.
+// Run by one warp (lanes 0..31 of the calling block). With progress
+// non-null, lane 0 publishes the number of records done every kPublishBatches
+// batches and after the last (after a fence, so that their m_in and the
+// start and uncertain values in dst are visible first; the fence waits for
+// the walk's stores, hence not after every batch).
 template <class T>
-__global__ void __launch_bounds__(32) chain_walk_kernel(const T* src, T* dst, const SegRec* segs,
-                                                        const int64_t* nseg_total,
-                                                        int64_t seg_cap, int64_t* m_in,
-                                                        int* fail, const uint32_t* meta,
-                                                        int64_t K, T* final_out) {
+__device__ __forceinline__ void walk_body(const T* src, T* dst, const SegRec* segs,
+                                          const int64_t* nseg_total, int64_t seg_cap,
+                                          int64_t* m_in, int* fail, const uint32_t* meta,
+                                          int64_t K, T* final_out,
+                                          unsigned long long* progress) {
   __shared__ Hot hot[2][32];
   __shared__ SegRec cold[2][32];
   __shared__ int cold_batch[2];
@@ -929,12 +935,25 @@ __global__ void __launch_bounds__(32) chain_walk_kernel(const T* src, T* dst, co
         }
       }
       bad = bad || !ok;
+      if (bad) atomicExch(fail, 1);
+      if (progress != nullptr && ((it + 1) % kPublishBatches == 0 || b0 + 32 >= nseg)) {
+        __threadfence();  // m_in and dst before the count that releases them
+        atomicExch(progress, (unsigned long long)(b0 + cnt));
+      }
     }
     __syncwarp();
   }
-  if (lane == 0 && bad) atomicExch(fail, 1);
   if (lane == 0 && final_out != nullptr && !bad)  // A = M after the last segment's map
     *final_out = cval ? C : m_to_value<T>(A, m_e(meta[K - 1]));
+}
+
+template <class T>
+__global__ void __launch_bounds__(32) chain_walk_kernel(const T* src, T* dst, const SegRec* segs,
+                                                        const int64_t* nseg_total,
+                                                        int64_t seg_cap, int64_t* m_in,
+                                                        int* fail, const uint32_t* meta,
+                                                        int64_t K, T* final_out) {
+  walk_body<T>(src, dst, segs, nseg_total, seg_cap, m_in, fail, meta, K, final_out, nullptr);
 }
 
 // Every rise of the walk, checked in parallel: A = (previous record's map
@@ -942,22 +961,28 @@ __global__ void __launch_bounds__(32) chain_walk_kernel(const T* src, T* dst, co
 // (integer comparisons on hi = floor(A / 2^d)). A failure sends the chain
 // to the serial fallback.
 template <class T>
+__device__ __forceinline__ void verify_record(const SegRec* segs, const int64_t* m_in, int64_t j,
+                                              int* fail) {
+  const uint32_t m = segs[j].meta;
+  if (j == 0 || m_type(m) != kUp) return;
+  const Map g = segs[j - 1].map;
+  const int64_t A = (int64_t)apply(g, (uint64_t)__ldcg(m_in + j - 1)) + segs[j].q;
+  const int d = m_d(m);
+  const int64_t hi = A >> d;
+  const uint64_t lo = (uint64_t)A & ((uint64_t(1) << d) - 1);
+  const bool fpos = m_fcls(m) != kFZero;
+  if (!in_binade64<T>(hi, m_neg(m), lo == 0 && !fpos)) atomicExch(fail, 1);
+}
+
+template <class T>
 __global__ void __launch_bounds__(256) chain_verify_kernel(const SegRec* segs,
                                                            const int64_t* nseg_total,
                                                            int64_t seg_cap, const int64_t* m_in,
                                                            int* fail) {
   const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t nseg = *nseg_total;
-  if (j == 0 || j >= nseg || j >= seg_cap || *fail) return;
-  const uint32_t m = segs[j].meta;
-  if (m_type(m) != kUp) return;
-  const Map g = segs[j - 1].map;
-  const int64_t A = (int64_t)apply(g, (uint64_t)m_in[j - 1]) + segs[j].q;
-  const int d = m_d(m);
-  const int64_t hi = A >> d;
-  const uint64_t lo = (uint64_t)A & ((uint64_t(1) << d) - 1);
-  const bool fpos = m_fcls(m) != kFZero;
-  if (!in_binade64<T>(hi, m_neg(m), lo == 0 && !fpos)) atomicExch(fail, 1);
+  if (j >= nseg || j >= seg_cap || *fail) return;
+  verify_record<T>(segs, m_in, j, fail);
 }
 
 // ---------------------------------------------------------------- pass 8
@@ -976,48 +1001,90 @@ __device__ __forceinline__ T m_to_value_normal(int64_t M, int e) {
   return F::from_bits(b);
 }
 
-template <class T>
-__global__ void __launch_bounds__(kCT) chain_fill_kernel(const int64_t* qv, const uint32_t* meta,
-                                                         int64_t K, const int64_t* seg_base,
-                                                         const Summ* thr_in, const Map* entry,
-                                                         const int64_t* entry_rec,
-                                                         int64_t seg_cap, const int64_t* m_in,
-                                                         T* dst, int* fail) {
-  const int t = threadIdx.x;
-  const int64_t tile0 = (int64_t)blockIdx.x * kCTile;
-  const int64_t k0 = tile0 + (int64_t)t * kCE;
-  if (*fail || k0 >= K) return;
-  const int64_t n = K - k0 < kCE ? K - k0 : kCE;
-  const Summ in = thr_in[blockIdx.x * kCT + t];
-  int64_t seg = seg_base[blockIdx.x] + in.brk - 1;
-  int64_t qr[kCE];
+// The 16 steps of thread t (of kCT) of chain tile c, from its segment's
+// entry value, in two parts: fill_prep issues the loads that do not depend
+// on the walk (in the fused form, before waiting for it), fill_finish reads
+// the walk's results (all of them at once) and evaluates the steps.
+struct FillPrep {
+  int64_t qr[kCE];    // q of each step; a record step's m_in once read
   uint32_t mr[kCE];
-  load_run(qv + k0, n, qr);
-  load_run(meta + k0, n, mr);
-  uint64_t M = 0;
-  if (in.brk > 0) {
-    if (seg < seg_cap) M = apply(in.map, (uint64_t)m_in[seg]);
-  } else if (blockIdx.x > 0) {  // the tile's leading run: enters from an earlier tile
-    const int64_t r = entry_rec[blockIdx.x];
-    if (r >= 0 && r < seg_cap) M = apply(in.map, apply(entry[blockIdx.x], (uint64_t)m_in[r]));
+  Map in_map, entry;
+  int64_t seg;        // the record before the thread's first step
+  int64_t entry_rec;  // no break before the thread: the record its run enters from
+  int brk;
+  int n;              // steps (0: none)
+};
+
+__device__ __forceinline__ void fill_prep(int64_t c, int t, const int64_t* qv,
+                                          const uint32_t* meta, int64_t K,
+                                          const int64_t* seg_base, const Summ* thr_in,
+                                          const Map* entry, const int64_t* entry_rec,
+                                          FillPrep& p) {
+  const int64_t k0 = c * kCTile + (int64_t)t * kCE;
+  p.n = 0;
+  if (k0 >= K) return;
+  p.n = (int)(K - k0 < kCE ? K - k0 : kCE);
+  const Summ in = thr_in[c * kCT + t];
+  p.in_map = in.map;
+  p.brk = in.brk;
+  p.seg = seg_base[c] + in.brk - 1;
+  p.entry_rec = -1;
+  if (c > 0) {  // the tile's leading run enters from an earlier tile
+    p.entry_rec = entry_rec[c];
+    p.entry = entry[c];
   }
-  bool ok = true;
+  load_run(qv + k0, p.n, p.qr);
+  load_run(meta + k0, p.n, p.mr);
+}
+
+template <class T>
+__device__ __forceinline__ void fill_finish(int64_t c, int t, FillPrep& p, int64_t seg_cap,
+                                            const int64_t* m_in, T* dst, int* fail) {
+  if (p.n == 0) return;
+  const int64_t k0 = c * kCTile + (int64_t)t * kCE;
+  // the walk's results, read from L2 (__ldcg: in the fused form the walk
+  // writes them during this launch), all loads issued together: the entry
+  // record's M, each record step's M and the walk's start and uncertain
+  // values
+  uint64_t Me = 0;
+  const bool from_seg = p.brk > 0 && p.seg < seg_cap;
+  const bool from_entry = p.brk == 0 && c > 0 && p.entry_rec >= 0 && p.entry_rec < seg_cap;
+  if (from_seg) Me = (uint64_t)__ldcg(m_in + p.seg);
+  else if (from_entry) Me = (uint64_t)__ldcg(m_in + p.entry_rec);
   T out[kCE];
+  {
+    int64_t s = p.seg;
+#pragma unroll
+    for (int i = 0; i < kCE; ++i) {
+      out[i] = T(0);
+      const uint32_t type = m_type(p.mr[i]);
+      if (i < p.n && type != kMap) {
+        s += 1;
+        if (s < seg_cap) {
+          p.qr[i] = __ldcg(m_in + s);
+          if (type != kUp && dst != nullptr) out[i] = __ldcg(dst + k0 + i);
+        }
+      }
+    }
+  }
+  uint64_t M = 0;
+  if (from_seg) M = apply(p.in_map, Me);
+  else if (from_entry) M = apply(p.in_map, apply(p.entry, Me));
+  bool ok = true;
+  int64_t seg = p.seg;
 #pragma unroll
   for (int i = 0; i < kCE; ++i) {
-    out[i] = T(0);
-    if (i < n) {
-      const uint32_t m = mr[i];
+    if (i < p.n) {
+      const uint32_t m = p.mr[i];
       const uint32_t type = m_type(m);
       if (type != kMap) {  // enter the next segment
         seg += 1;
         if (seg >= seg_cap) {
           ok = false;
         } else {
-          M = (uint64_t)m_in[seg];
-          // the walk wrote start and uncertain steps; keep them
-          if (dst != nullptr)
-            out[i] = type == kUp ? m_to_value_normal<T>((int64_t)M, m_e(m)) : dst[k0 + i];
+          M = (uint64_t)p.qr[i];
+          // the walk wrote start and uncertain steps (read above); keep them
+          if (type == kUp) out[i] = m_to_value_normal<T>((int64_t)M, m_e(m));
         }
         continue;
       }
@@ -1025,10 +1092,10 @@ __global__ void __launch_bounds__(kCT) chain_fill_kernel(const int64_t* qv, cons
       const uint32_t f = m_fcls(m);
       int64_t A64;
       if (d <= 9) {  // |M 2^d| <= 2^63 / 2 and |q| < 2^62: no overflow
-        A64 = (int64_t)(M << d) + qr[i];
+        A64 = (int64_t)(M << d) + p.qr[i];
         if (!in_binade64<T>(A64, m_neg(m), f == kFZero)) ok = false;
       } else {
-        const __int128 A = (__int128)(int64_t)M * ((__int128)1 << d) + (__int128)qr[i];
+        const __int128 A = (__int128)(int64_t)M * ((__int128)1 << d) + (__int128)p.qr[i];
         if (!in_binade<T>(A, m_neg(m), f)) ok = false;
         A64 = (int64_t)A;
       }
@@ -1036,8 +1103,21 @@ __global__ void __launch_bounds__(kCT) chain_fill_kernel(const int64_t* qv, cons
       out[i] = m_to_value_normal<T>((int64_t)M, m_e(m));
     }
   }
-  if (dst != nullptr) store_run(dst + k0, n, out);  // else: validation only
+  if (dst != nullptr) store_run(dst + k0, p.n, out);  // else: validation only
   if (!ok) atomicExch(fail, 1);
+}
+
+template <class T>
+__global__ void __launch_bounds__(kCT) chain_fill_kernel(const int64_t* qv, const uint32_t* meta,
+                                                         int64_t K, const int64_t* seg_base,
+                                                         const Summ* thr_in, const Map* entry,
+                                                         const int64_t* entry_rec,
+                                                         int64_t seg_cap, const int64_t* m_in,
+                                                         T* dst, int* fail) {
+  if (*fail) return;
+  FillPrep p;
+  fill_prep(blockIdx.x, threadIdx.x, qv, meta, K, seg_base, thr_in, entry, entry_rec, p);
+  fill_finish<T>(blockIdx.x, threadIdx.x, p, seg_cap, m_in, dst, fail);
 }
 
 // ---------------------------------------------------------------- pass 9
@@ -1111,6 +1191,268 @@ __global__ void __launch_bounds__(32) chain_serial_kernel(const T* src, T* dst, 
   if (lane == 0 && final_out != nullptr) *final_out = c;
 }
 
+// ---------------------------------------------------------------- fused
+// The walk, verify and fill of the chain, fused with the fix-up of a block
+// scan that waits for the chain's carries: out[i] = C_{k-1} op out[i] for
+// the elements i of blocks k >= 1 (B = 2^logB elements a block). Launched
+// cooperatively (every block resident), three roles:
+//   block 0, first warp   the walk; publishes how many records are done;
+//   blocks 1 .. F         fill tiles c = b - 1, b - 1 + F, ...: wait for the
+//                         walk to pass the tile's records, check their rises,
+//                         write the tile's carries (a whole block: short
+//                         latency), raise the tile's flag;
+//   the other blocks      every warp on its own: fix-up items w, w + W, ...
+//                         (kFixItem elements each) in order, each after the
+//                         flags of the (at most two) tiles holding its
+//                         carries, streamed in sub-chunks whose elements and
+//                         carries are loaded one sub-chunk ahead.
+// Waits run walk <- fills <- fix-up only, so all of them end; each also
+// gives up after kWaitLimitNs and sets fail. Any failure (validation,
+// overflow, time limit) leaves out partly fixed: the caller's recovery
+// passes, which run only when fail is set, recompute the local values, the
+// carries (serially) and the fix-up. The fix-up warps need no block
+// barrier, so the warps of an SM stay in different phases (loads, FP64
+// adds, stores) as a plain streaming kernel's would.
+#ifndef CR_FUSED_FILL_BLOCKS
+#define CR_FUSED_FILL_BLOCKS 96
+#endif
+#ifndef CR_FUSED_FILL_DIV
+#define CR_FUSED_FILL_DIV 4
+#endif
+constexpr int64_t kMaxFillBlocks = CR_FUSED_FILL_BLOCKS;
+constexpr int kFixPer = 16;                    // elements a lane per sub-chunk
+constexpr int64_t kFixSub = 32 * kFixPer;      // 512 elements a sub-chunk
+constexpr int kFixSubs = 16;                   // sub-chunks an item
+constexpr int64_t kFixItem = kFixSub * kFixSubs;  // 8192 elements a warp item
+constexpr int kFailTimeout = 3;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second
+constexpr uint32_t kWaitMaxSpins = 1u << 24;
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned long long ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// One thread: waits until *v >= need (an acquire load: what was written
+// before the matching release is visible after it), with a growing sleep.
+// Returns false once fail is set, setting it itself at the limit.
+template <class V>
+__device__ bool wait_at_least(const V* v, unsigned long long need, int* fail) {
+  if (ld_acquire(v) >= need) return true;
+  const volatile int* vf = fail;
+  const uint64_t t0 = global_ns();
+  uint32_t spins = 0, ns = 32;
+  for (;;) {
+    if (*vf != 0) return false;
+    if (++spins > kWaitMaxSpins || global_ns() - t0 > kWaitLimitNs) {
+      atomicCAS(fail, 0, kFailTimeout);
+      return false;
+    }
+    __nanosleep(ns);
+    if (ns < 2048) ns *= 2;
+    if (ld_acquire(v) >= need) return true;
+  }
+}
+
+struct FusedArgs {
+  const SegRec* segs;
+  const int64_t* total;     // records
+  int64_t seg_cap;
+  int64_t* m_in;
+  int* fail;
+  const uint32_t* meta;
+  const int64_t* qv;
+  int64_t K;                // chain steps
+  int64_t ntiles;
+  const int64_t* seg_base;  // first record of each tile
+  const int64_t* tile_nseg; // records of each tile
+  const Summ* thr_in;
+  const Map* entry;
+  const int64_t* entry_rec;
+  unsigned long long* progress;
+  unsigned* tile_done;
+  int64_t n;                // fix-up: elements of out
+  int logB;
+  int64_t nfill;            // fill blocks
+  int64_t nitems;           // fix-up items (kFixItem elements)
+  int debug_fail;           // test hook: fail once the walk is half-way
+};
+
+// A fix-up sub-chunk of one warp: elements [i0, i0 + kFixSub) of out, a lane
+// taking 2 runs of 8 (coalesced across the warp), with the carries they
+// need: a run of 8 lies in one block for B >= 8 (NC = 1), in up to 4 for
+// B = 2, 4 (NC = 4; carry q of a run is that of block (i0 >> logB) + q).
+template <class T, int NC>
+struct FixRegs {
+  T v[kFixPer / 8][8];
+  T c[kFixPer / 8][NC];
+};
+
+// The sub-chunk's elements (independent of the chain: may be loaded before
+// the carries are ready).
+template <class T, int NC>
+__device__ __forceinline__ void fix_load_values(const T* out, int64_t i0s, int64_t n, int logB,
+                                                int lane, FixRegs<T, NC>& r) {
+  const int64_t Bk = int64_t(1) << logB;
+#pragma unroll
+  for (int g = 0; g < kFixPer / 8; ++g) {
+    const int64_t i0 = i0s + (int64_t)g * 32 * 8 + (int64_t)lane * 8;
+    const int64_t cnt = n - i0 < 0 ? 0 : (n - i0 < 8 ? n - i0 : 8);
+    if (i0 + 8 > Bk) load_run(out + i0, cnt, r.v[g]);  // not all in block 0
+  }
+}
+
+// Its carries (only once the tiles holding them are flagged).
+template <class T, int NC>
+__device__ __forceinline__ void fix_load_carries(const T* carries, int64_t i0s, int64_t n,
+                                                 int logB, int lane, FixRegs<T, NC>& r) {
+  const int64_t Bk = int64_t(1) << logB;
+#pragma unroll
+  for (int g = 0; g < kFixPer / 8; ++g) {
+    const int64_t i0 = i0s + (int64_t)g * 32 * 8 + (int64_t)lane * 8;
+    if (i0 >= n || i0 + 8 <= Bk) continue;
+    const int64_t k0 = i0 >> logB, k1 = ((i0 + 8 < n ? i0 + 8 : n) - 1) >> logB;
+#pragma unroll
+    for (int q = 0; q < NC; ++q)
+      if (k0 + q >= 1 && k0 + q <= k1) r.c[g][q] = __ldcg(carries + k0 + q - 1);
+  }
+}
+
+template <class T, int NC>
+__device__ __forceinline__ void fix_apply(T* out, int64_t i0s, int64_t n, int logB, int lane,
+                                          FixRegs<T, NC>& r) {
+  const int64_t Bk = int64_t(1) << logB;
+#pragma unroll
+  for (int g = 0; g < kFixPer / 8; ++g) {
+    const int64_t i0 = i0s + (int64_t)g * 32 * 8 + (int64_t)lane * 8;
+    if (i0 >= n || i0 + 8 <= Bk) continue;
+    const int64_t cnt = n - i0 < 8 ? n - i0 : 8;
+    if (NC == 1) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) r.v[g][e] = add_rn(r.c[g][0], r.v[g][e]);
+      store_run(out + i0, cnt, r.v[g]);
+    } else {
+      const int64_t k0 = i0 >> logB;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int64_t i = i0 + e;
+        const int q = (int)((i >> logB) - k0);
+        T c = r.c[g][0];
+#pragma unroll
+        for (int u = 1; u < NC; ++u)
+          if (q == u) c = r.c[g][u];
+        if (e < cnt && i >= Bk) out[i] = add_rn(c, r.v[g][e]);
+      }
+    }
+  }
+}
+
+// Fix-up items w0, w0 + W, ... of one warp (kFixItem elements each).
+template <class T, int NC>
+__device__ __forceinline__ void fix_items(T* out, const T* carries, const FusedArgs& f,
+                                          int64_t w0, int64_t W) {
+  const unsigned full = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  for (int64_t j = w0; j < f.nitems; j += W) {
+    const int64_t lo = j * kFixItem;
+    const int64_t end = lo + kFixItem < f.n ? lo + kFixItem : f.n;
+    FixRegs<T, NC> a, b;
+    fix_load_values<T, NC>(out, lo, end, f.logB, lane, a);  // ahead of the wait
+    int go = 0;
+    if (lane == 0) {
+      // carries (lo >> logB) - 1 .. ((end - 1) >> logB) - 1 of its elements
+      const int64_t klo = (lo >> f.logB) - 1, khi = ((end - 1) >> f.logB) - 1;
+      go = khi >= 0;
+      if (go) go = wait_at_least(f.tile_done + khi / kCTile, 1ull, f.fail);
+      if (go && klo >= 0 && klo / kCTile != khi / kCTile)
+        go = wait_at_least(f.tile_done + klo / kCTile, 1ull, f.fail);
+    }
+    go = __shfl_sync(full, go, 0);
+    if (!go) continue;
+    fix_load_carries<T, NC>(carries, lo, end, f.logB, lane, a);
+#pragma unroll 1
+    for (int s = 0; s < kFixSubs; ++s) {
+      const int64_t i0 = lo + s * kFixSub;
+      if (i0 >= end) break;
+      const int64_t i1 = i0 + kFixSub;
+      if (s + 1 < kFixSubs && i1 < end) {  // the next sub-chunk in flight meanwhile
+        fix_load_values<T, NC>(out, i1, end, f.logB, lane, b);
+        fix_load_carries<T, NC>(carries, i1, end, f.logB, lane, b);
+      }
+      fix_apply<T, NC>(out, i0, end, f.logB, lane, a);
+      a = b;
+    }
+  }
+}
+
+#ifndef CR_FUSED_BLOCKS_PER_SM
+#define CR_FUSED_BLOCKS_PER_SM 2
+#endif
+template <class T>
+__global__ void __launch_bounds__(kCT, CR_FUSED_BLOCKS_PER_SM) chain_walk_fix_kernel(const T* src, T* dst, T* out,
+                                                                FusedArgs f) {
+  if (blockIdx.x == 0) {
+    if (threadIdx.x < 32) {
+      walk_body<T>(src, dst, f.segs, f.total, f.seg_cap, f.m_in, f.fail, f.meta, f.K, nullptr,
+                   f.progress);
+    } else if (threadIdx.x == 32 && f.debug_fail) {
+      const unsigned long long half = (unsigned long long)(*f.total / 2);
+      if (wait_at_least(f.progress, half, f.fail)) atomicCAS(f.fail, 0, 1);
+    }
+    return;
+  }
+  const int t = threadIdx.x;
+  if ((int64_t)blockIdx.x <= f.nfill) {  // a fill block
+    __shared__ int s_go;
+    for (int64_t c = blockIdx.x - 1; c < f.ntiles; c += f.nfill) {
+      FillPrep prep;  // in flight during the wait
+      fill_prep(c, t, f.qv, f.meta, f.K, f.seg_base, f.thr_in, f.entry, f.entry_rec, prep);
+      if (t == 0)
+        s_go = wait_at_least(f.progress, (unsigned long long)(f.seg_base[c] + f.tile_nseg[c]),
+                             f.fail);
+      __syncthreads();
+      const int go = s_go;
+      if (go) fill_finish<T>(c, t, prep, f.seg_cap, f.m_in, dst, f.fail);
+      __threadfence();  // the tile's carries before its flag
+      __syncthreads();  // (also: s_go read by every thread)
+      if (t == 0) atomicExch(f.tile_done + c, 1u);
+      if (go) {  // the check of the tile's rises, off the fix-up's path
+        const int64_t r0 = f.seg_base[c], r1 = r0 + f.tile_nseg[c];
+        for (int64_t r = r0 + t; r < r1 && r < f.seg_cap; r += kCT)
+          verify_record<T>(f.segs, f.m_in, r, f.fail);
+      }
+    }
+    return;
+  }
+  const int64_t W = (int64_t)(gridDim.x - 1 - f.nfill) * (kCT / 32);
+  const int64_t w0 = (int64_t)(blockIdx.x - 1 - f.nfill) * (kCT / 32) + (t >> 5);
+  if (f.logB >= 3) fix_items<T, 1>(out, dst, f, w0, W);
+  else fix_items<T, 4>(out, dst, f, w0, W);
+}
+
+// The fix-up again after a failure (grid-stride; nothing to do otherwise).
+template <class T>
+__global__ void __launch_bounds__(256) fixup_again_kernel(T* out, const T* carries, int64_t n,
+                                                          int logB, const int* only_if) {
+  if (*only_if == 0) return;
+  const int64_t Bk = int64_t(1) << logB;
+  for (int64_t i = Bk + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    out[i] = add_rn(carries[(i >> logB) - 1], out[i]);
+}
+
 size_t r256(size_t v) { return (v + 255) & ~size_t(255); }
 
 }  // namespace
@@ -1127,6 +1469,7 @@ ChainPlan plan_chain(int64_t K) {
   p.thr_off = off; off += r256(p.ntiles * kCT * sizeof(Summ));
   p.lead_off = off; off += r256(p.ntiles * sizeof(Map));
   p.leadsteps_off = off; off += r256(p.ntiles * sizeof(int));
+  p.done_off = off; off += r256(p.ntiles * sizeof(unsigned));  // right after: one memset
   p.entry_off = off; off += r256(p.ntiles * sizeof(Map));
   p.entryrec_off = off; off += r256(p.ntiles * sizeof(int64_t));
   p.q_off = off; off += r256(K * sizeof(int64_t));
@@ -1140,63 +1483,176 @@ ChainPlan plan_chain(int64_t K) {
   return p;
 }
 
+namespace {
+
+// The chain's workspace, carved by the plan's offsets.
+struct ChainWs {
+  double *tsum, *toff, *tmax, *bound;
+  Summ* thr_in;
+  Map *lead, *entry;
+  int* lead_steps;
+  unsigned* done;
+  int64_t *entry_rec, *qv, *nseg, *segbase, *m_in, *total;
+  uint32_t* meta;
+  SegRec* segs;
+  int* fail;
+  unsigned long long* progress;
+  ChainWs(const ChainPlan& p, char* ws) {
+    tsum = reinterpret_cast<double*>(ws + p.tsum_off);
+    toff = reinterpret_cast<double*>(ws + p.toff_off);
+    tmax = reinterpret_cast<double*>(ws + p.tmax_off);
+    thr_in = reinterpret_cast<Summ*>(ws + p.thr_off);
+    lead = reinterpret_cast<Map*>(ws + p.lead_off);
+    lead_steps = reinterpret_cast<int*>(ws + p.leadsteps_off);
+    done = reinterpret_cast<unsigned*>(ws + p.done_off);
+    entry = reinterpret_cast<Map*>(ws + p.entry_off);
+    entry_rec = reinterpret_cast<int64_t*>(ws + p.entryrec_off);
+    qv = reinterpret_cast<int64_t*>(ws + p.q_off);
+    meta = reinterpret_cast<uint32_t*>(ws + p.meta_off);
+    nseg = reinterpret_cast<int64_t*>(ws + p.nseg_off);
+    segbase = reinterpret_cast<int64_t*>(ws + p.segbase_off);
+    segs = reinterpret_cast<SegRec*>(ws + p.segs_off);
+    m_in = reinterpret_cast<int64_t*>(ws + p.min_off);
+    bound = reinterpret_cast<double*>(ws + p.misc_off);
+    total = reinterpret_cast<int64_t*>(ws + p.misc_off + 8);
+    fail = reinterpret_cast<int*>(ws + p.misc_off + 16);
+    progress = reinterpret_cast<unsigned long long*>(ws + p.misc_off + 24);
+  }
+};
+
+// Passes 1 to 6: tile sums, offsets and bound, classification, record
+// numbering, segments, links.
 template <class T>
-cudaError_t run_chain(const ChainPlan& p, const T* src, T* dst, char* ws, cudaStream_t s,
-                      T* final_out) {
-  if (p.K <= 0) return cudaSuccess;
-  double* tsum = reinterpret_cast<double*>(ws + p.tsum_off);
-  double* toff = reinterpret_cast<double*>(ws + p.toff_off);
-  double* tmax = reinterpret_cast<double*>(ws + p.tmax_off);
-  Summ* thr_in = reinterpret_cast<Summ*>(ws + p.thr_off);
-  Map* lead = reinterpret_cast<Map*>(ws + p.lead_off);
-  int* lead_steps = reinterpret_cast<int*>(ws + p.leadsteps_off);
-  Map* entry = reinterpret_cast<Map*>(ws + p.entry_off);
-  int64_t* entry_rec = reinterpret_cast<int64_t*>(ws + p.entryrec_off);
-  int64_t* qv = reinterpret_cast<int64_t*>(ws + p.q_off);
-  uint32_t* meta = reinterpret_cast<uint32_t*>(ws + p.meta_off);
-  int64_t* nseg = reinterpret_cast<int64_t*>(ws + p.nseg_off);
-  int64_t* segbase = reinterpret_cast<int64_t*>(ws + p.segbase_off);
-  SegRec* segs = reinterpret_cast<SegRec*>(ws + p.segs_off);
-  int64_t* m_in = reinterpret_cast<int64_t*>(ws + p.min_off);
-  double* bound = reinterpret_cast<double*>(ws + p.misc_off);
-  int64_t* total = reinterpret_cast<int64_t*>(ws + p.misc_off + 8);
-  int* fail = reinterpret_cast<int*>(ws + p.misc_off + 16);
+cudaError_t run_chain_front(const ChainPlan& p, const T* src, char* ws, const ChainWs& w,
+                            cudaStream_t s) {
   cudaError_t e = cudaMemsetAsync(ws + p.misc_off, 0, 256, s);
   if (e != cudaSuccess) return e;
   // per-segment MAP step counts are accumulated with atomics: clear them
-  e = cudaMemsetAsync(segs, 0, (size_t)p.seg_cap * sizeof(SegRec), s);
+  e = cudaMemsetAsync(w.segs, 0, (size_t)p.seg_cap * sizeof(SegRec), s);
   if (e != cudaSuccess) return e;
-  e = cudaMemsetAsync(lead_steps, 0, (size_t)p.ntiles * sizeof(int), s);
+  // the lead step counts and the fused form's tile flags (adjacent)
+  e = cudaMemsetAsync(w.lead_steps, 0, p.done_off + r256(p.ntiles * sizeof(unsigned)) -
+                                           p.leadsteps_off, s);
   if (e != cudaSuccess) return e;
   if (p.ntiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const unsigned g = (unsigned)p.ntiles;
   CR_LAUNCH(kKChainTileSum, s,
-            chain_tile_sum_kernel<T><<<g, kCT, 0, s>>>(src, p.K, tsum, tmax));
+            chain_tile_sum_kernel<T><<<g, kCT, 0, s>>>(src, p.K, w.tsum, w.tmax));
   CR_LAUNCH(kKChainOffsets, s,
-            chain_offsets_kernel<<<1, 1024, 0, s>>>(tsum, tmax, p.ntiles, toff, bound));
+            chain_offsets_kernel<<<1, 1024, 0, s>>>(w.tsum, w.tmax, p.ntiles, w.toff, w.bound));
   CR_LAUNCH(kKChainClassify, s,
-            chain_classify_kernel<T><<<g, kCT, 0, s>>>(src, p.K, toff, bound, qv, meta, nseg,
-                                                       thr_in));
+            chain_classify_kernel<T><<<g, kCT, 0, s>>>(src, p.K, w.toff, w.bound, w.qv, w.meta,
+                                                       w.nseg, w.thr_in));
   CR_LAUNCH(kKChainOffsets, s,
-            exclusive_scan_1block<int64_t><<<1, 1024, 0, s>>>(nseg, segbase, p.ntiles, total));
+            exclusive_scan_1block<int64_t><<<1, 1024, 0, s>>>(w.nseg, w.segbase, p.ntiles,
+                                                              w.total));
   CR_LAUNCH(kKChainSegments, s,
-            chain_segments_kernel<T><<<g, kCT, 0, s>>>(src, qv, meta, p.K, segbase, thr_in, segs,
-                                                       p.seg_cap, lead, lead_steps, fail));
+            chain_segments_kernel<T><<<g, kCT, 0, s>>>(src, w.qv, w.meta, p.K, w.segbase,
+                                                       w.thr_in, w.segs, p.seg_cap, w.lead,
+                                                       w.lead_steps, w.fail));
   CR_LAUNCH(kKChainLink, s,
-            chain_link_kernel<<<1, 1024, 0, s>>>(nseg, segbase, p.ntiles, segs, p.seg_cap, lead,
-                                                 lead_steps, entry, entry_rec));
+            chain_link_kernel<<<1, 1024, 0, s>>>(w.nseg, w.segbase, p.ntiles, w.segs, p.seg_cap,
+                                                 w.lead, w.lead_steps, w.entry, w.entry_rec));
+  return cudaGetLastError();
+}
+
+// Co-resident blocks of the fused kernel on this device (cached per device).
+template <class T>
+int fused_grid_limit() {
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cache[dev] == 0) {
+    int per_sm = 0, sms = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, chain_walk_fix_kernel<T>, kCT,
+                                                      0) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return 0;
+    cache[dev] = per_sm * sms;
+  }
+  return cache[dev];
+}
+
+}  // namespace
+
+template <class T>
+cudaError_t run_chain(const ChainPlan& p, const T* src, T* dst, char* ws, cudaStream_t s,
+                      T* final_out) {
+  if (p.K <= 0) return cudaSuccess;
+  const ChainWs w(p, ws);
+  cudaError_t e = run_chain_front<T>(p, src, ws, w, s);
+  if (e != cudaSuccess) return e;
+  const unsigned g = (unsigned)p.ntiles;
   CR_LAUNCH(kKChainWalk, s,
-            chain_walk_kernel<T><<<1, 32, 0, s>>>(src, dst, segs, total, p.seg_cap, m_in, fail,
-                                                  meta, p.K, final_out));
+            chain_walk_kernel<T><<<1, 32, 0, s>>>(src, dst, w.segs, w.total, p.seg_cap, w.m_in,
+                                                  w.fail, w.meta, p.K, final_out));
   if ((p.seg_cap + 255) / 256 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   CR_LAUNCH(kKChainVerify, s,
             chain_verify_kernel<T><<<(unsigned)((p.seg_cap + 255) / 256), 256, 0, s>>>(
-                segs, total, p.seg_cap, m_in, fail));
+                w.segs, w.total, p.seg_cap, w.m_in, w.fail));
   CR_LAUNCH(kKChainFill, s,
-            chain_fill_kernel<T><<<g, kCT, 0, s>>>(qv, meta, p.K, segbase, thr_in, entry,
-                                                   entry_rec, p.seg_cap, m_in, dst, fail));
+            chain_fill_kernel<T><<<g, kCT, 0, s>>>(w.qv, w.meta, p.K, w.segbase, w.thr_in,
+                                                   w.entry, w.entry_rec, p.seg_cap, w.m_in, dst,
+                                                   w.fail));
   CR_LAUNCH(kKChainFallback, s,
-            chain_serial_kernel<T><<<1, 32, 0, s>>>(src, dst, p.K, fail, final_out));
+            chain_serial_kernel<T><<<1, 32, 0, s>>>(src, dst, p.K, w.fail, final_out));
+  return cudaGetLastError();
+}
+
+template <class T>
+cudaError_t run_chain_fixup(const ChainPlan& p, const T* src, T* dst, char* ws, T* out,
+                            int64_t n, int logB, cudaStream_t s, const int** fail,
+                            bool debug_fail) {
+  const ChainWs w(p, ws);
+  *fail = w.fail;
+  if (p.K <= 0 || p.K > kMaxFusedChain || logB < 1 || logB > 40) return cudaErrorInvalidValue;
+  cudaError_t e = run_chain_front<T>(p, src, ws, w, s);
+  if (e != cudaSuccess) return e;
+  FusedArgs f{};
+  f.segs = w.segs;
+  f.total = w.total;
+  f.seg_cap = p.seg_cap;
+  f.m_in = w.m_in;
+  f.fail = w.fail;
+  f.meta = w.meta;
+  f.qv = w.qv;
+  f.K = p.K;
+  f.ntiles = p.ntiles;
+  f.seg_base = w.segbase;
+  f.tile_nseg = w.nseg;
+  f.thr_in = w.thr_in;
+  f.entry = w.entry;
+  f.entry_rec = w.entry_rec;
+  f.progress = w.progress;
+  f.tile_done = w.done;
+  f.n = n;
+  f.logB = logB;
+  f.debug_fail = debug_fail ? 1 : 0;
+  f.nitems = (n + kFixItem - 1) / kFixItem;
+  const int limit = fused_grid_limit<T>();
+  // fill blocks: enough for the fills to keep pace with the walk, and at
+  // least three quarters of the grid left for the fix-up
+  f.nfill = p.ntiles < kMaxFillBlocks ? p.ntiles : kMaxFillBlocks;
+  if (f.nfill > limit / CR_FUSED_FILL_DIV) f.nfill = limit / CR_FUSED_FILL_DIV;
+  if (f.nfill < 1) return cudaErrorInvalidConfiguration;
+  const int64_t fixers = (f.nitems + kCT / 32 - 1) / (kCT / 32);  // 8 warps a block
+  const int64_t room = limit - 1 - f.nfill;
+  const unsigned grid = (unsigned)(1 + f.nfill + (fixers < room ? fixers : room));
+  void* args[] = {(void*)&src, (void*)&dst, (void*)&out, (void*)&f};
+  CR_LAUNCH(kKChainWalkFix, s,
+            e = cudaLaunchCooperativeKernel((const void*)chain_walk_fix_kernel<T>, dim3(grid),
+                                            dim3(kCT), args, 0, s));
+  if (e != cudaSuccess) return e;
+  CR_LAUNCH(kKChainFallback, s,
+            chain_serial_kernel<T><<<1, 32, 0, s>>>(src, dst, p.K, w.fail, nullptr));
+  return cudaGetLastError();
+}
+
+template <class T>
+cudaError_t run_fixup_again(T* out, const T* carries, int64_t n, int logB, const int* fail,
+                            cudaStream_t s) {
+  CR_LAUNCH(kKFixupAgain, s,
+            fixup_again_kernel<T><<<1216, 256, 0, s>>>(out, carries, n, logB, fail));
   return cudaGetLastError();
 }
 
@@ -1214,6 +1670,16 @@ template cudaError_t run_serial_chain<float>(const float*, float*, int64_t, cuda
                                              float*);
 template cudaError_t run_chain<double>(const ChainPlan&, const double*, double*, char*,
                                        cudaStream_t, double*);
+template cudaError_t run_chain_fixup<double>(const ChainPlan&, const double*, double*, char*,
+                                             double*, int64_t, int, cudaStream_t, const int**,
+                                             bool);
+template cudaError_t run_chain_fixup<float>(const ChainPlan&, const float*, float*, char*,
+                                            float*, int64_t, int, cudaStream_t, const int**,
+                                            bool);
+template cudaError_t run_fixup_again<double>(double*, const double*, int64_t, int, const int*,
+                                             cudaStream_t);
+template cudaError_t run_fixup_again<float>(float*, const float*, int64_t, int, const int*,
+                                            cudaStream_t);
 template cudaError_t run_chain<float>(const ChainPlan&, const float*, float*, char*,
                                       cudaStream_t, float*);
 

@@ -11,7 +11,7 @@ namespace cr {
 struct ChainPlan {
   int64_t K = 0, ntiles = 0, seg_cap = 0;
   size_t tsum_off = 0, toff_off = 0, tmax_off = 0, thr_off = 0, lead_off = 0,
-         leadsteps_off = 0, entry_off = 0, entryrec_off = 0, q_off = 0, meta_off = 0,
+         leadsteps_off = 0, done_off = 0, entry_off = 0, entryrec_off = 0, q_off = 0, meta_off = 0,
          nseg_off = 0, segbase_off = 0, segs_off = 0, min_off = 0, misc_off = 0;
   size_t bytes = 0;  // workspace bytes (offsets are relative to the chain's base)
 };
@@ -33,6 +33,27 @@ cudaError_t run_chain(const ChainPlan& plan, const T* src, T* dst, char* ws, cud
 template <class T>
 cudaError_t run_serial_chain(const T* src, T* dst, int64_t K, cudaStream_t s,
                              T* final_out = nullptr);
+
+// The block carries fused with a block scan's fix-up: dst[k] = C_k for
+// k < K as run_chain (src: the K block totals of which the chain folds the
+// first K, dst: K carries) and out[i] = dst[(i >> logB) - 1] op out[i] for
+// 2^logB <= i < n, the fix-up running behind the chain's evaluation. On any
+// failure of the parallel evaluation *fail (device) is set and out is left
+// partly fixed; the serial chain has then rewritten dst, and the caller
+// recomputes out's local values and calls run_fixup_again (both conditional
+// on *fail, so nothing runs when it is clear). Chains longer than
+// kMaxFusedChain are not accepted (their walk could outlast the waits'
+// time limit).
+// debug_fail: a test hook; a second warp of the walking block sets *fail
+// once the walk is half-way, so that the recovery runs.
+template <class T>
+cudaError_t run_chain_fixup(const ChainPlan& plan, const T* src, T* dst, char* ws, T* out,
+                            int64_t n, int logB, cudaStream_t s, const int** fail,
+                            bool debug_fail = false);
+template <class T>
+cudaError_t run_fixup_again(T* out, const T* carries, int64_t n, int logB, const int* fail,
+                            cudaStream_t s);
+constexpr int64_t kMaxFusedChain = int64_t(1) << 26;
 
 // Longest binary32 chain the parallel evaluation is used for (K ulp must stay
 // small against the chain's values for its binade tests to be decisive).

@@ -44,7 +44,8 @@ const char* kernel_name(int id) {
       "scan_local_kernel",     "carry_fixup_kernel",    "scan_pairwise_kernel",
       "apply_init_kernel",     "fill_init_kernel",      "carry_fixup_shift_kernel",
       "scan_seq_block_kernel", "row_reduce_kernel",
-      "chain_link_kernel",     "chain_verify_kernel"};
+      "chain_link_kernel",     "chain_verify_kernel",   "chain_walk_fix_kernel",
+      "scan_local_again_kernel", "fixup_again_kernel"};
   return (id >= 0 && id < kKernelCount) ? names[id] : "unknown";
 }
 

@@ -36,6 +36,9 @@ enum KernelId : int {
   kKRowReduce,
   kKChainLink,
   kKChainVerify,
+  kKChainWalkFix,
+  kKScanLocalAgain,
+  kKFixupAgain,
   kKernelCount
 };
 

@@ -73,6 +73,14 @@ bool scan_args_ok(cr_policy p, int64_t B);
 // CR_ERR_TIMEOUT (-1 = off).
 int64_t debug_skip_publish();
 void set_debug_skip_publish(int64_t tile);
+// Test hook for the fused carry fix-up: 0 fused where it is used by default
+// (B <= 16), 1 the separate chain and fix-up passes, 2 fused for every B
+// with a failure raised half-way through the walk (the recovery passes then
+// run), 3 fused for every B.
+bool fused_fixup_disabled();
+bool debug_fused_fail();
+bool fused_fixup_forced();
+void set_debug_fused_mode(int mode);
 // out_mode: 0 inclusive, CR_EXCLUSIVE or CR_INCLUDE_INITIAL.
 ScanPlan plan_scan(int64_t batch, int64_t n, cr_policy p, int64_t B, size_t esize,
                    int out_mode = 0);
