@@ -1190,6 +1190,31 @@ struct Tiled {
     if (plan.parallel_chain) return run_chain<T>(plan.chain, src, carries, ws + plan.chain_ws, s);
     return run_serial_chain<T>(src, carries, plan.K - 1, s);
   }
+  // The carries C_k of the blocks whose elements lie in [e0, e1) (tile-
+  // aligned, B <= 2048), after those of every earlier block: a segment of
+  // the fold continued from C_{kb-1}, which replaces T_{kb-1} in the totals
+  // (no longer read: its own segment has run) so that the segment's first
+  // step reproduces it. Local + fix-up mode only.
+  cudaError_t middle_segment(int64_t e0, int64_t e1, cudaStream_t s) {
+    const int64_t kb = e0 >> plan.logB;
+    int64_t ke = (e1 + plan.B - 1) >> plan.logB;  // blocks [kb, ke) start in the range
+    if (ke > plan.K - 1) ke = plan.K - 1;         // C_{K-1} is not needed
+    if (ke <= kb) return cudaSuccess;
+    const int64_t first = kb > 0 ? kb - 1 : 0;    // the segment starts at C_{kb-1}
+    const int64_t len = ke - first;
+    cudaError_t e;
+    if (kb > 0 && (e = cudaMemcpyAsync(totals + first, carries + first, sizeof(T),
+                                       cudaMemcpyDeviceToDevice, s)) != cudaSuccess)
+      return e;
+    if (len < 2) return cudaSuccess;
+    const bool par = plan.parallel_chain && len >= kParallelChainMin &&
+                     (sizeof(T) == 8 || len <= kMaxParallelChainF32);
+    if (par) {
+      const ChainPlan cp = plan_chain(len);  // no larger than the whole chain's
+      return run_chain<T>(cp, totals + first, carries + first, ws + plan.chain_ws, s);
+    }
+    return run_serial_chain<T>(totals + first, carries + first, len, s);
+  }
   // The carries and the fix-up in one cooperative pass (inclusive local +
   // fix-up scans with the parallel chain; out != x, for the recovery
   // recomputes the local pass from x).
@@ -1397,6 +1422,37 @@ cudaError_t run_scan_host(const ScanPlan& plan, const T* x_host, T* out_host, T*
     e0 = t0 * kTile;
     e1 = t1 * kTile < plan.n ? t1 * kTile : plan.n;
   };
+  if (plan.mode == ScanPlan::kLocalFixup && nchunks > 1 && plan.K >= 2) {
+    // block_dyadic, B <= 2048: blocks do not straddle chunks (tile-aligned)
+    // and C_k depends on T_0 .. T_k only, so the carries are folded chunk by
+    // chunk (each segment continued from the last carry of the one before)
+    // and every chunk is fixed up and copied out as soon as its carries
+    // exist: the copies out overlap the copies in.
+    for (int64_t c = 0; c < nchunks; ++c) {
+      int64_t t0, t1, e0, e1;
+      range(c, t0, t1, e0, e1);
+      if ((e = cudaMemcpyAsync(x_dev + e0, x_host + e0, (size_t)(e1 - e0) * sizeof(T),
+                               cudaMemcpyHostToDevice, cin)) != cudaSuccess)
+        return e;
+      if ((e = cudaEventRecord(hp.ev_in[c], cin)) != cudaSuccess) return e;
+    }
+    for (int64_t c = 0; c < nchunks; ++c) {
+      int64_t t0, t1, e0, e1;
+      range(c, t0, t1, e0, e1);
+      if ((e = cudaStreamWaitEvent(s, hp.ev_in[c], 0)) != cudaSuccess) return e;
+      if ((e = tc.first(x_dev, out_dev, t0, t1, s)) != cudaSuccess) return e;
+      if ((e = tc.middle_segment(e0, e1, s)) != cudaSuccess) return e;
+      if ((e = tc.second(x_dev, out_dev, t0, t1, s)) != cudaSuccess) return e;
+      if ((e = cudaEventRecord(hp.ev_out[c], s)) != cudaSuccess) return e;
+      if ((e = cudaStreamWaitEvent(cout, hp.ev_out[c], 0)) != cudaSuccess) return e;
+      if ((e = cudaMemcpyAsync(out_host + e0, out_dev + e0, (size_t)(e1 - e0) * sizeof(T),
+                               cudaMemcpyDeviceToHost, cout)) != cudaSuccess)
+        return e;
+    }
+    if ((e = cudaStreamSynchronize(cout)) != cudaSuccess) return e;
+    if ((e = cudaStreamSynchronize(cin)) != cudaSuccess) return e;
+    return cudaStreamSynchronize(s);
+  }
   for (int64_t c = 0; c < nchunks; ++c) {  // copy in, first pass per chunk
     int64_t t0, t1, e0, e1;
     range(c, t0, t1, e0, e1);

@@ -1,5 +1,6 @@
 """Host-buffer forms (cr_inclusive_scan_host, cr_reduce_host): inputs and
-outputs in host memory, copies pipelined with the passes in chunks of tiles.
+outputs in host memory, copies pipelined with the passes in chunks of tiles
+(block_dyadic with B <= 2048: the carries folded chunk by chunk too).
 0 ULP against the oracle for every policy and kernel path, chunk-boundary
 sizes, page-locked and pageable host memory, and the benchmark size."""
 import numpy as np
@@ -45,6 +46,24 @@ def test_scan_host_pageable_and_out(scr):
     out = torch.empty(x.size, dtype=torch.float64)  # pageable output
     scr.inclusive_scan(torch.from_numpy(x).pin_memory(), "block_dyadic", 16, out=out)
     assert bits(out.numpy()) == bits(want)
+
+
+@pytest.mark.parametrize("B", [2, 16, 256, 2048])
+def test_scan_host_chunked_carries(scr, B):
+    """block_dyadic (B <= 2048) from host buffers folds the carries chunk by
+    chunk, each segment continued from the previous one's last carry, so
+    that chunks are copied out while later ones are copied in: the chain's
+    stress families at chunk-edge sizes (3 whole chunks; a last chunk of one
+    or two blocks; 8 chunks with a ragged last tile)."""
+    from tests.test_gpu_chain import CASES
+    for case in ("wide_exponents", "cancel_to_zero", "big_then_small", "halves_ties"):
+        for n in (2048 * 256 * 3, 2048 * 256 * 3 + B + 1, 2048 * 2100 - 1):
+            x = np.ascontiguousarray(CASES[case](n, np.float64))
+            got = scr.inclusive_scan(torch.from_numpy(x).pin_memory(), "block_dyadic", B).numpy()
+            want = oracle.scan(x, "block_dyadic", B)
+            gn, wn = np.isnan(got), np.isnan(want)
+            bad = ((got.view(np.uint64) != want.view(np.uint64)) & ~(gn & wn)) | (gn != wn)
+            assert not bad.any(), (case, n, int(np.argmax(bad)))
 
 
 @pytest.mark.parametrize("policy,B", [("iterated_pairwise", 1), ("block_dyadic", 16),
