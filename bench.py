@@ -487,14 +487,18 @@ def run_e2e(args, scr, torch, dev, hin, rows, world, dist):
             else:
                 scr.inclusive_scan_batched(h5, p["policy"], p["B"], dim=0)
 
-    step()
+    for _ in range(max(1, args.warmup)):  # allocations, page-locked buffers, plans
+        step()
     torch.cuda.synchronize(dev)
     if dist:
         dist.barrier()
+    steps = max(1, min(args.steps, 5))
+    step_ms = []
     t = time.perf_counter()
-    steps = max(1, min(args.steps, 3))
     for _ in range(steps):
-        step()
+        t1 = time.perf_counter()
+        step()  # every call returns host data: the step ends synchronised
+        step_ms.append(round((time.perf_counter() - t1) * 1e3, 2))
     torch.cuda.synchronize(dev)
     sec = time.perf_counter() - t
     if dist:
@@ -503,7 +507,8 @@ def run_e2e(args, scr, torch, dev, hin, rows, world, dist):
         sec = float(tt.item())
     step_bytes = sum(r[3] for r in rows)
     return {"value": round(step_bytes * steps * world / sec / 1e9, 2), "unit": "GB/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "step_ms": step_ms}
 
 
 # ------------------------------------------------------- oracle (CPU) leg

@@ -89,25 +89,49 @@ lane_pass_kernel(const T* __restrict__ in_base, int64_t in_seg, int64_t in_row,
     const T* p = in_base + b * in_seg + run0 * in_row + j * in_lane;
     int64_t k = 0;
     constexpr int VW = 16 / sizeof(T);  // elements per 16-byte vector
+    // blocks of U rows, the next block's loads in flight while the current
+    // block's tree is built (two register buffers)
     if (kContig && U % VW == 0 && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
       // one lane (L = 1 and the lane-result passes): the run is contiguous
-      for (; k + U <= cnt; k += U) {
-        T v[U];
-        const uint4* q = reinterpret_cast<const uint4*>(p + k);
+      auto load = [&](T (&v)[U], int64_t k0) {
+        const uint4* q = reinterpret_cast<const uint4*>(p + k0);
 #pragma unroll
         for (int u = 0; u < U / VW; ++u) {
           const uint4 d = __ldg(q + u);
 #pragma unroll
           for (int e = 0; e < VW; ++e) v[u * VW + e] = reinterpret_cast<const T*>(&d)[e];
         }
+      };
+      if (k + U <= cnt) {
+        T v[U];
+        load(v, k);
+        for (; k + 2 * U <= cnt; k += U) {
+          T w[U];
+          load(w, k + U);
+          st.push(perfect_tree<T, U>(v), LOGU);
+#pragma unroll
+          for (int u = 0; u < U; ++u) v[u] = w[u];
+        }
         st.push(perfect_tree<T, U>(v), LOGU);
+        k += U;
       }
     }
-    for (; k + U <= cnt; k += U) {
-      T v[U];
+    if (k + U <= cnt) {
+      auto load = [&](T (&v)[U], int64_t k0) {
 #pragma unroll
-      for (int u = 0; u < U; ++u) v[u] = ldg(p + (k + u) * in_row);
+        for (int u = 0; u < U; ++u) v[u] = ldg(p + (k0 + u) * in_row);
+      };
+      T v[U];
+      load(v, k);
+      for (; k + 2 * U <= cnt; k += U) {
+        T w[U];
+        load(w, k + U);
+        st.push(perfect_tree<T, U>(v), LOGU);
+#pragma unroll
+        for (int u = 0; u < U; ++u) v[u] = w[u];
+      }
       st.push(perfect_tree<T, U>(v), LOGU);
+      k += U;
     }
     for (; k < cnt; ++k) st.push(ldg(p + k * in_row), 0);
   }
