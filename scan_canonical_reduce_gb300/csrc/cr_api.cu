@@ -246,13 +246,26 @@ cr_status cr_reduce_host(const void* x_host, int64_t n, int32_t L, const void* i
   if (ws_ok != CR_OK) return ws_ok;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   char* base = static_cast<char*>(dev_buf);
-  if (n > 0 && cudaMemcpyAsync(base, x_host, (size_t)n * sz, cudaMemcpyHostToDevice, s) !=
-                   cudaSuccess)
-    return CR_ERR_CUDA;
-  const cr_status st = reduce_impl(n > 0 ? base : nullptr, base + arr, 1, n, 1, n, L, init_host,
-                                   dt, base + arr + 256, dev_bytes - arr - 256, stream);
-  if (st != CR_OK) return st;
-  if (cudaMemcpyAsync(out_host, base + arr, sz, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+  char* out_dev = base + arr;
+  char* ws = base + arr + 256;
+  const cr::ReducePlan plan = cr::plan_reduce(1, n, L, 1, n, sz);
+  if (clear_status(ws, s) != cudaSuccess) return CR_ERR_CUDA;
+  cudaError_t e;
+  if (dt == CR_F64) {
+    double init;
+    std::memcpy(&init, init_host, sizeof(init));
+    e = cr::run_reduce_host<double>(plan, static_cast<const double*>(x_host),
+                                    reinterpret_cast<double*>(base),
+                                    reinterpret_cast<double*>(out_dev), init, ws, s, n);
+  } else {
+    float init;
+    std::memcpy(&init, init_host, sizeof(init));
+    e = cr::run_reduce_host<float>(plan, static_cast<const float*>(x_host),
+                                   reinterpret_cast<float*>(base),
+                                   reinterpret_cast<float*>(out_dev), init, ws, s, n);
+  }
+  if (e != cudaSuccess) return CR_ERR_CUDA;
+  if (cudaMemcpyAsync(out_host, out_dev, sz, cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return CR_ERR_CUDA;
   return cudaStreamSynchronize(s) == cudaSuccess ? CR_OK : CR_ERR_CUDA;
 }

@@ -34,6 +34,36 @@ cudaEvent_t take_event() {
 
 }  // namespace
 
+cudaError_t HostPipe::ensure(int chunks) {
+  cudaError_t e;
+  if (in == nullptr) {
+    if ((e = cudaStreamCreateWithFlags(&in, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaStreamCreateWithFlags(&out, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&start, cudaEventDisableTiming)) != cudaSuccess) return e;
+  }
+  while ((int)ev_in.size() < chunks) {
+    cudaEvent_t a, b;
+    if ((e = cudaEventCreateWithFlags(&a, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&b, cudaEventDisableTiming)) != cudaSuccess) return e;
+    ev_in.push_back(a);
+    ev_out.push_back(b);
+  }
+  return cudaSuccess;
+}
+
+namespace {
+std::mutex g_pipe_mu;
+HostPipe g_pipes[64];
+}  // namespace
+
+std::mutex& host_pipe_mutex() { return g_pipe_mu; }
+
+HostPipe& host_pipe() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return g_pipes[(dev >= 0 && dev < 64) ? dev : 0];
+}
+
 const char* kernel_name(int id) {
   static const char* names[kKernelCount] = {
       "lane_pass_kernel",      "write_init_kernel",     "scan_up_kernel",

@@ -5,6 +5,8 @@
 #pragma once
 
 #include <cstdint>
+#include <mutex>
+#include <vector>
 
 #include <cuda_runtime.h>
 
@@ -51,6 +53,18 @@ struct LaunchScope {
   cudaStream_t stream;
   int slot;
 };
+
+// Streams and events of the host-buffer pipelines (copies in and out
+// overlapped with the passes), one set per device, created on first use and
+// kept. A call holds host_pipe_mutex() for its whole duration.
+struct HostPipe {
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr;
+  std::vector<cudaEvent_t> ev_in, ev_out;
+  cudaError_t ensure(int chunks);  // streams, and at least `chunks` event pairs
+};
+std::mutex& host_pipe_mutex();
+HostPipe& host_pipe();  // the current device's
 
 // Usage: CR_LAUNCH(kKScanUp, stream, kernel<<<grid, block, 0, stream>>>(...));
 #define CR_LAUNCH(ID, STREAM, ...)                  \

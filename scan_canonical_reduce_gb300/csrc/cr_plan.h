@@ -40,6 +40,7 @@ struct PassArgs {
   int32_t final_pass;    // everything left is tail; no next level
   int32_t fuse_cross;    // final pass also does the cross-lane tree and init
   int32_t first_level;   // no lane accumulator yet
+  int64_t item_base;     // first work item of this launch (leaf items, then tail)
 };
 
 struct PassPlan {
@@ -67,5 +68,13 @@ ReducePlan plan_reduce(int64_t batch, int64_t n, int64_t L, int64_t elem_stride,
 template <class T>
 cudaError_t run_reduce(const ReducePlan& plan, const T* x, T* out, T init, char* ws,
                        cudaStream_t s);
+
+// The same from a host buffer x_host (n elements, page-locked for overlap):
+// copied into x_dev in groups of the first pass's chunks on the host
+// pipeline's copy stream, each group reduced as soon as it has arrived.
+// out (device) is written on s; the caller copies it back and synchronises.
+template <class T>
+cudaError_t run_reduce_host(const ReducePlan& plan, const T* x_host, T* x_dev, T* out, T init,
+                            char* ws, cudaStream_t s, int64_t n);
 
 }  // namespace cr

@@ -55,7 +55,7 @@ lane_pass_kernel(const T* __restrict__ in_base, int64_t in_seg, int64_t in_row,
   const int jl = tid % a.W;
   const int g = tid / a.W;
 
-  int64_t item = blockIdx.x;
+  int64_t item = a.item_base + blockIdx.x;
   const bool leaf = item < a.n_leaf_items;
   int64_t b, c;
   int w;
@@ -417,6 +417,37 @@ ReducePlan plan_reduce(int64_t batch, int64_t n, int64_t L, int64_t elem_stride,
   return plan;
 }
 
+// Items [i0, i1) of one pass (leaf items first, then the tail items).
+template <class T>
+cudaError_t launch_pass(const PassPlan& pp, const T* x, T* out, T init, char* ws,
+                        cudaStream_t s, int64_t i0, int64_t i1) {
+  if (i1 <= i0) return cudaSuccess;
+  const T* in_base = pp.in.in_ws ? reinterpret_cast<const T*>(ws + pp.in.ws_off) : x;
+  T* next = pp.a.final_pass ? nullptr : reinterpret_cast<T*>(ws + pp.next_off);
+  T* acc = reinterpret_cast<T*>(ws + pp.acc_off);
+  int* has = reinterpret_cast<int*>(ws + pp.has_off);
+  if (i1 - i0 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  PassArgs a = pp.a;
+  a.item_base = i0;
+  const unsigned grid = (unsigned)(i1 - i0);
+  // runs shorter than 16 rows use smaller register blocks; one-lane passes
+  // (contiguous runs, 16-byte aligned) load with vector accesses
+  const bool contig = pp.in.row == 1 && (reinterpret_cast<uintptr_t>(in_base) & 15) == 0 &&
+                      (pp.in.seg * (int64_t)sizeof(T)) % 16 == 0;
+#define CR_LANE(UU, CC)                                                                   \
+  CR_LAUNCH(kKLanePass, s,                                                                \
+            (lane_pass_kernel<T, UU, CC><<<grid, kThreads, 0, s>>>(                       \
+                in_base, pp.in.seg, pp.in.row, pp.in.lane, next, acc, has, out, init, a)))
+  if (pp.a.P >= 16) {
+    if (contig) CR_LANE(16, true);
+    else CR_LANE(16, false);
+  } else {
+    CR_LANE(4, false);
+  }
+#undef CR_LANE
+  return cudaGetLastError();
+}
+
 template <class T>
 cudaError_t run_reduce(const ReducePlan& plan, const T* x, T* out, T init, char* ws,
                        cudaStream_t s) {
@@ -443,28 +474,54 @@ cudaError_t run_reduce(const ReducePlan& plan, const T* x, T* out, T init, char*
     return cudaGetLastError();
   }
   for (const PassPlan& pp : plan.passes) {
-    const T* in_base = pp.in.in_ws ? reinterpret_cast<const T*>(ws + pp.in.ws_off) : x;
-    T* next = pp.a.final_pass ? nullptr : reinterpret_cast<T*>(ws + pp.next_off);
-    T* acc = reinterpret_cast<T*>(ws + pp.acc_off);
-    int* has = reinterpret_cast<int*>(ws + pp.has_off);
-    if (pp.grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    // runs shorter than 16 rows use smaller register blocks; one-lane passes
-    // (contiguous runs, 16-byte aligned) load with vector accesses
-    const bool contig = pp.in.row == 1 && (reinterpret_cast<uintptr_t>(in_base) & 15) == 0 &&
-                        (pp.in.seg * (int64_t)sizeof(T)) % 16 == 0;
-#define CR_LANE(UU, CC)                                                                   \
-  CR_LAUNCH(kKLanePass, s,                                                                \
-            (lane_pass_kernel<T, UU, CC><<<(unsigned)pp.grid, kThreads, 0, s>>>(          \
-                in_base, pp.in.seg, pp.in.row, pp.in.lane, next, acc, has, out, init, pp.a)))
-    if (pp.a.P >= 16) {
-      if (contig) CR_LANE(16, true);
-      else CR_LANE(16, false);
-    } else {
-      CR_LANE(4, false);
-    }
-#undef CR_LANE
-    const cudaError_t e = cudaGetLastError();
+    const cudaError_t e = launch_pass<T>(pp, x, out, init, ws, s, 0, pp.grid);
     if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+template <class T>
+cudaError_t run_reduce_host(const ReducePlan& plan, const T* x_host, T* x_dev, T* out, T init,
+                            char* ws, cudaStream_t s, int64_t n) {
+  cudaError_t e;
+  const bool chunked = plan.batch == 1 && !plan.rows_lv && !plan.passes.empty() &&
+                       !plan.passes[0].a.final_pass && plan.passes[0].a.C >= 16;
+  if (!chunked) {  // one copy, then the passes
+    if (n > 0 && (e = cudaMemcpyAsync(x_dev, x_host, (size_t)n * sizeof(T),
+                                      cudaMemcpyHostToDevice, s)) != cudaSuccess)
+      return e;
+    return run_reduce<T>(plan, x_dev, out, init, ws, s);
+  }
+  // The first pass's leaf items reduce chunks of T rows of L consecutive
+  // elements each, independently: the chunks are copied in groups on the
+  // copy stream and each group's leaf items run once it has arrived; the
+  // tail items, which read the rows after the last chunk, and the later
+  // passes follow the last copy.
+  const PassPlan& p0 = plan.passes[0];
+  const int64_t C = p0.a.C, tiles = p0.a.tiles, per_chunk = p0.a.T * p0.a.L;
+  const int groups = C < 8 ? (int)C : 8;
+  std::lock_guard<std::mutex> lock(host_pipe_mutex());
+  HostPipe& hp = host_pipe();
+  if ((e = hp.ensure(groups + 1)) != cudaSuccess) return e;
+  if ((e = cudaEventRecord(hp.start, s)) != cudaSuccess) return e;  // after the caller's work
+  if ((e = cudaStreamWaitEvent(hp.in, hp.start, 0)) != cudaSuccess) return e;
+  for (int g = 0; g <= groups; ++g) {
+    const int64_t e0 = g < groups ? (C * g / groups) * per_chunk : C * per_chunk;
+    const int64_t e1 = g < groups ? (C * (g + 1) / groups) * per_chunk : n;
+    if (e1 > e0 && (e = cudaMemcpyAsync(x_dev + e0, x_host + e0, (size_t)(e1 - e0) * sizeof(T),
+                                        cudaMemcpyHostToDevice, hp.in)) != cudaSuccess)
+      return e;
+    if ((e = cudaEventRecord(hp.ev_in[g], hp.in)) != cudaSuccess) return e;
+  }
+  for (int g = 0; g <= groups; ++g) {
+    if ((e = cudaStreamWaitEvent(s, hp.ev_in[g], 0)) != cudaSuccess) return e;
+    const int64_t i0 = g < groups ? (C * g / groups) * tiles : C * tiles;
+    const int64_t i1 = g < groups ? (C * (g + 1) / groups) * tiles : p0.grid;
+    if ((e = launch_pass<T>(p0, x_dev, out, init, ws, s, i0, i1)) != cudaSuccess) return e;
+  }
+  for (size_t k = 1; k < plan.passes.size(); ++k) {
+    const PassPlan& pp = plan.passes[k];
+    if ((e = launch_pass<T>(pp, x_dev, out, init, ws, s, 0, pp.grid)) != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
@@ -473,5 +530,9 @@ template cudaError_t run_reduce<double>(const ReducePlan&, const double*, double
                                         char*, cudaStream_t);
 template cudaError_t run_reduce<float>(const ReducePlan&, const float*, float*, float, char*,
                                        cudaStream_t);
+template cudaError_t run_reduce_host<double>(const ReducePlan&, const double*, double*, double*,
+                                             double, char*, cudaStream_t, int64_t);
+template cudaError_t run_reduce_host<float>(const ReducePlan&, const float*, float*, float*,
+                                            float, char*, cudaStream_t, int64_t);
 
 }  // namespace cr

@@ -1049,40 +1049,6 @@ ScanPlan plan_scan(int64_t batch, int64_t n, cr_policy p, int64_t B, size_t esiz
   return plan;
 }
 
-// Streams and events of the host-buffer pipeline, one set per device,
-// created on first use and kept.
-struct HostPipe {
-  cudaStream_t in = nullptr, out = nullptr;
-  cudaEvent_t start = nullptr;
-  std::vector<cudaEvent_t> ev_in, ev_out;
-  cudaError_t ensure(int chunks) {
-    cudaError_t e;
-    if (in == nullptr) {
-      if ((e = cudaStreamCreateWithFlags(&in, cudaStreamNonBlocking)) != cudaSuccess) return e;
-      if ((e = cudaStreamCreateWithFlags(&out, cudaStreamNonBlocking)) != cudaSuccess) return e;
-      if ((e = cudaEventCreateWithFlags(&start, cudaEventDisableTiming)) != cudaSuccess) return e;
-    }
-    while ((int)ev_in.size() < chunks) {
-      cudaEvent_t a, b;
-      if ((e = cudaEventCreateWithFlags(&a, cudaEventDisableTiming)) != cudaSuccess) return e;
-      if ((e = cudaEventCreateWithFlags(&b, cudaEventDisableTiming)) != cudaSuccess) return e;
-      ev_in.push_back(a);
-      ev_out.push_back(b);
-    }
-    return cudaSuccess;
-  }
-};
-namespace {
-std::mutex g_pipe_mu;
-HostPipe g_pipes[64];
-}
-// The device's pipeline (callers hold g_pipe_mu for the whole call).
-HostPipe& host_pipe() {
-  int dev = 0;
-  cudaGetDevice(&dev);
-  return g_pipes[(dev >= 0 && dev < 64) ? dev : 0];
-}
-
 template <class T>
 cudaError_t launch_fixup(const ScanPlan& plan, T* out, const T* carries, int64_t start,
                          int64_t end, cudaStream_t s);
@@ -1406,7 +1372,7 @@ cudaError_t run_scan_host(const ScanPlan& plan, const T* x_host, T* out_host, T*
   int64_t per = (tiles + 7) / 8;
   if (per < 256) per = 256;
   const int64_t nchunks = (tiles + per - 1) / per;
-  std::lock_guard<std::mutex> lock(g_pipe_mu);  // host-buffer calls share the streams
+  std::lock_guard<std::mutex> lock(host_pipe_mutex());  // host-buffer calls share the streams
   HostPipe& hp = host_pipe();
   if ((e = hp.ensure((int)nchunks)) != cudaSuccess) return e;
   cudaStream_t cin = hp.in, cout = hp.out;

@@ -82,3 +82,22 @@ def test_reduce_host(scr, dtype):
             got = scr.reduce(torch.from_numpy(x).pin_memory(), L, 0.5)
             assert not got.is_cuda
             assert bits(got.numpy()[0]) == bits(oracle.reduce(x, L, dtype(0.5))), (n, L)
+
+
+@pytest.mark.parametrize("L", [1, 3, 16, 128, 1024, 5000])
+def test_reduce_host_chunked(scr, L):
+    """From host buffers the first pass reduces groups of its chunks as they
+    arrive: sizes with a ragged tail, a last group of one chunk, and the
+    benchmark size (every lane count, fp64)."""
+    for n in (2048 * 1024 * 3 + 17, (1 << 24) + 5):
+        x = W.family2(n)
+        got = scr.reduce(torch.from_numpy(x).pin_memory(), L, -0.25)
+        assert bits(got.numpy()[0]) == bits(oracle.reduce(x, L, -0.25)), (n, L)
+
+
+def test_reduce_host_full_size(scr):
+    x = W.family2(1 << 28)
+    h = torch.from_numpy(x).pin_memory()
+    for L in (16, 128, 1024):
+        got = scr.reduce(h, L, 0.0)
+        assert bits(got.numpy()[0]) == bits(oracle.reduce(x, L, 0.0)), L
