@@ -493,13 +493,13 @@ cudaError_t run_reduce_host(const ReducePlan& plan, const T* x_host, T* x_dev, T
     return run_reduce<T>(plan, x_dev, out, init, ws, s);
   }
   // The first pass's leaf items reduce chunks of T rows of L consecutive
-  // elements each, independently: the chunks are copied in groups on the
+  // elements each, independently: the chunks are copied in (up to 32) groups on the
   // copy stream and each group's leaf items run once it has arrived; the
   // tail items, which read the rows after the last chunk, and the later
   // passes follow the last copy.
   const PassPlan& p0 = plan.passes[0];
   const int64_t C = p0.a.C, tiles = p0.a.tiles, per_chunk = p0.a.T * p0.a.L;
-  const int groups = C < 8 ? (int)C : 8;
+  const int groups = C < 32 ? (int)C : 32;
   std::lock_guard<std::mutex> lock(host_pipe_mutex());
   HostPipe& hp = host_pipe();
   if ((e = hp.ensure(groups + 1)) != cudaSuccess) return e;

@@ -1349,6 +1349,11 @@ cudaError_t run_scan(const ScanPlan& plan, const T* x, T* out, int64_t es, int64
   return tc.second(x, out, 0, plan.n_tiles, s);
 }
 
+#ifndef CR_HOST_CHUNKS
+#define CR_HOST_CHUNKS 32
+#endif
+constexpr int64_t kHostChunks = CR_HOST_CHUNKS;
+
 template <class T>
 cudaError_t run_scan_host(const ScanPlan& plan, const T* x_host, T* out_host, T* x_dev,
                           T* out_dev, char* ws, cudaStream_t s) {
@@ -1367,9 +1372,10 @@ cudaError_t run_scan_host(const ScanPlan& plan, const T* x_host, T* out_host, T*
       return e;
     return cudaStreamSynchronize(s);
   }
-  // about 8 chunks of whole tiles (at least 256 tiles each)
+  // about kHostChunks chunks of whole tiles (at least 256 tiles each): the
+  // first chunk's copy in and the last one's copy out overlap nothing
   const int64_t tiles = plan.n_tiles;
-  int64_t per = (tiles + 7) / 8;
+  int64_t per = (tiles + kHostChunks - 1) / kHostChunks;
   if (per < 256) per = 256;
   const int64_t nchunks = (tiles + per - 1) / per;
   std::lock_guard<std::mutex> lock(host_pipe_mutex());  // host-buffer calls share the streams
