@@ -100,6 +100,27 @@ __device__ __forceinline__ void local_scan(const T (&v)[E], T (&w)[E], T (&agg)[
   }
 }
 
+// The trees of a thread's kE elements only (no prefixes): the perfect tree
+// over all kE, whose level log2(S) holds the trees of the segments of S
+// (the same nodes local_scan builds). Returns the tree over all kE.
+template <class T, int S>
+__device__ __forceinline__ T tree_aggs(const T (&v)[kE], T (&agg)[kE / S]) {
+  T u[kE];
+#pragma unroll
+  for (int e = 0; e < kE; ++e) u[e] = v[e];
+#pragma unroll
+  for (int st = 1; st < kE; st *= 2) {
+#pragma unroll
+    for (int i = 0; i < kE; i += 2 * st) u[i] = add_rn(u[i], u[i + st]);
+    if (2 * st == S) {
+#pragma unroll
+      for (int s = 0; s < kE / S; ++s) agg[s] = u[s * S];
+    }
+  }
+  if (S == kE) agg[0] = u[0];
+  return u[0];
+}
+
 // w[e] = nd op w[e] for the thread's elements (nd is the left operand).
 template <class T>
 __device__ __forceinline__ void apply_node(T nd, T (&w)[kE]) {
@@ -257,54 +278,134 @@ __device__ __forceinline__ void build_tile_pyramid(T* lvl, int t, int full_threa
   }
 }
 
+// The same levels with every level's adds on the lowest threads (level p's
+// 256 >> p adds fill whole warps while they can): about 12 warp-wide adds a
+// tile instead of 43, for block barriers between the levels. An fp64 warp
+// add holds the fp64 pipe as long with one lane active as with 32, so the
+// binary64 passes take this form (2^28, block_dyadic<256> local pass 2.43 ->
+// 2.18 ms, the others 1-3 % faster); binary32 keeps the warp-local levels
+// (its adds are cheap and the barriers cost more: 2-9 % slower packed),
+// except in the up pass, which gains either way.
+template <class T>
+__device__ __forceinline__ void build_tile_pyramid_packed(T* lvl, int t, int full_threads,
+                                                          int top = 8) {
+  __syncthreads();
+  for (int p = 1; p <= top; ++p) {
+    const int c = full_threads >> p;  // complete nodes only
+    if (t < c)
+      lvl[lvl_base(p) + t] = add_rn(lvl[lvl_base(p - 1) + 2 * t], lvl[lvl_base(p - 1) + 2 * t + 1]);
+    __syncthreads();
+  }
+}
+
+template <bool kPacked, class T>
+__device__ __forceinline__ void tile_pyramid(T* lvl, int t, int full_threads, int top = 8) {
+  if (kPacked) build_tile_pyramid_packed(lvl, t, full_threads, top);
+  else build_tile_pyramid(lvl, t, full_threads, top);
+}
+
 // ------------------------------------------------------------------ up pass
+// A block takes kUpTiles consecutive tiles (the next tile's elements in
+// flight while the current tile's tree is built) and writes their
+// aggregates; for an aligned group of full tiles it also combines them into
+// the pyramid levels above (no tickets: the group is one subtree) and climbs
+// by arrival tickets from there, once per block instead of once per tile.
+constexpr int kUpTiles = 4;
+constexpr int kLogUpTiles = 2;
+
 template <class T, int S>
 __global__ void __launch_bounds__(kScanThreads)
 scan_up_kernel(const T* __restrict__ x, T* __restrict__ pyr, int* __restrict__ counters,
                T* __restrict__ totals, ScanArgs a) {
   __shared__ T lvl[2 * kScanThreads];
+  __shared__ T s_agg[kUpTiles];
   constexpr int NS = kE / S;
   constexpr int LS = Log2<S>::value;
   const int t = threadIdx.x;
-  const int64_t b = a.tile_base + blockIdx.x;
-  const int64_t i0 = b * kTile + (int64_t)t * kE;
-  const int64_t cnt = imax(0, imin(kE, a.n - i0));
-  const int full_threads = (int)imin(kScanThreads, (a.n - b * kTile) / kE);
-
-  T v[kE];
-#pragma unroll
-  for (int e = 0; e < kE; ++e) v[e] = (e < cnt) ? ldg(x + i0 + e) : T(0);
-  T w[kE], agg[NS];
-  local_scan<T, kE, S>(v, w, agg);
-  if (a.totals_level == 0) {  // blocks of B = S <= kE elements inside a thread
-#pragma unroll
-    for (int s = 0; s < NS; ++s)
-      if ((s + 1) * S <= cnt) totals[(i0 >> LS) + s] = agg[s];
+  const int64_t b0 = a.tile_base + (int64_t)blockIdx.x * kUpTiles;
+  const int64_t b_end = b0 + kUpTiles < a.tile_end ? b0 + kUpTiles : a.tile_end;
+  T vn[kE];
+  {
+    const int64_t i0 = b0 * kTile + (int64_t)t * kE;
+    load8(x + i0, imax(0, imin(kE, a.n - i0)), vn);
   }
-  T tagg;
-  if (NS == 1) {
-    tagg = agg[0];
+  for (int64_t b = b0; b < b_end; ++b) {
+    const int64_t i0 = b * kTile + (int64_t)t * kE;
+    const int64_t cnt = imax(0, imin(kE, a.n - i0));
+    const int full_threads = (int)imin(kScanThreads, (a.n - b * kTile) / kE);
+    T v[kE];
+#pragma unroll
+    for (int e = 0; e < kE; ++e) v[e] = vn[e];
+    if (b + 1 < b_end) {  // the next tile, in flight meanwhile
+      const int64_t j0 = i0 + kTile;
+      load8(x + j0, imax(0, imin(kE, a.n - j0)), vn);
+    }
+#pragma unroll
+    for (int e = 0; e < kE; ++e)
+      if (e >= cnt) v[e] = T(0);
+    T agg[NS];
+    const T tagg = tree_aggs<T, S>(v, agg);  // trees only: the prefixes are the down pass's
+    if (a.totals_level == 0) {  // blocks of B = S <= kE elements inside a thread
+#pragma unroll
+      for (int s = 0; s < NS; ++s)
+        if ((s + 1) * S <= cnt) totals[(i0 >> LS) + s] = agg[s];
+    }
+    if (t < full_threads) lvl[t] = tagg;
+    tile_pyramid<true>(lvl, t, full_threads);
+    // blocks of kE < B < kTile elements: complete nodes of the tile pyramid
+    if (a.totals_level > 0) {
+      const int p = a.totals_level;
+      if (t < (full_threads >> p)) totals[((b * kTile) >> a.logB) + t] = lvl[lvl_base(p) + t];
+    }
+    if (t == 0) s_agg[b - b0] = lvl[lvl_base(8)];
+    __syncthreads();  // lvl is rebuilt for the next tile
+  }
+  if (a.pyr_levels == 0 || t != 0) return;
+
+  // tile aggregates = level 0 of the global pyramid
+  for (int64_t b = b0; b < b_end && b < a.full_tiles; ++b) pyr[a.pyr_off[0] + b] = s_agg[b - b0];
+  const int loc = a.pyr_levels - 1 < kLogUpTiles ? a.pyr_levels - 1 : kLogUpTiles;
+  int64_t q;
+  int p0;
+  T node;
+  if (b_end - b0 == kUpTiles && (b0 & (kUpTiles - 1)) == 0 && b_end <= a.full_tiles) {
+    // an aligned group of full tiles: its subtree's levels 1 .. loc here
+    T cur[kUpTiles];
+#pragma unroll
+    for (int i = 0; i < kUpTiles; ++i) cur[i] = s_agg[i];
+    int width = kUpTiles;
+    for (int p = 1; p <= loc; ++p) {
+      width >>= 1;
+      for (int i = 0; i < width; ++i) {
+        cur[i] = add_rn(cur[2 * i], cur[2 * i + 1]);
+        pyr[a.pyr_off[p] + (b0 >> p) + i] = cur[i];
+      }
+    }
+    if (width != 1) return;  // the pyramid ends below the group's root
+    q = b0 >> loc;
+    p0 = loc + 1;
+    node = cur[0];
   } else {
-    T vv[kE];
-#pragma unroll
-    for (int e = 0; e < kE; ++e) vv[e] = v[e];
-    tagg = perfect_tree<T, kE>(vv);
+    // a partial group: each full tile climbs from level 0
+    for (int64_t b = b0; b < b_end && b < a.full_tiles; ++b) {
+      int64_t qq = b;
+      for (int p = 1; p < a.pyr_levels; ++p) {
+        const int64_t parent = qq >> 1;
+        if (parent >= (a.full_tiles >> p)) break;  // the parent is not a complete node
+        __threadfence();
+        const int ticket = atomicAdd(counters + a.cnt_off[p] + parent, 1);
+        if (ticket == 0) break;  // the sibling is still running; it will climb
+        __threadfence();
+        const T left = __ldcg(pyr + a.pyr_off[p - 1] + 2 * parent);
+        const T right = __ldcg(pyr + a.pyr_off[p - 1] + 2 * parent + 1);
+        pyr[a.pyr_off[p] + parent] = add_rn(left, right);
+        qq = parent;
+      }
+    }
+    return;
   }
-  if (t < full_threads) lvl[t] = tagg;
-  build_tile_pyramid(lvl, t, full_threads);
-
-  // blocks of kE < B < kTile elements: complete nodes of the tile pyramid
-  if (a.totals_level > 0) {
-    const int p = a.totals_level;
-    if (t < (full_threads >> p)) totals[((b * kTile) >> a.logB) + t] = lvl[lvl_base(p) + t];
-  }
-  if (a.pyr_levels == 0 || t != 0 || b >= a.full_tiles) return;
-
-  // tile aggregate = level 0 of the global pyramid; climb by arrival tickets
-  T node = lvl[lvl_base(8)];
-  pyr[a.pyr_off[0] + b] = node;
-  int64_t q = b;
-  for (int p = 1; p < a.pyr_levels; ++p) {
+  // climb by arrival tickets from the group's root
+  for (int p = p0; p < a.pyr_levels; ++p) {
     const int64_t parent = q >> 1;
     if (parent >= (a.full_tiles >> p)) break;  // the parent is not a complete node
     __threadfence();
@@ -358,11 +459,18 @@ scan_down_kernel(const T* x, T* out, const T* __restrict__ pyr, const T* __restr
     tagg = perfect_tree<T, kE>(vv);
   }
   if (t < full_threads) lvl[t] = tagg;
-  build_tile_pyramid(lvl, t, full_threads);  // also publishes tile_nodes/tile_carry
-  if (!kShift && cnt == 0) return;
+  tile_pyramid<sizeof(T) == 8>(lvl, t, full_threads);  // also publishes tile_nodes/tile_carry
 
-  // thread-level prefix nodes, lowest bit first (right-nested)
-  for (int p = 0; p < thread_bits; ++p) {
+  // thread-level prefix nodes, lowest bit first (right-nested): binary64
+  // takes the lane bits with the lanes paired across each bit (every lane of
+  // the warp takes part, so none leaves before them), then the warp bits
+  auto node_of = [&](int p) { return [&, p](int th) { return lvl[lvl_base(p) + (th >> p) - 1]; }; };
+  // (binary32: its adds are cheaper than the pairing's shuffles; each lane
+  // applies its own bits)
+  const int paired = sizeof(T) == 8 ? 5 : 0;
+  for (int p = 0; p < paired && p < thread_bits; ++p) apply_lane_bit(p, t, node_of(p), w);
+  if (!kShift && cnt == 0) return;
+  for (int p = paired; p < thread_bits; ++p) {
     if (((t >> p) & 1) && cnt > 0) {
       const T nd = lvl[lvl_base(p) + (t >> p) - 1];
       apply_node(nd, w);
@@ -493,7 +601,7 @@ scan_onepass_kernel(const T* x, T* out, T* pyr, int* counters, int* ready, int* 
   T w[kE], agg[1];
   local_scan<T, kE, kE>(v, w, agg);
   if (t < full_threads) lvl[t] = agg[0];
-  build_tile_pyramid(lvl, t, full_threads);
+  tile_pyramid<sizeof(T) == 8>(lvl, t, full_threads);
 
   if (t == 0 && b < a.full_tiles && a.pyr_levels > 0 && b != skip_publish)
     publish_and_climb(lvl[lvl_base(8)], b, pyr, counters, ready, a);
@@ -579,7 +687,7 @@ scan_pairwise_kernel(const T* x, T* out, const T* __restrict__ pyr, ScanArgs a, 
   const T p45 = add_rn(v[4], v[5]), p67 = add_rn(v[6], v[7]);
   const T q03 = add_rn(p01, p23), q47 = add_rn(p45, p67);
   if (t < full_threads) lvl[t] = add_rn(q03, q47);
-  build_tile_pyramid(lvl, t, full_threads);  // ends with a block barrier
+  tile_pyramid<sizeof(T) == 8>(lvl, t, full_threads);  // ends with a block barrier
 
   // warp prefixes: lane w of warp 0 folds Y_b (or Y_{b+1}) and the warp bits
   if (t <= kScanThreads / 32) {
@@ -671,7 +779,7 @@ __device__ __forceinline__ void local_tile(const T* x, T* out, T* __restrict__ t
   if (a.logB > kLogE) {  // blocks span threads: build the tile pyramid
     T tagg = agg[0];
     if (t < full_threads) lvl[t] = tagg;
-    build_tile_pyramid(lvl, t, full_threads, a.logB - kLogE);  // levels inside a block
+    tile_pyramid<sizeof(T) == 8>(lvl, t, full_threads, a.logB - kLogE);  // levels inside a block
     const int p = a.logB - kLogE;
     if (t < (full_threads >> p)) totals[((b * kTile) >> a.logB) + t] = lvl[lvl_base(p) + t];
     auto node_of = [&](int q) { return [&, q](int th) { return lvl[lvl_base(q) + (th >> q) - 1]; }; };
@@ -1141,10 +1249,12 @@ struct Tiled {
 #undef CR_LOCAL
       return cudaGetLastError();
     }
+    a.tile_end = t1;
+    const unsigned ugrid = (unsigned)((t1 - t0 + kUpTiles - 1) / kUpTiles);
     CR_LAUNCH(kKScanUp, s, {  // up pass: pairwise, blocks spanning tiles, binary32 iterated
-      if (S == 8) scan_up_kernel<T, 8><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
-      else if (S == 4) scan_up_kernel<T, 4><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
-      else scan_up_kernel<T, 2><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
+      if (S == 8) scan_up_kernel<T, 8><<<ugrid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
+      else if (S == 4) scan_up_kernel<T, 4><<<ugrid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
+      else scan_up_kernel<T, 2><<<ugrid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
     });
     return cudaGetLastError();
   }
@@ -1481,7 +1591,9 @@ cudaError_t run_block_totals(const ScanPlan& plan, const T* x, char* ws, cudaStr
       (e = cudaMemsetAsync(ws + plan.zero_ws, 0, plan.zero_bytes, s)) != cudaSuccess)
     return e;
   if (plan.n_tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  const unsigned grid = (unsigned)plan.n_tiles;
+  a.tile_base = 0;
+  a.tile_end = plan.n_tiles;
+  const unsigned grid = (unsigned)((plan.n_tiles + kUpTiles - 1) / kUpTiles);
   const int S = (int)(plan.B < kE ? plan.B : kE);
   CR_LAUNCH(kKScanUp, s, {
     if (S == 8) scan_up_kernel<T, 8><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);

@@ -24,6 +24,7 @@ struct ScanArgs {
   int32_t totals_level;      // block totals: 0 in-thread, p > 0 tile pyramid level, -1 global
   int32_t emit_last;         // shifted output of n + 1 entries: also write out[n]
   int64_t tile_base;         // tile index of blockIdx.x == 0 (chunked launches)
+  int64_t tile_end;          // up pass: one past the last tile of the launch
   int64_t pyr_off[kMaxLevels];  // element offset of each pyramid level
   int64_t cnt_off[kMaxLevels];  // offset of each level's arrival counters
 };
