@@ -285,7 +285,9 @@ void cr_debug_skip_publish(int64_t tile);
  * separate passes for every B; 2: the fused pass for every B, with a
  * validation failure raised once the chain's walk is half-way, so that its
  * recovery (the local pass again, the serial chain, the fix-up again) runs;
- * 3: the fused pass for every B. Every mode gives the same, exact output.
+ * 3: the fused pass for every B. Modes 0, 1 and 2 apply to the 1-D left
+ * fold too, which runs the fused pass without a fix-up. Every mode gives
+ * the same, exact output.
  * Process-wide. */
 void cr_debug_fused_fixup(int mode);
 

@@ -1605,7 +1605,9 @@ cudaError_t run_chain_fixup(const ChainPlan& p, const T* src, T* dst, char* ws, 
                             bool debug_fail) {
   const ChainWs w(p, ws);
   *fail = w.fail;
-  if (p.K <= 0 || p.K > kMaxFusedChain || logB < 1 || logB > 40) return cudaErrorInvalidValue;
+  if (p.K <= 0 || p.K > (out != nullptr ? kMaxFusedChain : kMaxFusedChainAlone) ||
+      (out != nullptr && (logB < 1 || logB > 40)))
+    return cudaErrorInvalidValue;
   cudaError_t e = run_chain_front<T>(p, src, ws, w, s);
   if (e != cudaSuccess) return e;
   FusedArgs f{};
@@ -1628,12 +1630,13 @@ cudaError_t run_chain_fixup(const ChainPlan& p, const T* src, T* dst, char* ws, 
   f.n = n;
   f.logB = logB;
   f.debug_fail = debug_fail ? 1 : 0;
-  f.nitems = (n + kFixItem - 1) / kFixItem;
+  f.nitems = out != nullptr ? (n + kFixItem - 1) / kFixItem : 0;
   const int limit = fused_grid_limit<T>();
   // fill blocks: enough for the fills to keep pace with the walk, and at
   // least three quarters of the grid left for the fix-up
   f.nfill = p.ntiles < kMaxFillBlocks ? p.ntiles : kMaxFillBlocks;
   if (f.nfill > limit / CR_FUSED_FILL_DIV) f.nfill = limit / CR_FUSED_FILL_DIV;
+  if (out == nullptr) f.nfill = p.ntiles < limit - 1 ? p.ntiles : limit - 1;  // all fill
   if (f.nfill < 1) return cudaErrorInvalidConfiguration;
   const int64_t fixers = (f.nitems + kCT / 32 - 1) / (kCT / 32);  // 8 warps a block
   const int64_t room = limit - 1 - f.nfill;

@@ -43,7 +43,9 @@ cudaError_t run_serial_chain(const T* src, T* dst, int64_t K, cudaStream_t s,
 // recomputes out's local values and calls run_fixup_again (both conditional
 // on *fail, so nothing runs when it is clear). Chains longer than
 // kMaxFusedChain are not accepted (their walk could outlast the waits'
-// time limit).
+// time limit). With out == nullptr the pass is the chain alone (its fill
+// overlapping the walk); the serial chain has then already rewritten dst on
+// a failure, and nothing else is needed.
 // debug_fail: a test hook; a second warp of the walking block sets *fail
 // once the walk is half-way, so that the recovery runs.
 template <class T>
@@ -54,6 +56,7 @@ template <class T>
 cudaError_t run_fixup_again(T* out, const T* carries, int64_t n, int logB, const int* fail,
                             cudaStream_t s);
 constexpr int64_t kMaxFusedChain = int64_t(1) << 26;
+constexpr int64_t kMaxFusedChainAlone = int64_t(1) << 28;
 
 // Longest binary32 chain the parallel evaluation is used for (K ulp must stay
 // small against the chain's values for its binade tests to be decisive).

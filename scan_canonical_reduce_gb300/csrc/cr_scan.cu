@@ -1435,6 +1435,13 @@ cudaError_t run_scan(const ScanPlan& plan, const T* x, T* out, int64_t es, int64
         }
         if (!plan.parallel_chain) {
           if ((e = run_serial_chain<T>(src, dst, K, s)) != cudaSuccess) return e;
+        } else if (K <= kMaxFusedChainAlone && !fused_fixup_disabled()) {
+          // the fill of each tile overlaps the rest of the walk (one
+          // cooperative pass); on a failure the serial chain rewrites dst
+          const int* fail = nullptr;
+          if ((e = run_chain_fixup<T>(plan.chain, src, dst, ws + plan.chain_ws, nullptr, 0, 0, s,
+                                      &fail, debug_fused_fail())) != cudaSuccess)
+            return e;
         } else if ((e = run_chain<T>(plan.chain, src, dst, ws + plan.chain_ws, s)) !=
                    cudaSuccess) {
           return e;

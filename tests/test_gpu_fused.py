@@ -2,7 +2,8 @@
 exact chain, inclusive, out != x; used by default for B <= 16, forced here
 for every B from 2 to 2048 through the library's test hook): the chain's
 walk, checks and fill run in one cooperative pass with the fix-up
-out[i] = C_{k-1} + P(i) behind them. Against the oracle at 0 ULP, over
+out[i] = C_{k-1} + P(i) behind them. The 1-D left fold runs the same pass
+without a fix-up (the fills overlapping the walk). Against the oracle at 0 ULP, over
 several chain tiles (4096 carries each) with ragged ends, and bit-equal to
 the separate passes and to the recovery that runs after a failure raised
 half-way through the walk (the hook sets a flag; no fault)."""
@@ -120,3 +121,47 @@ def test_bench_size_modes(scr):
     head = 1 << 20
     want = oracle.scan(x[:head].copy(), "block_dyadic", 16)
     assert first_diff(fused[:head].cpu().numpy(), want) is None
+
+
+def fold_mode(scr, x, mode, form="inclusive"):
+    scr.lib().cr_debug_fused_fixup(mode)
+    try:
+        xd = torch.from_numpy(x).to(DEV)
+        if form == "inclusive":
+            return scr.inclusive_scan(xd, "left_fold", 1).cpu().numpy()
+        f = scr.exclusive_scan if form == "exclusive" else scr.scan_include_initial
+        return f(xd, "left_fold", 1, 0.375).cpu().numpy()
+    finally:
+        scr.lib().cr_debug_fused_fixup(0)
+
+
+@pytest.mark.parametrize("n", [1025, 4096, 4097, 3 * 4096 + 17, 300007, (1 << 22) + 5])
+def test_left_fold_fused(scr, n):
+    """The 1-D left fold: fused (default), separate passes, and fused with a
+    failure raised half-way through the walk; all against the oracle."""
+    x = W.uniform_pm1(n, W.seed_for(34, n % 97))
+    want = oracle.scan(x, "left_fold", 1)
+    for mode in (0, 1, 2):
+        got = fold_mode(scr, x, mode)
+        assert first_diff(got, want) is None, (n, mode, first_diff(got, want))
+
+
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_left_fold_fused_families(scr, case):
+    n = 200003
+    x = np.ascontiguousarray(CASES[case](n, np.float64))
+    want = oracle.scan(x, "left_fold", 1)
+    for mode in (0, 2):
+        got = fold_mode(scr, x, mode)
+        gn, wn = np.isnan(got), np.isnan(want)
+        bad = (got.view(np.uint64) != want.view(np.uint64)) & ~(gn & wn) | (gn != wn)
+        assert not bad.any(), (case, mode, int(np.argmax(bad)))
+
+
+@pytest.mark.parametrize("form", ["exclusive", "include_initial"])
+def test_left_fold_fused_shifted(scr, form):
+    x = W.family3(100003)
+    want = oracle.scan_ex(x, "left_fold", 1, 0.375, form)
+    for mode in (0, 2):
+        got = fold_mode(scr, x, mode, form)
+        assert first_diff(got, want) is None, (form, mode)
