@@ -119,6 +119,25 @@ def host_inputs():
     }
 
 
+# ------------------------------------------------------------- ranks
+def max_over_ranks(x: float, dist, dev) -> float:
+    """The largest value of x over the ranks (a job takes as long as its
+    slowest rank); x itself on one process. dev: a device of the process
+    group's backend (the rank's GPU for NCCL, the CPU for gloo)."""
+    if not dist or not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_step: int, steps: int, world: int, seconds: float) -> float:
+    """Whole-job throughput of `world` replicas: every rank processed
+    bytes_per_step each step; the job's time is the slowest rank's."""
+    return bytes_per_step * steps * world / seconds / 1e9
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     """nvidia-smi samples of the SM clock and throttle reasons while running."""
@@ -272,16 +291,13 @@ def run_native(args):
     launches = scr.launch_count() - launches0
     prof = scr.profile_collect()
     clocks = sampler.stop()
-    ms_total = t0.elapsed_time(t1)
+    ms_total = max_over_ranks(t0.elapsed_time(t1), dist, dev)
     if dist:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
         dist.barrier()
 
     step_bytes = sum(r[3] for r in rows)
     ms_per_step = ms_total / args.steps
-    value = step_bytes * args.steps * world / (ms_total * 1e-3) / 1e9
+    value = job_gbs(step_bytes, args.steps, world, ms_total * 1e-3)
     peaks = measured_peaks()
     hbm_peak = peaks.get("hbm_gbs")
 
@@ -500,22 +516,15 @@ def run_e2e(args, scr, torch, dev, hin, rows, world, dist):
         step()  # every call returns host data: the step ends synchronised
         step_ms.append(round((time.perf_counter() - t1) * 1e3, 2))
     torch.cuda.synchronize(dev)
-    sec = time.perf_counter() - t
-    if dist:
-        tt = torch.tensor([sec], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        sec = float(tt.item())
+    sec = max_over_ranks(time.perf_counter() - t, dist, dev)
     step_bytes = sum(r[3] for r in rows)
     # the host link of this pool stalls at random (plain 2 GB copies: ~10 %
     # of them 36-144 ms instead of 21 ms), so the value is taken at the
     # median step; the mean and every step's time are reported beside it
-    med = sorted(step_ms)[len(step_ms) // 2] / 1e3
-    if dist:
-        mt = torch.tensor([med], device=dev)
-        dist.all_reduce(mt, op=dist.ReduceOp.MAX)
-        med = float(mt.item())
-    return {"value": round(step_bytes * world / med / 1e9, 2), "unit": "GB/s",
-            "estimator": "median step", "mean_value": round(step_bytes * steps * world / sec / 1e9, 2),
+    med = max_over_ranks(sorted(step_ms)[len(step_ms) // 2] / 1e3, dist, dev)
+    return {"value": round(job_gbs(step_bytes, 1, world, med), 2), "unit": "GB/s",
+            "estimator": "median step",
+            "mean_value": round(job_gbs(step_bytes, steps, world, sec), 2),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "step_ms": step_ms}
 
