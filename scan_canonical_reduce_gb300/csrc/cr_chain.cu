@@ -1213,13 +1213,10 @@ __global__ void __launch_bounds__(32) chain_serial_kernel(const T* src, T* dst, 
 // carries (serially) and the fix-up. The fix-up warps need no block
 // barrier, so the warps of an SM stay in different phases (loads, FP64
 // adds, stores) as a plain streaming kernel's would.
-#ifndef CR_FUSED_FILL_BLOCKS
-#define CR_FUSED_FILL_BLOCKS 96
-#endif
-#ifndef CR_FUSED_FILL_DIV
-#define CR_FUSED_FILL_DIV 4
-#endif
-constexpr int64_t kMaxFillBlocks = CR_FUSED_FILL_BLOCKS;
+// Fill blocks: at most 96 and a quarter of the resident blocks (48 and a
+// third measured alike at B = 16; half of them starve the fix-up).
+constexpr int64_t kMaxFillBlocks = 96;
+constexpr int kFillShareDiv = 4;
 constexpr int kFixPer = 16;                    // elements a lane per sub-chunk
 constexpr int64_t kFixSub = 32 * kFixPer;      // 512 elements a sub-chunk
 constexpr int kFixSubs = 16;                   // sub-chunks an item
@@ -1397,12 +1394,11 @@ __device__ __forceinline__ void fix_items(T* out, const T* carries, const FusedA
   }
 }
 
-#ifndef CR_FUSED_BLOCKS_PER_SM
-#define CR_FUSED_BLOCKS_PER_SM 2
-#endif
+// 2 blocks per SM (128 registers): an earlier, ticket-driven form of this
+// pass took 2.4 ms at B = 16 with 2 blocks per SM and 4.1 ms with 1.
 template <class T>
-__global__ void __launch_bounds__(kCT, CR_FUSED_BLOCKS_PER_SM) chain_walk_fix_kernel(const T* src, T* dst, T* out,
-                                                                FusedArgs f) {
+__global__ void __launch_bounds__(kCT, 2)
+    chain_walk_fix_kernel(const T* src, T* dst, T* out, FusedArgs f) {
   if (blockIdx.x == 0) {
     if (threadIdx.x < 32) {
       walk_body<T>(src, dst, f.segs, f.total, f.seg_cap, f.m_in, f.fail, f.meta, f.K, nullptr,
@@ -1635,7 +1631,7 @@ cudaError_t run_chain_fixup(const ChainPlan& p, const T* src, T* dst, char* ws, 
   // fill blocks: enough for the fills to keep pace with the walk, and at
   // least three quarters of the grid left for the fix-up
   f.nfill = p.ntiles < kMaxFillBlocks ? p.ntiles : kMaxFillBlocks;
-  if (f.nfill > limit / CR_FUSED_FILL_DIV) f.nfill = limit / CR_FUSED_FILL_DIV;
+  if (f.nfill > limit / kFillShareDiv) f.nfill = limit / kFillShareDiv;
   if (out == nullptr) f.nfill = p.ntiles < limit - 1 ? p.ntiles : limit - 1;  // all fill
   if (f.nfill < 1) return cudaErrorInvalidConfiguration;
   const int64_t fixers = (f.nitems + kCT / 32 - 1) / (kCT / 32);  // 8 warps a block

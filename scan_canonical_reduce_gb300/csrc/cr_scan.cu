@@ -1466,10 +1466,7 @@ cudaError_t run_scan(const ScanPlan& plan, const T* x, T* out, int64_t es, int64
   return tc.second(x, out, 0, plan.n_tiles, s);
 }
 
-#ifndef CR_HOST_CHUNKS
-#define CR_HOST_CHUNKS 32
-#endif
-constexpr int64_t kHostChunks = CR_HOST_CHUNKS;
+constexpr int64_t kHostChunks = 32;  // 2^28 fp64 from host: 8 14.6, 16 13.8, 32 13.4 ms
 
 template <class T>
 cudaError_t run_scan_host(const ScanPlan& plan, const T* x_host, T* out_host, T* x_dev,
