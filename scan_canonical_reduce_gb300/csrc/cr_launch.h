@@ -41,6 +41,7 @@ enum KernelId : int {
   kKChainWalkFix,
   kKScanLocalAgain,
   kKFixupAgain,
+  kKPairwisePrefix,
   kKernelCount
 };
 

@@ -658,27 +658,43 @@ scan_onepass_kernel(const T* x, T* out, T* pyr, int* counters, int* ready, int* 
 // first by the up pass (scan_up_kernel), and this pass only reads it. (A
 // single pass that waits for the nodes measured 2.5x slower here: a tile's
 // own add work is too short to hide the pyramid's completion latency.)
+// Y_b = W(2048 b), b = 1 .. full_tiles: the tile-level nodes of b folded
+// left-nested, highest bit first (the prefix every output of tile b starts
+// from), one thread a tile, all its nodes' loads issued before the folds.
+template <class T>
+__global__ void __launch_bounds__(256)
+pairwise_tile_prefix_kernel(const T* __restrict__ pyr, T* __restrict__ ypre, ScanArgs a) {
+  const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x + 1;
+  if (b > a.full_tiles) return;
+  T nd[kMaxLevels];
+#pragma unroll
+  for (int p = 0; p < kMaxLevels; ++p)
+    if (p < a.pyr_levels && ((b >> p) & 1)) nd[p] = pyr[a.pyr_off[p] + (b >> p) - 1];
+  T acc = T(0);
+  bool has = false;
+#pragma unroll
+  for (int p = kMaxLevels - 1; p >= 0; --p) {
+    if (p < a.pyr_levels && ((b >> p) & 1)) {
+      acc = has ? add_rn(acc, nd[p]) : nd[p];
+      has = true;
+    }
+  }
+  ypre[b] = acc;
+}
+
 template <class T, bool kShift>
 __global__ void __launch_bounds__(kScanThreads)
-scan_pairwise_kernel(const T* x, T* out, const T* __restrict__ pyr, ScanArgs a, T init) {
+scan_pairwise_kernel(const T* x, T* out, const T* __restrict__ ypre, ScanArgs a, T init) {
   __shared__ T lvl[2 * kScanThreads];
   __shared__ T s_last[kScanThreads / 32];
-  __shared__ T nodes_b[32], nodes_b1[32];  // tile-level nodes of b and of b + 1
-  __shared__ T s_base[kScanThreads / 32 + 1];  // E_{32 w}, w = 0..8 (E_256 = Y_{b+1})
-  const unsigned full = 0xffffffffu;
-  const int t = threadIdx.x, lane = t & 31, wp = t >> 5;
+  __shared__ T s_E[kScanThreads + 1];  // E_t = W(8 t) of the tile; E_256 = Y_{b+1}
+  const int t = threadIdx.x;
   const int64_t b = a.tile_base + blockIdx.x;
   const int64_t i0 = b * kTile + (int64_t)t * kE;
   const int64_t cnt = imax(0, imin(kE, a.n - i0));
   const int full_threads = (int)imin(kScanThreads, (a.n - b * kTile) / kE);
   const int64_t b1 = b + 1;
   const bool complete = (b1 <= a.full_tiles);  // its last output is W(2048 (b + 1))
-  const int tile_bits = a.pyr_levels;
-
-  // tile-level nodes of b (threads 0..31) and of b + 1 (threads 32..63)
-  if (t < tile_bits && ((b >> t) & 1)) nodes_b[t] = pyr[a.pyr_off[t] + (b >> t) - 1];
-  if (complete && t >= 32 && t < 32 + tile_bits && ((b1 >> (t - 32)) & 1))
-    nodes_b1[t - 32] = pyr[a.pyr_off[t - 32] + (b1 >> (t - 32)) - 1];
 
   T v[kE];
   load8(x + i0, cnt, v);
@@ -689,22 +705,17 @@ scan_pairwise_kernel(const T* x, T* out, const T* __restrict__ pyr, ScanArgs a, 
   if (t < full_threads) lvl[t] = add_rn(q03, q47);
   tile_pyramid<sizeof(T) == 8>(lvl, t, full_threads);  // ends with a block barrier
 
-  // warp prefixes: lane w of warp 0 folds Y_b (or Y_{b+1}) and the warp bits
+  // warp prefixes E_{32 w}: thread w of warp 0 takes Y_b (the tile prefix,
+  // computed once for every tile) and folds the warp bits; thread 8 takes
+  // Y_{b+1}
   if (t <= kScanThreads / 32) {
-    const bool next = (t == kScanThreads / 32);
-    const int64_t bb = next ? b1 : b;
     T acc = T(0);
     bool has = false;
-    if (!next || complete) {
-      for (int p = tile_bits - 1; p >= 0; --p) {
-        if ((bb >> p) & 1) {
-          const T nd = next ? nodes_b1[p] : nodes_b[p];
-          acc = has ? add_rn(acc, nd) : nd;
-          has = true;
-        }
+    if (t < kScanThreads / 32) {
+      if (b > 0) {  // W(0) is empty
+        acc = ypre[b];
+        has = true;
       }
-    }
-    if (!next) {
       const int th = t * 32;  // first thread of warp t
       for (int p = 7; p >= 5; --p) {
         if ((th >> p) & 1) {
@@ -713,25 +724,27 @@ scan_pairwise_kernel(const T* x, T* out, const T* __restrict__ pyr, ScanArgs a, 
           has = true;
         }
       }
+    } else if (complete) {
+      acc = ypre[b1];
     }
-    s_base[t] = acc;  // W(0) is empty; s_base[8] is used only when complete
+    s_E[t * 32] = acc;  // W(0) is empty; E_256 is used only when complete
   }
   __syncthreads();
-  // no early exit: every lane takes part in the shuffles; lanes past the end
-  // compute on values they never store
-
-  // lane down-sweep: E_t = E_{t - lowbit} op node(lowbit), highest lane bit first
-  T E = s_base[wp];
+  // lane levels, highest first: E_t = E_{t - 2^p} op node_p for the threads
+  // whose lowest set bit is 2^p (p < 5), the 256 >> (p + 1) adds of a level
+  // on the lowest threads (no early exit: values past the end are computed
+  // and never stored)
 #pragma unroll
   for (int p = 4; p >= 0; --p) {
-    const T src = __shfl_sync(full, E, (lane - (1 << p)) & 31);
-    if ((lane & ((2 << p) - 1)) == (1 << p)) {  // lowbit(lane) == 2^p
-      const T nd = lvl[lvl_base(p) + (t >> p) - 1];
-      E = (b == 0 && t == (1 << p)) ? nd : add_rn(src, nd);  // W(0) is empty
+    if (t < (kScanThreads >> (p + 1))) {
+      const int tt = (2 * t + 1) << p;
+      const T nd = lvl[lvl_base(p) + (tt >> p) - 1];
+      s_E[tt] = (b == 0 && tt == (1 << p)) ? nd : add_rn(s_E[tt - (1 << p)], nd);
     }
+    __syncthreads();
   }
-  const T E_down = __shfl_down_sync(full, E, 1);
-  const T E1 = (lane == 31) ? s_base[wp + 1] : E_down;
+  const T E = s_E[t];
+  const T E1 = s_E[t + 1];
 
   T w[kE];
   if (b == 0 && t == 0) {  // W(0) is empty
@@ -749,7 +762,7 @@ scan_pairwise_kernel(const T* x, T* out, const T* __restrict__ pyr, ScanArgs a, 
   w[6] = add_rn(w[5], v[6]);
   w[7] = E1;
   if (kShift)  // y[2048 b - 1] = W(2048 b) = Y_b
-    emit_shifted<T, true>(out, i0, cnt, w, s_base[0], init, a, s_last);
+    emit_shifted<T, true>(out, i0, cnt, w, s_E[0], init, a, s_last);
   else
     store8(out + i0, cnt, w);
 }
@@ -1122,6 +1135,10 @@ ScanPlan plan_scan(int64_t batch, int64_t n, cr_policy p, int64_t B, size_t esiz
   }
   plan.pyr_ws = off;
   off += round256((size_t)pyr_elems * esize);
+  if (p == CR_PAIRWISE) {
+    plan.ypre_ws = off;
+    off += round256((size_t)(plan.full_tiles + 1) * esize);
+  }
   // arrival counters, ready flags (one pass) and the tile counter: one
   // region cleared by a single memset per call
   plan.zero_ws = off;
@@ -1186,7 +1203,7 @@ struct Tiled {
   bool block, shift;
   int S;
   ScanArgs a{};
-  T *pyr, *totals, *carries;
+  T *pyr, *ypre, *totals, *carries;
   int* counters;
   Tiled(const ScanPlan& p, char* w, T i) : plan(p), ws(w), init(i) {
     block = plan.policy == CR_BLOCK_DYADIC;
@@ -1204,6 +1221,7 @@ struct Tiled {
       a.cnt_off[l] = plan.cnt_off[l];
     }
     pyr = reinterpret_cast<T*>(ws + plan.pyr_ws);
+    ypre = reinterpret_cast<T*>(ws + plan.ypre_ws);
     counters = reinterpret_cast<int*>(ws + plan.cnt_ws);
     totals = block ? reinterpret_cast<T*>(ws + plan.totals_ws) : nullptr;
     carries = block ? reinterpret_cast<T*>(ws + plan.carries_ws) : nullptr;
@@ -1260,6 +1278,14 @@ struct Tiled {
   }
   // block carries: C_0..C_{K-2} from the block totals
   cudaError_t middle(cudaStream_t s) {
+    if (plan.policy == CR_PAIRWISE) {  // every complete tile's prefix Y_b, once
+      if (plan.full_tiles < 1) return cudaSuccess;
+      const int64_t blocks = (plan.full_tiles + 255) / 256;
+      if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+      CR_LAUNCH(kKPairwisePrefix, s,
+                pairwise_tile_prefix_kernel<T><<<(unsigned)blocks, 256, 0, s>>>(pyr, ypre, a));
+      return cudaGetLastError();
+    }
     if (!block || plan.K < 2) return cudaSuccess;
     const T* src = plan.mode == ScanPlan::kLocalFixup ? totals
                                                        : pyr + plan.pyr_off[plan.logB - kLogTile];
@@ -1338,9 +1364,9 @@ struct Tiled {
     if (plan.policy == CR_PAIRWISE) {
       CR_LAUNCH(kKScanPairwise, s, {
         if (shift)
-          scan_pairwise_kernel<T, true><<<grid, kScanThreads, 0, s>>>(x, out, pyr, a, init);
+          scan_pairwise_kernel<T, true><<<grid, kScanThreads, 0, s>>>(x, out, ypre, a, init);
         else
-          scan_pairwise_kernel<T, false><<<grid, kScanThreads, 0, s>>>(x, out, pyr, a, init);
+          scan_pairwise_kernel<T, false><<<grid, kScanThreads, 0, s>>>(x, out, ypre, a, init);
       });
       return cudaGetLastError();
     }
