@@ -577,11 +577,12 @@ __device__ __forceinline__ T wait_node(const T* pyr, const int* ready, int* stat
 }
 
 // ------------------------------------------- iterated_pairwise, one pass
-// 8 blocks per SM for the inclusive form (32 registers, a few bytes
-// spilled): more tiles in flight cover the tile-pyramid barriers and the
-// waits (measured 8.28 -> 7.90 ms at 2^28 fp64 against 5 blocks per SM).
+// 8 blocks per SM (32 registers; a few bytes spilled in the inclusive form,
+// about 560 in the shifted one): more tiles in flight cover the
+// tile-pyramid barriers and the waits (2^28 fp64 against 5 blocks per SM:
+// inclusive 8.28 -> 7.90 ms, exclusive 8.92 -> 8.60 ms).
 template <class T, bool kShift>
-__global__ void __launch_bounds__(kScanThreads, kShift ? 5 : 8)
+__global__ void __launch_bounds__(kScanThreads, 8)
 scan_onepass_kernel(const T* x, T* out, T* pyr, int* counters, int* ready, int* tile_ctr,
                     int* status, ScanArgs a, int64_t skip_publish, T init) {
   __shared__ T lvl[2 * kScanThreads];
