@@ -420,9 +420,9 @@ def measured_peaks():
 # size to the benchmark's n = 2^28 by elements processed (traffic grows in
 # proportion); None when the kernel changed after the capture.
 NCU_TRAFFIC = {
-    # profiles/scan_onepass_kernel_iterated_pairwise_n2e25.md: 268.94 MB read +
-    # 232.41 MB written at n = 2^25, x 8
-    "scan_onepass_kernel": (268.94e6 + 232.41e6) * 8,
+    # profiles/scan_onepass_kernel_iterated_pairwise_n2e25.md: 268.93 MB read +
+    # 262.90 MB written at n = 2^25, x 8
+    "scan_onepass_kernel": (268.93e6 + 262.90e6) * 8,
     # profiles/lane_pass_kernel_reduce_f64_L16_n2e25.md: level-0 pass, x 8
     "lane_pass_kernel": (268.52e6 + 3.70e6) * 8,
 }

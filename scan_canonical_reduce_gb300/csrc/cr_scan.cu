@@ -292,8 +292,11 @@ __device__ __forceinline__ void build_tile_pyramid_packed(T* lvl, int t, int ful
   __syncthreads();
   for (int p = 1; p <= top; ++p) {
     const int c = full_threads >> p;  // complete nodes only
-    if (t < c)
-      lvl[lvl_base(p) + t] = add_rn(lvl[lvl_base(p - 1) + 2 * t], lvl[lvl_base(p - 1) + 2 * t + 1]);
+    // a loop, not an if: a one-add if body is compiled to a predicated add
+    // that every warp issues (and an fp64 warp add holds the pipe with its
+    // lanes off as with them on); the loop leaves the warps past c out
+    for (int q = t; q < c; q += kScanThreads)
+      lvl[lvl_base(p) + q] = add_rn(lvl[lvl_base(p - 1) + 2 * q], lvl[lvl_base(p - 1) + 2 * q + 1]);
     __syncthreads();
   }
 }
@@ -737,8 +740,8 @@ scan_pairwise_kernel(const T* x, T* out, const T* __restrict__ ypre, ScanArgs a,
   // and never stored)
 #pragma unroll
   for (int p = 4; p >= 0; --p) {
-    if (t < (kScanThreads >> (p + 1))) {
-      const int tt = (2 * t + 1) << p;
+    for (int i = t; i < (kScanThreads >> (p + 1)); i += kScanThreads) {  // a loop: see above
+      const int tt = (2 * i + 1) << p;
       const T nd = lvl[lvl_base(p) + (tt >> p) - 1];
       s_E[tt] = (b == 0 && tt == (1 << p)) ? nd : add_rn(s_E[tt - (1 << p)], nd);
     }
