@@ -525,13 +525,12 @@ __global__ void __launch_bounds__(kCT) chain_classify_kernel(
 #pragma unroll
   for (int i = 0; i < kCE; ++i) tsum += (double)tv[i];  // zero past the end
   double run = toff[blockIdx.x] + block_excl_sum(tsum, sh_w);  // P~ just before k0
-  bool pc = false, pn = false;
+  bool pc = false, pneg = false;  // pc, pe: the previous step's certainty and binade
   int pe = 0;
-  if (k0 > 0 && n > 0) classify<T>(run, mu, pc, pn, pe);
+  if (k0 > 0 && n > 0) classify<T>(run, mu, pc, pneg, pe);
   int nbrk = 0;
   Summ me{map_id(), 0};
   constexpr int H = kCE / 2;  // outputs written in two halves: fewer live registers
-  int first_type = -1;  // (kept for symmetry with the segment pass)
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
   int64_t q_out[H];
@@ -568,7 +567,6 @@ __global__ void __launch_bounds__(kCT) chain_classify_kernel(
       }
       m_out[j] = make_meta(type, c, ng, f, d, e);
       q_out[j] = q;
-      if (i == 0) first_type = (int)type;
       if (type != kMap) {
         me.map = map_id();
         me.brk += 1;
@@ -577,7 +575,6 @@ __global__ void __launch_bounds__(kCT) chain_classify_kernel(
         me.map = compose(me.map, step_map(d, q, f));
       }
       pc = c;
-      pn = ng;
       pe = e;
     }
   }
@@ -587,8 +584,6 @@ __global__ void __launch_bounds__(kCT) chain_classify_kernel(
     store_run(meta + k0 + h * H, nh, m_out);
   }
   }
-  (void)pn;
-  (void)first_type;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) nbrk += __shfl_down_sync(full, nbrk, off);
   if (lane == 0) cnt[w] = nbrk;

@@ -1,6 +1,7 @@
-"""The integer-pipe binary64 add that libcr's fp64 kernels use for part of
-their adds: bit-for-bit equal to IEEE-754 round-to-nearest-even addition
-(numpy on the host), NaNs compared as a class."""
+"""libcr's integer-pipe binary64 add (a measured alternative to the FP64
+pipe, exposed through cr_add_pairs_int; the kernels do not use it):
+bit-for-bit equal to IEEE-754 round-to-nearest-even addition (numpy on the
+host), NaNs compared as a class."""
 import numpy as np
 import pytest
 import torch
