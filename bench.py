@@ -109,6 +109,35 @@ def rows_spec():
     return rs
 
 
+HBM_NOMINAL_GBS = 7900.0  # GB300's nominal HBM3e bandwidth (8 stacks)
+
+
+def row_elems(r) -> int:
+    """Input elements of a row: n for the 1-D rows, rows x cols, levels x columns."""
+    kind = r[1]
+    if kind == "rows":
+        return ROWS_R * ROWS_C
+    if kind == "cols":
+        return COLS_LEVELS * COLS_N
+    return N
+
+
+def rate_stats(r, ms: float, hbm_peak, dadd_rate: float, fadd_rate: float) -> dict:
+    """One row's rates at a median time of ms: algorithmic GB/s against the
+    measured copy peak and the nominal HBM figure, elements/s, and adds/s
+    against the measured add rate of the row's type."""
+    sec = ms * 1e-3
+    gbs = r[3] / sec / 1e9
+    add_rate = r[4] / sec
+    peak_add = dadd_rate if r[5] == "f64" else fadd_rate
+    return {"ms": round(ms, 4), "gb_s": round(gbs, 1),
+            "hbm_frac": round(gbs / hbm_peak, 4) if hbm_peak else None,
+            "hbm_frac_nominal": round(gbs / HBM_NOMINAL_GBS, 4),
+            "elems_per_s": row_elems(r) / sec,
+            "adds_per_s": add_rate, "alu_frac": round(add_rate / peak_add, 4),
+            "bytes": r[3], "adds": r[4], "dtype": r[5]}
+
+
 # ----------------------------------------------------------------- inputs
 def host_inputs():
     return {
@@ -304,13 +333,7 @@ def run_native(args):
     row_stats = {}
     for r in rows:
         ms = statistics.median([a.elapsed_time(b) for a, b in ev[r[0]]])
-        gbs = r[3] / (ms * 1e-3) / 1e9
-        add_rate = r[4] / (ms * 1e-3)
-        peak_add = dadd_rate if r[5] == "f64" else fadd_rate
-        row_stats[r[0]] = {"ms": round(ms, 4), "gb_s": round(gbs, 1),
-                           "hbm_frac": round(gbs / hbm_peak, 4) if hbm_peak else None,
-                           "adds_per_s": add_rate, "alu_frac": round(add_rate / peak_add, 4),
-                           "bytes": r[3], "adds": r[4], "dtype": r[5]}
+        row_stats[r[0]] = rate_stats(r, ms, hbm_peak, dadd_rate, fadd_rate)
 
     # per-row kernel times: the launch list is in issue order, rows in turn
     per_row = {r[0]: {} for r in rows}
@@ -394,17 +417,11 @@ def run_extras(args, scr, torch, dev, stream, run_row, dadd_rate, fadd_rate, hbm
         scr.profile_enable(False)
         prof = scr.profile_collect()
         ms = statistics.median([a.elapsed_time(b) for a, b in evs])
-        gbs = r[3] / (ms * 1e-3) / 1e9
-        add_rate = r[4] / (ms * 1e-3)
-        peak_add = dadd_rate if r[5] == "f64" else fadd_rate
         kms = {}
         for name, t in prof:
             kms[name] = kms.get(name, 0.0) + t / args.steps
-        out[r[0]] = {"ms": round(ms, 4), "gb_s": round(gbs, 1),
-                     "hbm_frac": round(gbs / hbm_peak, 4) if hbm_peak else None,
-                     "adds_per_s": add_rate, "alu_frac": round(add_rate / peak_add, 4),
-                     "bytes": r[3], "adds": r[4], "dtype": r[5],
-                     "kernels_ms": {k: round(v, 4) for k, v in kms.items()}}
+        out[r[0]] = rate_stats(r, ms, hbm_peak, dadd_rate, fadd_rate)
+        out[r[0]]["kernels_ms"] = {k: round(v, 4) for k, v in kms.items()}
     return out
 
 

@@ -1,0 +1,37 @@
+"""bench.py's per-row rates (CPU, no GPU): algorithmic GB/s against the
+measured and the nominal HBM figures, elements/s, adds/s against the add
+rate of the row's type, and the element count of every row of the step."""
+import pytest
+
+import bench
+
+
+def test_rate_stats_by_hand():
+    # 8 GB read in 2 ms = 4000 GB/s; 2^28 elements; 2^28 adds
+    r = ("reduce_f64_L16", "reduce", {"L": 16}, 8 * 10**9, 1 << 28, "f64")
+    s = bench.rate_stats(r, 2.0, 8000.0, 0.5e12, 40e12)
+    assert s["gb_s"] == 4000.0
+    assert s["hbm_frac"] == 0.5
+    assert s["hbm_frac_nominal"] == pytest.approx(4000.0 / 7900.0, abs=1e-4)
+    assert s["elems_per_s"] == pytest.approx(bench.N / 2e-3)
+    assert s["adds_per_s"] == pytest.approx((1 << 28) / 2e-3)
+    assert s["alu_frac"] == pytest.approx((1 << 28) / 2e-3 / 0.5e12, abs=1e-4)
+
+
+def test_rate_stats_f32_uses_the_f32_add_rate():
+    r = ("reduce_rows_f32_L128", "rows", {"L": 128}, 10**9, 10**9, "f32")
+    s = bench.rate_stats(r, 1.0, None, 0.5e12, 40e12)
+    assert s["hbm_frac"] is None
+    assert s["alu_frac"] == pytest.approx(1e12 / 40e12, abs=1e-4)
+    assert s["elems_per_s"] == pytest.approx(bench.ROWS_R * bench.ROWS_C / 1e-3)
+
+
+def test_every_row_has_its_element_count():
+    want = {"reduce": bench.N, "scan": bench.N, "scan_ex": bench.N,
+            "rows": bench.ROWS_R * bench.ROWS_C, "cols": bench.COLS_LEVELS * bench.COLS_N}
+    for r in bench.rows_spec() + bench.extra_rows():
+        assert bench.row_elems(r) == want[r[1]], r[0]
+        # bytes per element: 8 (fp64 reduce), 16 (fp64 scans), 4 (fp32 rows) + outputs
+        per = r[3] / bench.row_elems(r)
+        assert per in (8, 16) or (r[1] == "rows" and 4 <= per < 4.01) or \
+            (r[1] == "scan_ex" and 16 <= per < 16.01), (r[0], per)
