@@ -149,6 +149,15 @@ def host_inputs():
 
 
 # ------------------------------------------------------------- ranks
+def job_config(world: int) -> dict:
+    """The workload both arms name: every hot-path row at its full size."""
+    return {"workload": "all hot-path rows at n = 2^28 fp64 (reduce L=16/128/1024, "
+                        "iterated_pairwise and block_dyadic<16>/<256> scans) + 65536x4096 "
+                        "fp32 row reduce + 90x200000 fp64 column scans",
+            "n": N, "l2": "every input larger than L2 (>=144 MB); no flush",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
 def max_over_ranks(x: float, dist, dev) -> float:
     """The largest value of x over the ranks (a job takes as long as its
     slowest rank); x itself on one process. dev: a device of the process
@@ -380,12 +389,7 @@ def run_native(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded SplitMix64 families; no dataset)",
-            "config": {"workload": "all hot-path rows at n = 2^28 fp64 "
-                                   "(reduce L=16/128/1024, iterated_pairwise and "
-                                   "block_dyadic<16>/<256> scans) + 65536x4096 fp32 "
-                                   "row reduce + 90x200000 fp64 column scans",
-                       "n": N, "l2": "every input larger than L2 (>=144 MB); no flush",
-                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "config": job_config(world),
             "rows": row_stats, "kernels": kernels, "roofline": roofline, "extras": extras,
             "peaks": {"hbm_gbs": hbm_peak, "dadd_per_s": dadd_rate, "dadd_latency_ns": dadd_lat,
                       "fadd_per_s": fadd_rate},
@@ -579,18 +583,28 @@ def cpu_sample_rows(scale: int):
     return n, rs
 
 
-def oracle_step(scale: int, cache={}):
+def sample_inputs(base: int, cache={}):
+    """The oracle sample's inputs at 1/base of every row, generated once; a
+    smaller sample is their prefix (the generators are counter-based)."""
+    if base not in cache:
+        cache.clear()
+        cc = max(1, COLS_N // base)
+        cache[base] = {
+            "f2": W.family2(N // base), "f3": W.family3(N // base),
+            "f4": W.family4(ROWS_R, ROWS_C, first_rows=max(1, ROWS_R // base)),
+            "f5": W.family5(COLS_LEVELS, COLS_N).reshape(COLS_LEVELS, COLS_N)[:, :cc].copy(),
+        }
+    return cache[base]
+
+
+def oracle_step(scale: int, base: int | None = None):
+    """One pass of the oracle over every row at 1/scale of its size (inputs
+    from the sample at 1/base, base dividing scale): (bytes, seconds, n)."""
     import oracle
     n, rs = cpu_sample_rows(scale)
-    if scale not in cache:
-        cache.clear()
-        cache[scale] = {
-            "f2": W.family2(n), "f3": W.family3(n),
-            "f4": W.family4(ROWS_R, ROWS_C)[: max(1, ROWS_R // scale)].copy(),
-            "f5": W.family5(COLS_LEVELS, COLS_N).reshape(COLS_LEVELS, COLS_N)
-                 [:, : max(1, COLS_N // scale)].copy().reshape(-1),
-        }
-    c = cache[scale]
+    s0 = sample_inputs(base or scale)
+    c = {"f2": s0["f2"][:n], "f3": s0["f3"][:n], "f4": s0["f4"][: max(1, ROWS_R // scale)],
+         "f5": s0["f5"][:, : max(1, COLS_N // scale)].copy().reshape(-1)}
     t = time.perf_counter()
     for name, kind, p, _ in rs:
         if kind == "reduce":
@@ -609,13 +623,13 @@ def oracle_step(scale: int, cache={}):
 def cpu_baseline(seconds: float = 15.0):
     """The oracle as it stands, single-threaded on this host, on a bounded
     sample of the same workload (every row at 1/scale of its size)."""
+    # double the sample (1/64 of every row, then 1/32, ... down to 1/4) until
+    # one measured pass takes at least 40 % of the budget
     scale = 64
-    b, s, n = oracle_step(scale)
-    # grow or shrink the sample toward the time budget
-    if s < seconds / 4 and scale > 8:
-        scale = max(8, int(scale * s / (seconds / 2)))
-        scale = 1 << max(3, int(np.log2(max(1, scale))))
-        b, s, n = oracle_step(scale)
+    b, s, n = oracle_step(scale, base=4)
+    while scale > 4 and s < 0.4 * seconds:
+        scale //= 2
+        b, s, n = oracle_step(scale, base=4)
     return {"value": round(b / s / 1e9, 4), "unit": "GB/s", "cores": 1,
             "host_cores_visible": len(os.sched_getaffinity(0)), "kind": "oracle",
             "seconds": round(s, 2),
@@ -644,10 +658,10 @@ def run_reference(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(tot_s / args.steps * 1e3, 2), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "all hot-path rows, each at 1/%d of the GPU arm's size "
-                               "(the oracle is single-threaded)" % scale, "n": n},
+        "config": job_config(world),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": "every row at 1/%d of its size" % scale},
+                         "sample": "every row at 1/%d of its size (1-D n = %d; the oracle "
+                                   "is single-threaded)" % (scale, n)},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

@@ -1,6 +1,7 @@
-"""bench.py's per-row rates (CPU, no GPU): algorithmic GB/s against the
-measured and the nominal HBM figures, elements/s, adds/s against the add
-rate of the row's type, and the element count of every row of the step."""
+"""bench.py's host-side pieces (CPU, no GPU): the per-row rates (algorithmic
+GB/s against the measured and the nominal HBM figures, elements/s, adds/s
+against the add rate of the row's type), the element count of every row of
+the step, and the oracle sample's input rows."""
 import pytest
 
 import bench
@@ -35,3 +36,16 @@ def test_every_row_has_its_element_count():
         per = r[3] / bench.row_elems(r)
         assert per in (8, 16) or (r[1] == "rows" and 4 <= per < 4.01) or \
             (r[1] == "scan_ex" and 16 <= per < 16.01), (r[0], per)
+
+
+def test_family4_first_rows_is_the_matrix_prefix():
+    """The reference arm's row sample generates only the rows it times: the
+    same values as the first rows of the full matrix (per-element counters,
+    per-row scales), for the bench shape's seed and another."""
+    import numpy as np
+    import workloads as W
+    for rows in (65536, 300):
+        full = W.family4(rows, 4)
+        part = W.family4(rows, 4, first_rows=37)
+        assert part.shape == (37, 4)
+        assert np.array_equal(part.view(np.uint32), full[:37].view(np.uint32))

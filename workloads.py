@@ -170,8 +170,11 @@ def family3(n: int) -> np.ndarray:
     return uniform_pm1(n, seed_for(3))
 
 
-def family4(rows: int = 65536, cols: int = 4096) -> np.ndarray:
-    return row_scaled_normal(rows, cols, seed_for(4, 0 if rows == 65536 else 1))
+def family4(rows: int = 65536, cols: int = 4096, first_rows: int | None = None) -> np.ndarray:
+    """The rows x cols matrix, or only its first ``first_rows`` rows (the same
+    values: element i and row r's scale depend on i and r alone)."""
+    k = rows if first_rows is None else min(first_rows, rows)
+    return row_scaled_normal(k, cols, seed_for(4, 0 if rows == 65536 else 1))
 
 
 def family5(levels: int = 90, cols: int = 200000) -> np.ndarray:
