@@ -623,13 +623,13 @@ def oracle_step(scale: int, base: int | None = None):
 def cpu_baseline(seconds: float = 15.0):
     """The oracle as it stands, single-threaded on this host, on a bounded
     sample of the same workload (every row at 1/scale of its size)."""
-    # double the sample (1/64 of every row, then 1/32, ... down to 1/4) until
+    # double the sample (1/64 of every row, then 1/32, ... up to 1/2) until
     # one measured pass takes at least 40 % of the budget
     scale = 64
-    b, s, n = oracle_step(scale, base=4)
-    while scale > 4 and s < 0.4 * seconds:
+    b, s, n = oracle_step(scale, base=2)
+    while scale > 2 and s < 0.4 * seconds:
         scale //= 2
-        b, s, n = oracle_step(scale, base=4)
+        b, s, n = oracle_step(scale, base=2)
     return {"value": round(b / s / 1e9, 4), "unit": "GB/s", "cores": 1,
             "host_cores_visible": len(os.sched_getaffinity(0)), "kind": "oracle",
             "seconds": round(s, 2),
