@@ -22,6 +22,11 @@
 // coarser unit: an exact division by 2^j with round-half-even) and a step
 // whose binade is uncertain (a real add). These are "breaks", evaluated in
 // order by one thread from integers only (real adds only when uncertain).
+// A rise by d after the thread's own steps since its last break have dropped
+// j >= d binades is the exception: 2^j M is then a multiple of 2^d, so the
+// rounding no longer depends on M's low bits and the rise folds into the map
+// (fold_rise). A chain that oscillates across binade boundaries rises mostly
+// back into binades it just left, so most rises fold.
 //
 // Passes (tile = 4096 steps, 16 consecutive steps per thread):
 //   1 tile sums and the largest |T| of each tile (coalesced);
@@ -30,9 +35,9 @@
 //     and sign of s_k from it, certain when the whole interval P~_k +- mu
 //     (mu = K ulp(2B) bounds both |C_k - P_k| and |P~_k - P_k|) lies inside
 //     one binade, decided on the bits with integers only; step types MAP
-//     (same or lower binade), UP (higher binade, integer break), FP
-//     (uncertain: real add); each thread's composed map after its last
-//     break, scanned across the tile;
+//     (same or lower binade, or a folded rise), UP (higher binade, integer
+//     break), FP (uncertain: real add); each thread's composed map after its
+//     last break, scanned across the tile;
 //   5 segment bases (one block), 6 segment records: each break and the
 //     composed map of the MAP steps that follow it in its tile; the steps
 //     before a tile's first break are folded into the previous tile's last
@@ -92,6 +97,10 @@ __device__ __forceinline__ bool m_neg(uint32_t m) { return m & 8u; }
 __device__ __forceinline__ uint32_t m_fcls(uint32_t m) { return (m >> 4) & 3u; }
 __device__ __forceinline__ int m_d(uint32_t m) { return (int)((m >> 6) & 63u); }
 __device__ __forceinline__ int m_e(uint32_t m) { return (int)((m >> 12) & 0xFFFu) - 2048; }
+// A rise folded into its run's map (type kMap; d is the rise, q and the f
+// class split T in the old unit, as for kUp).
+constexpr uint32_t kFolded = 1u << 24;
+__device__ __forceinline__ bool m_folded(uint32_t m) { return (m & kFolded) != 0; }
 
 // ---- integer maps M -> a M + b[parity(M)] (mod 2^64)
 struct Map {
@@ -116,6 +125,33 @@ __device__ __forceinline__ Map step_map(int d, int64_t q, uint32_t fcls) {
   if (d == 0) return Map{1, uq + delta(fcls, uq & 1), uq + delta(fcls, (uq & 1) ^ 1)};
   const uint64_t b = uq + delta(fcls, uq & 1);  // 2^d M is even
   return Map{a, b, b};
+}
+
+// A rise by d binades after a map g = 2^j M + b[p] with d <= j: the rise
+// rounds A = g(M) + q to the coarser unit, M1 = (A + 2^(d-1) - 1 + x) >> d
+// with x = [f > 0] | bit d of A (half to even). 2^j M is a multiple of 2^d,
+// so M1 = 2^(j-d) M + ((B + 2^(d-1) - 1 + x) >> d), B = b[p] + q, and bit d
+// of A is bit d of B (plus M's parity when j = d): again a map of the same
+// form. Exact when B is the true integer: along a valid chain |b[p]| <
+// 2^53 + 2^(53+j) and |q| < 2^(53+d), so j <= kFoldMaxDrop keeps it in int64.
+constexpr int kFoldMaxDrop = 7;
+__device__ __forceinline__ bool rise_foldable(const Map& g, int d) {
+  if (g.a == 0 || (g.a & (g.a - 1)) != 0) return false;
+  const int j = __ffsll((long long)g.a) - 1;
+  return d >= 1 && d <= j && j <= kFoldMaxDrop;
+}
+__device__ __forceinline__ Map fold_rise(const Map& g, int d, int64_t q, bool fpos) {
+  const int j = __ffsll((long long)g.a) - 1;
+  const uint64_t c = (uint64_t(1) << (d - 1)) - 1;
+  uint64_t b[2];
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    const uint64_t B = (p ? g.b1 : g.b0) + (uint64_t)q;
+    const uint64_t bit = ((B >> d) ^ (j == d ? (uint64_t)p : 0ull)) & 1ull;
+    const uint64_t x = fpos ? 1ull : bit;
+    b[p] = (uint64_t)((int64_t)(B + c + x) >> d);
+  }
+  return Map{g.a >> d, b[0], b[1]};
 }
 
 // ---- exact conversions between T values and (integer, binade) pairs
@@ -227,7 +263,7 @@ __device__ __forceinline__ bool in_binade64(int64_t A, bool neg, bool fz) {
 template <class T>
 __device__ __forceinline__ uint64_t up_step(uint64_t M, int64_t q, uint32_t fcls, int d,
                                             bool neg, bool& ok) {
-  const int64_t A = (int64_t)M + q;  // |M| <= 2^54, |q| < 2^62
+  const int64_t A = (int64_t)(M + (uint64_t)q);  // |M| <= 2^54, |q| < 2^62
   const int64_t hi = A >> d;         // floor
   const uint64_t lo = (uint64_t)A & ((uint64_t(1) << d) - 1);
   const uint64_t half = uint64_t(1) << (d - 1);
@@ -550,6 +586,7 @@ __global__ void __launch_bounds__(kCT) chain_classify_kernel(
       int d = 0;
       int64_t q = 0;
       uint32_t f = 0;
+      bool folded = false;
       if (k == 0) {
         type = kStart;
       } else if (!c || !pc) {
@@ -557,22 +594,28 @@ __global__ void __launch_bounds__(kCT) chain_classify_kernel(
       } else if (e <= pe) {  // same or lower binade: a composable step
         d = pe - e;
         type = (d <= 63 && split_unit<T>(tv[i], e, q, f)) ? kMap : kFp;
-      } else {  // rise: integer break, T split in the old (finer) unit
+      } else {  // rise: T split in the old (finer) unit; a break unless the
+                // run's map since its start or last break dropped far enough
         d = e - pe;
         type = (d <= 8 && split_unit<T>(tv[i], pe, q, f)) ? kUp : kFp;
+        if (type == kUp && rise_foldable(me.map, d)) {
+          type = kMap;
+          folded = true;
+        }
       }
       if (type == kFp) {
         d = 0;
         q = 0;
       }
-      m_out[j] = make_meta(type, c, ng, f, d, e);
+      m_out[j] = make_meta(type, c, ng, f, d, e) | (folded ? kFolded : 0u);
       q_out[j] = q;
       if (type != kMap) {
         me.map = map_id();
         me.brk += 1;
         nbrk += 1;
       } else {
-        me.map = compose(me.map, step_map(d, q, f));
+        me.map = folded ? fold_rise(me.map, d, q, f != kFZero)
+                        : compose(me.map, step_map(d, q, f));
       }
       pc = c;
       pe = e;
@@ -630,7 +673,11 @@ __global__ void __launch_bounds__(kCT) chain_segments_kernel(
   load_run(qv + (k0 < K ? k0 : 0), n, qr);
   load_run(meta + (k0 < K ? k0 : 0), n, mr);
   int64_t ord = in.brk - 1;  // segment open at my first step (-1: the leading run)
-  Map cur = in.map;
+  // The open segment's map is in.map then my steps (before my first break),
+  // or my steps since my last break. My steps are composed on their own, as
+  // the classify pass composed them: a folded rise folds into that map.
+  Map local = map_id();
+  bool own = false;  // one of my breaks opened the segment
   int steps = 0;  // MAP steps of the open segment seen by this thread
   const int64_t base = seg_base[blockIdx.x];
 #pragma unroll
@@ -639,6 +686,7 @@ __global__ void __launch_bounds__(kCT) chain_segments_kernel(
     const int64_t k = k0 + i;
     const uint32_t m = mr[i];
     if (m_type(m) != kMap) {
+      const Map cur = own ? local : compose(in.map, local);
       if (ord >= 0 && base + ord < seg_cap) {  // close the open segment
         segs[base + ord].map = cur;
         if (steps) atomicAdd(&segs[base + ord].nsteps, steps);
@@ -647,7 +695,8 @@ __global__ void __launch_bounds__(kCT) chain_segments_kernel(
         if (steps) atomicAdd(&lead_steps[blockIdx.x], steps);
       }
       ord += 1;
-      cur = map_id();
+      local = map_id();
+      own = true;
       steps = 0;
       if (base + ord < seg_cap) {
         SegRec& r = segs[base + ord];
@@ -662,12 +711,14 @@ __global__ void __launch_bounds__(kCT) chain_segments_kernel(
         atomicExch(fail, 2);
       }
     } else {
-      cur = compose(cur, step_map(m_d(m), qr[i], m_fcls(m)));
+      local = m_folded(m) ? fold_rise(local, m_d(m), qr[i], m_fcls(m) != kFZero)
+                          : compose(local, step_map(m_d(m), qr[i], m_fcls(m)));
       steps += 1;
     }
   }
   // my trailing MAP steps belong to the segment still open; the thread
   // holding the tile's last step closes it
+  const Map cur = own ? local : compose(in.map, local);
   const int64_t last = (tile0 + kCTile < K ? tile0 + kCTile : K) - 1;
   const bool closer = k0 <= last && last < k0 + kCE;
   if (ord >= 0 && base + ord < seg_cap) {
@@ -1085,6 +1136,11 @@ __device__ __forceinline__ void fill_finish(int64_t c, int t, FillPrep& p, int64
       }
       const int d = m_d(m);
       const uint32_t f = m_fcls(m);
+      if (m_folded(m)) {  // a rise folded into its run's map: the rise itself
+        M = up_step<T>(M, p.qr[i], f, d, m_neg(m), ok);
+        out[i] = m_to_value_normal<T>((int64_t)M, m_e(m));
+        continue;
+      }
       int64_t A64;
       if (d <= 9) {  // |M 2^d| <= 2^63 / 2 and |q| < 2^62: no overflow
         A64 = (int64_t)(M << d) + p.qr[i];

@@ -165,3 +165,28 @@ def test_left_fold_fused_shifted(scr, form):
     for mode in (0, 2):
         got = fold_mode(scr, x, mode, form)
         assert first_diff(got, want) is None, (form, mode)
+
+
+RECOVERY = ("chain_fallback_kernel", "scan_local_again_kernel", "fixup_again_kernel")
+
+
+@pytest.mark.parametrize("policy,B,n", [("block_dyadic", 16, 1 << 28),
+                                        ("block_dyadic", 256, 1 << 28),
+                                        ("left_fold", 1, 1 << 24)])
+def test_parallel_chain_needs_no_recovery(scr, policy, B, n):
+    """On the benchmark's value family the exact parallel chain validates
+    every step: its recovery kernels (the serial chain, the local pass again,
+    the fix-up again) read the chain's flag and return at once, taking
+    microseconds, where a recovery of 2^20 or more steps takes milliseconds."""
+    x = torch.from_numpy(W.family3(n)).to(DEV)
+    y = torch.empty_like(x)
+    scr.inclusive_scan(x, policy, B, out=y)
+    torch.cuda.synchronize()
+    scr.profile_enable(True)
+    scr.inclusive_scan(x, policy, B, out=y)
+    torch.cuda.synchronize()
+    scr.profile_enable(False)
+    prof = scr.profile_collect()
+    rec = [(k, ms) for k, ms in prof if k in RECOVERY]
+    assert rec, prof  # launched, as on every call
+    assert all(ms < 0.5 for _, ms in rec), rec
