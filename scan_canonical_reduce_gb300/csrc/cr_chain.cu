@@ -55,6 +55,7 @@
 #include <cstdint>
 
 #include "cr_chain.h"
+#include "cr_chain_map.h"
 #include "cr_device.cuh"
 #include "cr_launch.h"
 
@@ -102,20 +103,7 @@ __device__ __forceinline__ int m_e(uint32_t m) { return (int)((m >> 12) & 0xFFFu
 constexpr uint32_t kFolded = 1u << 24;
 __device__ __forceinline__ bool m_folded(uint32_t m) { return (m & kFolded) != 0; }
 
-// ---- integer maps M -> a M + b[parity(M)] (mod 2^64)
-struct Map {
-  uint64_t a, b0, b1;
-};
-__device__ __forceinline__ Map map_id() { return Map{1, 0, 0}; }
-__device__ __forceinline__ uint64_t bsel(const Map& g, uint64_t p) { return p ? g.b1 : g.b0; }
-__device__ __forceinline__ Map compose(const Map& g, const Map& h) {  // first g, then h
-  const uint64_t p0 = (g.b0 & 1);                         // parity after g, from even M
-  const uint64_t p1 = ((g.a & 1) ^ g.b1) & 1;            // parity after g, from odd M
-  return Map{h.a * g.a, h.a * g.b0 + bsel(h, p0), h.a * g.b1 + bsel(h, p1)};
-}
-__device__ __forceinline__ uint64_t apply(const Map& g, uint64_t M) {
-  return g.a * M + bsel(g, M & 1);
-}
+// ---- integer maps M -> a M + b[parity(M)] (mod 2^64): cr_chain_map.h
 __device__ __forceinline__ uint32_t delta(uint32_t fcls, uint64_t parity) {
   return fcls == kFHigh ? 1u : (fcls == kFHalf ? (uint32_t)(parity & 1) : 0u);
 }
@@ -125,33 +113,6 @@ __device__ __forceinline__ Map step_map(int d, int64_t q, uint32_t fcls) {
   if (d == 0) return Map{1, uq + delta(fcls, uq & 1), uq + delta(fcls, (uq & 1) ^ 1)};
   const uint64_t b = uq + delta(fcls, uq & 1);  // 2^d M is even
   return Map{a, b, b};
-}
-
-// A rise by d binades after a map g = 2^j M + b[p] with d <= j: the rise
-// rounds A = g(M) + q to the coarser unit, M1 = (A + 2^(d-1) - 1 + x) >> d
-// with x = [f > 0] | bit d of A (half to even). 2^j M is a multiple of 2^d,
-// so M1 = 2^(j-d) M + ((B + 2^(d-1) - 1 + x) >> d), B = b[p] + q, and bit d
-// of A is bit d of B (plus M's parity when j = d): again a map of the same
-// form. Exact when B is the true integer: along a valid chain |b[p]| <
-// 2^53 + 2^(53+j) and |q| < 2^(53+d), so j <= kFoldMaxDrop keeps it in int64.
-constexpr int kFoldMaxDrop = 7;
-__device__ __forceinline__ bool rise_foldable(const Map& g, int d) {
-  if (g.a == 0 || (g.a & (g.a - 1)) != 0) return false;
-  const int j = __ffsll((long long)g.a) - 1;
-  return d >= 1 && d <= j && j <= kFoldMaxDrop;
-}
-__device__ __forceinline__ Map fold_rise(const Map& g, int d, int64_t q, bool fpos) {
-  const int j = __ffsll((long long)g.a) - 1;
-  const uint64_t c = (uint64_t(1) << (d - 1)) - 1;
-  uint64_t b[2];
-#pragma unroll
-  for (int p = 0; p < 2; ++p) {
-    const uint64_t B = (p ? g.b1 : g.b0) + (uint64_t)q;
-    const uint64_t bit = ((B >> d) ^ (j == d ? (uint64_t)p : 0ull)) & 1ull;
-    const uint64_t x = fpos ? 1ull : bit;
-    b[p] = (uint64_t)((int64_t)(B + c + x) >> d);
-  }
-  return Map{g.a >> d, b[0], b[1]};
 }
 
 // ---- exact conversions between T values and (integer, binade) pairs
