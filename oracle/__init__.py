@@ -18,7 +18,6 @@ arithmetic type: no widening).
 from __future__ import annotations
 
 import ctypes
-import os
 
 import numpy as np
 

@@ -3,7 +3,6 @@
 test hook makes one tile skip publishing: the waits that need it give up,
 the call still completes, and cr_sync_status reports CR_ERR_TIMEOUT. The
 next call, hook off, is correct and reports CR_OK. No fault, no hang."""
-import numpy as np
 import pytest
 import torch
 

@@ -16,7 +16,6 @@ off by one, init applied in the wrong place or twice) fails at least one:
 Definitions: "Canonical Parallel Reduction and Scan" (github README
 andyD123/canonical-reduce), P4016R0 and P4229R0 Key Design Points.
 """
-import itertools
 import os
 import random
 
