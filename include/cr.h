@@ -121,7 +121,11 @@ size_t cr_scan_workspace_bytes(int64_t n, cr_policy p, int64_t B, cr_dtype dt);
  * B is used only by CR_BLOCK_DYADIC and must then be a power of two >= 1.
  * x, out device, n contiguous elements; out == x (in place) is allowed, any
  * other overlap is INVALID_ARG. n == 0 writes nothing. No init: a scan
- * observes the expression itself. */
+ * observes the expression itself.
+ * Cost: the carry chain of CR_LEFT_FOLD and CR_BLOCK_DYADIC (ceil(n/B)
+ * dependent adds) is evaluated exactly in parallel for binary64, and for
+ * binary32 chains of at most 4096 carries; a longer binary32 chain runs one
+ * add at a time on the device (about 3 ns an add on GB300). */
 cr_status cr_inclusive_scan(const void* x, void* out, int64_t n, cr_policy p, int64_t B,
                             cr_dtype dt, void* ws, size_t ws_bytes, void* stream);
 
