@@ -1147,11 +1147,14 @@ __global__ void __launch_bounds__(32) chain_serial_kernel(const T* src, T* dst, 
   __shared__ __align__(16) T buf[kBuf];
   const int lane = threadIdx.x;
   if (only_if != nullptr && *only_if == 0) return;
+  // past the end the buffer holds -0.0, the exact identity of the add: the
+  // last group's padding steps leave c (and so final_out) unchanged, a -0.0
+  // included (+0.0 would turn it into +0.0)
   T nxt[kPer];
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
     const int64_t k = lane + 32 * i;
-    nxt[i] = k < K ? src[k] : T(0);
+    nxt[i] = k < K ? src[k] : -T(0);
   }
   T c = T(0);
   for (int64_t base = 0; base < K; base += kBuf) {
@@ -1161,7 +1164,7 @@ __global__ void __launch_bounds__(32) chain_serial_kernel(const T* src, T* dst, 
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {  // the next buffer, in flight during the fold
       const int64_t k = base + kBuf + lane + 32 * i;
-      nxt[i] = k < K ? src[k] : T(0);
+      nxt[i] = k < K ? src[k] : -T(0);
     }
     if (lane == 0) {  // 32 steps at a time through registers (16-byte smem moves)
       const int cnt = (int)(K - base < kBuf ? K - base : kBuf);

@@ -65,3 +65,18 @@ def test_pairwise_root_is_the_tree(scr):
 def test_reduce_policy_rejects_empty(scr):
     with pytest.raises(ValueError):
         scr.reduce_policy(torch.empty(0, dtype=torch.float64, device=DEV), "left_fold")
+
+
+@pytest.mark.parametrize("dtype", [np.float64, np.float32])
+@pytest.mark.parametrize("policy,B", [("left_fold", 1), ("block_dyadic", 2)])
+@pytest.mark.parametrize("n", [2, 5, 64, 65, 1000, 1023])
+def test_reduce_policy_ends_at_minus_zero(scr, dtype, policy, B, n):
+    """Chains short enough for the serial kernel whose value ends at -0.0 (an
+    add gives -0.0 only from two -0.0 operands, so every operand is -0.0):
+    the root keeps its sign, so the kernel's padding past the last step must
+    be the identity -0.0, not +0.0."""
+    x = np.full(n, -0.0, dtype=dtype)
+    want = oracle.reduce_policy(x, policy, B)
+    assert np.signbit(want)
+    got = scr.reduce_policy(torch.from_numpy(x).to(DEV), policy, B).cpu().numpy()[0]
+    assert bits(np.array([got])) == bits(np.array([want])), (got, want)
