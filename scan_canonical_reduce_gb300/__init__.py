@@ -152,6 +152,11 @@ _WS = _Workspace()
 
 
 def workspace(device, stream=None, nbytes: int = 4096) -> torch.Tensor:
+    """The binding's cached workspace for (device, stream), at least nbytes:
+    a uint8 device tensor that grows on demand and is reused by every call
+    on that stream (calls on one stream run in order). A capture into a CUDA
+    graph should make one call first, so that no allocation happens inside
+    the capture."""
     return _WS.get(torch.device(device), stream, nbytes)
 
 
