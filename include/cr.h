@@ -23,8 +23,9 @@
  *   - All work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream). Calls return without synchronising; results are
  *     valid once the stream reaches that point.
- *   - Sizes and strides are counted in ELEMENTS, not bytes. x must be aligned
- *     to its element size.
+ *   - Sizes and strides are counted in ELEMENTS, not bytes, and are >= 0
+ *     (a negative stride is INVALID_ARG). x must be aligned to its element
+ *     size.
  *   - ws is a device workspace of at least the size the matching
  *     *_workspace_bytes() call returns, 256-byte aligned. A call may use it
  *     until the stream passes the call; two calls that overlap in time must
@@ -92,10 +93,11 @@ size_t cr_reduce_batched_workspace_bytes(int64_t batch, int64_t n, int32_t L, cr
 
 /* A batch of independent canonical reductions with one L and one init:
  * sequence b has elements x[b*batch_stride + i*elem_stride], i < n, and
- * out_dev[b] = reduce(sequence b, n, L, init). Strides may be any values
+ * out_dev[b] = reduce(sequence b, n, L, init). Strides are any values >= 0
  * (e.g. rows: elem_stride 1, batch_stride ncols; columns of a level-major
- * array: elem_stride ncols, batch_stride 1), but sequences must not alias
- * out_dev. batch >= 0, n >= 0, L >= 1. */
+ * array: elem_stride ncols, batch_stride 1; 0 repeats an element or a
+ * sequence), but sequences must not alias out_dev. batch >= 0, n >= 0,
+ * L >= 1; a negative stride is INVALID_ARG. */
 cr_status cr_reduce_batched(const void* x, void* out_dev, int64_t batch, int64_t n,
                             int64_t elem_stride, int64_t batch_stride, int32_t L,
                             const void* init_host, cr_dtype dt, void* ws, size_t ws_bytes,
@@ -138,7 +140,8 @@ size_t cr_scan_batched_workspace_bytes(int64_t batch, int64_t n, cr_policy p, in
  * positions of out (out uses x's strides). Typical use: columns of a
  * level-major (levels x ncols) array scanned along the levels, elem_stride =
  * ncols, batch_stride = 1. out == x is allowed; sequences must not overlap
- * one another. */
+ * one another (a zero elem_stride with n >= 2, or a zero batch_stride with
+ * batch >= 2, sends two outputs to one element: INVALID_ARG). */
 cr_status cr_inclusive_scan_batched(const void* x, void* out, int64_t batch, int64_t n,
                                     int64_t elem_stride, int64_t batch_stride, cr_policy p,
                                     int64_t B, cr_dtype dt, void* ws, size_t ws_bytes,
@@ -198,7 +201,9 @@ size_t cr_scan_ex_batched_workspace_bytes(int64_t batch, int64_t n, cr_policy p,
  * levels of each column of a level-major array give n + 1 interface values
  * (CR_INCLUDE_INITIAL, out_elem_stride = ncols, out_batch_stride = 1). If
  * out == x the output strides must equal the input strides; otherwise the
- * output must not overlap the input or itself across sequences. */
+ * output must not overlap the input or itself across sequences (a zero
+ * out_elem_stride with m >= 2, or a zero out_batch_stride with batch >= 2,
+ * is INVALID_ARG). */
 cr_status cr_scan_ex_batched(const void* x, void* out, int64_t batch, int64_t n,
                              int64_t elem_stride, int64_t batch_stride,
                              int64_t out_elem_stride, int64_t out_batch_stride, cr_policy p,

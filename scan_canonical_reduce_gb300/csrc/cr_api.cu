@@ -36,6 +36,7 @@ cr_status reduce_impl(const void* x, void* out, int64_t batch, int64_t n, int64_
                       size_t ws_bytes, void* stream) {
   const size_t sz = esize(dt);
   if (sz == 0 || n < 0 || batch < 0 || L < 1 || init_host == nullptr) return CR_ERR_INVALID_ARG;
+  if (es < 0 || bs < 0) return CR_ERR_INVALID_ARG;
   if (batch > 0 && out == nullptr) return CR_ERR_INVALID_ARG;
   if (batch > 0 && n > 0 && x == nullptr) return CR_ERR_INVALID_ARG;
   if ((x && !aligned(x, sz)) || (out && !aligned(out, sz))) return CR_ERR_INVALID_ARG;
@@ -128,6 +129,9 @@ static cr_status scan_impl(const void* x, void* out, int64_t batch, int64_t n, i
   if (sz == 0 || n < 0 || batch < 0 || !cr::scan_args_ok(p, B)) return CR_ERR_INVALID_ARG;
   if (mode != 0 && (!mode_ok(mode) || init_host == nullptr)) return CR_ERR_INVALID_ARG;
   const int64_t m = n + (mode == CR_INCLUDE_INITIAL ? 1 : 0);
+  if (es < 0 || bs < 0 || oes < 0 || obs < 0) return CR_ERR_INVALID_ARG;
+  // a zero output stride would send two outputs to one element
+  if ((m >= 2 && oes == 0) || (batch >= 2 && m >= 1 && obs == 0)) return CR_ERR_INVALID_ARG;
   if (batch > 0 && m > 0 && out == nullptr) return CR_ERR_INVALID_ARG;
   if (batch > 0 && n > 0 && x == nullptr) return CR_ERR_INVALID_ARG;
   if ((x && !aligned(x, sz)) || (out && !aligned(out, sz))) return CR_ERR_INVALID_ARG;

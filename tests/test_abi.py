@@ -142,3 +142,31 @@ def test_reduce_policy_host_side_argument_errors(scr):
     assert L.cr_reduce_policy(fake, 10, 9, 1, 2, fake, fake, 1 << 20, None) == 1
     assert L.cr_reduce_policy(fake, 10, 2, 1, 2, None, fake, 1 << 20, None) == 1
     assert L.cr_reduce_policy(fake, 1 << 20, 3, 16, 2, fake, fake, 256, None) == 3
+
+
+def test_stride_errors(scr):
+    """Negative strides, and zero output strides that would send two outputs
+    to one element, are rejected on the host (nothing is enqueued)."""
+    L = scr.lib()
+    one = ctypes.c_double(0.0)
+    fake = ctypes.c_void_p(0x10000)
+    ws = ctypes.c_void_p(0x100000)
+    for es, bs in ((-1, 10), (10, -1)):
+        assert L.cr_reduce_batched(fake, ws, 4, 10, es, bs, 16, ctypes.byref(one), 2, fake,
+                                   1 << 20, None) == 1
+        assert L.cr_inclusive_scan_batched(fake, ws, 4, 10, es, bs, 0, 1, 2, fake, 1 << 20,
+                                           None) == 1
+    # zero strides: a read-only repeat is fine for a reduce (fails later, on the
+    # fake workspace being too small, not on the strides)
+    assert L.cr_reduce_batched(fake, ws, 4, 10, 0, 0, 16, ctypes.byref(one), 2, fake, 8,
+                               None) == 3
+    # scans: two outputs of one sequence, or two sequences, on one element
+    assert L.cr_inclusive_scan_batched(fake, ws, 4, 10, 0, 1, 0, 1, 2, fake, 1 << 20, None) == 1
+    assert L.cr_inclusive_scan_batched(fake, ws, 4, 10, 4, 0, 0, 1, 2, fake, 1 << 20, None) == 1
+    assert L.cr_scan_ex_batched(fake, ws, 4, 10, 4, 1, 0, 1, 0, 1, 2, ctypes.byref(one), 2,
+                                fake, 1 << 20, None) == 1
+    assert L.cr_scan_ex_batched(fake, ws, 4, 10, 4, 1, 4, -1, 0, 1, 2, ctypes.byref(one), 2,
+                                fake, 1 << 20, None) == 1
+    # one sequence of one output may use a zero output stride (workspace check next)
+    assert L.cr_scan_ex_batched(fake, ws, 1, 0, 1, 1, 0, 0, 0, 1, 2, ctypes.byref(one), 2,
+                                fake, 8, None) == 3
