@@ -15,6 +15,8 @@ e2e   = the same through the public API with pinned host buffers, the
         result inside the timed region.
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+  python bench.py --one-row {reduce,scan,rows,cols} [--n --L --policy --B --rows
+                  --cols --levels --dtype --warmup --steps]   (one row, for ncu)
 
 With N > 1 (torchrun) every rank runs the same step on its own GPU
 (replicas: the rows are independent problems, no exchange); rank 0 prints.
@@ -74,18 +76,45 @@ def adds_pairwise(n: int) -> int:
     return (n - bin(n).count("1")) + (n - n.bit_length())
 
 
+SWEEP_N = (1 << 20, 1 << 24, 1 << 28, (1 << 28) + 37, 1 << 30)
+N_MAX = 1 << 30
+ROWS_B = (1024, 262144)
+
+
+def size_tag(n: int) -> str:
+    """2^k, or 2^k + r, as "2e<k>" or "2e<k>p<r>"."""
+    k = n.bit_length() - 1
+    r = n - (1 << k)
+    return "2e%d" % k + ("p%d" % r if r else "")
+
+
 def extra_rows():
-    """Rows beyond the headline step (the next policies), timed on their own
-    after it and reported under "extras"; not part of value."""
-    return [("scan_pairwise", "scan", {"policy": "pairwise", "B": 1}, 16 * N,
-             adds_pairwise(N), "f64"),
-            # init combined once with each of the n - 1 (n) observations
-            ("scan_iterated_pairwise_exclusive", "scan_ex",
-             {"policy": "iterated_pairwise", "B": 1, "mode": "exclusive"}, 16 * N,
-             adds_iterated(N) - 1 + (N - 1), "f64"),
-            ("scan_block_dyadic_16_include_initial", "scan_ex",
-             {"policy": "block_dyadic", "B": 16, "mode": "include_initial"}, 16 * N + 8,
-             adds_block_dyadic(N, 16) + N, "f64")]
+    """Rows beyond the headline step, timed on their own after it and
+    reported under "extras"; not part of value: the next policies, the
+    reduce sweep over sizes, binary32 and lane counts, the U[0, 1) reduce at
+    2^20 and the 1,024 x 262,144 row reduce."""
+    rs = [("scan_pairwise", "scan", {"policy": "pairwise", "B": 1}, 16 * N,
+           adds_pairwise(N), "f64"),
+          # init combined once with each of the n - 1 (n) observations
+          ("scan_iterated_pairwise_exclusive", "scan_ex",
+           {"policy": "iterated_pairwise", "B": 1, "mode": "exclusive"}, 16 * N,
+           adds_iterated(N) - 1 + (N - 1), "f64"),
+          ("scan_block_dyadic_16_include_initial", "scan_ex",
+           {"policy": "block_dyadic", "B": 16, "mode": "include_initial"}, 16 * N + 8,
+           adds_block_dyadic(N, 16) + N, "f64")]
+    for dt, es in (("f64", 8), ("f32", 4)):
+        for n in SWEEP_N:
+            for L in (16, 128, 1024):
+                rs.append(("sweep_reduce_%s_n%s_L%d" % (dt, size_tag(n), L), "reduce",
+                           {"L": L, "n": n, "dt": dt}, es * n, n, dt))
+    for L in (16, 128):
+        rs.append(("reduce_u01_f64_n2e20_L%d" % L, "reduce_u01", {"L": L, "n": 1 << 20},
+                   8 << 20, 1 << 20, "f64"))
+    r, c = ROWS_B
+    rs.append(("reduce_rows_f32_L128_%dx%d" % (r, c), "rows_b", {"L": 128, "rows": r,
+                                                                  "cols": c},
+               4 * r * c + 4 * r, r * c, "f32"))
+    return rs
 
 
 def rows_spec():
@@ -114,12 +143,14 @@ HBM_NOMINAL_GBS = 7900.0  # GB300's nominal HBM3e bandwidth (8 stacks)
 
 def row_elems(r) -> int:
     """Input elements of a row: n for the 1-D rows, rows x cols, levels x columns."""
-    kind = r[1]
+    kind, p = r[1], r[2]
     if kind == "rows":
         return ROWS_R * ROWS_C
+    if kind == "rows_b":
+        return p["rows"] * p["cols"]
     if kind == "cols":
         return COLS_LEVELS * COLS_N
-    return N
+    return p.get("n", N)
 
 
 def rate_stats(r, ms: float, hbm_peak, dadd_rate: float, fadd_rate: float) -> dict:
@@ -140,10 +171,17 @@ def rate_stats(r, ms: float, hbm_peak, dadd_rate: float, fadd_rate: float) -> di
 
 # ----------------------------------------------------------------- inputs
 def host_inputs():
+    """Every row's input, generated once on the host. The reduce rows of the
+    step and of the size sweep read prefixes of one 2^30-element array per
+    type (the generator is counter-based: family2(n) is the first n elements
+    of family2(2^30))."""
     return {
-        "f2": W.family2(N),                      # reduce
+        "f2": W.family2(N_MAX),                  # reduce (step: the first 2^28)
+        "f2f": W.family2(N_MAX, np.float32),     # binary32 reduce sweep
+        "f1": W.family1(1 << 20),                # U[0, 1) reduce at 2^20
         "f3": W.family3(N),                      # 1-D scans
         "f4": W.family4(ROWS_R, ROWS_C),         # row reduce
+        "f4b": W.family4(*ROWS_B),               # row reduce, 1,024 x 262,144
         "f5": W.family5(COLS_LEVELS, COLS_N),    # column scans
     }
 
@@ -255,7 +293,11 @@ def run_native(args):
     rows = rows_spec()
     hin = host_inputs()
     # device-resident inputs and outputs
-    x2 = torch.from_numpy(hin["f2"]).to(dev)
+    x2_all = torch.from_numpy(hin["f2"]).to(dev)
+    x2 = x2_all[:N]
+    x2f_all = torch.from_numpy(hin["f2f"]).to(dev)
+    x1 = torch.from_numpy(hin["f1"]).to(dev)
+    x4b = torch.from_numpy(hin["f4b"]).to(dev)
     x3 = torch.from_numpy(hin["f3"]).to(dev)
     x4 = torch.from_numpy(hin["f4"]).to(dev)
     x5 = torch.from_numpy(hin["f5"]).to(dev).view(COLS_LEVELS, COLS_N)
@@ -263,13 +305,22 @@ def run_native(args):
     y_scan1 = torch.empty(N + 1, dtype=x3.dtype, device=dev)  # include_initial: n + 1
     y_cols = torch.empty_like(x5)
     r_out = torch.empty(1, dtype=torch.float64, device=dev)
+    r_out32 = torch.empty(1, dtype=torch.float32, device=dev)
     rows_out = torch.empty(ROWS_R, dtype=torch.float32, device=dev)
+    rows_out_b = torch.empty(ROWS_B[0], dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def run_row(row):
         name, kind, p = row[0], row[1], row[2]
         if kind == "reduce":
-            scr.reduce(x2, p["L"], 0.0, out=r_out)
+            if p.get("dt", "f64") == "f32":
+                scr.reduce(x2f_all[:p["n"]], p["L"], 0.0, out=r_out32)
+            else:
+                scr.reduce(x2_all[:p.get("n", N)], p["L"], 0.0, out=r_out)
+        elif kind == "reduce_u01":
+            scr.reduce(x1, p["L"], 0.0, out=r_out)
+        elif kind == "rows_b":
+            scr.reduce_batched(x4b, p["L"], 0.0, dim=-1, out=rows_out_b)
         elif kind == "scan":
             scr.inclusive_scan(x3, p["policy"], p["B"], out=y_scan)
         elif kind == "scan_ex":
@@ -387,7 +438,8 @@ def run_native(args):
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 3),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "mixed: f64 (every row but one), f32 (the 65536 x 4096 row reduce)",
             "data": "synthetic (seeded SplitMix64 families; no dataset)",
             "config": job_config(world),
             "rows": row_stats, "kernels": kernels, "roofline": roofline, "extras": extras,
@@ -400,17 +452,26 @@ def run_native(args):
         dist.destroy_process_group()
 
 
+L2_FLUSH_BYTES = 512 << 20  # more than the 126 MB L2
+
+
 def run_extras(args, scr, torch, dev, stream, run_row, dadd_rate, fadd_rate, hbm_peak):
     """Each extra row timed alone: W warm-up calls, then K calls bracketed by
-    CUDA events on the launching stream (inputs larger than L2)."""
+    CUDA events on the launching stream. A row whose input is smaller than
+    twice the L2 gets a 512 MB write between its timed calls (outside the
+    events), so that every call starts from HBM."""
     out = {}
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     for r in extra_rows():
+        small = r[3] < 2 * L2_FLUSH_BYTES // 4
         for _ in range(args.warmup):
             run_row(r)
         torch.cuda.synchronize(dev)
         scr.profile_enable(True)
         evs = []
         for _ in range(args.steps):
+            if small:
+                flush.zero_()
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
@@ -426,6 +487,9 @@ def run_extras(args, scr, torch, dev, stream, run_row, dadd_rate, fadd_rate, hbm
             kms[name] = kms.get(name, 0.0) + t / args.steps
         out[r[0]] = rate_stats(r, ms, hbm_peak, dadd_rate, fadd_rate)
         out[r[0]]["kernels_ms"] = {k: round(v, 4) for k, v in kms.items()}
+        if small:
+            out[r[0]]["l2"] = "flushed between calls"
+    del flush
     return out
 
 
@@ -437,16 +501,40 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "note": "fallback"}
 
 
-# DRAM bytes per launch from ncu captures (profiles/), scaled from the captured
-# size to the benchmark's n = 2^28 by elements processed (traffic grows in
-# proportion); None when the kernel changed after the capture.
+# DRAM bytes (read + written) per launch from one ncu capture of the kernel,
+# scaled from the captured size to the benchmark's n = 2^28 by elements
+# processed (traffic grows in proportion). Each figure holds only for the
+# sources it was captured from: "sources" maps each file to the first 16 hex
+# digits of its SHA-256 at capture time, and the figure reads as None once
+# any of them differs (the kernel changed after the capture).
+CSRC_DIR = os.path.join(ROOT, "scan_canonical_reduce_gb300", "csrc")
 NCU_TRAFFIC = {
-    # profiles/scan_onepass_kernel_iterated_pairwise_n2e25.md: 268.93 MB read +
-    # 262.90 MB written at n = 2^25, x 8
-    "scan_onepass_kernel": (268.93e6 + 262.90e6) * 8,
-    # profiles/lane_pass_kernel_reduce_f64_L16_n2e25.md: level-0 pass, x 8
-    "lane_pass_kernel": (268.52e6 + 3.70e6) * 8,
+    # one-row iterated_pairwise scan, n = 2^25: 268.93 MB read + 262.90 MB
+    # written, x 8
+    "scan_onepass_kernel": {"bytes": (268.93e6 + 262.90e6) * 8, "sources": {}},
+    # one-row reduce, n = 2^25, L = 16, level-0 pass, x 8
+    "lane_pass_kernel": {"bytes": (268.52e6 + 3.70e6) * 8, "sources": {}},
 }
+
+
+def source_digest(name: str) -> str | None:
+    import hashlib
+    try:
+        with open(os.path.join(CSRC_DIR, name), "rb") as f:
+            return hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return None
+
+
+def ncu_traffic(kernel: str):
+    """The recorded traffic of `kernel` per launch, or None when there is no
+    capture or its sources have changed since."""
+    t = NCU_TRAFFIC.get(kernel)
+    if not t or not t["sources"]:
+        return None
+    if any(source_digest(f) != d for f, d in t["sources"].items()):
+        return None
+    return t["bytes"]
 
 
 def dominant_roofline(kernels, prof, row_stats, dadd_rate, dadd_lat, hbm_peak, steps,
@@ -469,7 +557,7 @@ def dominant_roofline(kernels, prof, row_stats, dadd_rate, dadd_lat, hbm_peak, s
         achieved = adds / (avg_ms * 1e-3)
         return {"kernel": top, "bound": "alu", "achieved": achieved, "peak": dadd_nominal,
                 "unit": "fp64 adds/s", "frac": round(achieved / dadd_nominal, 4),
-                "traffic": NCU_TRAFFIC.get(top),
+                "traffic": ncu_traffic(top),
                 "work_per_launch": {"adds": adds, "bytes": nbytes},
                 "measured_peak": {"value": dadd_rate, "frac": round(achieved / dadd_rate, 4)},
                 "hbm": {"achieved_gbs": round(nbytes / (avg_ms * 1e-3) / 1e9, 1),
@@ -478,7 +566,8 @@ def dominant_roofline(kernels, prof, row_stats, dadd_rate, dadd_lat, hbm_peak, s
                 "note": "peak = SMs x 2 fp64 adds a clock x max SM clock (GB300's nominal "
                         "1.25 TFLOP/s fp64); measured_peak = libcr's calibration kernel "
                         "(independent round-to-nearest adds on all SMs); traffic from an "
-                        "ncu capture at n = 2^25 scaled by 8"}
+                        "ncu capture at n = 2^25 scaled by 8, null when the kernel's sources "
+                        "changed after the capture"}
     if top == "lane_pass_kernel":
         r = row_stats["reduce_f64_L16"]
         achieved = r["bytes"] / (r["ms"] * 1e-3) / 1e9
@@ -487,7 +576,7 @@ def dominant_roofline(kernels, prof, row_stats, dadd_rate, dadd_lat, hbm_peak, s
                 "frac": round(r["adds"] / (r["ms"] * 1e-3) / dadd_nominal, 4),
                 "measured_peak": {"value": dadd_rate,
                                   "frac": round(r["adds"] / (r["ms"] * 1e-3) / dadd_rate, 4)},
-                "traffic": NCU_TRAFFIC.get(top),
+                "traffic": ncu_traffic(top),
                 "hbm": {"achieved_gbs": round(achieved, 1), "peak_gbs": hbm_peak,
                         "frac": round(achieved / hbm_peak, 4)}}
     if top == "carry_chain_kernel":
@@ -506,7 +595,7 @@ def dominant_roofline(kernels, prof, row_stats, dadd_rate, dadd_lat, hbm_peak, s
 def run_e2e(args, scr, torch, dev, hin, rows, world, dist):
     """Same rows through the public API on pinned host tensors: each call
     copies its input in and its result out, inside the timed region."""
-    h2 = torch.from_numpy(hin["f2"]).pin_memory()
+    h2 = torch.from_numpy(hin["f2"][:N]).pin_memory()
     h3 = torch.from_numpy(hin["f3"]).pin_memory()
     h4 = torch.from_numpy(hin["f4"]).pin_memory()
     h5 = torch.from_numpy(hin["f5"]).view(COLS_LEVELS, COLS_N).pin_memory()
@@ -668,6 +757,41 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+# ------------------------------------------------------- one row (profilers)
+def run_one_row(args):
+    """One hot-path row at a chosen size, called --warmup + --steps times and
+    then synchronised, for a profiler (ncu) to capture; prints no JSON line.
+    Inputs are the benchmark's seeded families."""
+    import torch
+
+    import scan_canonical_reduce_gb300 as scr
+
+    dev = torch.device("cuda:0")
+    f32 = args.dtype == "f32"
+    if args.one_row == "reduce":
+        x = torch.from_numpy(W.family2(args.n, np.float32 if f32 else np.float64)).to(dev)
+        fn = lambda: scr.reduce(x, args.L, 0.0)  # noqa: E731
+    elif args.one_row == "scan":
+        x = torch.from_numpy(W.family3(args.n)).to(dev)
+        if f32:
+            x = x.float()
+        y = torch.empty_like(x)
+        fn = lambda: scr.inclusive_scan(x, args.policy, args.B, out=y)  # noqa: E731
+    elif args.one_row == "rows":
+        x = torch.from_numpy(W.family4(args.rows, args.cols)).to(dev)
+        fn = lambda: scr.reduce_batched(x, args.L, 0.0, dim=-1)  # noqa: E731
+    else:
+        x = torch.from_numpy(W.family5(args.levels, args.cols)).to(dev).view(args.levels,
+                                                                           args.cols)
+        y = torch.empty_like(x)
+        fn = lambda: scr.inclusive_scan_batched(x, args.policy, args.B, dim=0,  # noqa: E731
+                                                out=y)
+    for _ in range(args.warmup + args.steps):
+        fn()
+    torch.cuda.synchronize(dev)
+    print("ok", args.one_row, args.n)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -677,7 +801,20 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-scale", type=int, default=32)
+    # --one-row: a single row for a profiler (no timing, no JSON line)
+    ap.add_argument("--one-row", choices=["reduce", "scan", "rows", "cols"])
+    ap.add_argument("--n", type=int, default=1 << 25)
+    ap.add_argument("--L", type=int, default=16)
+    ap.add_argument("--policy", default="iterated_pairwise")
+    ap.add_argument("--B", type=int, default=1)
+    ap.add_argument("--rows", type=int, default=8192)
+    ap.add_argument("--cols", type=int, default=4096)
+    ap.add_argument("--levels", type=int, default=90)
+    ap.add_argument("--dtype", default="f64", choices=["f64", "f32"])
     args = ap.parse_args()
+    if args.one_row:
+        run_one_row(args)
+        return
     if args.warmup < 3 and args.impl == "native":
         raise SystemExit("--warmup must be >= 3")
     if args.impl == "reference":

@@ -97,7 +97,11 @@ size_t cr_reduce_batched_workspace_bytes(int64_t batch, int64_t n, int32_t L, cr
  * (e.g. rows: elem_stride 1, batch_stride ncols; columns of a level-major
  * array: elem_stride ncols, batch_stride 1; 0 repeats an element or a
  * sequence), but sequences must not alias out_dev. batch >= 0, n >= 0,
- * L >= 1; a negative stride is INVALID_ARG. */
+ * L >= 1; a negative stride is INVALID_ARG. With two or more sequences
+ * laid out densely (rows: elem_stride 1, batch_stride n; or level-major
+ * columns: batch_stride 1, elem_stride batch), an out_dev range that meets
+ * the input is INVALID_ARG; for other layouts keeping them apart is the
+ * caller's duty. */
 cr_status cr_reduce_batched(const void* x, void* out_dev, int64_t batch, int64_t n,
                             int64_t elem_stride, int64_t batch_stride, int32_t L,
                             const void* init_host, cr_dtype dt, void* ws, size_t ws_bytes,
@@ -140,8 +144,11 @@ size_t cr_scan_batched_workspace_bytes(int64_t batch, int64_t n, cr_policy p, in
  * positions of out (out uses x's strides). Typical use: columns of a
  * level-major (levels x ncols) array scanned along the levels, elem_stride =
  * ncols, batch_stride = 1. out == x is allowed; sequences must not overlap
- * one another (a zero elem_stride with n >= 2, or a zero batch_stride with
- * batch >= 2, sends two outputs to one element: INVALID_ARG). */
+ * one another (a zero elem_stride with n >= 2, a zero batch_stride with
+ * batch >= 2, or elem_stride == batch_stride with batch >= 2 and n >= 2
+ * sends two outputs to one element: INVALID_ARG). With out != x and both
+ * laid out densely (rows or level-major columns), an out that meets x is
+ * INVALID_ARG; for other layouts keeping them apart is the caller's duty. */
 cr_status cr_inclusive_scan_batched(const void* x, void* out, int64_t batch, int64_t n,
                                     int64_t elem_stride, int64_t batch_stride, cr_policy p,
                                     int64_t B, cr_dtype dt, void* ws, size_t ws_bytes,
@@ -202,8 +209,10 @@ size_t cr_scan_ex_batched_workspace_bytes(int64_t batch, int64_t n, cr_policy p,
  * (CR_INCLUDE_INITIAL, out_elem_stride = ncols, out_batch_stride = 1). If
  * out == x the output strides must equal the input strides; otherwise the
  * output must not overlap the input or itself across sequences (a zero
- * out_elem_stride with m >= 2, or a zero out_batch_stride with batch >= 2,
- * is INVALID_ARG). */
+ * out_elem_stride with m >= 2, a zero out_batch_stride with batch >= 2, or
+ * out_elem_stride == out_batch_stride with batch >= 2 and m >= 2 is
+ * INVALID_ARG, and so is an output that meets the input when both are laid
+ * out densely: rows or level-major columns). */
 cr_status cr_scan_ex_batched(const void* x, void* out, int64_t batch, int64_t n,
                              int64_t elem_stride, int64_t batch_stride,
                              int64_t out_elem_stride, int64_t out_batch_stride, cr_policy p,
@@ -229,6 +238,33 @@ cr_status cr_reduce_host(const void* x_host, int64_t n, int32_t L, const void* i
                          cr_dtype dt, void* out_host, void* dev_buf, size_t dev_bytes,
                          void* stream);
 
+/* Host-buffer forms of the batched calls: the same operations and strides
+ * as cr_reduce_batched and cr_inclusive_scan_batched, with x and out in host
+ * memory. The batch is moved in groups of whole sequences (about 16 MB each,
+ * at most 16): each group is copied in, computed and copied out on three
+ * streams ordered by events, so that transfers overlap kernels; the call
+ * returns when out is written. Host layouts: sequences contiguous
+ * (elem_stride 1, batch_stride >= n: rows) or element k of every sequence
+ * contiguous (batch_stride 1, elem_stride >= batch: columns of a level-major
+ * array); any other layout is CR_ERR_UNSUPPORTED. The scan's out uses x's
+ * strides; out == x (in place) is allowed, any other overlap of their
+ * address ranges is INVALID_ARG (for the reduce, out_host's batch elements
+ * must not meet x's range). dev_buf: caller-owned device memory of at least
+ * the bytes the query returns (256-byte aligned). Errors otherwise as for the
+ * device forms. */
+size_t cr_reduce_batched_host_workspace_bytes(int64_t batch, int64_t n, int32_t L,
+                                              cr_dtype dt);
+cr_status cr_reduce_batched_host(const void* x_host, void* out_host, int64_t batch, int64_t n,
+                                 int64_t elem_stride, int64_t batch_stride, int32_t L,
+                                 const void* init_host, cr_dtype dt, void* dev_buf,
+                                 size_t dev_bytes, void* stream);
+size_t cr_inclusive_scan_batched_host_workspace_bytes(int64_t batch, int64_t n, cr_policy p,
+                                                      int64_t B, cr_dtype dt);
+cr_status cr_inclusive_scan_batched_host(const void* x_host, void* out_host, int64_t batch,
+                                         int64_t n, int64_t elem_stride, int64_t batch_stride,
+                                         cr_policy p, int64_t B, cr_dtype dt, void* dev_buf,
+                                         size_t dev_bytes, void* stream);
+
 /* Allocation-free canonical reduction. The paper has no counterpart: this
  * serves callers that cannot allocate device memory, such as a plugin whose
  * host framework owns all device memory through its own pool, or a
@@ -240,8 +276,12 @@ cr_status cr_reduce_host(const void* x_host, int64_t n, int32_t L, const void* i
  *   - Calls whose cr_reduce_workspace_bytes(n, L, dt) exceeds 16 MiB return
  *     CR_ERR_WORKSPACE and enqueue nothing (every n <= 2^28 fits for
  *     L <= 4096).
- *   - The first call on a device (that device current) looks up the array's
- *     device address; make that first call before any stream capture.
+ *   - Each call that is not being captured into a CUDA graph looks up the
+ *     array's device address on the current device (so the address stays
+ *     right after cudaDeviceReset); a call made during stream capture reuses
+ *     the address found by an earlier call on that device, so make the first
+ *     call on a device before any stream capture (otherwise
+ *     CR_ERR_UNSUPPORTED).
  *   - All calls on a device share the one array, which keeps the previous
  *     call's contents: two calls that may overlap on the GPU (different
  *     streams, no ordering between them) race and give wrong results.
@@ -294,9 +334,11 @@ void cr_debug_skip_publish(int64_t tile);
  * separate passes for every B; 2: the fused pass for every B, with a
  * validation failure raised once the chain's walk is half-way, so that its
  * recovery (the local pass again, the serial chain, the fix-up again) runs;
- * 3: the fused pass for every B. Modes 0, 1 and 2 apply to the 1-D left
- * fold too, which runs the fused pass without a fix-up. Every mode gives
- * the same, exact output.
+ * 3: the fused pass for every B; 4: the fused pass for every B, taken as if
+ * the device had refused its cooperative launch, so that the fallback to
+ * the separate passes and a plain fix-up runs. Modes 0, 1, 2 and 4 apply to
+ * the 1-D left fold too, which runs the fused pass without a fix-up. Every
+ * mode gives the same, exact output.
  * Process-wide. */
 void cr_debug_fused_fixup(int mode);
 

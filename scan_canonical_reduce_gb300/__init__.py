@@ -59,6 +59,12 @@ SIGNATURES = {
     "cr_inclusive_scan_host": (_INT, [_P, _P, _I64, _INT, _I64, _INT, _P, _SZ, _P]),
     "cr_reduce_host_workspace_bytes": (_SZ, [_I64, _I32, _INT]),
     "cr_reduce_host": (_INT, [_P, _I64, _I32, _P, _INT, _P, _P, _SZ, _P]),
+    "cr_reduce_batched_host_workspace_bytes": (_SZ, [_I64, _I64, _I32, _INT]),
+    "cr_reduce_batched_host": (_INT, [_P, _P, _I64, _I64, _I64, _I64, _I32, _P, _INT, _P, _SZ,
+                                      _P]),
+    "cr_inclusive_scan_batched_host_workspace_bytes": (_SZ, [_I64, _I64, _INT, _I64, _INT]),
+    "cr_inclusive_scan_batched_host": (_INT, [_P, _P, _I64, _I64, _I64, _I64, _INT, _I64, _INT,
+                                              _P, _SZ, _P]),
     "cr_sync_status": (_INT, [_P, _P]),
     "cr_status_string": (ctypes.c_char_p, [_INT]),
     "cr_version": (_INT, []),
@@ -238,6 +244,8 @@ def reduce_batched(x: torch.Tensor, L: int, init=0.0, dim: int = -1,
     strides): dim=-1 reduces rows, dim=0 reduces columns."""
     if x.dim() != 2:
         raise ValueError("reduce_batched expects a 2-D tensor")
+    if not x.is_cuda:  # host buffers: one C call, transfers pipelined with the kernels
+        return _reduce_batched_host(x, L, init, dim, out, stream)
     xd, host = _on_device(x, stream)
     dt = _dtype_code(xd)
     d = dim % 2
@@ -255,6 +263,40 @@ def reduce_batched(x: torch.Tensor, L: int, init=0.0, dim: int = -1,
                                    ctypes.byref(ini), dt, ws.data_ptr(), ws.numel(), sp),
            "cr_reduce_batched")
     return _to_host(o, stream) if host else o
+
+
+def _host_layout(x: torch.Tensor, dim: int):
+    """(n, batch, elem_stride, batch_stride) of the lines of a 2-D tensor along
+    dim, and x itself or a contiguous copy when its layout is neither rows nor
+    level-major columns (the layouts the host-buffer calls move in groups)."""
+    d = dim % 2
+    n, batch = x.shape[d], x.shape[1 - d]
+    es, bs = x.stride(d), x.stride(1 - d)
+    rows = es == 1 and (bs >= n or batch == 1)
+    cols = bs == 1 and (es >= batch or n == 1)
+    if not (rows or cols or batch <= 1 or n <= 1):
+        x = x.contiguous()
+        es, bs = x.stride(d), x.stride(1 - d)
+    return x, n, batch, es, bs
+
+
+def _reduce_batched_host(x, L, init, dim, out, stream):
+    x, n, batch, es, bs = _host_layout(x, dim)
+    dt = _dtype_code(x)
+    o = out if out is not None else torch.empty(batch, dtype=x.dtype, pin_memory=True)
+    if o.is_cuda or o.numel() != batch or o.dtype != x.dtype or not o.is_contiguous():
+        raise ValueError("out must be a contiguous host tensor of %d elements" % batch)
+    nb = lib().cr_reduce_batched_host_workspace_bytes(batch, n, int(L), dt)
+    if nb == 0:
+        raise ValueError("invalid reduce_batched arguments")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    ws = _WS.get(dev, stream, nb)
+    ini = _init_buffer(init, dt)
+    _check(lib().cr_reduce_batched_host(x.data_ptr() if x.numel() else None, o.data_ptr(),
+                                        batch, n, es, bs, int(L), ctypes.byref(ini), dt,
+                                        ws.data_ptr(), ws.numel(), _stream_ptr(stream)),
+           "cr_reduce_batched_host")
+    return o
 
 
 # ------------------------------------------------------------------ scan
@@ -308,6 +350,24 @@ def inclusive_scan_batched(x: torch.Tensor, policy="left_fold", B: int = 1, dim:
     strides."""
     if x.dim() != 2:
         raise ValueError("inclusive_scan_batched expects a 2-D tensor")
+    if not x.is_cuda:  # host buffers: one C call, transfers pipelined with the kernels
+        xh, n, batch, es, bs = _host_layout(x, dim)
+        dt = _dtype_code(xh)
+        o = out if out is not None else torch.empty_strided(
+            xh.shape, xh.stride(), dtype=xh.dtype, pin_memory=True)
+        if o.is_cuda or o.stride() != xh.stride() or o.dtype != xh.dtype:
+            raise ValueError("out must be a host tensor with x's strides")
+        p = _policy(policy)
+        nb = lib().cr_inclusive_scan_batched_host_workspace_bytes(batch, n, p, int(B), dt)
+        if nb == 0:
+            raise ValueError("invalid scan arguments")
+        dev = torch.device("cuda", torch.cuda.current_device())
+        ws = _WS.get(dev, stream, nb)
+        _check(lib().cr_inclusive_scan_batched_host(
+            xh.data_ptr() if xh.numel() else None, o.data_ptr() if o.numel() else None, batch,
+            n, es, bs, p, int(B), dt, ws.data_ptr(), ws.numel(), _stream_ptr(stream)),
+            "cr_inclusive_scan_batched_host")
+        return o
     xd, host = _on_device(x, stream)
     dt = _dtype_code(xd)
     d = dim % 2

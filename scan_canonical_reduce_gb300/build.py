@@ -18,8 +18,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libcr.so")
-SOURCES = ["cr_api.cu", "cr_calibrate.cu", "cr_chain.cu", "cr_launch.cu", "cr_noalloc.cu",
-           "cr_reduce.cu", "cr_reduce_policy.cu", "cr_scan.cu"]
+SOURCES = ["cr_api.cu", "cr_calibrate.cu", "cr_chain.cu", "cr_host_batched.cu", "cr_launch.cu",
+           "cr_noalloc.cu", "cr_reduce.cu", "cr_reduce_policy.cu", "cr_scan.cu"]
 HEADERS = ["cr_chain.h", "cr_chain_map.h", "cr_device.cuh", "cr_launch.h", "cr_plan.h",
            "cr_scan.h"]
 

@@ -26,6 +26,23 @@ cr_status check_ws(void* ws, size_t ws_bytes, size_t need) {
 
 cr_status from_cuda(cudaError_t e) { return e == cudaSuccess ? CR_OK : CR_ERR_CUDA; }
 
+// A batch of `batch` sequences of `len` elements with strides (es, bs) that
+// fills its address range exactly: rows (es = 1, bs = len), columns of a
+// level-major array (bs = 1, es = batch), or one sequence or element a row.
+bool dense_layout(int64_t len, int64_t batch, int64_t es, int64_t bs) {
+  if (len <= 0 || batch <= 0 || len > INT64_MAX / batch) return false;
+  if (batch == 1) return len == 1 || es == 1;
+  if (len == 1) return bs == 1;
+  return (es == 1 && bs == len) || (bs == 1 && es == batch);
+}
+
+// Do the byte ranges [a, a + na) and [b, b + nb) meet?
+bool ranges_meet(const void* a, size_t na, const void* b, size_t nb) {
+  const char* pa = static_cast<const char*>(a);
+  const char* pb = static_cast<const char*>(b);
+  return pa < pb + nb && pb < pa + na;
+}
+
 // Every call starts by clearing the workspace status word (see cr_sync_status).
 cudaError_t clear_status(void* ws, cudaStream_t s) {
   return cudaMemsetAsync(ws, 0, sizeof(int), s);
@@ -40,6 +57,11 @@ cr_status reduce_impl(const void* x, void* out, int64_t batch, int64_t n, int64_
   if (batch > 0 && out == nullptr) return CR_ERR_INVALID_ARG;
   if (batch > 0 && n > 0 && x == nullptr) return CR_ERR_INVALID_ARG;
   if ((x && !aligned(x, sz)) || (out && !aligned(out, sz))) return CR_ERR_INVALID_ARG;
+  // several sequences over one dense block of memory: the results must not
+  // land on inputs that another sequence may still read
+  if (batch >= 2 && n > 0 && dense_layout(n, batch, es, bs) &&
+      ranges_meet(x, (size_t)(n * batch) * sz, out, (size_t)batch * sz))
+    return CR_ERR_INVALID_ARG;
   const cr::ReducePlan plan = cr::plan_reduce(batch, n, L, es, bs, sz);
   const cr_status ws_ok = check_ws(ws, ws_bytes, plan.ws_bytes);
   if (ws_ok != CR_OK) return ws_ok;
@@ -130,8 +152,12 @@ static cr_status scan_impl(const void* x, void* out, int64_t batch, int64_t n, i
   if (mode != 0 && (!mode_ok(mode) || init_host == nullptr)) return CR_ERR_INVALID_ARG;
   const int64_t m = n + (mode == CR_INCLUDE_INITIAL ? 1 : 0);
   if (es < 0 || bs < 0 || oes < 0 || obs < 0) return CR_ERR_INVALID_ARG;
-  // a zero output stride would send two outputs to one element
-  if ((m >= 2 && oes == 0) || (batch >= 2 && m >= 1 && obs == 0)) return CR_ERR_INVALID_ARG;
+  // a zero output stride would send two outputs to one element, and so would
+  // equal output strides with two or more sequences of two or more outputs
+  // (output (b + 1, k) is output (b, k + 1))
+  if (batch > 0 && ((m >= 2 && oes == 0) || (batch >= 2 && m >= 1 && obs == 0)))
+    return CR_ERR_INVALID_ARG;
+  if (batch >= 2 && m >= 2 && oes == obs) return CR_ERR_INVALID_ARG;
   if (batch > 0 && m > 0 && out == nullptr) return CR_ERR_INVALID_ARG;
   if (batch > 0 && n > 0 && x == nullptr) return CR_ERR_INVALID_ARG;
   if ((x && !aligned(x, sz)) || (out && !aligned(out, sz))) return CR_ERR_INVALID_ARG;
@@ -141,6 +167,12 @@ static cr_status scan_impl(const void* x, void* out, int64_t batch, int64_t n, i
     if (a < o + (size_t)m * sz && o < a + (size_t)n * sz) return CR_ERR_INVALID_ARG;
   }
   if (!contiguous && x == out && x != nullptr && (oes != es || obs != bs))
+    return CR_ERR_INVALID_ARG;
+  // out != x over dense layouts on both sides: any shared byte is a partial
+  // overlap (an output would overwrite an input another sequence reads)
+  if (!contiguous && x != out && batch > 0 && n > 0 && m > 0 &&
+      dense_layout(n, batch, es, bs) && dense_layout(m, batch, oes, obs) &&
+      ranges_meet(x, (size_t)(n * batch) * sz, out, (size_t)(m * batch) * sz))
     return CR_ERR_INVALID_ARG;
   const cr::ScanPlan plan = cr::plan_scan(batch, n, p, B, sz, mode);
   const cr_status ws_ok = check_ws(ws, ws_bytes, plan.ws_bytes);

@@ -1586,13 +1586,13 @@ int fused_grid_limit() {
 
 }  // namespace
 
+namespace {
+
+// Passes 7 to 9 as separate launches: the walk, the check of its rises, the
+// fill, and the serial chain that runs only when any of them failed.
 template <class T>
-cudaError_t run_chain(const ChainPlan& p, const T* src, T* dst, char* ws, cudaStream_t s,
-                      T* final_out) {
-  if (p.K <= 0) return cudaSuccess;
-  const ChainWs w(p, ws);
-  cudaError_t e = run_chain_front<T>(p, src, ws, w, s);
-  if (e != cudaSuccess) return e;
+cudaError_t run_chain_back(const ChainPlan& p, const T* src, T* dst, const ChainWs& w,
+                           cudaStream_t s, T* final_out) {
   const unsigned g = (unsigned)p.ntiles;
   CR_LAUNCH(kKChainWalk, s,
             chain_walk_kernel<T><<<1, 32, 0, s>>>(src, dst, w.segs, w.total, p.seg_cap, w.m_in,
@@ -1610,12 +1610,25 @@ cudaError_t run_chain(const ChainPlan& p, const T* src, T* dst, char* ws, cudaSt
   return cudaGetLastError();
 }
 
+}  // namespace
+
+template <class T>
+cudaError_t run_chain(const ChainPlan& p, const T* src, T* dst, char* ws, cudaStream_t s,
+                      T* final_out) {
+  if (p.K <= 0) return cudaSuccess;
+  const ChainWs w(p, ws);
+  cudaError_t e = run_chain_front<T>(p, src, ws, w, s);
+  if (e != cudaSuccess) return e;
+  return run_chain_back<T>(p, src, dst, w, s, final_out);
+}
+
 template <class T>
 cudaError_t run_chain_fixup(const ChainPlan& p, const T* src, T* dst, char* ws, T* out,
                             int64_t n, int logB, cudaStream_t s, const int** fail,
-                            bool debug_fail) {
+                            bool* fused, bool debug_fail, bool debug_refuse) {
   const ChainWs w(p, ws);
   *fail = w.fail;
+  *fused = false;
   if (p.K <= 0 || p.K > (out != nullptr ? kMaxFusedChain : kMaxFusedChainAlone) ||
       (out != nullptr && (logB < 1 || logB > 40)))
     return cudaErrorInvalidValue;
@@ -1648,18 +1661,27 @@ cudaError_t run_chain_fixup(const ChainPlan& p, const T* src, T* dst, char* ws, 
   f.nfill = p.ntiles < kMaxFillBlocks ? p.ntiles : kMaxFillBlocks;
   if (f.nfill > limit / kFillShareDiv) f.nfill = limit / kFillShareDiv;
   if (out == nullptr) f.nfill = p.ntiles < limit - 1 ? p.ntiles : limit - 1;  // all fill
-  if (f.nfill < 1) return cudaErrorInvalidConfiguration;
-  const int64_t fixers = (f.nitems + kCT / 32 - 1) / (kCT / 32);  // 8 warps a block
-  const int64_t room = limit - 1 - f.nfill;
-  const unsigned grid = (unsigned)(1 + f.nfill + (fixers < room ? fixers : room));
-  void* args[] = {(void*)&src, (void*)&dst, (void*)&out, (void*)&f};
-  CR_LAUNCH(kKChainWalkFix, s,
-            e = cudaLaunchCooperativeKernel((const void*)chain_walk_fix_kernel<T>, dim3(grid),
-                                            dim3(kCT), args, 0, s));
-  if (e != cudaSuccess) return e;
-  CR_LAUNCH(kKChainFallback, s,
-            chain_serial_kernel<T><<<1, 32, 0, s>>>(src, dst, p.K, w.fail, nullptr));
-  return cudaGetLastError();
+  if (f.nfill >= 1 && !debug_refuse) {
+    const int64_t fixers = (f.nitems + kCT / 32 - 1) / (kCT / 32);  // 8 warps a block
+    const int64_t room = limit - 1 - f.nfill;
+    const unsigned grid = (unsigned)(1 + f.nfill + (fixers < room ? fixers : room));
+    void* args[] = {(void*)&src, (void*)&dst, (void*)&out, (void*)&f};
+    CR_LAUNCH(kKChainWalkFix, s,
+              e = cudaLaunchCooperativeKernel((const void*)chain_walk_fix_kernel<T>, dim3(grid),
+                                              dim3(kCT), args, 0, s));
+    if (e == cudaSuccess) {
+      *fused = true;
+      CR_LAUNCH(kKChainFallback, s,
+                chain_serial_kernel<T><<<1, 32, 0, s>>>(src, dst, p.K, w.fail, nullptr));
+      return cudaGetLastError();
+    }
+    // The cooperative launch was refused (fewer resident blocks than the
+    // occupancy query promised: another context on the device, a smaller SM
+    // partition). A refused launch enqueues nothing and its error is not
+    // sticky: clear it and take the separate passes, whose result is the same.
+    (void)cudaGetLastError();
+  }
+  return run_chain_back<T>(p, src, dst, w, s, nullptr);
 }
 
 template <class T>
@@ -1686,10 +1708,10 @@ template cudaError_t run_chain<double>(const ChainPlan&, const double*, double*,
                                        cudaStream_t, double*);
 template cudaError_t run_chain_fixup<double>(const ChainPlan&, const double*, double*, char*,
                                              double*, int64_t, int, cudaStream_t, const int**,
-                                             bool);
+                                             bool*, bool, bool);
 template cudaError_t run_chain_fixup<float>(const ChainPlan&, const float*, float*, char*,
                                             float*, int64_t, int, cudaStream_t, const int**,
-                                            bool);
+                                            bool*, bool, bool);
 template cudaError_t run_fixup_again<double>(double*, const double*, int64_t, int, const int*,
                                              cudaStream_t);
 template cudaError_t run_fixup_again<float>(float*, const float*, int64_t, int, const int*,

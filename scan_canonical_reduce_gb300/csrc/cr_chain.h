@@ -46,12 +46,16 @@ cudaError_t run_serial_chain(const T* src, T* dst, int64_t K, cudaStream_t s,
 // time limit). With out == nullptr the pass is the chain alone (its fill
 // overlapping the walk); the serial chain has then already rewritten dst on
 // a failure, and nothing else is needed.
+// *fused tells whether the cooperative pass ran. When the device refuses
+// the cooperative launch (or debug_refuse asks to act as if it had), the
+// chain runs as separate passes (the same values in dst) and out is left
+// untouched: the caller then applies the carries with a plain fix-up.
 // debug_fail: a test hook; a second warp of the walking block sets *fail
 // once the walk is half-way, so that the recovery runs.
 template <class T>
 cudaError_t run_chain_fixup(const ChainPlan& plan, const T* src, T* dst, char* ws, T* out,
                             int64_t n, int logB, cudaStream_t s, const int** fail,
-                            bool debug_fail = false);
+                            bool* fused, bool debug_fail = false, bool debug_refuse = false);
 template <class T>
 cudaError_t run_fixup_again(T* out, const T* carries, int64_t n, int logB, const int* fail,
                             cudaStream_t s);

@@ -58,10 +58,10 @@ HostPipe g_pipes[64];
 
 std::mutex& host_pipe_mutex() { return g_pipe_mu; }
 
-HostPipe& host_pipe() {
-  int dev = 0;
-  cudaGetDevice(&dev);
-  return g_pipes[(dev >= 0 && dev < 64) ? dev : 0];
+HostPipe* host_pipe() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  return &g_pipes[dev];
 }
 
 const char* kernel_name(int id) {

@@ -65,7 +65,9 @@ struct HostPipe {
   cudaError_t ensure(int chunks);  // streams, and at least `chunks` event pairs
 };
 std::mutex& host_pipe_mutex();
-HostPipe& host_pipe();  // the current device's
+// The current device's; nullptr when there is no current device or its index
+// is 64 or more (the callers then fail with cudaErrorInvalidDevice).
+HostPipe* host_pipe();
 
 // Usage: CR_LAUNCH(kKScanUp, stream, kernel<<<grid, block, 0, stream>>>(...));
 #define CR_LAUNCH(ID, STREAM, ...)                  \

@@ -10,9 +10,13 @@
 // exits. It allocates no device memory and calls no allocating routine.
 //
 // Host code never passes `g_noalloc_scratch` itself to a kernel: on the host
-// that name is only a stand-in for the device symbol. The first call on each
-// device looks up the symbol's device address with cudaGetSymbolAddress (that
-// device current) and keeps it; later calls on that device reuse it.
+// that name is only a stand-in for the device symbol. Every call that is not
+// being captured into a CUDA graph looks up the symbol's device address with
+// cudaGetSymbolAddress (the call's device current) and keeps it; a call made
+// while its stream is capturing reuses the address kept for that device, so
+// the first call on a device must come before any capture. Looking the
+// address up again outside capture keeps it valid after cudaDeviceReset,
+// which reloads the module at a new address.
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -30,17 +34,21 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device (set up once).
-cr_status scratch_on_current_device(void** ptr) {
+// Device address of the scratch array on the current device.
+cr_status scratch_on_current_device(cudaStream_t s, void** ptr) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return CR_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return CR_ERR_UNSUPPORTED;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return CR_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
+  if (cap == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
       return CR_ERR_CUDA;
     g_scratch_ptr[dev] = p;
+  } else if (g_scratch_ptr[dev] == nullptr) {
+    return CR_ERR_UNSUPPORTED;  // no call on this device before the capture
   }
   *ptr = g_scratch_ptr[dev];
   return CR_OK;
@@ -60,10 +68,10 @@ extern "C" cr_status cr_reduce_noalloc(const void* x, int64_t n, int32_t L,
     return CR_ERR_INVALID_ARG;
   const cr::ReducePlan plan = cr::plan_reduce(1, n, L, 1, n, sz);
   if (plan.ws_bytes > kNoAllocScratchBytes) return CR_ERR_WORKSPACE;  // too large for it
-  void* ws = nullptr;
-  const cr_status st = scratch_on_current_device(&ws);
-  if (st != CR_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  const cr_status st = scratch_on_current_device(s, &ws);
+  if (st != CR_OK) return st;
   // the array keeps the previous call's contents: clear the status word; the
   // reduce passes initialise every other word they read before reading it
   if (cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return CR_ERR_CUDA;

@@ -501,7 +501,9 @@ cudaError_t run_reduce_host(const ReducePlan& plan, const T* x_host, T* x_dev, T
   const int64_t C = p0.a.C, tiles = p0.a.tiles, per_chunk = p0.a.T * p0.a.L;
   const int groups = C < 32 ? (int)C : 32;
   std::lock_guard<std::mutex> lock(host_pipe_mutex());
-  HostPipe& hp = host_pipe();
+  HostPipe* pipe = host_pipe();
+  if (pipe == nullptr) return cudaErrorInvalidDevice;
+  HostPipe& hp = *pipe;
   if ((e = hp.ensure(groups + 1)) != cudaSuccess) return e;
   if ((e = cudaEventRecord(hp.start, s)) != cudaSuccess) return e;  // after the caller's work
   if ((e = cudaStreamWaitEvent(hp.in, hp.start, 0)) != cudaSuccess) return e;

@@ -1037,6 +1037,7 @@ std::atomic<int> g_fused_mode{0};
 }
 bool fused_fixup_disabled() { return g_fused_mode.load() == 1; }
 bool debug_fused_fail() { return g_fused_mode.load() == 2; }
+bool debug_coop_refused() { return g_fused_mode.load() == 4; }
 bool fused_fixup_forced() { return g_fused_mode.load() >= 2; }
 void set_debug_fused_mode(int mode) { g_fused_mode.store(mode); }
 
@@ -1326,9 +1327,12 @@ struct Tiled {
   // recomputes the local pass from x).
   cudaError_t fused_middle_second(const T* x, T* out, cudaStream_t s) {
     const int* fail = nullptr;
+    bool fused = false;
     cudaError_t e = run_chain_fixup<T>(plan.chain, totals, carries, ws + plan.chain_ws, out,
-                                       plan.n, plan.logB, s, &fail, debug_fused_fail());
+                                       plan.n, plan.logB, s, &fail, &fused, debug_fused_fail(),
+                                       debug_coop_refused());
     if (e != cudaSuccess) return e;
+    if (!fused) return second(x, out, 0, plan.n_tiles, s);  // carries ready: plain fix-up
     a.tile_base = 0;
     const unsigned grid = (unsigned)(plan.n_tiles < 1216 ? plan.n_tiles : 1216);
     CR_LAUNCH(kKScanLocalAgain, s, {
@@ -1469,8 +1473,10 @@ cudaError_t run_scan(const ScanPlan& plan, const T* x, T* out, int64_t es, int64
           // the fill of each tile overlaps the rest of the walk (one
           // cooperative pass); on a failure the serial chain rewrites dst
           const int* fail = nullptr;
+          bool fused = false;
           if ((e = run_chain_fixup<T>(plan.chain, src, dst, ws + plan.chain_ws, nullptr, 0, 0, s,
-                                      &fail, debug_fused_fail())) != cudaSuccess)
+                                      &fail, &fused, debug_fused_fail(),
+                                      debug_coop_refused())) != cudaSuccess)
             return e;
         } else if ((e = run_chain<T>(plan.chain, src, dst, ws + plan.chain_ws, s)) !=
                    cudaSuccess) {
@@ -1523,7 +1529,9 @@ cudaError_t run_scan_host(const ScanPlan& plan, const T* x_host, T* out_host, T*
   if (per < 256) per = 256;
   const int64_t nchunks = (tiles + per - 1) / per;
   std::lock_guard<std::mutex> lock(host_pipe_mutex());  // host-buffer calls share the streams
-  HostPipe& hp = host_pipe();
+  HostPipe* pipe = host_pipe();
+  if (pipe == nullptr) return cudaErrorInvalidDevice;
+  HostPipe& hp = *pipe;
   if ((e = hp.ensure((int)nchunks)) != cudaSuccess) return e;
   cudaStream_t cin = hp.in, cout = hp.out;
   // the caller's stream may hold earlier work on these buffers: start after it

@@ -170,3 +170,78 @@ def test_stride_errors(scr):
     # one sequence of one output may use a zero output stride (workspace check next)
     assert L.cr_scan_ex_batched(fake, ws, 1, 0, 1, 1, 0, 0, 0, 1, 2, ctypes.byref(one), 2,
                                 fake, 8, None) == 3
+
+
+def test_batched_overlap_errors(scr):
+    """Batched layouts whose outputs would meet: equal output strides with two
+    or more sequences of two or more outputs, and an output that partially
+    overlaps a densely laid out input (rows or level-major columns). A zero
+    output stride in an empty batch, and interleaved (non-dense) layouts,
+    are not rejected for that reason (the fake workspace fails next)."""
+    L = scr.lib()
+    one = ctypes.c_double(0.0)
+    x = 0x10000
+    ws = ctypes.c_void_p(0x100000)
+
+    def p(addr):
+        return ctypes.c_void_p(addr)
+
+    # out == x with element and sequence strides both 1: (b + 1, k) is (b, k + 1)
+    assert L.cr_inclusive_scan_batched(p(x), p(x), 2, 10, 1, 1, 0, 1, 2, ws, 1 << 20,
+                                       None) == 1
+    assert L.cr_scan_ex_batched(p(x), p(0x90000), 2, 10, 1, 10, 1, 1, 0, 1, 2,
+                                ctypes.byref(one), 2, ws, 1 << 20, None) == 1
+    # an empty batch may carry any output strides
+    assert L.cr_scan_ex_batched(p(x), p(0x90000), 0, 10, 1, 10, 0, 0, 0, 1, 2,
+                                ctypes.byref(one), 2, ws, 8, None) == 3
+    # rows of 10: out one element after x overlaps every row but the first
+    assert L.cr_inclusive_scan_batched(p(x), p(x + 8), 4, 10, 1, 10, 0, 1, 2, ws, 1 << 20,
+                                       None) == 1
+    # level-major columns: out one level below x
+    assert L.cr_inclusive_scan_batched(p(x), p(x + 8 * 4), 4, 10, 4, 1, 0, 1, 2, ws, 1 << 20,
+                                       None) == 1
+    # include_initial output rows of 11 ending inside the input rows
+    assert L.cr_scan_ex_batched(p(x + 8 * 40 - 8), p(x), 4, 10, 1, 10, 1, 11, 0, 1, 2,
+                                ctypes.byref(one), 2, ws, 1 << 20, None) == 1
+    # a batched reduce writing its results into its own rows
+    assert L.cr_reduce_batched(p(x), p(x + 16), 4, 10, 1, 10, 16, ctypes.byref(one), 2, ws,
+                               1 << 20, None) == 1
+    # interleaved: x on even elements, out on odd ones (not dense): allowed
+    assert L.cr_inclusive_scan_batched(p(x), p(x + 8), 4, 10, 2, 20, 0, 1, 2, ws, 8,
+                                       None) == 3
+    assert L.cr_reduce_batched(p(x), p(x + 8 * 40), 4, 10, 1, 10, 16, ctypes.byref(one), 2,
+                               ws, 8, None) == 3
+
+
+def test_batched_host_argument_errors(scr):
+    """The host-buffer batched calls check their arguments, the device
+    buffer and the host layout before any CUDA call."""
+    L = scr.lib()
+    one = ctypes.c_double(0.0)
+    x, o = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x90000)
+    ws = ctypes.c_void_p(0x100000)
+    need = L.cr_reduce_batched_host_workspace_bytes(10, 10, 16, 2)
+    assert need >= 256 and need % 256 == 0
+    assert L.cr_reduce_batched_host_workspace_bytes(10, 10, 0, 2) == 0
+    assert L.cr_inclusive_scan_batched_host_workspace_bytes(10, 10, 3, 3, 2) == 0
+    # negative strides, bad dtype
+    assert L.cr_reduce_batched_host(x, o, 10, 10, -1, 10, 16, ctypes.byref(one), 2, ws,
+                                    need, None) == 1
+    assert L.cr_reduce_batched_host(x, o, 10, 10, 1, 10, 16, ctypes.byref(one), 7, ws,
+                                    need, None) == 1
+    # the device buffer too small
+    assert L.cr_reduce_batched_host(x, o, 10, 10, 1, 10, 16, ctypes.byref(one), 2, ws,
+                                    need - 256, None) == 3
+    # neither rows nor level-major columns
+    assert L.cr_reduce_batched_host(x, o, 10, 10, 2, 3, 16, ctypes.byref(one), 2, ws,
+                                    need, None) == 2
+    sneed = L.cr_inclusive_scan_batched_host_workspace_bytes(10, 10, 0, 1, 2)
+    assert L.cr_inclusive_scan_batched_host(x, o, 10, 10, 2, 30, 0, 1, 2, ws, sneed,
+                                            None) == 2
+    # a zero stride sends two outputs to one element
+    assert L.cr_inclusive_scan_batched_host(x, o, 10, 10, 0, 1, 0, 1, 2, ws, sneed,
+                                            None) == 2
+    # empty batches need no GPU
+    assert L.cr_reduce_batched_host(x, o, 0, 10, 1, 10, 16, ctypes.byref(one), 2, ws, 256,
+                                    None) == 0
+    assert L.cr_inclusive_scan_batched_host(x, o, 10, 0, 1, 0, 0, 1, 2, ws, 256, None) == 0

@@ -190,3 +190,24 @@ def test_parallel_chain_needs_no_recovery(scr, policy, B, n):
     rec = [(k, ms) for k, ms in prof if k in RECOVERY]
     assert rec, prof  # launched, as on every call
     assert all(ms < 0.5 for _, ms in rec), rec
+
+
+@pytest.mark.parametrize("B", [2, 16, 256])
+def test_cooperative_launch_refused(scr, B):
+    """A device that refuses the cooperative launch (acted out by the
+    library's hook, mode 4: nothing is launched that could fail): the chain
+    runs as separate passes and a plain fix-up applies its carries; 0 ULP
+    against the oracle, bit-equal to the fused pass."""
+    n = B * (3 * 4096 + 5) + B // 2 + 1
+    x = W.uniform_pm1(n, W.seed_for(35, B))
+    want = oracle.scan(x, "block_dyadic", B)
+    refused = scan_mode(scr, x, B, 4)
+    assert first_diff(refused, want) is None, (B, first_diff(refused, want))
+    assert first_diff(scan_mode(scr, x, B, 3), refused) is None
+
+
+def test_left_fold_cooperative_launch_refused(scr):
+    x = W.uniform_pm1(300007, W.seed_for(35, 1))
+    want = oracle.scan(x, "left_fold", 1)
+    got = fold_mode(scr, x, 4)
+    assert first_diff(got, want) is None, first_diff(got, want)

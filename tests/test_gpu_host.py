@@ -101,3 +101,101 @@ def test_reduce_host_full_size(scr):
     for L in (16, 128, 1024):
         got = scr.reduce(h, L, 0.0)
         assert bits(got.numpy()[0]) == bits(oracle.reduce(x, L, 0.0)), L
+
+
+@pytest.mark.parametrize("dtype", [np.float64, np.float32])
+def test_reduce_batched_host(scr, dtype):
+    """cr_reduce_batched_host: rows and level-major columns, padded rows,
+    one group and several groups (a ragged last one), against the oracle."""
+    for rows, cols in ((3, 1000), (300, 4096 + 37), (2100, 16384 + 5)):
+        buf = W.signed_pow2(rows * cols, W.seed_for(4, rows % 61), dtype)
+        t = torch.from_numpy(buf).view(rows, cols).pin_memory()
+        for L in (1, 16, 128):
+            got = scr.reduce_batched(t, L, 0.5, dim=-1)
+            assert not got.is_cuda
+            want = oracle.reduce_batched(buf, rows, cols, 1, cols, L, dtype(0.5))
+            assert bits(got.numpy()) == bits(want), (rows, cols, L)
+            gotc = scr.reduce_batched(t, L, 0.5, dim=0)
+            wantc = oracle.reduce_batched(buf, cols, rows, cols, 1, L, dtype(0.5))
+            assert bits(gotc.numpy()) == bits(wantc), (rows, cols, L)
+    # rows with padding (batch_stride > n), pageable memory
+    rows, cols, pad = 500, 3000, 13
+    buf = W.signed_pow2(rows * (cols + pad), W.seed_for(4, 7), dtype)
+    view = torch.from_numpy(buf).view(rows, cols + pad)[:, :cols]
+    got = scr.reduce_batched(view, 16, -1.0, dim=-1)
+    want = oracle.reduce_batched(buf, rows, cols, 1, cols + pad, 16, dtype(-1.0))
+    assert bits(got.numpy()) == bits(want)
+
+
+def test_reduce_batched_host_full_size(scr):
+    """The benchmark's row reduces from host buffers (65,536 x 4,096 and
+    1,024 x 262,144 binary32, L = 128), sampled rows against the oracle."""
+    for rows, cols in ((65536, 4096), (1024, 262144)):
+        x = W.family4(rows, cols)
+        got = scr.reduce_batched(torch.from_numpy(x).pin_memory(), 128, 0.0).numpy()
+        dev = scr.reduce_batched(torch.from_numpy(x).cuda(), 128, 0.0).cpu().numpy()
+        assert bits(got) == bits(dev)
+        rng = np.random.default_rng(2)
+        for r in list(rng.choice(rows, 32, replace=False)) + [0, rows - 1]:
+            want = oracle.reduce(x[r].copy(), 128, np.float32(0.0))
+            assert bits(got[r]) == bits(want), r
+
+
+@pytest.mark.parametrize("dtype", [np.float64, np.float32])
+@pytest.mark.parametrize("policy,B", [("left_fold", 1), ("block_dyadic", 16),
+                                      ("iterated_pairwise", 1), ("pairwise", 1),
+                                      ("block_dyadic", 4)])
+def test_scan_batched_host(scr, dtype, policy, B):
+    """cr_inclusive_scan_batched_host on level-major columns (the column-scan
+    shape, several groups) and on rows, against the oracle; in place too."""
+    levels, ncols = 90, 20000 + 3
+    buf = W.lognormal(levels * ncols, W.seed_for(5, 3)).astype(dtype)
+    t = torch.from_numpy(buf).view(levels, ncols).pin_memory()
+    got = scr.inclusive_scan_batched(t, policy, B, dim=0)
+    assert not got.is_cuda
+    want = oracle.scan_batched(buf, ncols, levels, ncols, 1, policy, B)
+    assert bits(got.numpy().reshape(-1)) == bits(want)
+    # rows: 700 sequences of 5000 elements
+    rows, n = 700, 5000
+    rb = W.signed_pow2(rows * n, W.seed_for(5, 4), dtype)
+    tr = torch.from_numpy(rb).view(rows, n).pin_memory()
+    gr = scr.inclusive_scan_batched(tr, policy, B, dim=-1)
+    wr = oracle.scan_batched(rb, rows, n, 1, n, policy, B)
+    assert bits(gr.numpy().reshape(-1)) == bits(wr)
+    # in place (out is x)
+    scr.inclusive_scan_batched(t, policy, B, dim=0, out=t)
+    assert bits(t.numpy().reshape(-1)) == bits(want)
+
+
+def test_scan_batched_host_full_size(scr):
+    """The benchmark's column scans (90 x 200,000 fp64) from host buffers."""
+    x = W.family5(90, 200000)
+    t = torch.from_numpy(x).view(90, 200000).pin_memory()
+    for policy, B in (("block_dyadic", 16), ("left_fold", 1)):
+        got = scr.inclusive_scan_batched(t, policy, B, dim=0)
+        want = oracle.scan_batched(x, 200000, 90, 200000, 1, policy, B)
+        assert bits(got.numpy().reshape(-1)) == bits(want), policy
+
+
+def test_batched_host_layout_errors(scr):
+    """A layout that is neither rows nor level-major columns is unsupported
+    by the host-buffer calls; an output that partially overlaps the input is
+    rejected."""
+    import ctypes
+    L = scr.lib()
+    x = torch.zeros(4000, dtype=torch.float64).pin_memory()
+    out = torch.zeros(4000, dtype=torch.float64).pin_memory()
+    ws = scr.workspace("cuda", None, 1 << 24)
+    one = ctypes.c_double(0.0)
+    # element stride 2 and sequence stride 3: neither layout
+    assert L.cr_reduce_batched_host(x.data_ptr(), out.data_ptr(), 10, 10, 2, 3, 16,
+                                    ctypes.byref(one), 2, ws.data_ptr(), ws.numel(),
+                                    None) == 2
+    assert L.cr_inclusive_scan_batched_host(x.data_ptr(), out.data_ptr(), 10, 10, 2, 30, 0, 1,
+                                            2, ws.data_ptr(), ws.numel(), None) == 2
+    # out one element into x's rows
+    assert L.cr_inclusive_scan_batched_host(x.data_ptr(), x.data_ptr() + 8, 10, 10, 1, 10, 0,
+                                            1, 2, ws.data_ptr(), ws.numel(), None) == 1
+    assert L.cr_reduce_batched_host(x.data_ptr(), x.data_ptr() + 80, 10, 10, 1, 10, 16,
+                                    ctypes.byref(one), 2, ws.data_ptr(), ws.numel(),
+                                    None) == 1

@@ -167,3 +167,47 @@ def test_reduce_rows_one_warp_per_row(scr, dtype, L):
         got = scr.reduce_batched(view, L, -1.0).cpu().numpy()
         want = oracle.reduce_batched(x[off:].copy(), rows, cols, 1, stride, L, dtype(-1.0))
         assert bits(got) == bits(want), (pad, off)
+
+
+def _oracle_reduce_all(x, lanes, init):
+    """oracle.reduce for several lane counts at once (the oracle is
+    single-threaded; its ctypes calls release the GIL)."""
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(len(lanes)) as ex:
+        futs = {L: ex.submit(oracle.reduce, x, L, init) for L in lanes}
+        return {L: f.result() for L, f in futs.items()}
+
+
+@pytest.mark.parametrize("n", [(1 << 28), (1 << 28) + 37])
+def test_reduce_full_size_fp32(scr, n):
+    """The sweep's binary32 rows at n = 2^28 and 2^28 + 37 (family-2 values:
+    reassociation changes the bits), L = 16, 128 and 1024, 0 ULP: the deepest
+    binary32 pyramids."""
+    x = W.family2(n, np.float32)
+    xd = torch.from_numpy(x).to(DEV)
+    lanes = (16, 128, 1024)
+    want = _oracle_reduce_all(x, lanes, np.float32(0.0))
+    for L in lanes:
+        got = scr.reduce(xd, L, 0.0).cpu().numpy()[0]
+        assert bits(got) == bits(want[L]), (n, L)
+
+
+def test_reduce_full_size_fp64_two_to_thirty(scr):
+    """n = 2^30, family-2 values (not integers: every level of the pyramid,
+    the third included, decides bits), L = 16 and 1024, 0 ULP."""
+    n = 1 << 30
+    x = W.family2(n)
+    xd = torch.from_numpy(x).to(DEV)
+    lanes = (16, 1024)
+    want = _oracle_reduce_all(x, lanes, 0.0)
+    for L in lanes:
+        got = scr.reduce(xd, L, 0.0).cpu().numpy()[0]
+        assert bits(got) == bits(want[L]), L
+
+
+@pytest.mark.parametrize("L", [16, 128])
+def test_reduce_uniform01_two_to_twenty(scr, L):
+    """The golden-value setup's shape: binary64, n = 2^20, U[0, 1) values,
+    init +0.0, L = 16 and 128, 0 ULP."""
+    x = W.family1(1 << 20)
+    check_reduce(scr, x, L, 0.0)

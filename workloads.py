@@ -25,12 +25,17 @@ Workload families (the sizes are those of the benchmark configurations):
 """
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 
 GOLDEN = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 _CHUNK = 1 << 20
+_THREADS = max(1, min(16, len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity")
+                                else (os.cpu_count() or 1)))
 
 SEED_BASE = 0xC0DE0000
 
@@ -77,19 +82,33 @@ def splitmix64(seed: int, start: int, count: int) -> np.ndarray:
 
 def _fill(n: int, seed: int, dtype, fn) -> np.ndarray:
     """out[i] = fn(bits of stream ``seed`` at i, bits of stream ``seed ^ 0x5A5A``
-    at i) built chunk by chunk."""
+    at i) built chunk by chunk. Large arrays are built by several threads, each
+    on its own chunks (numpy's arithmetic releases the GIL); every element
+    depends on its index alone, so the result does not depend on the split."""
     out = np.empty(n, dtype=dtype)
     if n == 0:
         return out
-    c0 = min(_CHUNK, n)
-    st = _Stream(c0)
-    u = np.empty(c0, dtype=np.uint64)
-    v = np.empty(c0, dtype=np.uint64)
-    for s in range(0, n, _CHUNK):
-        c = min(_CHUNK, n - s)
-        uu = st.bits(seed, s, u[:c])
-        vv = st.bits(seed ^ 0x5A5A, s, v[:c]) if fn.__code__.co_argcount == 2 else None
-        out[s:s + c] = fn(uu, vv) if vv is not None else fn(uu)
+    two = fn.__code__.co_argcount == 2
+    nchunks = (n + _CHUNK - 1) // _CHUNK
+
+    def work(first: int, step: int) -> None:
+        c0 = min(_CHUNK, n)
+        st = _Stream(c0)
+        u = np.empty(c0, dtype=np.uint64)
+        v = np.empty(c0, dtype=np.uint64)
+        for j in range(first, nchunks, step):
+            s = j * _CHUNK
+            c = min(_CHUNK, n - s)
+            uu = st.bits(seed, s, u[:c])
+            out[s:s + c] = fn(uu, st.bits(seed ^ 0x5A5A, s, v[:c])) if two else fn(uu)
+
+    workers = min(_THREADS, nchunks)
+    if workers <= 1:
+        work(0, 1)
+    else:
+        with ThreadPoolExecutor(workers) as ex:
+            for f in [ex.submit(work, w, workers) for w in range(workers)]:
+                f.result()
     return out
 
 
