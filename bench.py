@@ -102,6 +102,14 @@ def extra_rows():
           ("scan_block_dyadic_16_include_initial", "scan_ex",
            {"policy": "block_dyadic", "B": 16, "mode": "include_initial"}, 16 * N + 8,
            adds_block_dyadic(N, 16) + N, "f64")]
+    # binary32 scans of the same input rounded to binary32 (the carry chains
+    # of left_fold and block_dyadic through the estimated-chain classification)
+    for pol, B in (("iterated_pairwise", 1), ("pairwise", 1), ("block_dyadic", 16),
+                   ("block_dyadic", 256), ("left_fold", 1)):
+        name = "scan_%s%s_f32" % (pol, "_%d" % B if pol == "block_dyadic" else "")
+        adds = {"iterated_pairwise": adds_iterated(N), "pairwise": adds_pairwise(N),
+                "block_dyadic": adds_block_dyadic(N, B), "left_fold": N - 1}[pol]
+        rs.append((name, "scan", {"policy": pol, "B": B, "dt": "f32"}, 8 * N, adds, "f32"))
     for dt, es in (("f64", 8), ("f32", 4)):
         for n in SWEEP_N:
             for L in (16, 128, 1024):
@@ -299,6 +307,8 @@ def run_native(args):
     x1 = torch.from_numpy(hin["f1"]).to(dev)
     x4b = torch.from_numpy(hin["f4b"]).to(dev)
     x3 = torch.from_numpy(hin["f3"]).to(dev)
+    x3f = x3.float()  # the 1-D scan input rounded to binary32
+    y_scan32 = torch.empty_like(x3f)
     x4 = torch.from_numpy(hin["f4"]).to(dev)
     x5 = torch.from_numpy(hin["f5"]).to(dev).view(COLS_LEVELS, COLS_N)
     y_scan = torch.empty_like(x3)
@@ -322,7 +332,10 @@ def run_native(args):
         elif kind == "rows_b":
             scr.reduce_batched(x4b, p["L"], 0.0, dim=-1, out=rows_out_b)
         elif kind == "scan":
-            scr.inclusive_scan(x3, p["policy"], p["B"], out=y_scan)
+            if p.get("dt", "f64") == "f32":
+                scr.inclusive_scan(x3f, p["policy"], p["B"], out=y_scan32)
+            else:
+                scr.inclusive_scan(x3, p["policy"], p["B"], out=y_scan)
         elif kind == "scan_ex":
             if p["mode"] == "exclusive":
                 scr.exclusive_scan(x3, p["policy"], p["B"], 0.5, out=y_scan)

@@ -129,9 +129,14 @@ size_t cr_scan_workspace_bytes(int64_t n, cr_policy p, int64_t B, cr_dtype dt);
  * other overlap is INVALID_ARG. n == 0 writes nothing. No init: a scan
  * observes the expression itself.
  * Cost: the carry chain of CR_LEFT_FOLD and CR_BLOCK_DYADIC (ceil(n/B)
- * dependent adds) is evaluated exactly in parallel for binary64, and for
- * binary32 chains of at most 4096 carries; a longer binary32 chain runs one
- * add at a time on the device (about 3 ns an add on GB300). */
+ * dependent adds) is evaluated exactly in parallel, every step checked
+ * exactly against the add it replaces. Binary64 steps are classified against
+ * a rigorous error bound; binary32 steps against an estimate of the binary32
+ * chain's own rounding with a statistical margin. Where a check fails (in
+ * practice: binary32 chains whose rounding is biased for long stretches,
+ * such as sums of positive values far below the chain's unit), the chain is
+ * recomputed one add at a time on the device (about 3 ns an add on GB300):
+ * the result is exact either way. */
 cr_status cr_inclusive_scan(const void* x, void* out, int64_t n, cr_policy p, int64_t B,
                             cr_dtype dt, void* ws, size_t ws_bytes, void* stream);
 

@@ -503,6 +503,49 @@ __device__ __forceinline__ double block_excl_sum(double v, double* sh_w) {
   return base + incl - v;
 }
 
+// The type, integer offset and meta word of step k from its classification
+// (certain c, sign ng, binade e) and the previous step's (pc, pe), and the
+// thread's composed map after it (me; nbrk counts breaks).
+template <class T>
+__device__ __forceinline__ void step_record(int64_t k, T t, bool c, bool ng, int e, bool pc,
+                                            int pe, Summ& me, int& nbrk, int64_t& q_out,
+                                            uint32_t& m_out) {
+  uint32_t type;
+  int d = 0;
+  int64_t q = 0;
+  uint32_t f = 0;
+  bool folded = false;
+  if (k == 0) {
+    type = kStart;
+  } else if (!c || !pc) {
+    type = kFp;
+  } else if (e <= pe) {  // same or lower binade: a composable step
+    d = pe - e;
+    type = (d <= 63 && split_unit<T>(t, e, q, f)) ? kMap : kFp;
+  } else {  // rise: T split in the old (finer) unit; a break unless the
+            // run's map since its start or last break dropped far enough
+    d = e - pe;
+    type = (d <= 8 && split_unit<T>(t, pe, q, f)) ? kUp : kFp;
+    if (type == kUp && rise_foldable(me.map, d)) {
+      type = kMap;
+      folded = true;
+    }
+  }
+  if (type == kFp) {
+    d = 0;
+    q = 0;
+  }
+  m_out = make_meta(type, c, ng, f, d, e) | (folded ? kFolded : 0u);
+  q_out = q;
+  if (type != kMap) {
+    me.map = map_id();
+    me.brk += 1;
+    nbrk += 1;
+  } else {
+    me.map = folded ? fold_rise(me.map, d, q, f != kFZero) : compose(me.map, step_map(d, q, f));
+  }
+}
+
 template <class T>
 __global__ void __launch_bounds__(kCT) chain_classify_kernel(
     const T* src, int64_t K, const double* toff, const double* bound, int64_t* qv,
@@ -543,41 +586,7 @@ __global__ void __launch_bounds__(kCT) chain_classify_kernel(
       bool c, ng;
       int e;
       classify<T>(run, mu, c, ng, e);
-      uint32_t type;
-      int d = 0;
-      int64_t q = 0;
-      uint32_t f = 0;
-      bool folded = false;
-      if (k == 0) {
-        type = kStart;
-      } else if (!c || !pc) {
-        type = kFp;
-      } else if (e <= pe) {  // same or lower binade: a composable step
-        d = pe - e;
-        type = (d <= 63 && split_unit<T>(tv[i], e, q, f)) ? kMap : kFp;
-      } else {  // rise: T split in the old (finer) unit; a break unless the
-                // run's map since its start or last break dropped far enough
-        d = e - pe;
-        type = (d <= 8 && split_unit<T>(tv[i], pe, q, f)) ? kUp : kFp;
-        if (type == kUp && rise_foldable(me.map, d)) {
-          type = kMap;
-          folded = true;
-        }
-      }
-      if (type == kFp) {
-        d = 0;
-        q = 0;
-      }
-      m_out[j] = make_meta(type, c, ng, f, d, e) | (folded ? kFolded : 0u);
-      q_out[j] = q;
-      if (type != kMap) {
-        me.map = map_id();
-        me.brk += 1;
-        nbrk += 1;
-      } else {
-        me.map = folded ? fold_rise(me.map, d, q, f != kFZero)
-                        : compose(me.map, step_map(d, q, f));
-      }
+      step_record<T>(k, tv[i], c, ng, e, pc, pe, me, nbrk, q_out[j], m_out[j]);
       pc = c;
       pe = e;
     }
@@ -587,6 +596,438 @@ __global__ void __launch_bounds__(kCT) chain_classify_kernel(
     store_run(qv + k0 + h * H, nh, q_out);
     store_run(meta + k0 + h * H, nh, m_out);
   }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) nbrk += __shfl_down_sync(full, nbrk, off);
+  if (lane == 0) cnt[w] = nbrk;
+  const Summ in = block_summ_scan(me, sh);  // synchronises: cnt visible
+  thr_in[blockIdx.x * kCT + t] = in;
+  if (t == 0) {  // one segment per break
+    int total = 0;
+    for (int i = 0; i < kCT / 32; ++i) total += cnt[i];
+    tile_nseg[blockIdx.x] = total;
+  }
+}
+
+// ---------------------------------------------------------------- binary32
+// A binary32 chain rounds to 24 bits, so over K steps its value drifts from
+// the exact prefix P_k by up to K ulp: a bound that rigorous leaves every
+// step of a long chain uncertain. For binary32 the classification therefore
+// compares against a better approximation of the chain itself and a
+// statistical margin; the exact checks of the later passes (and the serial
+// chain behind them) keep every result exact whatever the margin.
+//
+// The approximation is one Jacobi step from the exact prefix. Take the
+// binades from P (e of P_k for the sum of step k, ep of P_{k-1} for the
+// value before it). A step that stays in or drops to binade e adds T_k to a
+// multiple of u_e = 2^(e-23), so its rounding error is RN(T_k / u_e) u_e -
+// T_k, known from T_k's bits alone; then A_k = P_k + R_{k-1} with R the sum
+// of these errors approximates the exact sum of step k far better than P_k.
+// What stays unknown is the rounding of a tie (the chain value's parity
+// decides: error +-u/2) and of a rise (the previous value's low bits decide:
+// error within +-u/2 of the coarser unit). Counted as zero, they leave the
+// approximation a random error with variance V_{k-1} = sum of u^2/4 per tie
+// and u^2/12 per rise, and the margin of step k is kF32Sigmas sqrt(V_{k-1}).
+// On random-walk chains (the benchmark's U[-1, 1) block totals and left
+// folds, normal and power-of-two-scaled values) a host simulation of this
+// estimate found the largest error at 3.8 standard deviations over 2^28
+// steps. Chains whose rounding is biased for long stretches (positive values
+// far below the chain's unit) can leave the estimate off by more; their
+// checks then fail and the serial chain recomputes the result.
+//
+// P and R are kept as 128-bit fixed-point integers, value = I 2^-F, with F
+// chosen from the chain's length K and largest |T| so that every prefix fits
+// with 7 bits to spare: the sums are exact (each T and each estimated error
+// is rounded to the unit once, adding at most K units over the chain, a
+// rigorous part of the margin), every thread sees exactly the values its
+// neighbours computed, and no binary64 arithmetic is needed (GB300 issues
+// two binary64 operations a clock per SM, and integer ones at full rate).
+constexpr double kF32Sigmas = 8.0;
+using i128 = __int128;
+using u128 = unsigned __int128;
+
+// Index of the highest set bit of a nonzero value.
+__device__ __forceinline__ int hibit128(u128 v) {
+  const uint64_t hi = (uint64_t)(v >> 64);
+  return hi ? 127 - __clzll((long long)hi) : 63 - __clzll((long long)(uint64_t)v);
+}
+__device__ __forceinline__ u128 abs128(i128 v) { return v < 0 ? (u128)(-v) : (u128)v; }
+
+// The fixed-point scale F of a binary32 chain of K steps whose largest |T|
+// has the bit pattern maxbits: |every prefix| <= K max|T| < 2^(120 - F).
+// False when a T is not finite (every step is then left uncertain).
+__device__ __forceinline__ bool fix_scale(uint32_t maxbits, int64_t K, int& F) {
+  const int x = (int)((maxbits >> 23) & 0xFF);
+  if (x == 0xFF) return false;
+  const int emax = x == 0 ? -127 : x - 127;        // max|T| < 2^(emax + 1)
+  const int eK = 64 - __clzll((long long)K);        // K < 2^eK
+  F = 120 - eK - (emax + 1);
+  return true;
+}
+
+// t 2^F rounded to the nearest integer (halves away from zero).
+__device__ __forceinline__ i128 f32_to_fix(float t, int F) {
+  const uint32_t b = __float_as_uint(t);
+  const int x = (int)((b >> 23) & 0xFF);
+  uint32_t m = b & 0x7FFFFFu;
+  if (x == 0xFF || (x == 0 && m == 0)) return 0;
+  int et;  // |t| = m 2^et
+  if (x == 0) {
+    et = -149;
+  } else {
+    m |= 0x800000u;
+    et = x - 150;
+  }
+  const int sh = et + F;  // <= 96 by the choice of F
+  u128 mag;
+  if (sh >= 0) mag = (u128)m << sh;
+  else if (sh <= -26) mag = 0;
+  else mag = (u128)((m + (1u << (-sh - 1))) >> (-sh));
+  return (b >> 31) ? -(i128)mag : (i128)mag;
+}
+
+// The binade e (|value| in [2^e, 2^(e+1))) of a nonzero fixed-point value.
+__device__ __forceinline__ int fix_binade(i128 a, int F) { return hibit128(abs128(a)) - F; }
+
+// Rounding estimate of one binary32 step (see above): sp ~ C_{k-1} and s ~
+// the step's exact sum, in fixed point; t = T_k. r: the error RN(s) - s in
+// fixed point when known (else 0); v: the variance added when it is not.
+__device__ __forceinline__ void f32_round_est(i128 sp, i128 s, float t, int F, i128& r,
+                                              double& v) {
+  r = 0;
+  v = 0.0;
+  if (sp == 0 || s == 0) return;
+  const int e = fix_binade(s, F), ep = fix_binade(sp, F);
+  if (e > 127) return;                           // beyond binary32's range
+  const int ue = e - 23 < -149 ? -149 : e - 23;  // binary32 unit of binade e
+  if (e > ep) {                                  // a rise: u^2 / 12
+    v = __longlong_as_double((long long)(2 * ue - 4 + 1023) << 52) * (4.0 / 3.0);
+    return;
+  }
+  const uint32_t tb = __float_as_uint(t);
+  const int tx = (int)((tb >> 23) & 0xFF);
+  uint32_t m = tb & 0x7FFFFFu;
+  if (tx == 0xFF || (tx == 0 && m == 0)) return;
+  int et;  // |t| = m 2^et
+  if (tx == 0) {
+    et = -149;
+  } else {
+    m |= 0x800000u;
+    et = tx - 150;
+  }
+  const int sh = ue - et;  // |t| / u = m / 2^sh
+  if (sh <= 0) return;     // a multiple of u: added exactly
+  uint32_t err;            // |RN(|t|) - |t|| / 2^et
+  bool up;
+  if (sh >= 25) {  // |t| < u / 2: rounds to zero
+    err = m;
+    up = false;
+  } else {
+    const uint32_t U = 1u << sh, rem = m & (U - 1u), half = U >> 1;
+    if (rem == half) {  // a tie: u^2 / 4
+      v = __longlong_as_double((long long)(2 * ue - 2 + 1023) << 52);
+      return;
+    }
+    up = rem > half;
+    err = up ? U - rem : rem;
+  }
+  const int fs = et + F;  // err 2^et in units of 2^-F
+  u128 mag;
+  if (fs >= 0) mag = (u128)err << fs;
+  else if (fs <= -27) mag = 0;
+  else mag = (u128)(((uint64_t)err + (1ull << (-fs - 1))) >> (-fs));
+  r = (up != ((tb >> 31) != 0)) ? (i128)mag : -(i128)mag;
+}
+
+// The margin of a step in fixed-point units: kF32Sigmas sqrt(V) 2^F,
+// rounded up, plus K + 16 units for the rounding of the fixed-point sums
+// themselves. 2^126 (every step uncertain) when it does not fit.
+__device__ __forceinline__ u128 fix_margin(double V, int F, int64_t K) {
+  const u128 huge = (u128)1 << 126;
+  if (F < -1000 || F > 1000) return huge;
+  const double m = kF32Sigmas * sqrt(V > 0.0 ? V : 0.0) *
+                   __longlong_as_double((long long)(F + 1023) << 52);
+  const u128 rig = (u128)(uint64_t)K + 16u;
+  if (!(m < 0x1p125)) return huge;
+  if (m < 1.0) return rig + (m > 0.0 ? 1u : 0u);
+  const uint64_t b = (uint64_t)__double_as_longlong(m);
+  const int ex = (int)((b >> 52) & 0x7FF) - 1023;  // 0 <= ex < 125
+  const uint64_t mant = (b & ((uint64_t(1) << 52) - 1)) | (uint64_t(1) << 52);
+  const u128 q = ex >= 52 ? (u128)mant << (ex - 52) : (u128)((mant >> (52 - ex)) + 1);
+  return q + rig;
+}
+
+// The binary32 binade e and sign of the exact sum from its fixed-point
+// approximation a, certain when [|a| - mu, |a| + mu + ulp_32(e)) lies inside
+// [2^e, 2^(e+1)) (and e well inside binary32's normal range), as classify()
+// decides it for a binary64 approximation.
+__device__ __forceinline__ void classify_fix(i128 a, u128 mu, int F, bool& certain, bool& neg,
+                                             int& e) {
+  neg = a < 0;
+  certain = false;
+  e = 0;
+  const u128 m = abs128(a);
+  if (m == 0) return;
+  const int p = hibit128(m);
+  const int ee = p - F;
+  if (ee < FP<float>::EMIN + 2 || ee > FP<float>::EMAX - 2) return;
+  const u128 lo = (u128)1 << p;
+  const u128 ulp = p >= FP<float>::P ? ((u128)1 << (p - FP<float>::P)) : (u128)1;
+  if (mu >= lo || m - lo < mu || m + mu + ulp >= 2 * lo) return;
+  certain = true;
+  e = ee;
+}
+
+// Sum of one 128-bit value per thread over the block (thread 0's result).
+__device__ __forceinline__ i128 shfl_down128(i128 v, int off) {
+  const unsigned full = 0xffffffffu;
+  const uint64_t lo = __shfl_down_sync(full, (unsigned long long)(uint64_t)v, off);
+  const uint64_t hi = __shfl_down_sync(full, (unsigned long long)(uint64_t)((u128)v >> 64), off);
+  return (i128)(((u128)hi << 64) | lo);
+}
+__device__ __forceinline__ i128 shfl_up128(i128 v, int off) {
+  const unsigned full = 0xffffffffu;
+  const uint64_t lo = __shfl_up_sync(full, (unsigned long long)(uint64_t)v, off);
+  const uint64_t hi = __shfl_up_sync(full, (unsigned long long)(uint64_t)((u128)v >> 64), off);
+  return (i128)(((u128)hi << 64) | lo);
+}
+
+// Exclusive sum of one 128-bit value per thread across the block (exact).
+__device__ __forceinline__ i128 block_excl_sum128(i128 v, i128* sh_w) {
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  i128 incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const i128 o = shfl_up128(incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) sh_w[w] = incl;
+  __syncthreads();
+  i128 base = 0;
+  for (int i = 0; i < w; ++i) base += sh_w[i];
+  __syncthreads();
+  return base + incl - v;
+}
+
+// Total of one 128-bit value per thread across the block (thread 0).
+__device__ __forceinline__ i128 block_sum128(i128 v, i128* sh_w) {
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += shfl_down128(v, off);
+  if (lane == 0) sh_w[w] = v;
+  __syncthreads();
+  i128 tot = 0;
+  if (t == 0)
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += sh_w[i];
+  return tot;
+}
+
+// Pass 1 (binary32): the largest |T| of the chain, as a bit pattern (NaN
+// patterns exceed infinity's: either makes the chain's values non-finite).
+__global__ void __launch_bounds__(256) chain_absmax_kernel(const float* src, int64_t K,
+                                                           unsigned* maxbits) {
+  unsigned m = 0;
+  for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < K;
+       i += (int64_t)gridDim.x * 256) {
+    const unsigned b = __float_as_uint(src[i]) & 0x7FFFFFFFu;
+    m = b > m ? b : m;
+  }
+  m = __reduce_max_sync(0xffffffffu, m);
+  if ((threadIdx.x & 31) == 0) atomicMax(maxbits, m);
+}
+
+// Pass 2 (binary32): per tile, the exact fixed-point sum of T.
+__global__ void __launch_bounds__(kCT) chain_fixsum_kernel(const float* src, int64_t K,
+                                                           const unsigned* maxbits,
+                                                           i128* tsum) {
+  __shared__ i128 sh_w[kCT / 32];
+  const int t = threadIdx.x;
+  const int64_t k0 = (int64_t)blockIdx.x * kCTile + (int64_t)t * kCE;
+  const int64_t n = k0 < K ? (K - k0 < kCE ? K - k0 : kCE) : 0;
+  int F = 0;
+  if (!fix_scale(*maxbits, K, F)) {
+    if (t == 0) tsum[blockIdx.x] = 0;
+    return;
+  }
+  float tv[kCE];
+  load_run(src + (k0 < K ? k0 : 0), n, tv);
+  i128 sum = 0;
+#pragma unroll
+  for (int i = 0; i < kCE; ++i) sum += f32_to_fix(tv[i], F);  // zero past the end
+  const i128 tot = block_sum128(sum, sh_w);
+  if (t == 0) tsum[blockIdx.x] = tot;
+}
+
+// Exclusive scan of n 128-bit values in one block of 1024 threads (exact).
+__global__ void __launch_bounds__(1024) exclusive_scan128_1block(const i128* in, i128* out,
+                                                                 int64_t n) {
+  __shared__ i128 sh_w[32];
+  const int t = threadIdx.x;
+  const int64_t per = (n + 1023) / 1024;
+  const int64_t a = t * per, b = a + per < n ? a + per : n;
+  i128 s = 0;
+  for (int64_t i = a; i < b; ++i) s += in[i];
+  i128 run = block_excl_sum128(s, sh_w);
+  for (int64_t i = a; i < b; ++i) {
+    const i128 v = in[i];
+    out[i] = run;
+    run += v;
+  }
+}
+
+// Pass 3 (binary32): per tile, the sums of the estimated errors r (fixed
+// point) and of their variances v, in the order the classification
+// recomputes them. P_{k0-1} enters each thread from the exact tile offsets.
+__global__ void __launch_bounds__(kCT) chain_round_sum_kernel(const float* src, int64_t K,
+                                                              const unsigned* maxbits,
+                                                              const i128* toff, i128* rsum,
+                                                              double* vsum) {
+  __shared__ i128 sh_w[kCT / 32];
+  __shared__ double sh_v[kCT / 32];
+  const unsigned full = 0xffffffffu;
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const int64_t k0 = (int64_t)blockIdx.x * kCTile + (int64_t)t * kCE;
+  const int64_t n = k0 < K ? (K - k0 < kCE ? K - k0 : kCE) : 0;
+  int F = 0;
+  if (!fix_scale(*maxbits, K, F)) {
+    if (t == 0) {
+      rsum[blockIdx.x] = 0;
+      vsum[blockIdx.x] = 0.0;
+    }
+    return;
+  }
+  float tv[kCE];
+  load_run(src + (k0 < K ? k0 : 0), n, tv);
+  i128 tsum = 0;
+#pragma unroll
+  for (int i = 0; i < kCE; ++i) tsum += f32_to_fix(tv[i], F);
+  i128 S = toff[blockIdx.x] + block_excl_sum128(tsum, sh_w);  // P_{k0-1}
+  i128 rs = 0;
+  double vs = 0.0;
+#pragma unroll
+  for (int i = 0; i < kCE; ++i) {
+    if (i < n) {
+      const i128 sp = S;
+      S += f32_to_fix(tv[i], F);
+      if (k0 + i > 0) {
+        i128 r;
+        double v;
+        f32_round_est(sp, S, tv[i], F, r, v);
+        rs += r;
+        vs += v;
+      }
+    }
+  }
+  const i128 rt = block_sum128(rs, sh_w);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) vs += __shfl_down_sync(full, vs, off);
+  if (lane == 0) sh_v[w] = vs;
+  __syncthreads();
+  if (t == 0) {
+    double b = 0.0;
+    for (int i = 0; i < kCT / 32; ++i) b += sh_v[i];
+    rsum[blockIdx.x] = rt;
+    vsum[blockIdx.x] = b;
+  }
+}
+
+// Pass 4 for binary32: as chain_classify_kernel, with A_k = P_k + R_{k-1}
+// (fixed point) in place of P_k and a margin per step from V_{k-1}
+// (recomputed when V changes: at ties and rises only).
+__global__ void __launch_bounds__(kCT) chain_classify_f32_kernel(
+    const float* src, int64_t K, const unsigned* maxbits, const i128* toff, const i128* roff,
+    const double* voff, int64_t* qv, uint32_t* meta, int64_t* tile_nseg, Summ* thr_in) {
+  __shared__ Summ sh[kCT];
+  __shared__ i128 sh_w[kCT / 32];
+  __shared__ double sh_d[kCT / 32];
+  __shared__ int cnt[kCT / 32];
+  const unsigned full = 0xffffffffu;
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const int64_t tile0 = (int64_t)blockIdx.x * kCTile;
+  const int64_t k0 = tile0 + (int64_t)t * kCE;
+  const int64_t n = k0 < K ? (K - k0 < kCE ? K - k0 : kCE) : 0;
+  int F = 0;
+  const bool finite = fix_scale(*maxbits, K, F);
+  float tv[kCE];
+  load_run(src + (k0 < K ? k0 : 0), n, tv);
+  i128 tsum = 0;
+#pragma unroll
+  for (int i = 0; i < kCE; ++i) tsum += f32_to_fix(tv[i], F);
+  i128 S = toff[blockIdx.x] + block_excl_sum128(tsum, sh_w);  // P_{k0-1}
+  // the estimated errors of my steps, summed as chain_round_sum_kernel does
+  i128 rs = 0;
+  double vs = 0.0;
+  {
+    i128 Sr = S;
+#pragma unroll
+    for (int i = 0; i < kCE; ++i) {
+      if (i < n) {
+        const i128 sp = Sr;
+        Sr += f32_to_fix(tv[i], F);
+        if (k0 + i > 0) {
+          i128 r;
+          double v;
+          f32_round_est(sp, Sr, tv[i], F, r, v);
+          rs += r;
+          vs += v;
+        }
+      }
+    }
+  }
+  i128 R = roff[blockIdx.x] + block_excl_sum128(rs, sh_w);  // R_{k0-1}
+  double V = voff[blockIdx.x] + block_excl_sum(vs, sh_d);   // V_{k0-1}
+  const u128 all = (u128)1 << 126;                          // no step certain
+  bool pc = false, pneg = false;  // the previous step's classification, made
+  int pe = 0;                     // exactly as its own thread made it
+  if (k0 > 0 && n > 0) {
+    const float tp = src[k0 - 1];
+    i128 rp = 0;
+    double vp = 0.0;
+    const i128 sp2 = S - f32_to_fix(tp, F);  // P_{k0-2}
+    if (k0 - 1 > 0) f32_round_est(sp2, S, tp, F, rp, vp);
+    const u128 mp = finite ? fix_margin(V - vp, F, K) : all;
+    classify_fix(S + (R - rp), mp, F, pc, pneg, pe);
+  }
+  u128 mu = finite ? fix_margin(V, F, K) : all;
+  int nbrk = 0;
+  Summ me{map_id(), 0};
+  constexpr int H = kCE / 2;  // outputs written in two halves: fewer live registers
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    int64_t q_out[H];
+    uint32_t m_out[H];
+#pragma unroll
+    for (int j = 0; j < H; ++j) {
+      const int i = h * H + j;
+      q_out[j] = 0;
+      m_out[j] = 0;
+      if (i < n) {
+        const int64_t k = k0 + i;
+        const i128 sp = S;
+        S += f32_to_fix(tv[i], F);
+        bool c, ng;
+        int e;
+        classify_fix(S + R, mu, F, c, ng, e);
+        step_record<float>(k, tv[i], c, ng, e, pc, pe, me, nbrk, q_out[j], m_out[j]);
+        pc = c;
+        pe = e;
+        if (k > 0) {  // this step's error, for the steps after it
+          i128 r;
+          double v;
+          f32_round_est(sp, S, tv[i], F, r, v);
+          R += r;
+          if (v != 0.0) {
+            V += v;
+            if (finite) mu = fix_margin(V, F, K);
+          }
+        }
+      }
+    }
+    const int64_t nh = n - h * H;
+    if (nh > 0) {
+      store_run(qv + k0 + h * H, nh, q_out);
+      store_run(meta + k0 + h * H, nh, m_out);
+    }
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) nbrk += __shfl_down_sync(full, nbrk, off);
@@ -1489,7 +1930,17 @@ ChainPlan plan_chain(int64_t K) {
   p.segbase_off = off; off += r256(p.ntiles * sizeof(int64_t));
   p.segs_off = off; off += r256(p.seg_cap * sizeof(SegRec));
   p.min_off = off; off += r256(p.seg_cap * sizeof(int64_t));
-  p.misc_off = off; off += 256;  // bound (8), total segments (8), fail (4)
+  // binary32: the estimated rounding errors' tile sums and offsets
+  // binary32: fixed-point tile sums of T and of the estimated errors (16
+  // bytes each), their offsets, and the errors' variances
+  p.tfix_off = off; off += r256(p.ntiles * 16);
+  p.tfoff_off = off; off += r256(p.ntiles * 16);
+  p.rsum_off = off; off += r256(p.ntiles * 16);
+  p.roff_off = off; off += r256(p.ntiles * 16);
+  p.vsum_off = off; off += r256(p.ntiles * sizeof(double));
+  p.voff_off = off; off += r256(p.ntiles * sizeof(double));
+  // bound (8), total segments (8), fail (4), progress (8), binary32 max|T| (4)
+  p.misc_off = off; off += 256;
   p.bytes = off;
   return p;
 }
@@ -1498,7 +1949,9 @@ namespace {
 
 // The chain's workspace, carved by the plan's offsets.
 struct ChainWs {
-  double *tsum, *toff, *tmax, *bound;
+  double *tsum, *toff, *tmax, *bound, *vsum, *voff;
+  i128 *tfix, *tfoff, *rsum, *roff;
+  unsigned* maxbits;
   Summ* thr_in;
   Map *lead, *entry;
   int* lead_steps;
@@ -1524,6 +1977,13 @@ struct ChainWs {
     segbase = reinterpret_cast<int64_t*>(ws + p.segbase_off);
     segs = reinterpret_cast<SegRec*>(ws + p.segs_off);
     m_in = reinterpret_cast<int64_t*>(ws + p.min_off);
+    tfix = reinterpret_cast<i128*>(ws + p.tfix_off);
+    tfoff = reinterpret_cast<i128*>(ws + p.tfoff_off);
+    rsum = reinterpret_cast<i128*>(ws + p.rsum_off);
+    roff = reinterpret_cast<i128*>(ws + p.roff_off);
+    vsum = reinterpret_cast<double*>(ws + p.vsum_off);
+    voff = reinterpret_cast<double*>(ws + p.voff_off);
+    maxbits = reinterpret_cast<unsigned*>(ws + p.misc_off + 32);
     bound = reinterpret_cast<double*>(ws + p.misc_off);
     total = reinterpret_cast<int64_t*>(ws + p.misc_off + 8);
     fail = reinterpret_cast<int*>(ws + p.misc_off + 16);
@@ -1547,13 +2007,36 @@ cudaError_t run_chain_front(const ChainPlan& p, const T* src, char* ws, const Ch
   if (e != cudaSuccess) return e;
   if (p.ntiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const unsigned g = (unsigned)p.ntiles;
-  CR_LAUNCH(kKChainTileSum, s,
-            chain_tile_sum_kernel<T><<<g, kCT, 0, s>>>(src, p.K, w.tsum, w.tmax));
-  CR_LAUNCH(kKChainOffsets, s,
-            chain_offsets_kernel<<<1, 1024, 0, s>>>(w.tsum, w.tmax, p.ntiles, w.toff, w.bound));
-  CR_LAUNCH(kKChainClassify, s,
-            chain_classify_kernel<T><<<g, kCT, 0, s>>>(src, p.K, w.toff, w.bound, w.qv, w.meta,
-                                                       w.nseg, w.thr_in));
+  if constexpr (sizeof(T) == 4) {  // binary32: classify against the estimated chain
+    const int64_t ab = p.ntiles * 16 < 1216 ? p.ntiles * 16 : 1216;
+    CR_LAUNCH(kKChainTileSum, s,
+              chain_absmax_kernel<<<(unsigned)ab, 256, 0, s>>>(src, p.K, w.maxbits));
+    CR_LAUNCH(kKChainTileSum, s,
+              chain_fixsum_kernel<<<g, kCT, 0, s>>>(src, p.K, w.maxbits, w.tfix));
+    CR_LAUNCH(kKChainOffsets, s,
+              exclusive_scan128_1block<<<1, 1024, 0, s>>>(w.tfix, w.tfoff, p.ntiles));
+    CR_LAUNCH(kKChainRoundSum, s,
+              chain_round_sum_kernel<<<g, kCT, 0, s>>>(src, p.K, w.maxbits, w.tfoff, w.rsum,
+                                                       w.vsum));
+    CR_LAUNCH(kKChainOffsets, s,
+              exclusive_scan128_1block<<<1, 1024, 0, s>>>(w.rsum, w.roff, p.ntiles));
+    CR_LAUNCH(kKChainOffsets, s,
+              exclusive_scan_1block<double><<<1, 1024, 0, s>>>(w.vsum, w.voff, p.ntiles,
+                                                               nullptr));
+    CR_LAUNCH(kKChainClassify, s,
+              chain_classify_f32_kernel<<<g, kCT, 0, s>>>(src, p.K, w.maxbits, w.tfoff, w.roff,
+                                                          w.voff, w.qv, w.meta, w.nseg,
+                                                          w.thr_in));
+  } else {
+    CR_LAUNCH(kKChainTileSum, s,
+              chain_tile_sum_kernel<T><<<g, kCT, 0, s>>>(src, p.K, w.tsum, w.tmax));
+    CR_LAUNCH(kKChainOffsets, s,
+              chain_offsets_kernel<<<1, 1024, 0, s>>>(w.tsum, w.tmax, p.ntiles, w.toff,
+                                                      w.bound));
+    CR_LAUNCH(kKChainClassify, s,
+              chain_classify_kernel<T><<<g, kCT, 0, s>>>(src, p.K, w.toff, w.bound, w.qv,
+                                                         w.meta, w.nseg, w.thr_in));
+  }
   CR_LAUNCH(kKChainOffsets, s,
             exclusive_scan_1block<int64_t><<<1, 1024, 0, s>>>(w.nseg, w.segbase, p.ntiles,
                                                               w.total));

@@ -12,7 +12,8 @@ struct ChainPlan {
   int64_t K = 0, ntiles = 0, seg_cap = 0;
   size_t tsum_off = 0, toff_off = 0, tmax_off = 0, thr_off = 0, lead_off = 0,
          leadsteps_off = 0, done_off = 0, entry_off = 0, entryrec_off = 0, q_off = 0, meta_off = 0,
-         nseg_off = 0, segbase_off = 0, segs_off = 0, min_off = 0, misc_off = 0;
+         nseg_off = 0, segbase_off = 0, segs_off = 0, min_off = 0, tfix_off = 0, tfoff_off = 0,
+         rsum_off = 0, roff_off = 0, vsum_off = 0, voff_off = 0, misc_off = 0;
   size_t bytes = 0;  // workspace bytes (offsets are relative to the chain's base)
 };
 
@@ -62,8 +63,5 @@ cudaError_t run_fixup_again(T* out, const T* carries, int64_t n, int logB, const
 constexpr int64_t kMaxFusedChain = int64_t(1) << 26;
 constexpr int64_t kMaxFusedChainAlone = int64_t(1) << 28;
 
-// Longest binary32 chain the parallel evaluation is used for (K ulp must stay
-// small against the chain's values for its binade tests to be decisive).
-constexpr int64_t kMaxParallelChainF32 = 4096;
 
 }  // namespace cr

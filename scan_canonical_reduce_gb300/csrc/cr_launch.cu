@@ -75,7 +75,8 @@ const char* kernel_name(int id) {
       "apply_init_kernel",     "fill_init_kernel",      "carry_fixup_shift_kernel",
       "scan_seq_block_kernel", "row_reduce_kernel",
       "chain_link_kernel",     "chain_verify_kernel",   "chain_walk_fix_kernel",
-      "scan_local_again_kernel", "fixup_again_kernel", "pairwise_tile_prefix_kernel"};
+      "scan_local_again_kernel", "fixup_again_kernel", "pairwise_tile_prefix_kernel",
+      "chain_round_sum_kernel"};
   return (id >= 0 && id < kKernelCount) ? names[id] : "unknown";
 }
 

@@ -42,6 +42,7 @@ enum KernelId : int {
   kKScanLocalAgain,
   kKFixupAgain,
   kKPairwisePrefix,
+  kKChainRoundSum,
   kKernelCount
 };
 

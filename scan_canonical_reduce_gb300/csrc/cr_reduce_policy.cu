@@ -41,7 +41,7 @@ PolicyReducePlan plan_policy_reduce(int64_t n, cr_policy p, int64_t B, size_t es
   plan.n = n;
   size_t off = kHeaderBytes;
   auto chain_for = [&](int64_t K) {
-    plan.parallel = K >= kParallelChainMinR && (esize == 8 || K <= kMaxParallelChainF32);
+    plan.parallel = K >= kParallelChainMinR;
     if (plan.parallel) {
       plan.chain = plan_chain(K);
       plan.chain_ws = off;

@@ -1096,8 +1096,7 @@ ScanPlan plan_scan(int64_t batch, int64_t n, cr_policy p, int64_t B, size_t esiz
     // the shifted forms, then init applied)
     plan.kind = ScanPlan::kChainOnly;
     plan.chain_n = shift ? plan.m - 1 : n;
-    if (plan.chain_n >= kParallelChainMin &&
-        (esize == 8 || plan.chain_n <= kMaxParallelChainF32)) {
+    if (plan.chain_n >= kParallelChainMin) {
       plan.parallel_chain = true;
       plan.chain = plan_chain(plan.chain_n);
       plan.chain_ws = off;
@@ -1166,7 +1165,7 @@ ScanPlan plan_scan(int64_t batch, int64_t n, cr_policy p, int64_t B, size_t esiz
     off += round256((size_t)plan.K * esize);
     plan.carries_ws = off;
     off += round256((size_t)plan.K * esize);
-    if (plan.K - 1 >= kParallelChainMin && (esize == 8 || plan.K - 1 <= kMaxParallelChainF32)) {
+    if (plan.K - 1 >= kParallelChainMin) {
       plan.parallel_chain = true;
       plan.chain = plan_chain(plan.K - 1);
       plan.chain_ws = off;
@@ -1314,8 +1313,7 @@ struct Tiled {
                                        cudaMemcpyDeviceToDevice, s)) != cudaSuccess)
       return e;
     if (len < 2) return cudaSuccess;
-    const bool par = plan.parallel_chain && len >= kParallelChainMin &&
-                     (sizeof(T) == 8 || len <= kMaxParallelChainF32);
+    const bool par = plan.parallel_chain && len >= kParallelChainMin;
     if (par) {
       const ChainPlan cp = plan_chain(len);  // no larger than the whole chain's
       return run_chain<T>(cp, totals + first, carries + first, ws + plan.chain_ws, s);

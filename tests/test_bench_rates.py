@@ -28,14 +28,33 @@ def test_rate_stats_f32_uses_the_f32_add_rate():
 
 
 def test_every_row_has_its_element_count():
-    want = {"reduce": bench.N, "scan": bench.N, "scan_ex": bench.N,
-            "rows": bench.ROWS_R * bench.ROWS_C, "cols": bench.COLS_LEVELS * bench.COLS_N}
+    """Element counts and algorithmic bytes per element of every row: the
+    step's rows and the extras (the reduce sweep over n, the binary32 scans,
+    the U[0, 1) reduce at 2^20 and the 1,024 x 262,144 row reduce)."""
+    rows_b = bench.ROWS_B[0] * bench.ROWS_B[1]
     for r in bench.rows_spec() + bench.extra_rows():
-        assert bench.row_elems(r) == want[r[1]], r[0]
-        # bytes per element: 8 (fp64 reduce), 16 (fp64 scans), 4 (fp32 rows) + outputs
+        kind, p = r[1], r[2]
+        want = {"reduce": p.get("n", bench.N), "reduce_u01": 1 << 20, "scan": bench.N,
+                "scan_ex": bench.N, "rows": bench.ROWS_R * bench.ROWS_C, "rows_b": rows_b,
+                "cols": bench.COLS_LEVELS * bench.COLS_N}[kind]
+        assert bench.row_elems(r) == want, r[0]
+        es = 4 if r[5] == "f32" else 8
         per = r[3] / bench.row_elems(r)
-        assert per in (8, 16) or (r[1] == "rows" and 4 <= per < 4.01) or \
-            (r[1] == "scan_ex" and 16 <= per < 16.01), (r[0], per)
+        if kind in ("reduce", "reduce_u01"):
+            assert per == es, (r[0], per)
+        elif kind in ("scan", "cols"):
+            assert per == 2 * es, (r[0], per)
+        elif kind == "scan_ex":
+            assert 16 <= per < 16.01, (r[0], per)
+        else:  # row reduces: the input and one output a row
+            assert 4 <= per < 4.01, (r[0], per)
+    names = [r[0] for r in bench.extra_rows()]
+    assert len(names) == len(set(names))
+    for dt in ("f64", "f32"):
+        for n in bench.SWEEP_N:
+            for L in (16, 128, 1024):
+                assert "sweep_reduce_%s_n%s_L%d" % (dt, bench.size_tag(n), L) in names
+    assert bench.size_tag((1 << 28) + 37) == "2e28p37"
 
 
 def test_family4_first_rows_is_the_matrix_prefix():
