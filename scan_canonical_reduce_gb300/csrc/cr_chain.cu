@@ -302,48 +302,46 @@ __device__ __forceinline__ void store_run(E* p, int64_t cnt, const E (&v)[N]) {
 }
 
 // ---------------------------------------------------------------- pass 1
-// Coalesced: thread t reads steps t, t + 256, ... of the tile. The tile sum
-// feeds the approximate prefix; the largest |T| (compared as bit patterns,
-// no floating-point work) feeds the bound of pass 2.
+// Binary64: per tile, the sum and the largest |T| (compared as bit
+// patterns, no floating-point work) of its steps, which feed the offsets and
+// the bound of pass 2; and each thread's exclusive prefix within the tile
+// over the run of kCE steps the classification gives it, summed exactly as
+// the classification would, which starts from the stored value.
+__device__ __forceinline__ double block_excl_sum(double v, double* sh_w);
 template <class T>
 __global__ void __launch_bounds__(kCT) chain_tile_sum_kernel(const T* src, int64_t K,
-                                                             double* tsum, double* tmax) {
-  __shared__ double sh_s[kCT / 32];
+                                                             double* tsum, double* tmax,
+                                                             double* thr_start) {
+  __shared__ double sh_w[kCT / 32];
   __shared__ uint64_t sh_m[kCT / 32];
   const unsigned full = 0xffffffffu;
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-  const int64_t tile0 = (int64_t)blockIdx.x * kCTile;
+  const int64_t k0 = (int64_t)blockIdx.x * kCTile + (int64_t)t * kCE;
+  const int64_t n = k0 < K ? (K - k0 < kCE ? K - k0 : kCE) : 0;
+  T tv[kCE];
+  load_run(src + (k0 < K ? k0 : 0), n, tv);
   double sum = 0.0;
   uint64_t mx = 0;
 #pragma unroll
-  for (int j = 0; j < kCE; ++j) {
-    const int64_t k = tile0 + (int64_t)j * kCT + t;
-    if (k < K) {
-      const double v = (double)src[k];
-      sum += v;
-      const uint64_t a = (uint64_t)__double_as_longlong(v) & 0x7FFFFFFFFFFFFFFFull;
-      mx = a > mx ? a : mx;
-    }
+  for (int i = 0; i < kCE; ++i) {  // zero past the end
+    const double v = (double)tv[i];
+    sum += v;
+    const uint64_t a = (uint64_t)__double_as_longlong(v) & 0x7FFFFFFFFFFFFFFFull;
+    mx = a > mx ? a : mx;
   }
+  const double excl = block_excl_sum(sum, sh_w);
+  thr_start[(int64_t)blockIdx.x * kCT + t] = excl;
+  if (t == kCT - 1) tsum[blockIdx.x] = excl + sum;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
-    sum += __shfl_down_sync(full, sum, off);
     const uint64_t o = __shfl_down_sync(full, mx, off);
     mx = o > mx ? o : mx;
   }
-  if (lane == 0) {
-    sh_s[w] = sum;
-    sh_m[w] = mx;
-  }
+  if (lane == 0) sh_m[w] = mx;
   __syncthreads();
   if (t == 0) {
-    double S = 0.0;
     uint64_t M = 0;
-    for (int i = 0; i < kCT / 32; ++i) {
-      S += sh_s[i];
-      M = sh_m[i] > M ? sh_m[i] : M;
-    }
-    tsum[blockIdx.x] = S;
+    for (int i = 0; i < kCT / 32; ++i) M = sh_m[i] > M ? sh_m[i] : M;
     tmax[blockIdx.x] = __longlong_as_double((long long)M);  // NaN patterns stay NaN
   }
 }
@@ -577,10 +575,9 @@ __device__ __forceinline__ void step_record(int64_t k, T t, bool c, bool ng, int
 
 template <class T>
 __global__ void __launch_bounds__(kCT) chain_classify_kernel(
-    const T* src, int64_t K, const double* toff, const double* bound, int64_t* qv,
-    uint32_t* meta, int64_t* tile_nseg, Summ* thr_in) {
+    const T* src, int64_t K, const double* toff, const double* thr_start, const double* bound,
+    int64_t* qv, uint32_t* meta, int64_t* tile_nseg, Summ* thr_in) {
   __shared__ Summ sh[kCT];
-  __shared__ double sh_w[kCT / 32];
   __shared__ int cnt[kCT / 32];
   const unsigned full = 0xffffffffu;
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
@@ -590,10 +587,8 @@ __global__ void __launch_bounds__(kCT) chain_classify_kernel(
   const MuInt mu = mu_from_bound<T>(*bound, K);
   T tv[kCE];
   load_run(src + (k0 < K ? k0 : 0), n, tv);
-  double tsum = 0.0;
-#pragma unroll
-  for (int i = 0; i < kCE; ++i) tsum += (double)tv[i];  // zero past the end
-  double run = toff[blockIdx.x] + block_excl_sum(tsum, sh_w);  // P~ just before k0
+  // P~ just before k0 (the tile-sum pass's prefix of the threads before mine)
+  double run = toff[blockIdx.x] + thr_start[(int64_t)blockIdx.x * kCT + t];
   bool pc = false, pneg = false;  // pc, pe: the previous step's certainty and binade
   int pe = 0;
   if (k0 > 0 && n > 0) classify<T>(run, mu, pc, pneg, pe);
@@ -1954,7 +1949,8 @@ size_t r256(size_t v) { return (v + 255) & ~size_t(255); }
 
 }  // namespace
 
-ChainPlan plan_chain(int64_t K) {
+ChainPlan plan_chain(int64_t K, size_t esize) {
+  const bool f32 = esize == 4;  // the binary32 classification's arrays
   ChainPlan p;
   p.K = K;
   p.ntiles = (K + kCTile - 1) / kCTile;
@@ -1978,15 +1974,17 @@ ChainPlan plan_chain(int64_t K) {
   // binary32: the estimated rounding errors' tile sums and offsets
   // binary32: fixed-point tile sums of T and of the estimated errors (16
   // bytes each), their offsets, and the errors' variances
-  p.tfix_off = off; off += r256(p.ntiles * 16);
-  p.tfoff_off = off; off += r256(p.ntiles * 16);
-  p.rsum_off = off; off += r256(p.ntiles * 16);
-  p.roff_off = off; off += r256(p.ntiles * 16);
-  p.vsum_off = off; off += r256(p.ntiles * sizeof(double));
-  p.voff_off = off; off += r256(p.ntiles * sizeof(double));
-  // binary32: each thread's starting prefix, errors and variance
-  p.thrs_off = off; off += r256(p.ntiles * kCT * 16);
-  p.thrr_off = off; off += r256(p.ntiles * kCT * 16);
+  const int64_t nf = f32 ? p.ntiles : 0, nt = f32 ? p.ntiles * kCT : 0;
+  p.tfix_off = off; off += r256(nf * 16);
+  p.tfoff_off = off; off += r256(nf * 16);
+  p.rsum_off = off; off += r256(nf * 16);
+  p.roff_off = off; off += r256(nf * 16);
+  p.vsum_off = off; off += r256(nf * sizeof(double));
+  p.voff_off = off; off += r256(nf * sizeof(double));
+  // binary32: each thread's starting prefix, errors and variance (binary64:
+  // the prefix alone, in the variance's slots)
+  p.thrs_off = off; off += r256(nt * 16);
+  p.thrr_off = off; off += r256(nt * 16);
   p.thrv_off = off; off += r256(p.ntiles * kCT * sizeof(double));
   // bound (8), total segments (8), fail (4), progress (8), binary32 max|T| (4)
   p.misc_off = off; off += 256;
@@ -2084,13 +2082,13 @@ cudaError_t run_chain_front(const ChainPlan& p, const T* src, char* ws, const Ch
                                                           w.qv, w.meta, w.nseg, w.thr_in));
   } else {
     CR_LAUNCH(kKChainTileSum, s,
-              chain_tile_sum_kernel<T><<<g, kCT, 0, s>>>(src, p.K, w.tsum, w.tmax));
+              chain_tile_sum_kernel<T><<<g, kCT, 0, s>>>(src, p.K, w.tsum, w.tmax, w.thr_v));
     CR_LAUNCH(kKChainOffsets, s,
               chain_offsets_kernel<<<1, 1024, 0, s>>>(w.tsum, w.tmax, p.ntiles, w.toff,
                                                       w.bound));
     CR_LAUNCH(kKChainClassify, s,
-              chain_classify_kernel<T><<<g, kCT, 0, s>>>(src, p.K, w.toff, w.bound, w.qv,
-                                                         w.meta, w.nseg, w.thr_in));
+              chain_classify_kernel<T><<<g, kCT, 0, s>>>(src, p.K, w.toff, w.thr_v, w.bound,
+                                                         w.qv, w.meta, w.nseg, w.thr_in));
   }
   CR_LAUNCH(kKChainOffsets, s,
             exclusive_scan_1block<int64_t><<<1, 1024, 0, s>>>(w.nseg, w.segbase, p.ntiles,

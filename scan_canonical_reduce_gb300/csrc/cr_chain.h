@@ -18,7 +18,8 @@ struct ChainPlan {
   size_t bytes = 0;  // workspace bytes (offsets are relative to the chain's base)
 };
 
-ChainPlan plan_chain(int64_t K);
+// esize: 8 for binary64, 4 for binary32 (whose classification needs more).
+ChainPlan plan_chain(int64_t K, size_t esize);
 
 // dst[k] = C_k for k < K. src and dst must not overlap (the fallback re-reads
 // src). ws: plan.bytes of 256-byte aligned device memory. With final_out

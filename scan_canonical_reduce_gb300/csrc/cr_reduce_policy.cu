@@ -43,7 +43,7 @@ PolicyReducePlan plan_policy_reduce(int64_t n, cr_policy p, int64_t B, size_t es
   auto chain_for = [&](int64_t K) {
     plan.parallel = K >= kParallelChainMinR;
     if (plan.parallel) {
-      plan.chain = plan_chain(K);
+      plan.chain = plan_chain(K, esize);
       plan.chain_ws = off;
       off += r256(plan.chain.bytes);
     }

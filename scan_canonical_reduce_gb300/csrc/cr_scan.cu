@@ -1103,7 +1103,7 @@ ScanPlan plan_scan(int64_t batch, int64_t n, cr_policy p, int64_t B, size_t esiz
     plan.chain_n = shift ? plan.m - 1 : n;
     if (plan.chain_n >= kParallelChainMin) {
       plan.parallel_chain = true;
-      plan.chain = plan_chain(plan.chain_n);
+      plan.chain = plan_chain(plan.chain_n, esize);
       plan.chain_ws = off;
       off += round256(plan.chain.bytes);
     }
@@ -1172,7 +1172,7 @@ ScanPlan plan_scan(int64_t batch, int64_t n, cr_policy p, int64_t B, size_t esiz
     off += round256((size_t)plan.K * esize);
     if (plan.K - 1 >= kParallelChainMin) {
       plan.parallel_chain = true;
-      plan.chain = plan_chain(plan.K - 1);
+      plan.chain = plan_chain(plan.K - 1, esize);
       plan.chain_ws = off;
       off += round256(plan.chain.bytes);
     }
@@ -1320,7 +1320,7 @@ struct Tiled {
     if (len < 2) return cudaSuccess;
     const bool par = plan.parallel_chain && len >= kParallelChainMin;
     if (par) {
-      const ChainPlan cp = plan_chain(len);  // no larger than the whole chain's
+      const ChainPlan cp = plan_chain(len, sizeof(T));  // no larger than the whole chain's
       return run_chain<T>(cp, totals + first, carries + first, ws + plan.chain_ws, s);
     }
     return run_serial_chain<T>(totals + first, carries + first, len, s);
