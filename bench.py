@@ -522,11 +522,14 @@ def measured_peaks():
 # any of them differs (the kernel changed after the capture).
 CSRC_DIR = os.path.join(ROOT, "scan_canonical_reduce_gb300", "csrc")
 NCU_TRAFFIC = {
-    # one-row iterated_pairwise scan, n = 2^25: 268.93 MB read + 262.90 MB
+    # one-row iterated_pairwise scan, n = 2^25: 268.93 MB read + 262.81 MB
     # written, x 8
-    "scan_onepass_kernel": {"bytes": (268.93e6 + 262.90e6) * 8, "sources": {}},
-    # one-row reduce, n = 2^25, L = 16, level-0 pass, x 8
-    "lane_pass_kernel": {"bytes": (268.52e6 + 3.70e6) * 8, "sources": {}},
+    "scan_onepass_kernel": {"bytes": (268.933632e6 + 262.812160e6) * 8,
+                            "sources": {'cr_scan.cu': 'fc104fc814384d6d', 'cr_scan.h': 'a3c3e3392b7551f8', 'cr_device.cuh': 'b3f5f88a2d146302'}},
+    # one-row reduce, n = 2^25, L = 16, level-0 pass: 268.47 MB read + 3.05 MB
+    # written, x 8
+    "lane_pass_kernel": {"bytes": (268.4736e6 + 3.046144e6) * 8,
+                         "sources": {'cr_reduce.cu': 'b542f00562895d30', 'cr_plan.h': 'd781220e97c4b36f', 'cr_device.cuh': 'b3f5f88a2d146302'}},
 }
 
 

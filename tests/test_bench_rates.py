@@ -68,3 +68,14 @@ def test_family4_first_rows_is_the_matrix_prefix():
         part = W.family4(rows, 4, first_rows=37)
         assert part.shape == (37, 4)
         assert np.array_equal(part.view(np.uint32), full[:37].view(np.uint32))
+
+
+def test_ncu_traffic_needs_the_captured_sources(monkeypatch):
+    """The recorded ncu traffic of a kernel is reported only while its source
+    files hash as they did at the capture; any change drops it (None)."""
+    rec = bench.NCU_TRAFFIC["scan_onepass_kernel"]
+    monkeypatch.setattr(bench, "source_digest", lambda name: rec["sources"].get(name))
+    assert bench.ncu_traffic("scan_onepass_kernel") == rec["bytes"]
+    monkeypatch.setattr(bench, "source_digest", lambda name: "0" * 16)
+    assert bench.ncu_traffic("scan_onepass_kernel") is None
+    assert bench.ncu_traffic("no_such_kernel") is None
