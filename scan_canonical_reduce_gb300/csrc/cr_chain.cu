@@ -47,10 +47,11 @@
 //     exact 128-bit test that s_k lies in the predicted binade and sign;
 //   9 if any test failed (or the segment buffer overflowed), the serial chain
 //     recomputes everything on the device (no host sync).
-// mu is a rigorous bound, so the evaluation pays only where K ulp is small
-// against the values: binary64 chains of any practical length, binary32
-// chains of a few thousand steps. Longer binary32 chains use the serial
-// chain directly (run_serial_chain).
+// mu is a rigorous bound for binary64, where K ulp stays small against the
+// values for chains of any practical length. Binary32 chains (24-bit
+// rounding over K steps) are classified against an estimate of the binary32
+// chain itself with a statistical margin instead (passes 1 to 4 below, see
+// "binary32"); the checks of passes 8 and 9 are the same.
 // Every add of the chain is therefore the real add or proven equal to it.
 #include <cstdint>
 
@@ -1971,7 +1972,6 @@ ChainPlan plan_chain(int64_t K, size_t esize) {
   p.segbase_off = off; off += r256(p.ntiles * sizeof(int64_t));
   p.segs_off = off; off += r256(p.seg_cap * sizeof(SegRec));
   p.min_off = off; off += r256(p.seg_cap * sizeof(int64_t));
-  // binary32: the estimated rounding errors' tile sums and offsets
   // binary32: fixed-point tile sums of T and of the estimated errors (16
   // bytes each), their offsets, and the errors' variances
   const int64_t nf = f32 ? p.ntiles : 0, nt = f32 ? p.ntiles * kCT : 0;

@@ -81,7 +81,7 @@ def test_value_families(scr, case):
 
 @pytest.mark.parametrize("B", [16, 2048])
 def test_binary32(scr, B):
-    """Binary32 carries take the parallel chain up to 4096 of them (one tile)."""
+    """Binary32 carries (about 4000: one chain tile) through every fused mode."""
     n = B * 4000 + 3
     x = W.uniform_pm1(n, W.seed_for(32, B)).astype(np.float32)
     want = oracle.scan(x, "block_dyadic", B)

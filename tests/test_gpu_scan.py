@@ -171,8 +171,9 @@ def test_pairwise_full_size(scr):
                                       ("block_dyadic", 256), ("block_dyadic", 4096)])
 def test_scan_f32_large(scr, policy, B):
     """binary32 at 2^26 + 5: iterated_pairwise through the up/down passes,
-    long carry chains through the streamed serial fold (the parallel
-    evaluation's error bound is too coarse for 24-bit chains this long)."""
+    long carry chains through the parallel chain with the binary32
+    classification (an estimate of the binary32 chain and a statistical
+    margin; every step still checked exactly)."""
     x = W.family3((1 << 26) + 5).astype(np.float32)
     got = scr.inclusive_scan(torch.from_numpy(x).to(DEV), policy, B).cpu().numpy()
     want = oracle.scan(x, policy, B)
