@@ -18,7 +18,8 @@
 //     returns its root; consistency means
 //     inclusive_scan<E>(xs)[i] == reduce<E>(xs[0..i+1)).
 //
-// Readings where the page is silent (each is listed in the design doc):
+// Readings where the page is silent (each one stated here is the one the CUDA
+// library implements too):
 //   * tree(): operands are pushed left to right; whenever the two topmost
 //     partial trees cover equally many operands they are replaced by
 //     op(lower, upper); at the end the remaining partial trees are folded
