@@ -32,7 +32,7 @@
  *     not share one workspace.
  *   - Errors: CR_ERR_INVALID_ARG for a bad argument (nothing is enqueued),
  *     CR_ERR_WORKSPACE when ws is NULL, misaligned or too small (nothing is
- *     enqueued), CR_ERR_UNSUPPORTED for a valid request this build does not
+ *     enqueued), CR_ERR_UNSUPPORTED for a valid request this library version does not
  *     implement, CR_ERR_CUDA when a launch fails. A device-side wait that
  *     gives up after its bounded spin is reported later by cr_sync_status().
  */
