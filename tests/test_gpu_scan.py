@@ -178,3 +178,24 @@ def test_scan_f32_large(scr, policy, B):
     got = scr.inclusive_scan(torch.from_numpy(x).to(DEV), policy, B).cpu().numpy()
     want = oracle.scan(x, policy, B)
     assert bits(got) == bits(want), first_diff(got, want)
+
+
+@pytest.mark.parametrize("dtype", [np.float64, np.float32])
+@pytest.mark.parametrize("policy,B", [("left_fold", 1), ("block_dyadic", 16),
+                                      ("block_dyadic", 4)])
+def test_columns_pitch_and_offset(scr, dtype, policy, B):
+    """Level-major columns with an even and an odd count, a row pitch wider
+    than the columns, and a base one element off an aligned address, against
+    the oracle: 37 levels (a ragged last block of levels), in place too."""
+    levels = 37
+    for ncols, pitch, off in ((1000, 1000, 0), (1001, 1001, 0), (1000, 1003, 0),
+                              (1000, 1000, 1)):
+        buf = W.lognormal(levels * pitch + off, W.seed_for(5, ncols % 7 + off)).astype(dtype)
+        base = torch.from_numpy(buf).to(DEV)
+        view = base[off:off + levels * pitch].view(levels, pitch)[:, :ncols]
+        got = scr.inclusive_scan_batched(view, policy, B, dim=0).cpu().numpy()
+        want = oracle.scan_batched(buf[off:].copy(), ncols, levels, pitch, 1, policy, B)
+        want = want[:levels * pitch].reshape(levels, pitch)[:, :ncols]
+        assert bits(got) == bits(np.ascontiguousarray(want)), (ncols, pitch, off)
+        scr.inclusive_scan_batched(view, policy, B, dim=0, out=view)  # in place
+        assert bits(view.cpu().numpy()) == bits(np.ascontiguousarray(want)), (ncols, pitch, off)
