@@ -1065,9 +1065,15 @@ struct SegRec {
 template <class T>
 __global__ void __launch_bounds__(kCT) chain_segments_kernel(
     const T* src, const int64_t* qv, const uint32_t* meta, int64_t K, const int64_t* seg_base,
-    const Summ* thr_in, SegRec* segs, int64_t seg_cap, Map* lead, int* lead_steps,
-    int* fail) {
+    const int64_t* tile_nseg, const Summ* thr_in, SegRec* segs, int64_t seg_cap, Map* lead,
+    int* lead_steps, int* fail) {
+  // MAP step counts of the records this tile opens (at most one a step),
+  // summed here and stored once: no record needs clearing beforehand
+  __shared__ int s_steps[kCTile];
   const int t = threadIdx.x;
+  const int64_t nrec = tile_nseg[blockIdx.x];
+  for (int64_t i = t; i < nrec && i < kCTile; i += kCT) s_steps[i] = 0;
+  __syncthreads();
   const int64_t tile0 = (int64_t)blockIdx.x * kCTile;
   const int64_t k0 = tile0 + (int64_t)t * kCE;
   const int64_t n = k0 < K ? (K - k0 < kCE ? K - k0 : kCE) : 0;
@@ -1093,7 +1099,7 @@ __global__ void __launch_bounds__(kCT) chain_segments_kernel(
       const Map cur = own ? local : compose(in.map, local);
       if (ord >= 0 && base + ord < seg_cap) {  // close the open segment
         segs[base + ord].map = cur;
-        if (steps) atomicAdd(&segs[base + ord].nsteps, steps);
+        if (steps) atomicAdd(&s_steps[ord], steps);
       } else if (ord < 0) {  // the tile's leading run ends here
         lead[blockIdx.x] = cur;
         if (steps) atomicAdd(&lead_steps[blockIdx.x], steps);
@@ -1126,12 +1132,15 @@ __global__ void __launch_bounds__(kCT) chain_segments_kernel(
   const int64_t last = (tile0 + kCTile < K ? tile0 + kCTile : K) - 1;
   const bool closer = k0 <= last && last < k0 + kCE;
   if (ord >= 0 && base + ord < seg_cap) {
-    if (steps) atomicAdd(&segs[base + ord].nsteps, steps);
+    if (steps) atomicAdd(&s_steps[ord], steps);
     if (closer) segs[base + ord].map = cur;
   } else if (ord < 0 && n > 0) {  // no break in the tile up to here
     if (steps) atomicAdd(&lead_steps[blockIdx.x], steps);
     if (closer) lead[blockIdx.x] = cur;
   }
+  __syncthreads();
+  for (int64_t i = t; i < nrec && i < kCTile; i += kCT)
+    if (base + i < seg_cap) segs[base + i].nsteps = s_steps[i];
 }
 
 // Link pass (one block): a segmented scan over the tiles. State after tile
@@ -2051,9 +2060,6 @@ cudaError_t run_chain_front(const ChainPlan& p, const T* src, char* ws, const Ch
                             cudaStream_t s) {
   cudaError_t e = cudaMemsetAsync(ws + p.misc_off, 0, 256, s);
   if (e != cudaSuccess) return e;
-  // per-segment MAP step counts are accumulated with atomics: clear them
-  e = cudaMemsetAsync(w.segs, 0, (size_t)p.seg_cap * sizeof(SegRec), s);
-  if (e != cudaSuccess) return e;
   // the lead step counts and the fused form's tile flags (adjacent)
   e = cudaMemsetAsync(w.lead_steps, 0, p.done_off + r256(p.ntiles * sizeof(unsigned)) -
                                            p.leadsteps_off, s);
@@ -2095,8 +2101,8 @@ cudaError_t run_chain_front(const ChainPlan& p, const T* src, char* ws, const Ch
                                                               w.total));
   CR_LAUNCH(kKChainSegments, s,
             chain_segments_kernel<T><<<g, kCT, 0, s>>>(src, w.qv, w.meta, p.K, w.segbase,
-                                                       w.thr_in, w.segs, p.seg_cap, w.lead,
-                                                       w.lead_steps, w.fail));
+                                                       w.nseg, w.thr_in, w.segs, p.seg_cap,
+                                                       w.lead, w.lead_steps, w.fail));
   CR_LAUNCH(kKChainLink, s,
             chain_link_kernel<<<1, 1024, 0, s>>>(w.nseg, w.segbase, p.ntiles, w.segs, p.seg_cap,
                                                  w.lead, w.lead_steps, w.entry, w.entry_rec));
