@@ -358,7 +358,30 @@ def run_native(args):
         step()
     torch.cuda.synchronize(dev)
 
-    # ---- timed region: K steps; per-row and per-launch events on the stream
+    # ---- per-kernel breakdown: K more steps with every libcr launch
+    # bracketed by CUDA events on its stream (not the timed region: the
+    # events add a little to each launch)
+    scr.profile_select(None)
+    scr.profile_enable(True)
+    row_launches = {r[0]: [] for r in rows}
+    for _ in range(args.steps):
+        for row in rows:
+            before = scr.launch_count()
+            run_row(row)
+            row_launches[row[0]].append(scr.launch_count() - before)
+    torch.cuda.synchronize(dev)
+    scr.profile_enable(False)
+    prof = scr.profile_collect()
+    kern = {}
+    for name, ms in prof:
+        k = kern.setdefault(name, [0, 0.0])
+        k[0] += 1
+        k[1] += ms
+    top_kernel = max(kern, key=lambda k: kern[k][1]) if kern else None
+
+    # ---- timed region: K steps, per-row events on the stream; of the
+    # launches, only the dominant kernel's carry events (its duration for
+    # the roofline)
     uuid = None
     try:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
@@ -371,9 +394,9 @@ def run_native(args):
     sampler.start()
     time.sleep(0.3)
     launches0 = scr.launch_count()
-    scr.profile_enable(True)
+    scr.profile_select(top_kernel)
+    scr.profile_enable(top_kernel is not None)
     ev = {r[0]: [] for r in rows}
-    row_launches = {r[0]: [] for r in rows}
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
@@ -382,16 +405,15 @@ def run_native(args):
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            before = scr.launch_count()
             run_row(row)
-            row_launches[row[0]].append(scr.launch_count() - before)
             b.record(stream)
             ev[row[0]].append((a, b))
     t1.record(stream)
     torch.cuda.synchronize(dev)
     scr.profile_enable(False)
+    scr.profile_select(None)
     launches = scr.launch_count() - launches0
-    prof = scr.profile_collect()
+    prof_top = scr.profile_collect()
     clocks = sampler.stop()
     ms_total = max_over_ranks(t0.elapsed_time(t1), dist, dev)
     if dist:
@@ -408,7 +430,8 @@ def run_native(args):
         ms = statistics.median([a.elapsed_time(b) for a, b in ev[r[0]]])
         row_stats[r[0]] = rate_stats(r, ms, hbm_peak, dadd_rate, fadd_rate)
 
-    # per-row kernel times: the launch list is in issue order, rows in turn
+    # per-row kernel times (profiled steps): the launch list is in issue
+    # order, rows in turn
     per_row = {r[0]: {} for r in rows}
     pos = 0
     for _ in range(args.steps):
@@ -420,23 +443,24 @@ def run_native(args):
     for r in rows:
         row_stats[r[0]]["kernels_ms"] = {k: round(v, 4) for k, v in per_row[r[0]].items()}
 
-    # per-kernel launch list from libcr's event pairs
-    kern = {}
-    for name, ms in prof:
-        k = kern.setdefault(name, [0, 0.0])
-        k[0] += 1
-        k[1] += ms
+    # per-kernel launch list (profiled steps), and the dominant kernel's
+    # launches in the timed region
     tot_k = sum(v[1] for v in kern.values()) or 1.0
     kernels = {k: {"launches": v[0], "ms_total": round(v[1], 3), "share": round(v[1] / tot_k, 4)}
                for k, v in sorted(kern.items(), key=lambda kv: -kv[1][1])}
+    timed_top = {}
+    for name, ms in prof_top:
+        k = timed_top.setdefault(name, {"launches": 0, "ms_total": 0.0})
+        k["launches"] += 1
+        k["ms_total"] += ms
     # fp64 add peak from unit counts and clocks: GB300's nominal 1.25 TFLOP/s
     # fp64 (FMA = 2 flops) over 152 SMs at 2.07 GHz is 2 fp64 adds per clock
     # per SM (a warp-wide add every 16 clocks)
     props = torch.cuda.get_device_properties(dev)
     sm_max_mhz = clocks.get("sm_max_mhz") or 2070.0
     dadd_nominal = props.multi_processor_count * 2 * sm_max_mhz * 1e6
-    roofline = dominant_roofline(kernels, prof, row_stats, dadd_rate, dadd_lat, hbm_peak,
-                                 args.steps, dadd_nominal)
+    roofline = dominant_roofline(timed_top or kernels, prof_top or prof, row_stats, dadd_rate,
+                                 dadd_lat, hbm_peak, args.steps, dadd_nominal)
 
     extras = run_extras(args, scr, torch, dev, stream, run_row, dadd_rate, fadd_rate, hbm_peak)
 
@@ -470,9 +494,10 @@ L2_FLUSH_BYTES = 512 << 20  # more than the 126 MB L2
 
 def run_extras(args, scr, torch, dev, stream, run_row, dadd_rate, fadd_rate, hbm_peak):
     """Each extra row timed alone: W warm-up calls, then K calls bracketed by
-    CUDA events on the launching stream. A row whose input is smaller than
-    twice the L2 gets a 512 MB write between its timed calls (outside the
-    events), so that every call starts from HBM."""
+    CUDA events on the launching stream (no per-launch events inside), then
+    one call with libcr's per-launch events for the kernel breakdown. A row
+    whose input is smaller than twice the L2 gets a 512 MB write between its
+    calls (outside the events), so that every call starts from HBM."""
     out = {}
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     for r in extra_rows():
@@ -480,7 +505,6 @@ def run_extras(args, scr, torch, dev, stream, run_row, dadd_rate, fadd_rate, hbm
         for _ in range(args.warmup):
             run_row(r)
         torch.cuda.synchronize(dev)
-        scr.profile_enable(True)
         evs = []
         for _ in range(args.steps):
             if small:
@@ -492,12 +516,19 @@ def run_extras(args, scr, torch, dev, stream, run_row, dadd_rate, fadd_rate, hbm
             b.record(stream)
             evs.append((a, b))
         torch.cuda.synchronize(dev)
+        ms = statistics.median([a.elapsed_time(b) for a, b in evs])
+        # kernel breakdown: one more call with every launch bracketed by
+        # events (outside the timed calls)
+        if small:
+            flush.zero_()
+        scr.profile_enable(True)
+        run_row(r)
+        torch.cuda.synchronize(dev)
         scr.profile_enable(False)
         prof = scr.profile_collect()
-        ms = statistics.median([a.elapsed_time(b) for a, b in evs])
         kms = {}
         for name, t in prof:
-            kms[name] = kms.get(name, 0.0) + t / args.steps
+            kms[name] = kms.get(name, 0.0) + t
         out[r[0]] = rate_stats(r, ms, hbm_peak, dadd_rate, fadd_rate)
         out[r[0]]["kernels_ms"] = {k: round(v, 4) for k, v in kms.items()}
         if small:

@@ -320,6 +320,12 @@ uint64_t cr_launch_count(void);
  * stream (a small per-launch cost); on == 0: stop recording. */
 void cr_profile_enable(int on);
 
+/* Restricts the recording of cr_profile_enable to the launches of one kernel
+ * (an id as cr_kernel_name() takes), so that a timed sequence of calls
+ * carries the events of that kernel only; -1 (or any id out of range)
+ * records every kernel again. Process-wide. */
+void cr_profile_select(int kernel_id);
+
 /* Waits for the recorded events, writes up to max_records (kernel id, device
  * milliseconds) pairs in launch order, forgets them and returns how many
  * launches were recorded (possibly more than max_records). */

@@ -72,6 +72,7 @@ SIGNATURES = {
     "cr_debug_skip_publish": (None, [_I64]),
     "cr_debug_fused_fixup": (None, [_INT]),
     "cr_profile_enable": (None, [_INT]),
+    "cr_profile_select": (None, [_INT]),
     "cr_profile_collect": (_INT, [_P, _P, _INT]),
     "cr_kernel_name": (ctypes.c_char_p, [_INT]),
     "cr_measure_add_peak_scratch_bytes": (_SZ, []),
@@ -513,6 +514,25 @@ def launch_count() -> int:
 def profile_enable(on: bool = True) -> None:
     """Bracket every later libcr launch with CUDA events on its stream."""
     lib().cr_profile_enable(1 if on else 0)
+
+
+def profile_select(kernel=None) -> None:
+    """Record only the launches of the kernel named ``kernel`` (a name
+    profile_collect returns) while profiling is on; None records every one."""
+    kid = -1
+    if kernel is not None:
+        for i in range(256):
+            nm = lib().cr_kernel_name(i).decode()
+            if nm == "unknown":
+                break
+            if nm == kernel:
+                kid = i
+                break
+        else:
+            kid = -1
+        if kid < 0:
+            raise ValueError("no libcr kernel named %r" % kernel)
+    lib().cr_profile_select(kid)
 
 
 def profile_collect():

@@ -11,6 +11,7 @@ namespace {
 
 std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_profiling{0};
+std::atomic<int> g_profile_only{-1};  // a kernel id, or -1 for every kernel
 
 struct Record {
   int id;
@@ -83,6 +84,8 @@ const char* kernel_name(int id) {
 LaunchScope::LaunchScope(int id_, cudaStream_t s) : id(id_), stream(s), slot(-1) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (!g_profiling.load(std::memory_order_relaxed)) return;
+  const int only = g_profile_only.load(std::memory_order_relaxed);
+  if (only >= 0 && only != id_) return;
   std::lock_guard<std::mutex> lk(g_mu);
   Record r{id_, take_event(), take_event()};
   if (!r.start || !r.stop) return;
@@ -104,6 +107,10 @@ extern "C" {
 uint64_t cr_launch_count(void) { return cr::g_launches.load(); }
 
 void cr_profile_enable(int on) { cr::g_profiling.store(on ? 1 : 0); }
+
+void cr_profile_select(int kernel_id) {
+  cr::g_profile_only.store(kernel_id >= 0 && kernel_id < cr::kKernelCount ? kernel_id : -1);
+}
 
 int cr_profile_collect(int* kernel_ids, float* ms, int max_records) {
   std::lock_guard<std::mutex> lk(cr::g_mu);
