@@ -307,6 +307,29 @@ __device__ __forceinline__ void tile_pyramid(T* lvl, int t, int full_threads, in
   else build_tile_pyramid(lvl, t, full_threads, top);
 }
 
+// Two consecutive values of a 16-byte aligned pair (one vector access for
+// binary64).
+template <class T>
+__device__ __forceinline__ void store_pair(T* p, T a, T b) {
+  if constexpr (sizeof(T) == 8) {
+    *reinterpret_cast<double2*>(p) = make_double2((double)a, (double)b);
+  } else {
+    p[0] = a;
+    p[1] = b;
+  }
+}
+template <class T>
+__device__ __forceinline__ void load_pair(const T* p, T& a, T& b) {
+  if constexpr (sizeof(T) == 8) {
+    const double2 d = __ldg(reinterpret_cast<const double2*>(p));
+    a = (T)d.x;
+    b = (T)d.y;
+  } else {
+    a = p[0];
+    b = p[1];
+  }
+}
+
 // ------------------------------------------------------------------ up pass
 // A block takes kUpTiles consecutive tiles (the next tile's elements in
 // flight while the current tile's tree is built) and writes their
@@ -321,10 +344,10 @@ __device__ __forceinline__ void tile_pyramid(T* lvl, int t, int full_threads, in
 constexpr int kUpTiles = 4;
 constexpr int kLogUpTiles = 2;
 
-template <class T, int S>
+template <class T, int S, bool kQuads = false>
 __global__ void __launch_bounds__(kScanThreads, sizeof(T) == 8 ? 6 : 8)
 scan_up_kernel(const T* __restrict__ x, T* __restrict__ pyr, int* __restrict__ counters,
-               T* __restrict__ totals, ScanArgs a) {
+               T* __restrict__ totals, ScanArgs a, T* __restrict__ quads) {
   __shared__ T lvl[2 * kScanThreads];
   __shared__ T s_agg[kUpTiles];
   constexpr int NS = kE / S;
@@ -352,11 +375,22 @@ scan_up_kernel(const T* __restrict__ x, T* __restrict__ pyr, int* __restrict__ c
     for (int e = 0; e < kE; ++e)
       if (e >= cnt) v[e] = T(0);
     T agg[NS];
-    const T tagg = tree_aggs<T, S>(v, agg);  // trees only: the prefixes are the down pass's
-    if (a.totals_level == 0) {  // blocks of B = S <= kE elements inside a thread
+    T tagg;
+    if (kQuads) {
+      // pairwise (S = kE): the same tree, its first quad and root kept for
+      // the down pass, which then needs only the pairs 01 and 45 of its own
+      const T p01 = add_rn(v[0], v[1]), p23 = add_rn(v[2], v[3]);
+      const T p45 = add_rn(v[4], v[5]), p67 = add_rn(v[6], v[7]);
+      const T q03 = add_rn(p01, p23), q47 = add_rn(p45, p67);
+      tagg = add_rn(q03, q47);
+      store_pair(quads + 2 * (b * kScanThreads + t), q03, tagg);
+    } else {
+      tagg = tree_aggs<T, S>(v, agg);  // trees only: the prefixes are the down pass's
+      if (a.totals_level == 0) {  // blocks of B = S <= kE elements inside a thread
 #pragma unroll
-      for (int s = 0; s < NS; ++s)
-        if ((s + 1) * S <= cnt) totals[(i0 >> LS) + s] = agg[s];
+        for (int s = 0; s < NS; ++s)
+          if ((s + 1) * S <= cnt) totals[(i0 >> LS) + s] = agg[s];
+      }
     }
     if (t < full_threads) lvl[t] = tagg;
     tile_pyramid<true>(lvl, t, full_threads);
@@ -691,9 +725,10 @@ pairwise_tile_prefix_kernel(const T* __restrict__ pyr, T* __restrict__ ypre, Sca
   ypre[b] = acc;
 }
 
-template <class T, bool kShift>
-__global__ void __launch_bounds__(kScanThreads)
-scan_pairwise_kernel(const T* x, T* out, const T* __restrict__ ypre, ScanArgs a, T init) {
+template <class T, bool kShift, bool kQuads = false>
+__global__ void __launch_bounds__(kScanThreads, 8)
+scan_pairwise_kernel(const T* x, T* out, const T* __restrict__ ypre, ScanArgs a, T init,
+                     const T* __restrict__ quads) {
   __shared__ T lvl[2 * kScanThreads];
   __shared__ T s_last[kScanThreads / 32];
   __shared__ T s_E[kScanThreads + 1];  // E_t = W(8 t) of the tile; E_256 = Y_{b+1}
@@ -707,11 +742,22 @@ scan_pairwise_kernel(const T* x, T* out, const T* __restrict__ ypre, ScanArgs a,
 
   T v[kE];
   load8(x + i0, cnt, v);
-  // the thread's nodes: pairs, quads, its aggregate
-  const T p01 = add_rn(v[0], v[1]), p23 = add_rn(v[2], v[3]);
-  const T p45 = add_rn(v[4], v[5]), p67 = add_rn(v[6], v[7]);
-  const T q03 = add_rn(p01, p23), q47 = add_rn(p45, p67);
-  if (t < full_threads) lvl[t] = add_rn(q03, q47);
+  // the thread's nodes: pairs, quads, its aggregate (the first quad and the
+  // aggregate from the up pass when it kept them)
+  T p01, q03, p45, tagg;
+  if (kQuads) {
+    load_pair(quads + 2 * (b * kScanThreads + t), q03, tagg);
+    p01 = add_rn(v[0], v[1]);
+    p45 = add_rn(v[4], v[5]);
+  } else {
+    p01 = add_rn(v[0], v[1]);
+    const T p23 = add_rn(v[2], v[3]);
+    p45 = add_rn(v[4], v[5]);
+    const T p67 = add_rn(v[6], v[7]);
+    q03 = add_rn(p01, p23);
+    tagg = add_rn(q03, add_rn(p45, p67));
+  }
+  if (t < full_threads) lvl[t] = tagg;
   tile_pyramid<sizeof(T) == 8>(lvl, t, full_threads);  // ends with a block barrier
 
   // warp prefixes E_{32 w}: thread w of warp 0 takes Y_b (the tile prefix,
@@ -1152,6 +1198,10 @@ ScanPlan plan_scan(int64_t batch, int64_t n, cr_policy p, int64_t B, size_t esiz
   if (p == CR_PAIRWISE) {
     plan.ypre_ws = off;
     off += round256((size_t)(plan.full_tiles + 1) * esize);
+    if (esize == 8) {  // binary64: each thread's first quad and aggregate
+      plan.quad_ws = off;
+      off += round256((size_t)plan.n_tiles * kScanThreads * 2 * esize);
+    }
   }
   // arrival counters, ready flags (one pass) and the tile counter: one
   // region cleared by a single memset per call
@@ -1217,7 +1267,7 @@ struct Tiled {
   bool block, shift;
   int S;
   ScanArgs a{};
-  T *pyr, *ypre, *totals, *carries;
+  T *pyr, *ypre, *totals, *carries, *quads;
   int* counters;
   Tiled(const ScanPlan& p, char* w, T i) : plan(p), ws(w), init(i) {
     block = plan.policy == CR_BLOCK_DYADIC;
@@ -1236,6 +1286,7 @@ struct Tiled {
     }
     pyr = reinterpret_cast<T*>(ws + plan.pyr_ws);
     ypre = reinterpret_cast<T*>(ws + plan.ypre_ws);
+    quads = plan.quad_ws ? reinterpret_cast<T*>(ws + plan.quad_ws) : nullptr;
     counters = reinterpret_cast<int*>(ws + plan.cnt_ws);
     totals = block ? reinterpret_cast<T*>(ws + plan.totals_ws) : nullptr;
     carries = block ? reinterpret_cast<T*>(ws + plan.carries_ws) : nullptr;
@@ -1284,9 +1335,11 @@ struct Tiled {
     a.tile_end = t1;
     const unsigned ugrid = (unsigned)((t1 - t0 + kUpTiles - 1) / kUpTiles);
     CR_LAUNCH(kKScanUp, s, {  // up pass: pairwise, blocks spanning tiles, binary32 iterated
-      if (S == 8) scan_up_kernel<T, 8><<<ugrid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
-      else if (S == 4) scan_up_kernel<T, 4><<<ugrid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
-      else scan_up_kernel<T, 2><<<ugrid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
+      if (S == 8 && quads != nullptr)
+        scan_up_kernel<T, 8, true><<<ugrid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a, quads);
+      else if (S == 8) scan_up_kernel<T, 8><<<ugrid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a, nullptr);
+      else if (S == 4) scan_up_kernel<T, 4><<<ugrid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a, nullptr);
+      else scan_up_kernel<T, 2><<<ugrid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a, nullptr);
     });
     return cudaGetLastError();
   }
@@ -1379,10 +1432,14 @@ struct Tiled {
     }
     if (plan.policy == CR_PAIRWISE) {
       CR_LAUNCH(kKScanPairwise, s, {
-        if (shift)
-          scan_pairwise_kernel<T, true><<<grid, kScanThreads, 0, s>>>(x, out, ypre, a, init);
+        if (shift && quads != nullptr)
+          scan_pairwise_kernel<T, true, true><<<grid, kScanThreads, 0, s>>>(x, out, ypre, a, init, quads);
+        else if (shift)
+          scan_pairwise_kernel<T, true><<<grid, kScanThreads, 0, s>>>(x, out, ypre, a, init, nullptr);
+        else if (quads != nullptr)
+          scan_pairwise_kernel<T, false, true><<<grid, kScanThreads, 0, s>>>(x, out, ypre, a, init, quads);
         else
-          scan_pairwise_kernel<T, false><<<grid, kScanThreads, 0, s>>>(x, out, ypre, a, init);
+          scan_pairwise_kernel<T, false><<<grid, kScanThreads, 0, s>>>(x, out, ypre, a, init, nullptr);
       });
       return cudaGetLastError();
     }
@@ -1646,9 +1703,9 @@ cudaError_t run_block_totals(const ScanPlan& plan, const T* x, char* ws, cudaStr
   const unsigned grid = (unsigned)((plan.n_tiles + kUpTiles - 1) / kUpTiles);
   const int S = (int)(plan.B < kE ? plan.B : kE);
   CR_LAUNCH(kKScanUp, s, {
-    if (S == 8) scan_up_kernel<T, 8><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
-    else if (S == 4) scan_up_kernel<T, 4><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
-    else scan_up_kernel<T, 2><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a);
+    if (S == 8) scan_up_kernel<T, 8><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a, nullptr);
+    else if (S == 4) scan_up_kernel<T, 4><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a, nullptr);
+    else scan_up_kernel<T, 2><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a, nullptr);
   });
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int64_t Kf = plan.n / plan.B;

@@ -53,6 +53,9 @@ struct ScanPlan {
   int64_t cnt_off[kMaxLevels] = {};
   size_t pyr_ws = 0, cnt_ws = 0, cnt_bytes = 0;
   size_t ypre_ws = 0;        // pairwise: Y_b = W(2048 b) of every complete tile
+  // pairwise, binary64: each thread's quad node x[8t..8t+4) and aggregate,
+  // written by the up pass and read by the down-sweep (0: none)
+  size_t quad_ws = 0;
   size_t ready_ws = 0, tilectr_ws = 0;  // one pass: node ready flags, tile counter
   size_t zero_ws = 0, zero_bytes = 0;   // cleared once per call
   int64_t K = 0;             // blocks (block_dyadic)
