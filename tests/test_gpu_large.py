@@ -52,3 +52,33 @@ def test_scans_and_reduce_past_2_31(scr, walk, dt):
         assert float(r[0]) == float(exact[-1]), (L, dt)
     del x, y, want
     torch.cuda.empty_cache()
+
+
+def test_batched_past_2_31(scr):
+    """A level-major column scan of 90 levels x 23,860,930 columns and a row
+    reduce of 16,385 rows x 131,072 columns: 2^31 elements and more in one
+    call, the per-sequence sums exact."""
+    g = torch.Generator(device=DEV)
+    g.manual_seed(0xC01D)
+    levels, cols = 90, 23860930
+    xi = torch.randint(-1, 2, (levels, cols), dtype=torch.int8, device=DEV, generator=g)
+    assert xi.numel() > (1 << 31)
+    exact = torch.cumsum(xi, 0, dtype=torch.int32)
+    x = xi.to(torch.float32)
+    y = torch.empty_like(x)
+    for policy, B in (("left_fold", 1), ("block_dyadic", 16)):
+        y.fill_(float("nan"))
+        scr.inclusive_scan_batched(x, policy, B, dim=0, out=y)
+        torch.cuda.synchronize()
+        assert torch.equal(y, exact.to(torch.float32)), policy
+    del xi, exact, x, y
+    torch.cuda.empty_cache()
+    rows, n = 16385, 131072
+    xi = torch.randint(-1, 2, (rows, n), dtype=torch.int8, device=DEV, generator=g)
+    assert xi.numel() > (1 << 31)
+    want = xi.sum(dim=1, dtype=torch.int32).to(torch.float32)
+    x = xi.to(torch.float32)
+    got = scr.reduce_batched(x, 128, 0.0, dim=-1)
+    assert torch.equal(got, want)
+    del xi, x, got, want
+    torch.cuda.empty_cache()
