@@ -47,16 +47,27 @@ def _stale(obj: str, src: str) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    os.makedirs(OUT_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, defines=(), out_dir: str | None = None) -> str:
+    """Compiles the sources (those changed since their object, or all with
+    force) and links the library; returns its path. `defines` ("NAME=value"
+    strings) override the decomposition knobs of the sources (run lengths,
+    tiles a block, fill blocks), which change no result; a build with
+    defines goes to its own out_dir and is always complete."""
+    out = OUT_DIR if out_dir is None else out_dir
+    if defines and out_dir is None:
+        raise ValueError("a build with overridden knobs needs its own out_dir")
+    lib = os.path.join(out, "libcr.so")
+    os.makedirs(out, exist_ok=True)
     nvcc = _nvcc()
+    flags = NVFLAGS + ["-D" + d for d in defines]
+    force = force or bool(defines)
     objs, jobs = [], []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(OUT_DIR, src.replace(".cu", ".o"))
+        o = os.path.join(out, src.replace(".cu", ".o"))
         objs.append(o)
         if force or _stale(o, s):
-            jobs.append([nvcc, *NVFLAGS, "-c", s, "-o", o])
+            jobs.append([nvcc, *flags, "-c", s, "-o", o])
     if jobs:
         with cf.ThreadPoolExecutor(max_workers=len(jobs)) as ex:
             for r in ex.map(lambda c: subprocess.run(c, capture_output=True, text=True), jobs):
@@ -64,11 +75,11 @@ def build(force: bool = False, verbose: bool = False) -> str:
                     print(r.stdout + r.stderr)
                 if r.returncode:
                     raise RuntimeError("nvcc failed: " + " ".join(r.args))
-    if force or jobs or not os.path.exists(LIB):
-        tmp = LIB + ".tmp.%d" % os.getpid()
+    if force or jobs or not os.path.exists(lib):
+        tmp = lib + ".tmp.%d" % os.getpid()
         subprocess.run([nvcc, *ARCH, "-shared", "--cudart", "static", "-o", tmp, *objs], check=True)
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -1717,7 +1717,10 @@ __global__ void __launch_bounds__(32) chain_serial_kernel(const T* src, T* dst, 
 // adds, stores) as a plain streaming kernel's would.
 // Fill blocks: at most 96 and a quarter of the resident blocks (48 and a
 // third measured alike at B = 16; half of them starve the fix-up).
-constexpr int64_t kMaxFillBlocks = 96;
+#ifndef CR_MAX_FILL_BLOCKS
+#define CR_MAX_FILL_BLOCKS 96
+#endif
+constexpr int64_t kMaxFillBlocks = CR_MAX_FILL_BLOCKS;  // (an override changes the schedule only)
 constexpr int kFillShareDiv = 4;
 constexpr int kFixPer = 16;                    // elements a lane per sub-chunk
 constexpr int64_t kFixSub = 32 * kFixPer;      // 512 elements a sub-chunk

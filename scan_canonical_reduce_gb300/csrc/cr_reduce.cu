@@ -41,6 +41,22 @@ namespace cr {
 constexpr int kThreads = 256;
 constexpr int kLV = 10;  // stack levels: a run of up to 512 operands
 
+// Decomposition knobs: the largest run of rows a thread reduces in a leaf
+// pass, and the leaf items a pass aims at (4 per SM of a GB300). Neither
+// changes a result, only which block forms which node (the canonical tree
+// is the same for every value; a compile-time override is how the tests
+// show it).
+#ifndef CR_REDUCE_MAX_RUN
+#define CR_REDUCE_MAX_RUN 256
+#endif
+#ifndef CR_REDUCE_LEAF_ITEMS
+#define CR_REDUCE_LEAF_ITEMS 608
+#endif
+constexpr int64_t kMaxRun = CR_REDUCE_MAX_RUN;  // a power of two, at most 256
+constexpr int64_t kLeafItems = CR_REDUCE_LEAF_ITEMS;
+static_assert(kMaxRun >= 2 && kMaxRun <= 256 && (kMaxRun & (kMaxRun - 1)) == 0,
+              "runs are powers of two up to 256 rows");
+
 template <class T, int U, bool kContig>
 __global__ void __launch_bounds__(kThreads)
 lane_pass_kernel(const T* __restrict__ in_base, int64_t in_seg, int64_t in_row,
@@ -357,14 +373,14 @@ void plan_tree(ReducePlan& plan, Bump& ws, int64_t batch, int64_t R, int64_t r,
       }
       return;
     }
-    const int64_t target = std::max<int64_t>(1, 608 / (batch * tiles));
+    const int64_t target = std::max<int64_t>(1, kLeafItems / (batch * tiles));
     int64_t P = pow2floor(std::max<int64_t>(1, R / (G * target)));
-    P = std::min<int64_t>(P, 256);
+    P = std::min<int64_t>(P, kMaxRun);
     if ((int64_t)G * P * W < 4096)
       P = std::min<int64_t>(pow2floor(std::max<int64_t>(1, R / G)),
                             pow2ceil((4096 + G * W - 1) / (G * W)));
     if (G * P < 2) P = 2;
-    P = std::min<int64_t>(P, 256);
+    P = std::min<int64_t>(P, kMaxRun);
     const int64_t T = G * P;
     const int64_t C = R / T;
     a.T = T;

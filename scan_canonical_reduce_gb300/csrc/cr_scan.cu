@@ -341,8 +341,13 @@ __device__ __forceinline__ void load_pair(const T* p, T& a, T& b) {
 // 1.84 -> 1.76 ms; 8 blocks per SM spill and gain less, 8 tiles a block
 // nothing). Binary32: 8 blocks per SM (32 registers), as it compiles
 // unbounded (a bound of 6 lets it take 40 and runs 14 % slower).
-constexpr int kUpTiles = 4;
-constexpr int kLogUpTiles = 2;
+// (Tiles a block, as a compile-time override: which block forms which node
+// of the pyramid, never the node.)
+#ifndef CR_UP_LOG_TILES
+#define CR_UP_LOG_TILES 2
+#endif
+constexpr int kLogUpTiles = CR_UP_LOG_TILES;
+constexpr int kUpTiles = 1 << kLogUpTiles;
 
 template <class T, int S, bool kQuads = false>
 __global__ void __launch_bounds__(kScanThreads, sizeof(T) == 8 ? 6 : 8)
