@@ -38,14 +38,18 @@
 
 namespace cr {
 
-constexpr int kThreads = 256;
+// Decomposition knobs: the threads of a block (lanes x runs a block holds;
+// 128 measured within 1 % of 256), the largest run of rows a thread reduces
+// in a leaf pass, and the leaf items a pass aims at (4 per SM of a GB300).
+// None changes a result, only which block forms which node (the canonical
+// tree is the same for every value; a compile-time override is how the
+// tests show it).
+#ifndef CR_REDUCE_THREADS
+#define CR_REDUCE_THREADS 256
+#endif
+constexpr int kThreads = CR_REDUCE_THREADS;  // a power of two
 constexpr int kLV = 10;  // stack levels: a run of up to 512 operands
 
-// Decomposition knobs: the largest run of rows a thread reduces in a leaf
-// pass, and the leaf items a pass aims at (4 per SM of a GB300). Neither
-// changes a result, only which block forms which node (the canonical tree
-// is the same for every value; a compile-time override is how the tests
-// show it).
 #ifndef CR_REDUCE_MAX_RUN
 #define CR_REDUCE_MAX_RUN 256
 #endif

@@ -1,5 +1,5 @@
 """Invariance under the decomposition: libcr built with other compile-time
-run lengths and leaf-item targets of the reduce, other tiles a block in the
+block widths, run lengths and leaf-item targets of the reduce, other tiles a block in the
 scans' up pass and other fill blocks in the fused chain pass forms the same
 nodes in other blocks and passes, so every call returns the default build's
 bits. The inputs are sized so that each knob changes the schedule: several
@@ -21,8 +21,8 @@ DEV = "cuda:0"
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 VARIANTS = {
-    "short_runs": ["CR_REDUCE_MAX_RUN=16", "CR_REDUCE_LEAF_ITEMS=5000", "CR_UP_LOG_TILES=0",
-                   "CR_MAX_FILL_BLOCKS=5"],
+    "short_runs": ["CR_REDUCE_THREADS=128", "CR_REDUCE_MAX_RUN=16", "CR_REDUCE_LEAF_ITEMS=5000",
+                   "CR_UP_LOG_TILES=0", "CR_MAX_FILL_BLOCKS=5"],
     "long_groups": ["CR_REDUCE_MAX_RUN=64", "CR_REDUCE_LEAF_ITEMS=64", "CR_UP_LOG_TILES=3",
                     "CR_MAX_FILL_BLOCKS=200"],
 }
