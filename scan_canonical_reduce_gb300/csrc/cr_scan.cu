@@ -1087,6 +1087,67 @@ scan_seq_block_kernel(const T* x, T* out, int64_t batch, int64_t n, int64_t es, 
   }
 }
 
+// The binary64 left fold of columns two at a time (inclusive, adjacent
+// columns: batch stride 1 in and out, element strides even, x and out
+// 16-byte aligned): thread q folds columns 2q and 2q + 1 with one 16-byte
+// load and one 16-byte store per level, half the memory instructions of one
+// column a thread, and two independent chains in every thread. The next BB
+// levels are loaded while the current BB are folded and stored. BB = 4 (56
+// registers, every column of 90 x 200,000 resident at once): 0.056 ->
+// 0.050 ms against one column a thread; BB = 2, 8 and 16 (16 without the
+// loads ahead) measured 0.054, 0.060 and 0.072 ms.
+template <int BB, bool kAhead>
+__global__ void __launch_bounds__(256)
+scan_seq_left2_kernel(const double* x, double* out, int64_t batch, int64_t n, int64_t es,
+                      int64_t oes) {
+  const int64_t c0 = 2 * ((int64_t)blockIdx.x * blockDim.x + threadIdx.x);
+  if (c0 >= batch) return;
+  const bool two = c0 + 1 < batch;
+  auto load = [&](int64_t k, double& a, double& b) {
+    if (two) {
+      const double2 d = __ldg(reinterpret_cast<const double2*>(x + k * es + c0));
+      a = d.x;
+      b = d.y;
+    } else {
+      a = x[k * es + c0];
+      b = 0.0;
+    }
+  };
+  double v0[BB], v1[BB];
+#pragma unroll
+  for (int e = 0; e < BB; ++e) {
+    v0[e] = 0.0;
+    v1[e] = 0.0;
+    if (e < n) load(e, v0[e], v1[e]);
+  }
+  double acc0 = 0.0, acc1 = 0.0;
+  for (int64_t k0 = 0; k0 < n; k0 += BB) {
+    double n0[BB], n1[BB];  // the next BB levels, in flight meanwhile
+#pragma unroll
+    for (int e = 0; e < BB; ++e) {
+      n0[e] = 0.0;
+      n1[e] = 0.0;
+      if (kAhead && k0 + BB + e < n) load(k0 + BB + e, n0[e], n1[e]);
+    }
+#pragma unroll
+    for (int e = 0; e < BB; ++e) {
+      const int64_t k = k0 + e;
+      if (k < n) {
+        acc0 = k == 0 ? v0[e] : add_rn(acc0, v0[e]);
+        acc1 = k == 0 ? v1[e] : add_rn(acc1, v1[e]);
+        if (two) *reinterpret_cast<double2*>(out + k * oes + c0) = make_double2(acc0, acc1);
+        else out[k * oes + c0] = acc0;
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < BB; ++e) {
+      v0[e] = n0[e];
+      v1[e] = n1[e];
+      if (!kAhead && k0 + BB + e < n) load(k0 + BB + e, v0[e], v1[e]);
+    }
+  }
+}
+
 // ---------------------------------------------------------------- planning
 namespace {
 std::atomic<int64_t> g_skip_publish{-1};
@@ -1509,7 +1570,18 @@ cudaError_t run_scan(const ScanPlan& plan, const T* x, T* out, int64_t es, int64
             (scan_seq_block_kernel<T, BBV, LEFT><<<grid, 256, 0, s>>>(                     \
                 x, out, plan.batch, plan.n, es, bs, oes, obs, shift ? 1 : 0, plan.m, init)))
       const bool bd = plan.policy == CR_BLOCK_DYADIC;
-      if (plan.policy == CR_LEFT_FOLD || (bd && plan.B == 1)) CR_SEQB(16, true);
+      const bool left = plan.policy == CR_LEFT_FOLD || (bd && plan.B == 1);
+      if (left && sizeof(T) == 8 && !shift && bs == 1 && obs == 1 && es % 2 == 0 &&
+          oes % 2 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
+          (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
+        const int64_t blocks2 = ((plan.batch + 1) / 2 + 255) / 256;
+        CR_LAUNCH(kKScanSeqBlock, s,
+                  scan_seq_left2_kernel<4, true><<<(unsigned)blocks2, 256, 0, s>>>(
+                      reinterpret_cast<const double*>(x), reinterpret_cast<double*>(out),
+                      plan.batch, plan.n, es, oes));
+        return cudaGetLastError();
+      }
+      if (left) CR_SEQB(16, true);
       else if (bd && plan.B == 16) CR_SEQB(16, false);
       else if (bd && plan.B == 8) CR_SEQB(8, false);
       else if (bd && plan.B == 4) CR_SEQB(4, false);
