@@ -476,7 +476,7 @@ def run_native(args):
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "mixed: f64 (every row but one), f32 (the 65536 x 4096 row reduce)",
+            "dtype": STEP_DTYPE,
             "data": "synthetic (seeded SplitMix64 families; no dataset)",
             "config": job_config(world),
             "rows": row_stats, "kernels": kernels, "roofline": roofline, "extras": extras,
@@ -489,7 +489,9 @@ def run_native(args):
         dist.destroy_process_group()
 
 
-L2_FLUSH_BYTES = 512 << 20  # more than the 126 MB L2
+L2_FLUSH_BYTES = 512 << 20
+# the arithmetic type of the step's rows (both arms)
+STEP_DTYPE = "mixed: f64 (every row but one), f32 (the 65536 x 4096 row reduce)"  # more than the 126 MB L2
 
 
 def run_extras(args, scr, torch, dev, stream, run_row, dadd_rate, fadd_rate, hbm_peak):
@@ -793,7 +795,7 @@ def run_reference(args):
         "metric": METRIC, "impl": "reference", "value": round(value, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(tot_s / args.steps * 1e3, 2), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": STEP_DTYPE, "data": "synthetic",
         "config": job_config(world),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": "every row at 1/%d of its size (1-D n = %d; the oracle "
