@@ -489,9 +489,9 @@ def run_native(args):
         dist.destroy_process_group()
 
 
-L2_FLUSH_BYTES = 512 << 20
+L2_FLUSH_BYTES = 512 << 20  # more than the 126 MB L2
 # the arithmetic type of the step's rows (both arms)
-STEP_DTYPE = "mixed: f64 (every row but one), f32 (the 65536 x 4096 row reduce)"  # more than the 126 MB L2
+STEP_DTYPE = "mixed: f64 (every row but one), f32 (the 65536 x 4096 row reduce)"
 
 
 def run_extras(args, scr, torch, dev, stream, run_row, dadd_rate, fadd_rate, hbm_peak):
