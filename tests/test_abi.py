@@ -245,3 +245,41 @@ def test_batched_host_argument_errors(scr):
     assert L.cr_reduce_batched_host(x, o, 0, 10, 1, 10, 16, ctypes.byref(one), 2, ws, 256,
                                     None) == 0
     assert L.cr_inclusive_scan_batched_host(x, o, 10, 0, 1, 0, 0, 1, 2, ws, 256, None) == 0
+
+
+def test_pairwise_binary64_workspace_keeps_quads(scr):
+    """The binary64 pairwise scan's up pass keeps 16 bytes a thread (a quad
+    and the thread's root, 8 elements a thread): its workspace exceeds the
+    binary32 one by at least 2 bytes an element; iterated_pairwise keeps
+    none."""
+    L = scr.lib()
+    n = 1 << 24
+    pw64 = L.cr_scan_workspace_bytes(n, 1, 1, 2)
+    pw32 = L.cr_scan_workspace_bytes(n, 1, 1, 1)
+    ip64 = L.cr_scan_workspace_bytes(n, 2, 1, 2)
+    assert pw64 >= pw32 + 2 * n
+    assert ip64 < 2 * n
+
+
+def test_profile_select_takes_any_id(scr):
+    """Selecting a kernel, an id out of range or none records nothing by
+    itself and needs no device."""
+    L = scr.lib()
+    for kid in (0, 5, -1, 10 ** 6):
+        L.cr_profile_select(kid)
+    L.cr_profile_select(-1)
+    assert L.cr_profile_collect(None, None, 0) == 0
+    with pytest.raises(ValueError):
+        scr.profile_select("no_such_kernel")
+
+
+def test_build_overrides_need_their_own_directory():
+    """A build with overridden decomposition knobs never replaces the
+    package's own library."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "_cr_build_check", os.path.join(ROOT, "scan_canonical_reduce_gb300", "build.py"))
+    build = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(build)
+    with pytest.raises(ValueError):
+        build.build(defines=["CR_REDUCE_MAX_RUN=16"])
