@@ -352,7 +352,8 @@ constexpr int kUpTiles = 1 << kLogUpTiles;
 template <class T, int S, bool kQuads = false>
 __global__ void __launch_bounds__(kScanThreads, sizeof(T) == 8 ? 6 : 8)
 scan_up_kernel(const T* __restrict__ x, T* __restrict__ pyr, int* __restrict__ counters,
-               T* __restrict__ totals, ScanArgs a, T* __restrict__ quads) {
+               T* __restrict__ totals, ScanArgs a, T* __restrict__ quads,
+               T* __restrict__ tpyr) {
   __shared__ T lvl[2 * kScanThreads];
   __shared__ T s_agg[kUpTiles];
   constexpr int NS = kE / S;
@@ -399,6 +400,9 @@ scan_up_kernel(const T* __restrict__ x, T* __restrict__ pyr, int* __restrict__ c
     }
     if (t < full_threads) lvl[t] = tagg;
     tile_pyramid<true>(lvl, t, full_threads);
+    // pairwise: a full tile's pyramid levels 1 .. 8 kept for the down-sweep
+    if (kQuads && full_threads == kScanThreads && t < kScanThreads - 1)
+      tpyr[b * (kScanThreads - 1) + t] = lvl[kScanThreads + t];
     // blocks of kE < B < kTile elements: complete nodes of the tile pyramid
     if (a.totals_level > 0) {
       const int p = a.totals_level;
@@ -733,7 +737,7 @@ pairwise_tile_prefix_kernel(const T* __restrict__ pyr, T* __restrict__ ypre, Sca
 template <class T, bool kShift, bool kQuads = false>
 __global__ void __launch_bounds__(kScanThreads, 8)
 scan_pairwise_kernel(const T* x, T* out, const T* __restrict__ ypre, ScanArgs a, T init,
-                     const T* __restrict__ quads) {
+                     const T* __restrict__ quads, const T* __restrict__ tpyr) {
   __shared__ T lvl[2 * kScanThreads];
   __shared__ T s_last[kScanThreads / 32];
   __shared__ T s_E[kScanThreads + 1];  // E_t = W(8 t) of the tile; E_256 = Y_{b+1}
@@ -747,6 +751,10 @@ scan_pairwise_kernel(const T* x, T* out, const T* __restrict__ ypre, ScanArgs a,
 
   T v[kE];
   load8(x + i0, cnt, v);
+  // a full tile's pyramid levels 1 .. 8, when the up pass kept them
+  const bool kept = kQuads && full_threads == kScanThreads;
+  T tp = T(0);
+  if (kept && t < kScanThreads - 1) tp = ldg(tpyr + b * (kScanThreads - 1) + t);
   // the thread's nodes: pairs, quads, its aggregate (the first quad and the
   // aggregate from the up pass when it kept them)
   T p01, q03, p45, tagg;
@@ -763,7 +771,12 @@ scan_pairwise_kernel(const T* x, T* out, const T* __restrict__ ypre, ScanArgs a,
     tagg = add_rn(q03, add_rn(p45, p67));
   }
   if (t < full_threads) lvl[t] = tagg;
-  tile_pyramid<sizeof(T) == 8>(lvl, t, full_threads);  // ends with a block barrier
+  if (kept) {
+    if (t < kScanThreads - 1) lvl[kScanThreads + t] = tp;
+    __syncthreads();
+  } else {
+    tile_pyramid<sizeof(T) == 8>(lvl, t, full_threads);  // ends with a block barrier
+  }
 
   // warp prefixes E_{32 w}: thread w of warp 0 takes Y_b (the tile prefix,
   // computed once for every tile) and folds the warp bits; thread 8 takes
@@ -1264,9 +1277,11 @@ ScanPlan plan_scan(int64_t batch, int64_t n, cr_policy p, int64_t B, size_t esiz
   if (p == CR_PAIRWISE) {
     plan.ypre_ws = off;
     off += round256((size_t)(plan.full_tiles + 1) * esize);
-    if (esize == 8) {  // binary64: each thread's first quad and aggregate
-      plan.quad_ws = off;
+    if (esize == 8) {  // binary64: each thread's first quad and aggregate,
+      plan.quad_ws = off;  // and each tile's pyramid levels 1 .. 8
       off += round256((size_t)plan.n_tiles * kScanThreads * 2 * esize);
+      plan.tpyr_ws = off;
+      off += round256((size_t)plan.n_tiles * (kScanThreads - 1) * esize);
     }
   }
   // arrival counters, ready flags (one pass) and the tile counter: one
@@ -1333,7 +1348,7 @@ struct Tiled {
   bool block, shift;
   int S;
   ScanArgs a{};
-  T *pyr, *ypre, *totals, *carries, *quads;
+  T *pyr, *ypre, *totals, *carries, *quads, *tpyr;
   int* counters;
   Tiled(const ScanPlan& p, char* w, T i) : plan(p), ws(w), init(i) {
     block = plan.policy == CR_BLOCK_DYADIC;
@@ -1353,6 +1368,7 @@ struct Tiled {
     pyr = reinterpret_cast<T*>(ws + plan.pyr_ws);
     ypre = reinterpret_cast<T*>(ws + plan.ypre_ws);
     quads = plan.quad_ws ? reinterpret_cast<T*>(ws + plan.quad_ws) : nullptr;
+    tpyr = plan.quad_ws ? reinterpret_cast<T*>(ws + plan.tpyr_ws) : nullptr;
     counters = reinterpret_cast<int*>(ws + plan.cnt_ws);
     totals = block ? reinterpret_cast<T*>(ws + plan.totals_ws) : nullptr;
     carries = block ? reinterpret_cast<T*>(ws + plan.carries_ws) : nullptr;
@@ -1402,10 +1418,10 @@ struct Tiled {
     const unsigned ugrid = (unsigned)((t1 - t0 + kUpTiles - 1) / kUpTiles);
     CR_LAUNCH(kKScanUp, s, {  // up pass: pairwise, blocks spanning tiles, binary32 iterated
       if (S == 8 && quads != nullptr)
-        scan_up_kernel<T, 8, true><<<ugrid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a, quads);
-      else if (S == 8) scan_up_kernel<T, 8><<<ugrid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a, nullptr);
-      else if (S == 4) scan_up_kernel<T, 4><<<ugrid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a, nullptr);
-      else scan_up_kernel<T, 2><<<ugrid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a, nullptr);
+        scan_up_kernel<T, 8, true><<<ugrid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a, quads, tpyr);
+      else if (S == 8) scan_up_kernel<T, 8><<<ugrid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a, nullptr, nullptr);
+      else if (S == 4) scan_up_kernel<T, 4><<<ugrid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a, nullptr, nullptr);
+      else scan_up_kernel<T, 2><<<ugrid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a, nullptr, nullptr);
     });
     return cudaGetLastError();
   }
@@ -1499,13 +1515,13 @@ struct Tiled {
     if (plan.policy == CR_PAIRWISE) {
       CR_LAUNCH(kKScanPairwise, s, {
         if (shift && quads != nullptr)
-          scan_pairwise_kernel<T, true, true><<<grid, kScanThreads, 0, s>>>(x, out, ypre, a, init, quads);
+          scan_pairwise_kernel<T, true, true><<<grid, kScanThreads, 0, s>>>(x, out, ypre, a, init, quads, tpyr);
         else if (shift)
-          scan_pairwise_kernel<T, true><<<grid, kScanThreads, 0, s>>>(x, out, ypre, a, init, nullptr);
+          scan_pairwise_kernel<T, true><<<grid, kScanThreads, 0, s>>>(x, out, ypre, a, init, nullptr, nullptr);
         else if (quads != nullptr)
-          scan_pairwise_kernel<T, false, true><<<grid, kScanThreads, 0, s>>>(x, out, ypre, a, init, quads);
+          scan_pairwise_kernel<T, false, true><<<grid, kScanThreads, 0, s>>>(x, out, ypre, a, init, quads, tpyr);
         else
-          scan_pairwise_kernel<T, false><<<grid, kScanThreads, 0, s>>>(x, out, ypre, a, init, nullptr);
+          scan_pairwise_kernel<T, false><<<grid, kScanThreads, 0, s>>>(x, out, ypre, a, init, nullptr, nullptr);
       });
       return cudaGetLastError();
     }
@@ -1780,9 +1796,9 @@ cudaError_t run_block_totals(const ScanPlan& plan, const T* x, char* ws, cudaStr
   const unsigned grid = (unsigned)((plan.n_tiles + kUpTiles - 1) / kUpTiles);
   const int S = (int)(plan.B < kE ? plan.B : kE);
   CR_LAUNCH(kKScanUp, s, {
-    if (S == 8) scan_up_kernel<T, 8><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a, nullptr);
-    else if (S == 4) scan_up_kernel<T, 4><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a, nullptr);
-    else scan_up_kernel<T, 2><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a, nullptr);
+    if (S == 8) scan_up_kernel<T, 8><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a, nullptr, nullptr);
+    else if (S == 4) scan_up_kernel<T, 4><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a, nullptr, nullptr);
+    else scan_up_kernel<T, 2><<<grid, kScanThreads, 0, s>>>(x, pyr, counters, totals, a, nullptr, nullptr);
   });
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int64_t Kf = plan.n / plan.B;

@@ -56,6 +56,7 @@ struct ScanPlan {
   // pairwise, binary64: each thread's quad node x[8t..8t+4) and aggregate,
   // written by the up pass and read by the down-sweep (0: none)
   size_t quad_ws = 0;
+  size_t tpyr_ws = 0;        // and each full tile's pyramid levels 1 .. 8
   size_t ready_ws = 0, tilectr_ws = 0;  // one pass: node ready flags, tile counter
   size_t zero_ws = 0, zero_bytes = 0;   // cleared once per call
   int64_t K = 0;             // blocks (block_dyadic)
