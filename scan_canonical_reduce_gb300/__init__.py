@@ -521,15 +521,13 @@ def profile_select(kernel=None) -> None:
     profile_collect returns) while profiling is on; None records every one."""
     kid = -1
     if kernel is not None:
-        for i in range(256):
+        for i in range(256):  # ids run from 0 until the name is "unknown"
             nm = lib().cr_kernel_name(i).decode()
             if nm == "unknown":
                 break
             if nm == kernel:
                 kid = i
                 break
-        else:
-            kid = -1
         if kid < 0:
             raise ValueError("no libcr kernel named %r" % kernel)
     lib().cr_profile_select(kid)
