@@ -11,7 +11,8 @@
 // from its lowest set bit up (right-nested). A node at level p starting at
 // q*2^p is the perfect tree over aligned thread (tile) aggregates.
 // pairwise: out[i] = ((N_1 op N_2) op ...) op N_m, the same nodes folded from
-// the left (largest first): the up pass builds the node pyramid, then a
+// the left (largest first): the up pass builds the node pyramid (binary64:
+// keeping each thread's first quad and root and each tile's pyramid), then a
 // down-sweep (scan_pairwise_kernel) writes every output.
 // block_dyadic<B>: the same restricted to the position inside the block (only
 // the bits below log2 B), then out[i] = C_{k-1} op P(i) for blocks k >= 1,
@@ -341,8 +342,8 @@ __device__ __forceinline__ void load_pair(const T* p, T& a, T& b) {
 // 1.84 -> 1.76 ms; 8 blocks per SM spill and gain less, 8 tiles a block
 // nothing). Binary32: 8 blocks per SM (32 registers), as it compiles
 // unbounded (a bound of 6 lets it take 40 and runs 14 % slower).
-// (Tiles a block, as a compile-time override: which block forms which node
-// of the pyramid, never the node.)
+// The tiles a block (2^CR_UP_LOG_TILES) can be overridden at compile time:
+// that changes which block forms which node of the pyramid, never a node.
 #ifndef CR_UP_LOG_TILES
 #define CR_UP_LOG_TILES 2
 #endif
