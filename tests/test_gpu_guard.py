@@ -1,4 +1,4 @@
-"""Writes stay inside their buffers: a stand-in for a device memory checker,
+"""Accesses stay inside their buffers: a stand-in for a device memory checker,
 which this pool does not run. Every call family runs through the C ABI on
 buffers placed inside larger allocations whose surroundings hold a canary
 byte pattern, with workspaces of exactly the size the matching
@@ -32,9 +32,10 @@ def scr():
 class Guarded:
     """nbytes of device memory between two canary bands of GUARD bytes."""
 
-    def __init__(self, nbytes):
+    def __init__(self, nbytes, fill=CANARY):
         self.nbytes = int(nbytes)
-        self.buf = torch.full((GUARD + self.nbytes + GUARD,), CANARY, dtype=torch.uint8,
+        self.fill = fill
+        self.buf = torch.full((GUARD + self.nbytes + GUARD,), fill, dtype=torch.uint8,
                               device=DEV)
         self.ptr = self.buf.data_ptr() + GUARD  # 256-byte aligned like the allocation
 
@@ -42,12 +43,15 @@ class Guarded:
         return self.buf[GUARD:GUARD + self.nbytes].view(dtype)
 
     def bands_intact(self):
-        return bool((self.buf[:GUARD] == CANARY).all()) and \
-            bool((self.buf[GUARD + self.nbytes:] == CANARY).all())
+        return bool((self.buf[:GUARD] == self.fill).all()) and \
+            bool((self.buf[GUARD + self.nbytes:] == self.fill).all())
 
 
 def guarded_input(values):
-    g = Guarded(values.nbytes)
+    """The input between bands of all-ones bytes, a NaN in either precision:
+    a read past the input that reached a result would make it NaN, and the
+    comparison with the binding's result would fail."""
+    g = Guarded(values.nbytes, fill=0xFF)
     g.view(torch.float64 if values.dtype == np.float64 else torch.float32).copy_(
         torch.from_numpy(values))
     return g
