@@ -53,6 +53,7 @@
 // chain itself with a statistical margin instead (passes 1 to 4 below, see
 // "binary32"); the checks of passes 8 and 9 are the same.
 // Every add of the chain is therefore the real add or proven equal to it.
+#include <atomic>
 #include <cstdint>
 
 #include "cr_chain.h"
@@ -2112,21 +2113,24 @@ cudaError_t run_chain_front(const ChainPlan& p, const T* src, char* ws, const Ch
   return cudaGetLastError();
 }
 
-// Co-resident blocks of the fused kernel on this device (cached per device).
+// Co-resident blocks of the fused kernel on this device (cached per device;
+// threads that race to fill an entry store the same value).
 template <class T>
 int fused_grid_limit() {
-  static int cache[64] = {};
+  static std::atomic<int> cache[64];  // static storage: starts at zero
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (cache[dev] == 0) {
+  int limit = cache[dev].load(std::memory_order_relaxed);
+  if (limit == 0) {
     int per_sm = 0, sms = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, chain_walk_fix_kernel<T>, kCT,
                                                       0) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return 0;
-    cache[dev] = per_sm * sms;
+    limit = per_sm * sms;
+    cache[dev].store(limit, std::memory_order_relaxed);
   }
-  return cache[dev];
+  return limit;
 }
 
 }  // namespace
