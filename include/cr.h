@@ -232,8 +232,11 @@ cr_status cr_scan_ex_batched(const void* x, void* out, int64_t batch, int64_t n,
  * in chunks over three streams (copy in, compute on `stream`, copy out),
  * so that the transfers overlap the kernels. dev_buf: caller-owned device
  * memory of at least the bytes the query returns (256-byte aligned); it
- * holds device copies of x and out and the workspace. Errors as for the
- * device forms. */
+ * holds the workspace first (its status word at dev_buf itself, so that
+ * cr_sync_status(dev_buf, stream) reports on the call), then device copies
+ * of x and out. As the call synchronises before it returns, it reports a
+ * bounded device-side wait that gave up itself (CR_ERR_TIMEOUT). Errors
+ * otherwise as for the device forms. */
 size_t cr_inclusive_scan_host_workspace_bytes(int64_t n, cr_policy p, int64_t B, cr_dtype dt);
 cr_status cr_inclusive_scan_host(const void* x_host, void* out_host, int64_t n, cr_policy p,
                                  int64_t B, cr_dtype dt, void* dev_buf, size_t dev_bytes,
@@ -255,8 +258,9 @@ cr_status cr_reduce_host(const void* x_host, int64_t n, int32_t L, const void* i
  * strides; out == x (in place) is allowed, any other overlap of their
  * address ranges is INVALID_ARG (for the reduce, out_host's batch elements
  * must not meet x's range). dev_buf: caller-owned device memory of at least
- * the bytes the query returns (256-byte aligned). Errors otherwise as for the
- * device forms. */
+ * the bytes the query returns (256-byte aligned), laid out and reporting
+ * CR_ERR_TIMEOUT as for the 1-D host-buffer forms above. Errors otherwise
+ * as for the device forms. */
 size_t cr_reduce_batched_host_workspace_bytes(int64_t batch, int64_t n, int32_t L,
                                               cr_dtype dt);
 cr_status cr_reduce_batched_host(const void* x_host, void* out_host, int64_t batch, int64_t n,

@@ -4,6 +4,7 @@
 #include <cstring>
 
 #include "cr.h"
+#include "cr_launch.h"
 #include "cr_plan.h"
 #include "cr_scan.h"
 
@@ -230,10 +231,21 @@ cr_status cr_scan_ex_batched(const void* x, void* out, int64_t batch, int64_t n,
 
 static size_t r256(size_t v) { return (v + 255) & ~size_t(255); }
 
+// A host-buffer call's result once its work is enqueued: CR_ERR_CUDA for a
+// failed step, else the status word of its workspace (the call's copies out
+// are then complete, and a wait that gave up is reported here).
+static cr_status host_result(cudaError_t e, const void* ws, cudaStream_t s) {
+  int status = 0;
+  if (e != cudaSuccess || cr::read_status(ws, s, &status) != cudaSuccess) return CR_ERR_CUDA;
+  return status == 0 ? CR_OK : CR_ERR_TIMEOUT;
+}
+
+// dev_buf of a host-buffer call: the workspace first (its status word at
+// dev_buf itself, where cr_sync_status looks), then the device copies.
 size_t cr_inclusive_scan_host_workspace_bytes(int64_t n, cr_policy p, int64_t B, cr_dtype dt) {
   const size_t sz = esize(dt);
   if (sz == 0 || n < 0 || !cr::scan_args_ok(p, B)) return 0;
-  return 2 * r256((size_t)n * sz) + cr::plan_scan(1, n, p, B, sz).ws_bytes;
+  return r256(cr::plan_scan(1, n, p, B, sz).ws_bytes) + 2 * r256((size_t)n * sz);
 }
 
 cr_status cr_inclusive_scan_host(const void* x_host, void* out_host, int64_t n, cr_policy p,
@@ -244,29 +256,31 @@ cr_status cr_inclusive_scan_host(const void* x_host, void* out_host, int64_t n, 
   if (n > 0 && (x_host == nullptr || out_host == nullptr)) return CR_ERR_INVALID_ARG;
   const cr::ScanPlan plan = cr::plan_scan(1, n, p, B, sz);
   const size_t arr = r256((size_t)n * sz);
-  const cr_status ws_ok = check_ws(dev_buf, dev_bytes, 2 * arr + plan.ws_bytes);
+  const size_t wsb = r256(plan.ws_bytes);
+  const cr_status ws_ok = check_ws(dev_buf, dev_bytes, wsb + 2 * arr);
   if (ws_ok != CR_OK) return ws_ok;
   if (!plan.supported) return CR_ERR_UNSUPPORTED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  char* base = static_cast<char*>(dev_buf);
-  char* ws = base + 2 * arr;
+  char* ws = static_cast<char*>(dev_buf);
+  char* x_dev = ws + wsb;
+  char* out_dev = x_dev + arr;
   if (clear_status(ws, s) != cudaSuccess) return CR_ERR_CUDA;
   cudaError_t e;
   if (dt == CR_F64)
     e = cr::run_scan_host<double>(plan, static_cast<const double*>(x_host),
-                                  static_cast<double*>(out_host), reinterpret_cast<double*>(base),
-                                  reinterpret_cast<double*>(base + arr), ws, s);
+                                  static_cast<double*>(out_host), reinterpret_cast<double*>(x_dev),
+                                  reinterpret_cast<double*>(out_dev), ws, s);
   else
     e = cr::run_scan_host<float>(plan, static_cast<const float*>(x_host),
-                                 static_cast<float*>(out_host), reinterpret_cast<float*>(base),
-                                 reinterpret_cast<float*>(base + arr), ws, s);
-  return from_cuda(e);
+                                 static_cast<float*>(out_host), reinterpret_cast<float*>(x_dev),
+                                 reinterpret_cast<float*>(out_dev), ws, s);
+  return host_result(e, ws, s);
 }
 
 size_t cr_reduce_host_workspace_bytes(int64_t n, int32_t L, cr_dtype dt) {
   const size_t sz = esize(dt);
   if (sz == 0 || n < 0 || L < 1) return 0;
-  return r256((size_t)n * sz) + 256 + cr::plan_reduce(1, n, L, 1, n, sz).ws_bytes;
+  return r256(cr::plan_reduce(1, n, L, 1, n, sz).ws_bytes) + 256 + r256((size_t)n * sz);
 }
 
 cr_status cr_reduce_host(const void* x_host, int64_t n, int32_t L, const void* init_host,
@@ -276,34 +290,31 @@ cr_status cr_reduce_host(const void* x_host, int64_t n, int32_t L, const void* i
   if (sz == 0 || n < 0 || L < 1 || init_host == nullptr || out_host == nullptr)
     return CR_ERR_INVALID_ARG;
   if (n > 0 && x_host == nullptr) return CR_ERR_INVALID_ARG;
-  const size_t arr = r256((size_t)n * sz);
-  const size_t need = arr + 256 + cr::plan_reduce(1, n, L, 1, n, sz).ws_bytes;
-  const cr_status ws_ok = check_ws(dev_buf, dev_bytes, need);
+  const cr::ReducePlan plan = cr::plan_reduce(1, n, L, 1, n, sz);
+  const size_t wsb = r256(plan.ws_bytes);
+  const cr_status ws_ok = check_ws(dev_buf, dev_bytes, wsb + 256 + r256((size_t)n * sz));
   if (ws_ok != CR_OK) return ws_ok;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  char* base = static_cast<char*>(dev_buf);
-  char* out_dev = base + arr;
-  char* ws = base + arr + 256;
-  const cr::ReducePlan plan = cr::plan_reduce(1, n, L, 1, n, sz);
+  char* ws = static_cast<char*>(dev_buf);
+  char* out_dev = ws + wsb;
+  char* x_dev = out_dev + 256;
   if (clear_status(ws, s) != cudaSuccess) return CR_ERR_CUDA;
   cudaError_t e;
   if (dt == CR_F64) {
     double init;
     std::memcpy(&init, init_host, sizeof(init));
     e = cr::run_reduce_host<double>(plan, static_cast<const double*>(x_host),
-                                    reinterpret_cast<double*>(base),
+                                    reinterpret_cast<double*>(x_dev),
                                     reinterpret_cast<double*>(out_dev), init, ws, s, n);
   } else {
     float init;
     std::memcpy(&init, init_host, sizeof(init));
     e = cr::run_reduce_host<float>(plan, static_cast<const float*>(x_host),
-                                   reinterpret_cast<float*>(base),
+                                   reinterpret_cast<float*>(x_dev),
                                    reinterpret_cast<float*>(out_dev), init, ws, s, n);
   }
-  if (e != cudaSuccess) return CR_ERR_CUDA;
-  if (cudaMemcpyAsync(out_host, out_dev, sz, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-    return CR_ERR_CUDA;
-  return cudaStreamSynchronize(s) == cudaSuccess ? CR_OK : CR_ERR_CUDA;
+  if (e == cudaSuccess) e = cudaMemcpyAsync(out_host, out_dev, sz, cudaMemcpyDeviceToHost, s);
+  return host_result(e, ws, s);
 }
 
 cr_status cr_sync_status(void* ws, void* stream) {
@@ -311,8 +322,7 @@ cr_status cr_sync_status(void* ws, void* stream) {
   if (cudaStreamSynchronize(s) != cudaSuccess) return CR_ERR_CUDA;
   if (ws == nullptr) return CR_ERR_WORKSPACE;
   int status = 0;
-  if (cudaMemcpy(&status, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
-    return CR_ERR_CUDA;
+  if (cr::read_status(ws, s, &status) != cudaSuccess) return CR_ERR_CUDA;
   return status == 0 ? CR_OK : CR_ERR_TIMEOUT;
 }
 

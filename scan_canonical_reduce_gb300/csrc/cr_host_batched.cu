@@ -152,15 +152,17 @@ cudaError_t pipeline(int64_t G, cudaStream_t s, const GroupFn& copy_in, const Gr
   return cudaStreamSynchronize(s);
 }
 
+// dev_buf of a batched host-buffer call: the workspace first (wsb bytes; its
+// status word at dev_buf itself, where cr_sync_status looks), then the device
+// copies of x and out.
 template <class T>
 cudaError_t reduce_batched_host(const T* xh, T* oh, int64_t batch, int64_t n, int64_t es,
-                                int64_t bs, Layout lay, int32_t L, T init, char* base,
-                                cudaStream_t s) {
+                                int64_t bs, Layout lay, int32_t L, T init, char* ws,
+                                size_t wsb, cudaStream_t s) {
   const size_t sz = sizeof(T);
   const int64_t G = group_count(batch, n, sz);
-  T* xd = reinterpret_cast<T*>(base);
-  T* od = reinterpret_cast<T*>(base + r256((size_t)(batch * n) * sz));
-  char* ws = base + r256((size_t)(batch * n) * sz) + r256((size_t)batch * sz);
+  T* xd = reinterpret_cast<T*>(ws + wsb);
+  T* od = reinterpret_cast<T*>(ws + wsb + r256((size_t)(batch * n) * sz));
   std::lock_guard<std::mutex> lock(cr::host_pipe_mutex());
   auto in = [&](int64_t g, cudaStream_t st) -> cudaError_t {
     int64_t b0, b1;
@@ -187,14 +189,13 @@ cudaError_t reduce_batched_host(const T* xh, T* oh, int64_t batch, int64_t n, in
 
 template <class T>
 cudaError_t scan_batched_host(const T* xh, T* oh, int64_t batch, int64_t n, int64_t es,
-                              int64_t bs, Layout lay, cr_policy p, int64_t B, char* base,
-                              cudaStream_t s) {
+                              int64_t bs, Layout lay, cr_policy p, int64_t B, char* ws,
+                              size_t wsb, cudaStream_t s) {
   const size_t sz = sizeof(T);
   const int64_t G = group_count(batch, n, sz);
   const size_t arr = r256((size_t)(batch * n) * sz);
-  T* xd = reinterpret_cast<T*>(base);
-  T* od = reinterpret_cast<T*>(base + arr);
-  char* ws = base + 2 * arr;
+  T* xd = reinterpret_cast<T*>(ws + wsb);
+  T* od = reinterpret_cast<T*>(ws + wsb + arr);
   std::lock_guard<std::mutex> lock(cr::host_pipe_mutex());
   auto in = [&](int64_t g, cudaStream_t st) -> cudaError_t {
     int64_t b0, b1;
@@ -229,6 +230,15 @@ bool ranges_meet(const void* a, size_t na, const void* b, size_t nb) {
   return pa < pb + nb && pb < pa + na;
 }
 
+// The call's result once its pipeline has returned: CR_ERR_CUDA for a failed
+// step, else the workspace status word (a wait that gave up is reported).
+cr_status host_result(cudaError_t e, const void* ws, cudaStream_t s) {
+  if (e == cudaErrorNotSupported) return CR_ERR_UNSUPPORTED;
+  int status = 0;
+  if (e != cudaSuccess || cr::read_status(ws, s, &status) != cudaSuccess) return CR_ERR_CUDA;
+  return status == 0 ? CR_OK : CR_ERR_TIMEOUT;
+}
+
 }  // namespace
 
 extern "C" {
@@ -239,8 +249,8 @@ size_t cr_reduce_batched_host_workspace_bytes(int64_t batch, int64_t n, int32_t 
   if (sz == 0 || batch < 0 || n < 0 || L < 1) return 0;
   if (batch == 0) return cr::kHeaderBytes;
   const int64_t G = group_count(batch, n, sz);
-  return r256((size_t)(batch * n) * sz) + r256((size_t)batch * sz) +
-         reduce_group_ws(batch, n, L, sz, G);
+  return r256(reduce_group_ws(batch, n, L, sz, G)) + r256((size_t)(batch * n) * sz) +
+         r256((size_t)batch * sz);
 }
 
 cr_status cr_reduce_batched_host(const void* x_host, void* out_host, int64_t batch, int64_t n,
@@ -265,8 +275,8 @@ cr_status cr_reduce_batched_host(const void* x_host, void* out_host, int64_t bat
   const Layout lay = n == 0 ? kRows : layout_of(batch, n, elem_stride, batch_stride);
   if (lay == kNone) return CR_ERR_UNSUPPORTED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  char* base = static_cast<char*>(dev_buf);
-  char* ws = base + r256((size_t)(batch * n) * sz) + r256((size_t)batch * sz);
+  char* ws = static_cast<char*>(dev_buf);
+  const size_t wsb = r256(reduce_group_ws(batch, n, L, sz, group_count(batch, n, sz)));
   if (cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return CR_ERR_CUDA;
   cudaError_t e;
   if (dt == CR_F64) {
@@ -274,15 +284,15 @@ cr_status cr_reduce_batched_host(const void* x_host, void* out_host, int64_t bat
     std::memcpy(&init, init_host, sizeof(init));
     e = reduce_batched_host<double>(static_cast<const double*>(x_host),
                                     static_cast<double*>(out_host), batch, n, elem_stride,
-                                    batch_stride, lay, L, init, base, s);
+                                    batch_stride, lay, L, init, ws, wsb, s);
   } else {
     float init;
     std::memcpy(&init, init_host, sizeof(init));
     e = reduce_batched_host<float>(static_cast<const float*>(x_host),
                                    static_cast<float*>(out_host), batch, n, elem_stride,
-                                   batch_stride, lay, L, init, base, s);
+                                   batch_stride, lay, L, init, ws, wsb, s);
   }
-  return e == cudaSuccess ? CR_OK : CR_ERR_CUDA;
+  return host_result(e, ws, s);
 }
 
 size_t cr_inclusive_scan_batched_host_workspace_bytes(int64_t batch, int64_t n, cr_policy p,
@@ -291,7 +301,7 @@ size_t cr_inclusive_scan_batched_host_workspace_bytes(int64_t batch, int64_t n, 
   if (sz == 0 || batch < 0 || n < 0 || !cr::scan_args_ok(p, B)) return 0;
   if (batch == 0 || n == 0) return cr::kHeaderBytes;
   const int64_t G = group_count(batch, n, sz);
-  return 2 * r256((size_t)(batch * n) * sz) + scan_group_ws(batch, n, p, B, sz, G);
+  return r256(scan_group_ws(batch, n, p, B, sz, G)) + 2 * r256((size_t)(batch * n) * sz);
 }
 
 cr_status cr_inclusive_scan_batched_host(const void* x_host, void* out_host, int64_t batch,
@@ -319,21 +329,19 @@ cr_status cr_inclusive_scan_batched_host(const void* x_host, void* out_host, int
     return CR_ERR_INVALID_ARG;
   if (dev_buf == nullptr || !aligned(dev_buf, 256) || dev_bytes < need) return CR_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  char* base = static_cast<char*>(dev_buf);
-  if (cudaMemsetAsync(base + 2 * r256((size_t)(batch * n) * sz), 0, sizeof(int), s) !=
-      cudaSuccess)
-    return CR_ERR_CUDA;
+  char* ws = static_cast<char*>(dev_buf);
+  const size_t wsb = r256(scan_group_ws(batch, n, p, B, sz, group_count(batch, n, sz)));
+  if (cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return CR_ERR_CUDA;
   cudaError_t e;
   if (dt == CR_F64)
     e = scan_batched_host<double>(static_cast<const double*>(x_host),
                                   static_cast<double*>(out_host), batch, n, elem_stride,
-                                  batch_stride, lay, p, B, base, s);
+                                  batch_stride, lay, p, B, ws, wsb, s);
   else
     e = scan_batched_host<float>(static_cast<const float*>(x_host),
                                  static_cast<float*>(out_host), batch, n, elem_stride,
-                                 batch_stride, lay, p, B, base, s);
-  if (e == cudaErrorNotSupported) return CR_ERR_UNSUPPORTED;
-  return e == cudaSuccess ? CR_OK : CR_ERR_CUDA;
+                                 batch_stride, lay, p, B, ws, wsb, s);
+  return host_result(e, ws, s);
 }
 
 }  // extern "C"

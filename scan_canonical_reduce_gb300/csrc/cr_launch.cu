@@ -100,6 +100,13 @@ LaunchScope::~LaunchScope() {
   if (slot < (int)g_records.size()) cudaEventRecord(g_records[slot].stop, stream);
 }
 
+cudaError_t read_status(const void* ws, cudaStream_t s, int* status) {
+  *status = 0;
+  cudaError_t e = cudaMemcpyAsync(status, ws, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  return e;
+}
+
 }  // namespace cr
 
 extern "C" {

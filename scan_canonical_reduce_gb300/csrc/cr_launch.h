@@ -70,6 +70,11 @@ std::mutex& host_pipe_mutex();
 // is 64 or more (the callers then fail with cudaErrorInvalidDevice).
 HostPipe* host_pipe();
 
+// Reads the status word at the start of workspace `ws` once the work before
+// it on `s` is done (synchronises s): 0, or the code a bounded device-side
+// wait recorded when it gave up.
+cudaError_t read_status(const void* ws, cudaStream_t s, int* status);
+
 // Usage: CR_LAUNCH(kKScanUp, stream, kernel<<<grid, block, 0, stream>>>(...));
 #define CR_LAUNCH(ID, STREAM, ...)                  \
   do {                                              \
