@@ -77,7 +77,7 @@ const char* kernel_name(int id) {
       "scan_seq_block_kernel", "row_reduce_kernel",
       "chain_link_kernel",     "chain_verify_kernel",   "chain_walk_fix_kernel",
       "scan_local_again_kernel", "fixup_again_kernel", "pairwise_tile_prefix_kernel",
-      "chain_round_sum_kernel"};
+      "chain_round_sum_kernel", "scan_seq_left2_kernel"};
   return (id >= 0 && id < kKernelCount) ? names[id] : "unknown";
 }
 

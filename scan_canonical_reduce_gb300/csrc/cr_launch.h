@@ -43,6 +43,7 @@ enum KernelId : int {
   kKFixupAgain,
   kKPairwisePrefix,
   kKChainRoundSum,
+  kKScanSeqLeft2,
   kKernelCount
 };
 

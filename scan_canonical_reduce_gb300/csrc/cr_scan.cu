@@ -1592,7 +1592,7 @@ cudaError_t run_scan(const ScanPlan& plan, const T* x, T* out, int64_t es, int64
           oes % 2 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
           (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
         const int64_t blocks2 = ((plan.batch + 1) / 2 + 255) / 256;
-        CR_LAUNCH(kKScanSeqBlock, s,
+        CR_LAUNCH(kKScanSeqLeft2, s,
                   scan_seq_left2_kernel<4, true><<<(unsigned)blocks2, 256, 0, s>>>(
                       reinterpret_cast<const double*>(x), reinterpret_cast<double*>(out),
                       plan.batch, plan.n, es, oes));
