@@ -224,10 +224,13 @@ def job_gbs(bytes_per_step: int, steps: int, world: int, seconds: float) -> floa
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    """nvidia-smi samples of the SM clock and throttle reasons while running."""
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+    """nvidia-smi samples of the SM clock and throttle reasons while running,
+    every INTERVAL_MS; stop() keeps the samples stamped inside the timed
+    window (all of them if none falls inside)."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 20
 
     def __init__(self, gpu_uuid: str | None):
         self.uuid = gpu_uuid
@@ -236,7 +239,7 @@ class ClockSampler:
 
     def start(self):
         cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-               "-lms", "200"]
+               "-lms", str(self.INTERVAL_MS)]
         if self.uuid:
             cmd += ["-i", self.uuid]
         try:
@@ -252,7 +255,8 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
-    def stop(self):
+    def stop(self, window=None):
+        """window: (t0, t1) in time.time() seconds, the timed region."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -261,23 +265,34 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.t.join(timeout=2)
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in self.lines:
-            f = [x.strip() for x in l.split(",")]
-            if len(f) < 7:
-                continue
-            try:
-                sm.append(float(f[0]))
-                mx.append(float(f[1]))
-            except ValueError:
-                continue
-            for nm, v in zip(names, f[3:7]):
-                if v.lower().startswith("active"):
-                    reasons.add(nm)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+        return summarize_clock_lines(self.lines, window, self.INTERVAL_MS)
+
+
+def summarize_clock_lines(lines, window, interval_ms):
+    """Median SM clock, max clock and the throttle reasons seen, over the
+    samples stamped inside `window` (local-time stamps of nvidia-smi), or over
+    all samples when none is inside."""
+    import datetime
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    samples = []  # (seconds, sm, max, reasons)
+    for l in lines:
+        f = [x.strip() for x in l.split(",")]
+        if len(f) < 8:
+            continue
+        try:
+            ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            sm, mx = float(f[1]), float(f[2])
+        except ValueError:
+            continue
+        samples.append((ts, sm, mx, {nm for nm, v in zip(names, f[4:8])
+                                     if v.lower().startswith("active")}))
+    inside = [x for x in samples if window and window[0] <= x[0] <= window[1]]
+    use = inside or samples
+    reasons = set().union(*(x[3] for x in use)) if use else set()
+    return {"sm_mhz": statistics.median(x[1] for x in use) if use else None,
+            "sm_max_mhz": max(x[2] for x in use) if use else None,
+            "samples": len(use), "samples_in_timed_region": len(inside),
+            "interval_ms": interval_ms, "reasons": sorted(reasons)}
 
 
 # ------------------------------------------------------------- GPU arm
@@ -399,6 +414,7 @@ def run_native(args):
     ev = {r[0]: [] for r in rows}
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
     t0.record(stream)
     for _ in range(args.steps):
         for row in rows:
@@ -410,11 +426,12 @@ def run_native(args):
             ev[row[0]].append((a, b))
     t1.record(stream)
     torch.cuda.synchronize(dev)
+    wall1 = time.time()
     scr.profile_enable(False)
     scr.profile_select(None)
     launches = scr.launch_count() - launches0
     prof_top = scr.profile_collect()
-    clocks = sampler.stop()
+    clocks = sampler.stop((wall0, wall1))
     ms_total = max_over_ranks(t0.elapsed_time(t1), dist, dev)
     if dist:
         dist.barrier()

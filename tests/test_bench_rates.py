@@ -79,3 +79,26 @@ def test_ncu_traffic_needs_the_captured_sources(monkeypatch):
     monkeypatch.setattr(bench, "source_digest", lambda name: "0" * 16)
     assert bench.ncu_traffic("scan_onepass_kernel") is None
     assert bench.ncu_traffic("no_such_kernel") is None
+
+
+def test_clock_samples_inside_the_timed_window():
+    """Only samples stamped inside the timed region count (with their throttle
+    reasons); with none inside, all samples are reported and the count says
+    so; unparsable lines are skipped."""
+    import datetime
+
+    def line(t, sm, cap):
+        stamp = datetime.datetime.fromtimestamp(t).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return "%s, %d, 2070, 900.0, Not Active, Not Active, Not Active, %s" % (
+            stamp, sm, "Active" if cap else "Not Active")
+
+    t = 1.8e9
+    lines = [line(t - 0.3, 900, True), line(t + 0.01, 2070, False),
+             line(t + 0.03, 2055, False), "not a sample"]
+    c = bench.summarize_clock_lines(lines, (t, t + 0.05), 20)
+    assert c["samples"] == 2 and c["samples_in_timed_region"] == 2
+    assert c["sm_mhz"] == pytest.approx(2062.5) and c["sm_max_mhz"] == 2070.0
+    assert c["reasons"] == []  # the power-cap sample lies before the window
+    c = bench.summarize_clock_lines(lines, (t + 1, t + 2), 20)
+    assert c["samples"] == 3 and c["samples_in_timed_region"] == 0
+    assert c["reasons"] == ["sw_power_cap"]
